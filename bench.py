@@ -1,0 +1,403 @@
+"""Benchmark of the per-step unmask-decision hot path on GB300.
+
+One "step" = the whole path over one batch: the fused row-statistics pass over
+every masked position's current and previous logit rows, then the four
+selection rules (Fast-dLLM threshold, DepGA-Block boundary, CAP-Decoding,
+DAPD graph + Welsh-Powell) for every sequence.
+
+Workload (batched serving): 64 independent sequences x 32 masked positions,
+vocab 152064, bf16 current and previous logits (1.25 GB per step, larger than
+L2, so no flush is needed between steps), fp16 attention 10 layers x 28 heads
+over 512 positions.  Inputs are synthetic (``synth``), seeded, and resident in
+HBM before the timed region.
+
+Prints one JSON line: decisions/s (masked positions decided per second, all
+ranks), the row pass's achieved HBM bandwidth against the measured peak, the
+end-to-end number through host buffers, the SM clocks seen, and the fp64 CPU
+oracle timed on a bounded sample.  ``--impl reference`` times the oracle
+itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "masked-position decisions/sec per decode step; logit-read GB/s vs HBM peak"
+WORKLOAD = "batched"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=1004)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
+    ap.add_argument("--compact-attn", action="store_true",
+                    help="hold only the attention block [B, L, H, blk, blk] on the device (small profiling cases)")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_desc(cfg):
+    return (f"batched serving: B={cfg.batch} sequences x {cfg.blk} masked positions, V={cfg.vocab} bf16 "
+            f"current+previous logits, fp16 attention {cfg.n_layers}x{cfg.n_heads} over {cfg.seq_len} "
+            f"positions; all four rules per sequence")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, window=None):
+        """Median SM clock and throttle reasons of the samples taken inside
+        ``window`` (host wall-clock interval of the timed region) -- or, if
+        the region was shorter than a few sampling periods, of the load phase
+        run just before it."""
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        lines = self.lines
+        inside = [x for x in lines if window and window[0] <= x[0] <= window[1]]
+        used = "timed region"
+        if len(inside) >= 3:
+            lines = inside
+        else:
+            used = "load phase + timed region"
+        for _, ln in lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "window": used}
+
+
+# ------------------------------------------------------------------ native
+def run_native(args, rank, world, local):
+    import torch
+
+    import diffusion_decoding_token_gb300 as dlm
+    import synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = synth.CONFIGS[WORKLOAD]
+    if args.batch:
+        cfg = synth.scaled(cfg, batch=args.batch)
+    B, blk, V = cfg.batch, cfg.blk, cfg.vocab
+    w = synth.make(cfg, seed=args.seed + 100 * rank)
+
+    def dev16(a, dt):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(dt)
+
+    cur = dev16(w.cur, torch.bfloat16)
+    prev = dev16(w.prev, torch.bfloat16)
+    masked = torch.from_numpy(w.masked).to(dev)
+    N, bs = cfg.seq_len, cfg.block_start
+    if args.compact_attn:
+        attn, bs = dev16(w.attn, torch.float16), 0
+    else:
+        attn = torch.zeros((B, cfg.n_layers, cfg.n_heads, N, N), dtype=torch.float16, device=dev)
+        attn[:, :, :, bs:bs + blk, bs:bs + blk] = dev16(w.attn, torch.float16)
+
+    status = dlm.new_status(dev)
+    stream = torch.cuda.current_stream(dev)
+    common = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
+                  gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
+                  bulk_frac=cfg.bulk_frac, status=status)
+    plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, **common)
+
+    for _ in range(args.warmup):
+        plan.run(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        # load phase (untimed): keeps the GPU busy for ~1 s so the clock
+        # samples reflect the clocks under this load
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            for _ in range(50):
+                plan.run(stream)
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    t0.record(stream)
+    for k in range(args.steps):
+        plan.run(stream, events=evs[k])
+    t1.record(stream)
+    host_ms = (time.time() - w0) * 1000.0 / args.steps
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop((w0, w1)) if sampler else None
+    total_ms = t0.elapsed_time(t1)
+    k1 = [e[0].elapsed_time(e[1]) for e in evs]
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+
+    # the four rules alone, on the statistics of the last step
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        plan.run(stream, rules_only=True)
+    r0.record(stream)
+    for _ in range(100):
+        plan.run(stream, rules_only=True)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    rules_ms = r0.elapsed_time(r1) / 100
+
+    # --- end to end through host buffers (pinned), same public API
+    e2e = None
+    if args.e2e_steps > 0:
+        cur_h = torch.from_numpy(w.cur.view(np.int16)).view(torch.bfloat16).pin_memory()
+        prev_h = torch.from_numpy(w.prev.view(np.int16)).view(torch.bfloat16).pin_memory()
+        attn_h = torch.from_numpy(w.attn.view(np.int16)).view(torch.float16).pin_memory()
+        masked_h = torch.from_numpy(w.masked).pin_memory()
+        cur_d2 = torch.empty_like(cur)
+        prev_d2 = torch.empty_like(prev)
+        attn_c = torch.empty(attn_h.shape, dtype=torch.float16, device=dev)
+        masked_d2 = torch.empty_like(masked)
+        outs_h = [torch.empty((B, blk), dtype=torch.uint8).pin_memory() for _ in range(3)]
+        nsel_h = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(3)]
+        blen_h = torch.empty(B, dtype=torch.int32).pin_memory()
+
+        plan2 = dlm.StepPlan(cur_d2, prev_d2, masked_d2, attn=attn_c, block_start=0, **common)
+
+        def e2e_step():
+            cur_d2.copy_(cur_h, non_blocking=True)
+            prev_d2.copy_(prev_h, non_blocking=True)
+            attn_c.copy_(attn_h, non_blocking=True)
+            masked_d2.copy_(masked_h, non_blocking=True)
+            plan2.run(stream)
+            for i, k in enumerate(("threshold", "cap", "dapd")):
+                outs_h[i].copy_(plan2.out[k][0], non_blocking=True)
+                nsel_h[i].copy_(plan2.out[k][1], non_blocking=True)
+            blen_h.copy_(plan2.block_len, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a0.elapsed_time(a1) / args.e2e_steps
+        h2d = (cur_h.numel() + prev_h.numel() + attn_h.numel()) * 2 + masked_h.numel()
+        d2h = sum(t.numel() for t in outs_h) + sum(t.numel() * 4 for t in nsel_h) + blen_h.numel() * 4
+        e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, clocks=clocks, e2e=e2e, host_ms=host_ms,
+                cfg=cfg, launches=plan.n_launches * args.steps, w=w)
+
+
+# ------------------------------------------------------------------ oracle
+def oracle_sample(w, n_seq):
+    """The oracle's whole path (stats + four rules) on the first n_seq sequences."""
+    import oracle
+    import synth
+
+    cfg = w.cfg
+    blk = cfg.blk
+    rows = n_seq * blk
+    cur = np.ascontiguousarray(w.cur[:rows])
+    prev = np.ascontiguousarray(w.prev[:rows])
+    masked = np.ascontiguousarray(w.masked[:n_seq])
+    t = time.perf_counter()
+    o = oracle.row_stats(cur, prev, dtype=synth.BF16)
+    conf = o["conf"].reshape(n_seq, blk)
+    oracle.select_threshold(conf, masked, cfg.tau)
+    oracle.depcap_boundary(o["kl"].reshape(n_seq, blk), o["entropy"].reshape(n_seq, blk), cfg.lam, cfg.L_min)
+    oracle.cap_select(cur, o["argmax"].reshape(n_seq, blk), conf, o["lse"].reshape(n_seq, blk), masked,
+                      cfg.tau_low, cfg.tau_high, cfg.gamma, cfg.p_max, dtype=synth.BF16)
+    oracle.dapd(np.ascontiguousarray(w.attn[:n_seq]), masked, conf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac,
+                dtype=synth.F16)
+    return time.perf_counter() - t, int(masked.sum())
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The oracle, as it stands, on repeated passes over a bounded sample of
+    the same workload until about ``budget_s`` seconds of CPU work."""
+    import oracle
+    oracle.build()
+    dt1, _ = oracle_sample(w, 1)
+    n_seq = int(max(1, min(w.cfg.batch, budget_s / max(dt1, 1e-3))))
+    total, count, reps = 0.0, 0, 0
+    while total < budget_s and reps < 10000:
+        dt, n = oracle_sample(w, n_seq)
+        total += dt
+        count += n
+        reps += 1
+    return {"value": count / total, "unit": "decisions/s", "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"{reps} pass(es) of the full path (stats + four rules) over {n_seq} of {w.cfg.batch} "
+                      f"sequences ({count} decisions) of the same workload, {total:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    import synth
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[WORKLOAD]
+    w = synth.make(cfg, seed=args.seed)
+    import oracle
+    oracle.build()
+    dt1, _ = oracle_sample(w, 1)
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    n_seq = int(max(1, min(cfg.batch, per_step_budget / max(dt1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample(w, n_seq)
+    times, n = [], 0
+    for _ in range(args.steps):
+        dt, n = oracle_sample(w, n_seq)
+        times.append(dt)
+    total = sum(times)
+    value = n * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "decisions/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_desc(cfg) + f"; each step a sample of {n_seq} sequences"},
+            "cpu_baseline": {"value": value, "unit": "decisions/s", "cores": oracle.get_threads(), "kind": "oracle",
+                             "sample": f"{n_seq} of {cfg.batch} sequences per step"},
+            "e2e": {"value": value, "unit": "decisions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl" if args.impl == "native" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    import torch
+    r = run_native(args, rank, world, local)
+    cfg = r["cfg"]
+    total_ms = r["total_ms"]
+    if world > 1:
+        t = torch.tensor([total_ms], device=f"cuda:{local}")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if rank != 0:
+        return
+    decisions = cfg.batch * cfg.blk * world * args.steps
+    value = decisions / (total_ms / 1000.0)
+    ms_step = total_ms / args.steps
+    k1_ms = statistics.mean(r["k1"])
+    k1_bytes = 2 * cfg.batch * cfg.blk * cfg.vocab * 2  # cur + prev bf16 rows
+    k1_gbs = k1_bytes / (k1_ms / 1000.0) / 1e9
+    peak, peak_kind = load_peaks()
+    line = {
+        "metric": METRIC, "value": value, "unit": "decisions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "batch_per_gpu": cfg.batch, "masked_per_seq": cfg.blk,
+                   "vocab": cfg.vocab, "logits": "bf16", "attention": "f16",
+                   "l2": "no flush: 1.25 GB of logit rows per step, larger than L2", "parallelism": f"dp{world}"},
+        "logit_gbps": k1_gbs,
+        "kernels_ms": {"row_stats": k1_ms, "four_rules": r["rules_ms"]},
+        "host_enqueue_ms_per_step": r["host_ms"],
+        "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
+                     "traffic": None, "kernel": "row_stats", "peak_kind": peak_kind,
+                     "algorithmic_bytes": k1_bytes},
+        "gpu_launches": r["launches"],
+    }
+    if r["clocks"]:
+        line["clocks"] = r["clocks"]
+    if r["e2e"]:
+        e = r["e2e"]
+        line["e2e"] = {"value": cfg.batch * cfg.blk * world / (e["ms_per_step"] / 1000.0), "unit": "decisions/s",
+                       "h2d_bytes_per_step": e["h2d_bytes_per_step"], "d2h_bytes_per_step": e["d2h_bytes_per_step"],
+                       "ms_per_step": e["ms_per_step"]}
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(r["w"])
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

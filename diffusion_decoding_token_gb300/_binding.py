@@ -1,0 +1,350 @@
+"""ctypes binding of libdlm.so (argument marshalling only).
+
+Every function takes CUDA tensors, checks their dtype/shape/device, passes raw
+pointers and the current CUDA stream to the C ABI declared in
+``include/dlm.h``, and raises on a non-OK status.  Nothing here computes a
+decision; there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdlm.so")
+
+DLM_F32, DLM_BF16, DLM_F16 = 0, 1, 2
+DEV_NONFINITE, DEV_POOL_CLIPPED = 1, 2
+MAX_BLK = 256
+
+_DT = {torch.float32: DLM_F32, torch.bfloat16: DLM_BF16, torch.float16: DLM_F16}
+
+_lib = None
+
+
+class DepcapParams(ctypes.Structure):
+    _fields_ = [("lambda_", ctypes.c_float), ("L_min", ctypes.c_int32),
+                ("smooth_w", ctypes.c_int32), ("norm_mode", ctypes.c_int32)]
+
+
+class CapParams(ctypes.Structure):
+    _fields_ = [("tau_low", ctypes.c_float), ("tau_high", ctypes.c_float), ("gamma", ctypes.c_float),
+                ("p_max", ctypes.c_int32), ("high_tier_unconditional", ctypes.c_int32)]
+
+
+class DapdParams(ctypes.Structure):
+    _fields_ = [("tau_edge", ctypes.c_float), ("bulk_conf", ctypes.c_float),
+                ("bulk_frac", ctypes.c_float), ("order_mode", ctypes.c_int32)]
+
+
+class DlmError(RuntimeError):
+    pass
+
+
+def lib():
+    """Load libdlm.so; raise if it has not been built (there is no fallback)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, F, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        L.dlm_status_string.restype = ctypes.c_char_p
+        L.dlm_status_string.argtypes = [ctypes.c_int]
+        L.dlm_version.restype = ctypes.c_int
+        L.dlm_row_stats.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, P, P, P, P, P, P, P, P]
+        L.dlm_select_threshold.argtypes = [P, P, I32, I32, F, P, P, P]
+        L.dlm_depcap_boundary.argtypes = [P, P, I32, I32, P, ctypes.POINTER(DepcapParams), P, P, P]
+        L.dlm_cap_workspace_size.restype = Z
+        L.dlm_cap_workspace_size.argtypes = [I32, I32]
+        L.dlm_cap_select.argtypes = [P, ctypes.c_int, I64, I64, P, P, P, P, P, I32, I32,
+                                     ctypes.POINTER(CapParams), P, P, P, P, Z, P, P]
+        L.dlm_dapd_workspace_size.restype = Z
+        L.dlm_dapd_workspace_size.argtypes = [I32, I32]
+        L.dlm_dapd_graph_mis.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
+                                         P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
+        for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
+                  "dlm_dapd_graph_mis"):
+            getattr(L, f).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise DlmError(f"libdlm: {lib().dlm_status_string(status).decode()} (status {status})")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libdlm takes CUDA tensors only")
+
+
+def _dt(t: torch.Tensor) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {t.dtype}") from None
+
+
+def _u8(m: torch.Tensor) -> torch.Tensor:
+    m = m if m.dtype == torch.uint8 else m.to(torch.uint8)
+    return m.contiguous()
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word (uint32 semantics in an int32 tensor)."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+class RowStats(NamedTuple):
+    argmax: torch.Tensor
+    conf: torch.Tensor
+    lse: torch.Tensor
+    entropy: torch.Tensor
+    kl: torch.Tensor | None
+    lse_prev: torch.Tensor | None
+
+
+def alloc_row_stats(n: int, device, with_prev: bool = True) -> RowStats:
+    f = dict(dtype=torch.float32, device=device)
+    return RowStats(torch.empty(n, dtype=torch.int32, device=device), torch.empty(n, **f),
+                    torch.empty(n, **f), torch.empty(n, **f),
+                    torch.empty(n, **f) if with_prev else None, torch.empty(n, **f) if with_prev else None)
+
+
+def row_stats(cur: torch.Tensor, prev: torch.Tensor | None = None, *, row_index: torch.Tensor | None = None,
+              out: RowStats | None = None, status: torch.Tensor | None = None) -> RowStats:
+    """dlm_row_stats over the rows of ``cur`` ([rows, V] with unit column stride)."""
+    _need_cuda(cur, prev, row_index)
+    if cur.dim() != 2 or cur.stride(1) != 1:
+        raise ValueError("cur must be [rows, V] with contiguous rows")
+    if prev is not None and (prev.shape != cur.shape or prev.stride() != cur.stride() or prev.dtype != cur.dtype):
+        raise ValueError("prev must match cur in shape, strides and dtype")
+    rows, V = cur.shape
+    if out is None:
+        out = alloc_row_stats(rows, cur.device, prev is not None)
+    n = rows
+    if row_index is not None:
+        row_index = row_index.to(torch.int32).contiguous()
+        n = row_index.numel()
+    _check(lib().dlm_row_stats(_p(cur), _p(prev), _dt(cur), n, V, cur.stride(0), _p(row_index),
+                               _p(out.argmax), _p(out.conf), _p(out.lse), _p(out.entropy),
+                               _p(out.kl) if prev is not None else None,
+                               _p(out.lse_prev) if prev is not None else None, _p(status),
+                               _stream(cur.device)))
+    return out
+
+
+def select_threshold(conf: torch.Tensor, masked: torch.Tensor, tau: float = 0.9, *, selected=None,
+                     n_selected=None):
+    """dlm_select_threshold: conf/masked are [B, blk]; returns (selected u8, n_selected i32)."""
+    _need_cuda(conf, masked)
+    B, blk = masked.shape
+    conf = conf.reshape(B, blk).contiguous()
+    masked = _u8(masked)
+    if selected is None:
+        selected = torch.empty((B, blk), dtype=torch.uint8, device=conf.device)
+    if n_selected is None:
+        n_selected = torch.empty(B, dtype=torch.int32, device=conf.device)
+    _check(lib().dlm_select_threshold(_p(conf), _p(masked), B, blk, float(tau), _p(selected), _p(n_selected),
+                                      _stream(conf.device)))
+    return selected, n_selected
+
+
+def depcap_boundary(kl: torch.Tensor, entropy: torch.Tensor, lam: float = 1.0, L_min: int = 8,
+                    smooth_w: int = 1, norm_mode: int = 0, cold_start: torch.Tensor | None = None, *,
+                    block_len=None, score=None):
+    """dlm_depcap_boundary over [B, L_window] KL / entropy; returns (block_len, score)."""
+    _need_cuda(kl, entropy, cold_start)
+    B, Lw = kl.shape
+    kl = kl.contiguous()
+    entropy = entropy.reshape(B, Lw).contiguous()
+    if cold_start is not None:
+        cold_start = _u8(cold_start)
+    if block_len is None:
+        block_len = torch.empty(B, dtype=torch.int32, device=kl.device)
+    if score is None:
+        score = torch.empty((B, Lw), dtype=torch.float32, device=kl.device)
+    prm = DepcapParams(float(lam), int(L_min), int(smooth_w), int(norm_mode))
+    _check(lib().dlm_depcap_boundary(_p(kl), _p(entropy), B, Lw, _p(cold_start), ctypes.byref(prm),
+                                     _p(block_len), _p(score), _stream(kl.device)))
+    return block_len, score
+
+
+def cap_workspace(batch: int, p_max: int, device) -> torch.Tensor:
+    n = lib().dlm_cap_workspace_size(batch, p_max)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def cap_select(logits: torch.Tensor, argmax: torch.Tensor, conf: torch.Tensor, lse: torch.Tensor,
+               masked: torch.Tensor, tau_low: float = 0.8, tau_high: float = 0.95, gamma: float = -16.0,
+               p_max: int | None = None, high_tier_unconditional: bool = False,
+               scope_len: torch.Tensor | None = None, *, D_out=None, workspace=None, status=None,
+               selected=None, n_selected=None):
+    """dlm_cap_select; logits are the [B*blk, V] current rows.  Returns (selected, n_selected)."""
+    _need_cuda(logits, argmax, conf, lse, masked, scope_len, D_out)
+    B, blk = masked.shape
+    if logits.dim() != 2 or logits.stride(1) != 1 or logits.shape[0] < B * blk:
+        raise ValueError("logits must be [B*blk, V] with contiguous rows")
+    p_max = blk if p_max is None else int(p_max)
+    masked = _u8(masked)
+    dev = logits.device
+    if workspace is None:
+        workspace = cap_workspace(B, p_max, dev)
+    if selected is None:
+        selected = torch.empty((B, blk), dtype=torch.uint8, device=dev)
+    if n_selected is None:
+        n_selected = torch.empty(B, dtype=torch.int32, device=dev)
+    if scope_len is not None:
+        scope_len = scope_len.to(torch.int32).contiguous()
+    prm = CapParams(float(tau_low), float(tau_high), float(gamma), p_max, int(bool(high_tier_unconditional)))
+    _check(lib().dlm_cap_select(_p(logits), _dt(logits), logits.shape[1], logits.stride(0),
+                                _p(argmax.contiguous()), _p(conf.contiguous()), _p(lse.contiguous()), _p(masked),
+                                _p(scope_len), B, blk, ctypes.byref(prm), _p(selected), _p(n_selected), _p(D_out),
+                                _p(workspace), workspace.numel(), _p(status), _stream(dev)))
+    return selected, n_selected
+
+
+def dapd_workspace(batch: int, blk: int, device) -> torch.Tensor:
+    n = lib().dlm_dapd_workspace_size(batch, blk)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device)
+
+
+def dapd_graph_mis(attn: torch.Tensor, masked: torch.Tensor, conf: torch.Tensor, tau_edge: float = 0.01,
+                   bulk_conf: float = 0.9, bulk_frac: float = 0.5, order_mode: int = 0, block_start: int = 0, *,
+                   s_out=None, dtilde_out=None, deg_out=None, workspace=None, status=None, selected=None,
+                   n_selected=None):
+    """dlm_dapd_graph_mis on ``attn`` = [B, L, H, N, N] (any element strides with unit
+    column stride).  The block is rows/cols [block_start, block_start+blk)."""
+    _need_cuda(attn, masked, conf, s_out, dtilde_out, deg_out)
+    if attn.dim() != 5 or attn.stride(4) != 1:
+        raise ValueError("attn must be [B, L, H, N, N] with unit column stride")
+    B, L, H = attn.shape[:3]
+    blk = masked.shape[1]
+    if masked.shape[0] != B or block_start + blk > min(attn.shape[3], attn.shape[4]):
+        raise ValueError("block outside the attention maps")
+    masked = _u8(masked)
+    dev = attn.device
+    if workspace is None:
+        workspace = dapd_workspace(B, blk, dev)
+    if selected is None:
+        selected = torch.empty((B, blk), dtype=torch.uint8, device=dev)
+    if n_selected is None:
+        n_selected = torch.empty(B, dtype=torch.int32, device=dev)
+    sb, sl, sh, sr, _ = attn.stride()
+    prm = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
+    _check(lib().dlm_dapd_graph_mis(_p(attn), _dt(attn), B, L, H, sb, sl, sh, sr, int(block_start), blk,
+                                    _p(masked), _p(conf.reshape(B, blk).contiguous()), ctypes.byref(prm),
+                                    _p(selected), _p(n_selected), _p(s_out), _p(dtilde_out), _p(deg_out),
+                                    _p(workspace), workspace.numel(), _p(status), _stream(dev)))
+    return selected, n_selected
+
+
+class StepPlan:
+    """One decode step's five C-ABI calls with every argument marshalled once.
+
+    Built from preallocated CUDA tensors; :meth:`run` only issues the calls
+    (row statistics, then the four rules) on the current stream, so the host
+    cost per step is a handful of ctypes calls.  Any rule can be left out.
+    The tensors must stay alive and keep their storage while the plan is used.
+    """
+
+    def __init__(self, cur, prev, masked, *, tau=0.9, lam=1.0, L_min=8, smooth_w=1, norm_mode=0,
+                 tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=None, high_tier_unconditional=False,
+                 cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
+                 bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None):
+        _need_cuda(cur, prev, masked, attn)
+        L = lib()
+        dev = cur.device
+        B, blk = masked.shape
+        if cur.dim() != 2 or cur.stride(1) != 1 or cur.shape[0] != B * blk:
+            raise ValueError("cur must be [B*blk, V] with contiguous rows")
+        self.B, self.blk, self.dev = B, blk, dev
+        self.masked = _u8(masked)
+        self.status = status if status is not None else new_status(dev)
+        self.stats = alloc_row_stats(B * blk, dev, prev is not None)
+        self.rules = tuple(rules)
+        self.keep = [cur, prev, attn, self.masked]
+        st = self.stats
+        self._calls = []
+        self._calls.append((L.dlm_row_stats, (_p(cur), _p(prev), _dt(cur), B * blk, cur.shape[1], cur.stride(0), None,
+                                               _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
+                                               _p(st.lse_prev), _p(self.status))))
+        u8 = dict(dtype=torch.uint8, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.out = {}
+        if "threshold" in rules:
+            s, n = torch.zeros((B, blk), **u8), torch.zeros(B, **i32)
+            self.out["threshold"] = (s, n)
+            self._calls.append((L.dlm_select_threshold, (_p(st.conf), _p(self.masked), B, blk, ctypes.c_float(tau),
+                                                          _p(s), _p(n))))
+        self.block_len = None
+        if "boundary" in rules:
+            if prev is None:
+                raise ValueError("the boundary rule needs the previous step's logits")
+            self.block_len = torch.zeros(B, **i32)
+            self.score = torch.zeros((B, blk), dtype=torch.float32, device=dev)
+            self._dep = DepcapParams(float(lam), int(L_min), int(smooth_w), int(norm_mode))
+            self._calls.append((L.dlm_depcap_boundary, (_p(st.kl), _p(st.entropy), B, blk, None,
+                                                         ctypes.byref(self._dep), _p(self.block_len),
+                                                         _p(self.score))))
+        if "cap" in rules:
+            p_max = blk if p_max is None else int(p_max)
+            s, n = torch.zeros((B, blk), **u8), torch.zeros(B, **i32)
+            self.out["cap"] = (s, n)
+            self.cap_ws = cap_workspace(B, p_max, dev)
+            self._cap = CapParams(float(tau_low), float(tau_high), float(gamma), p_max,
+                                  int(bool(high_tier_unconditional)))
+            scope = self.block_len if cap_scope_from_boundary else None
+            self._calls.append((L.dlm_cap_select, (_p(cur), _dt(cur), cur.shape[1], cur.stride(0), _p(st.argmax),
+                                                    _p(st.conf), _p(st.lse), _p(self.masked), _p(scope), B, blk,
+                                                    ctypes.byref(self._cap), _p(s), _p(n), None, _p(self.cap_ws),
+                                                    self.cap_ws.numel(), _p(self.status))))
+        if "dapd" in rules:
+            if attn is None or attn.dim() != 5 or attn.stride(4) != 1:
+                raise ValueError("the DAPD rule needs attn [B, L, H, N, N] with unit column stride")
+            s, n = torch.zeros((B, blk), **u8), torch.zeros(B, **i32)
+            self.out["dapd"] = (s, n)
+            self.dapd_ws = dapd_workspace(B, blk, dev)
+            self._dapd = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
+            sb, sl, sh, sr, _ = attn.stride()
+            self._calls.append((L.dlm_dapd_graph_mis, (_p(attn), _dt(attn), B, attn.shape[1], attn.shape[2], sb, sl,
+                                                        sh, sr, int(block_start), blk, _p(self.masked), _p(st.conf),
+                                                        ctypes.byref(self._dapd), _p(s), _p(n), None, None, None,
+                                                        _p(self.dapd_ws), self.dapd_ws.numel(), _p(self.status))))
+
+    @property
+    def n_launches(self) -> int:
+        """Kernels launched per step: 1 row pass + 1 threshold + 1 boundary + 3 CAP + 3 DAPD."""
+        per = {"threshold": 1, "boundary": 1, "cap": 3, "dapd": 3}
+        return 1 + sum(per[r] for r in self.rules)
+
+    def run(self, stream=None, events=None, rules_only=False):
+        """Issue the step on ``stream`` (default: the current stream).  With
+        ``events`` = (e0, e1), e0/e1 are recorded around the row pass.
+        ``rules_only`` re-runs the four rules on the statistics already in
+        the plan's buffers (for timing them apart)."""
+        st = stream or torch.cuda.current_stream(self.dev)
+        s = ctypes.c_void_p(st.cuda_stream)
+        for k, (fn, args) in enumerate(self._calls):
+            if rules_only and k == 0:
+                continue
+            if events is not None and k == 0:
+                events[0].record(st)
+            _check(fn(*args, s))
+            if events is not None and k == 0:
+                events[1].record(st)

@@ -1,0 +1,226 @@
+// api.cu -- the exported C ABI of libdlm: argument checks, then launches.
+//
+// Every check runs on the host before anything is enqueued, so a rejected
+// call leaves the stream untouched.  Device attributes (SM count) are read
+// once per device and cached.
+#include <math.h>
+#include <stdint.h>
+
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
+    if (dev >= kMaxDevices) dev = kMaxDevices - 1;
+    if (g_sm_count[dev] <= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int dtype_size(int dt) { return dt == DLM_F32 ? 4 : 2; }
+
+inline bool dtype_ok(int dt) { return dt == DLM_F32 || dt == DLM_BF16 || dt == DLM_F16; }
+
+inline dlm_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DLM_OK : DLM_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* dlm_status_string(dlm_status s) {
+    switch (s) {
+    case DLM_OK: return "ok";
+    case DLM_ERR_INVALID_ARG: return "invalid argument";
+    case DLM_ERR_ALIGNMENT: return "misaligned pointer or stride";
+    case DLM_ERR_UNSUPPORTED: return "unsupported dtype";
+    case DLM_ERR_WORKSPACE: return "workspace missing or too small";
+    case DLM_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+    }
+}
+
+int dlm_version(void) { return 100; }
+
+dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
+                         int64_t vocab, int64_t row_stride, const int32_t* row_index,
+                         int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
+                         float* lse_prev, uint32_t* dev_status, dlm_stream_t stream) {
+    if (!dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
+    if (n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL || row_stride < vocab) return DLM_ERR_INVALID_ARG;
+    if (n_rows == 0) return DLM_OK;
+    if (!cur || !argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    const int esz = dtype_size(dtype);
+    if (!aligned16(cur) || (prev && !aligned16(prev)) || (row_stride * esz) % 16 != 0) return DLM_ERR_ALIGNMENT;
+    const int epv = dlm::row_stats_elems_per_vector(dtype);
+    const int64_t nvec = vocab / epv;
+    const int threads = dlm::row_stats_threads();
+    // split a row over a cluster of CTAs only when the rows alone cannot fill
+    // the GPU and each CTA still gets at least two vectors per thread
+    const int64_t target = 2LL * sm_count();
+    int split = 1;
+    while (split < 8 && n_rows * split < target && nvec / (split * 2) >= 2LL * threads) split *= 2;
+    if (n_rows * split > 0x7fffffffLL) return DLM_ERR_INVALID_ARG;
+    dlm::RowStatsArgs a;
+    a.cur = cur;
+    a.prev = prev;
+    a.n_rows = n_rows;
+    a.vocab = vocab;
+    a.row_stride = row_stride;
+    a.row_index = row_index;
+    a.argmax = argmax;
+    a.conf = conf;
+    a.lse = lse;
+    a.entropy = entropy;
+    a.kl = kl;
+    a.lse_prev = lse_prev;
+    a.dev_status = dev_status;
+    a.split = split;
+    return from_cuda(dlm::launch_row_stats(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_select_threshold(const float* conf, const uint8_t* masked, int32_t batch,
+                                int32_t blk, float tau, uint8_t* selected, int32_t* n_selected,
+                                dlm_stream_t stream) {
+    if (batch < 0 || blk < 1 || blk > DLM_MAX_BLK) return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!conf || !masked || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
+    dlm::ThresholdArgs a{conf, masked, batch, blk, tau, selected, n_selected};
+    return from_cuda(dlm::launch_threshold(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_depcap_boundary(const float* kl, const float* entropy, int32_t batch,
+                               int32_t L_window, const uint8_t* cold_start,
+                               const dlm_depcap_params* params, int32_t* block_len,
+                               float* score, dlm_stream_t stream) {
+    if (!params || batch < 0 || L_window < 1 || L_window > 1024) return DLM_ERR_INVALID_ARG;
+    if (params->L_min < 1 || params->smooth_w < 1 || params->smooth_w > 63 || (params->smooth_w % 2) == 0 ||
+        params->norm_mode < 0 || params->norm_mode > 2 || !isfinite(params->lambda))
+        return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!kl || !entropy || !block_len) return DLM_ERR_INVALID_ARG;
+    dlm::BoundaryArgs a{kl, entropy, batch, L_window, cold_start, params->lambda,
+                        params->L_min, params->smooth_w, params->norm_mode, block_len, score};
+    return from_cuda(dlm::launch_boundary(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t dlm_cap_workspace_size(int32_t batch, int32_t p_max) {
+    if (batch < 0 || p_max < 1 || p_max > DLM_MAX_BLK) return 0;
+    return dlm::cap_workspace_bytes(batch, p_max);
+}
+
+dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
+                          const int32_t* argmax, const float* conf, const float* lse,
+                          const uint8_t* masked, const int32_t* scope_len, int32_t batch,
+                          int32_t blk, const dlm_cap_params* params, uint8_t* selected,
+                          int32_t* n_selected, float* D_out, void* workspace, size_t ws_bytes,
+                          uint32_t* dev_status, dlm_stream_t stream) {
+    if (!dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
+    if (!params || batch < 0 || blk < 1 || blk > DLM_MAX_BLK || vocab < 1 || row_stride < vocab ||
+        params->p_max < 1 || params->p_max > DLM_MAX_BLK ||
+        (params->high_tier_unconditional != 0 && params->high_tier_unconditional != 1))
+        return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!logits || !argmax || !conf || !lse || !masked || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < dlm::cap_workspace_bytes(batch, params->p_max)) return DLM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DLM_ERR_ALIGNMENT;
+    dlm::CapArgs a{};
+    a.logits = logits;
+    a.dtype = dtype;
+    a.row_stride = row_stride;
+    a.argmax = argmax;
+    a.conf = conf;
+    a.lse = lse;
+    a.masked = masked;
+    a.scope_len = scope_len;
+    a.batch = batch;
+    a.blk = blk;
+    a.tau_low = params->tau_low;
+    a.tau_high = params->tau_high;
+    a.gamma = params->gamma;
+    a.p_max = params->p_max;
+    a.high_tier_unconditional = params->high_tier_unconditional;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.D_out = D_out;
+    a.dev_status = dev_status;
+    dlm::cap_carve(a, workspace);
+    return from_cuda(dlm::launch_cap(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t dlm_dapd_workspace_size(int32_t batch, int32_t blk) {
+    if (batch < 0 || blk < 1 || blk > DLM_MAX_BLK) return 0;
+    return dlm::dapd_workspace_bytes(batch, blk);
+}
+
+dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
+                              int32_t n_heads, int64_t stride_b, int64_t stride_l,
+                              int64_t stride_h, int64_t stride_row, int32_t block_start,
+                              int32_t blk, const uint8_t* masked, const float* conf,
+                              const dlm_dapd_params* params, uint8_t* selected,
+                              int32_t* n_selected, float* s_out, float* dtilde_out,
+                              int32_t* deg_out, void* workspace, size_t ws_bytes,
+                              uint32_t* dev_status, dlm_stream_t stream) {
+    if (!dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
+    if (!params || batch < 0 || n_layers < 1 || n_heads < 1 || (int64_t)n_layers * n_heads > (1 << 20) ||
+        blk < 1 || blk > DLM_MAX_BLK || block_start < 0 || stride_b < 0 || stride_l < 0 || stride_h < 0 ||
+        stride_row < blk || (params->order_mode != 0 && params->order_mode != 1) || !isfinite(params->tau_edge))
+        return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!attn || !masked || !conf || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < dlm::dapd_workspace_bytes(batch, blk)) return DLM_ERR_WORKSPACE;
+    const int esz = dtype_size(dtype);
+    const char* first = static_cast<const char*>(attn) + ((int64_t)block_start * stride_row + block_start) * esz;
+    if (!aligned16(first) || !aligned16(workspace) || (stride_b * esz) % 16 || (stride_l * esz) % 16 ||
+        (stride_h * esz) % 16 || (stride_row * esz) % 16)
+        return DLM_ERR_ALIGNMENT;
+    const double LH = (double)n_layers * (double)n_heads;
+    const double unit = 2.0 * LH * 4294967296.0;   // 2 L H 2^32: s = I / unit
+    double t = floor((double)params->tau_edge * unit);  // exact: tau is fp32, unit < 2^53
+    long long thr;
+    if (t >= 9.2e18)
+        thr = 0x7fffffffffffffffLL;
+    else if (t <= -9.2e18)
+        thr = -0x7fffffffffffffffLL - 1;
+    else
+        thr = (long long)t;
+    dlm::DapdArgs a{};
+    a.attn = attn;
+    a.dtype = dtype;
+    a.batch = batch;
+    a.n_layers = n_layers;
+    a.n_heads = n_heads;
+    a.sb = stride_b;
+    a.sl = stride_l;
+    a.sh = stride_h;
+    a.sr = stride_row;
+    a.block_start = block_start;
+    a.blk = blk;
+    a.masked = masked;
+    a.conf = conf;
+    a.tau_edge = params->tau_edge;
+    a.bulk_conf = params->bulk_conf;
+    a.bulk_frac = params->bulk_frac;
+    a.order_mode = params->order_mode;
+    a.edge_thresh = thr;
+    a.s_scale = (float)(1.0 / unit);
+    a.selected = selected;
+    a.n_selected = n_selected;
+    a.s_out = s_out;
+    a.dtilde_out = dtilde_out;
+    a.deg_out = deg_out;
+    a.dev_status = dev_status;
+    dlm::dapd_carve(a, workspace);
+    return from_cuda(dlm::launch_dapd(a, sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

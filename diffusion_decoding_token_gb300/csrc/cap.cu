@@ -1,0 +1,197 @@
+// cap.cu -- DepCap CAP-Decoding: confidence pool, pairwise conflict score,
+// greedy conflict-free selection (DepCap, "Methodology"; defaults in
+// "Experiments").
+//
+// Three launches on the caller's stream:
+//   cap_pool     one CTA per sequence: candidates (masked, conf >= tau_low)
+//                ranked by (conf desc, position asc) with an all-pairs rank
+//                count, clipped to p_max;
+//   cap_conflict one warp per pool row: D_ij = log p_i(yhat_j) + log p_j(yhat_i)
+//                from two scattered logit reads per pair, conflict bits packed
+//                with a warp ballot (one 32-bit word per 32 partners);
+//   cap_greedy   one CTA per sequence: the greedy scan over the pool order on
+//                the shared-memory bitmask, or the top-confidence fallback.
+// The pool order and the two bitmask passes live in the caller's workspace.
+#include "common.cuh"
+#include "launch.h"
+
+namespace dlm {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kConflictWarps = 8;
+
+__device__ __forceinline__ float load_logit(const void* base, int dtype, int64_t i) {
+    if (dtype == DLM_BF16) return __uint_as_float((uint32_t) static_cast<const uint16_t*>(base)[i] << 16);
+    if (dtype == DLM_F16) return __half2float(static_cast<const __half*>(base)[i]);
+    return static_cast<const float*>(base)[i];
+}
+
+__device__ __forceinline__ int scope_of(const CapArgs& a, int b) {
+    int sc = a.blk;
+    if (a.scope_len) sc = min(sc, max(0, a.scope_len[b]));
+    return sc;
+}
+
+__global__ void __launch_bounds__(kThreads) cap_pool_kernel(CapArgs a) {
+    __shared__ float s_c[kThreads];
+    __shared__ int s_cand[kThreads];
+    const int b = blockIdx.x, i = threadIdx.x;
+    const int scope = scope_of(a, b);
+    const int64_t o = (int64_t)b * a.blk + i;
+    const bool cand = i < scope && a.masked[o] != 0 && a.conf[o] >= a.tau_low;
+    s_c[i] = cand ? a.conf[o] : 0.f;
+    s_cand[i] = cand;
+    const int n = __syncthreads_count(cand);
+    if (cand) {
+        const float c = s_c[i];
+        int rank = 0;
+        for (int j = 0; j < scope; ++j) {
+            if (!s_cand[j]) continue;
+            const float cj = s_c[j];
+            rank += (cj > c) || (cj == c && j < i);
+        }
+        if (rank < a.p_max) a.pool[(int64_t)b * a.p_max + rank] = i;
+    }
+    if (i == 0) {
+        a.pool_n[b] = min(n, a.p_max);
+        if (n > a.p_max) raise_status(a.dev_status, DLM_DEV_POOL_CLIPPED);
+    }
+}
+
+__global__ void __launch_bounds__(kConflictWarps * 32) cap_conflict_kernel(CapArgs a) {
+    const int b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = blockIdx.x * kConflictWarps + warp;
+    const int n = a.pool_n[b];
+    if (slot >= n) return;
+    const int32_t* pool = a.pool + (int64_t)b * a.p_max;
+    const int pi = pool[slot];
+    const int64_t ri = (int64_t)b * a.blk + pi;
+    const int yi = a.argmax[ri];
+    const float li = a.lse[ri];
+    uint32_t* adj = a.adj + ((int64_t)b * a.p_max + slot) * a.words;
+    const int nw = (n + 31) >> 5;
+    for (int c = 0; c < nw; ++c) {
+        const int e = c * 32 + lane;
+        bool conflict = false;
+        if (e < n && e != slot) {
+            const int pj = pool[e];
+            const int64_t rj = (int64_t)b * a.blk + pj;
+            const float g1 = load_logit(a.logits, a.dtype, ri * a.row_stride + a.argmax[rj]) - li;
+            const float g2 = load_logit(a.logits, a.dtype, rj * a.row_stride + yi) - a.lse[rj];
+            const float d = g1 + g2;
+            conflict = d > a.gamma;
+            if (a.D_out) a.D_out[((int64_t)b * a.blk + pi) * a.blk + pj] = d;
+        }
+        const uint32_t word = __ballot_sync(DLM_FULL_MASK, conflict);
+        if (lane == 0) adj[c] = word;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) cap_greedy_kernel(CapArgs a) {
+    __shared__ uint32_t s_adj[DLM_MAX_BLK * (DLM_MAX_BLK / 32)];
+    __shared__ uint32_t s_kept[DLM_MAX_BLK / 32];
+    __shared__ unsigned char s_tier[DLM_MAX_BLK];
+    __shared__ float s_v[kThreads / 32];
+    __shared__ int s_i[kThreads / 32];
+    const int b = blockIdx.x, t = threadIdx.x;
+    const int n = a.pool_n[b];
+    const int scope = scope_of(a, b);
+    uint8_t* sel = a.selected + (int64_t)b * a.blk;
+    const int32_t* pool = a.pool + (int64_t)b * a.p_max;
+    if (t < a.blk) sel[t] = 0;
+    if (n == 0) {
+        // no candidate: the highest-confidence masked position of the scope
+        const int64_t o = (int64_t)b * a.blk + t;
+        const bool m = t < scope && a.masked[o] != 0;
+        float v = m ? a.conf[o] : -INFINITY;
+        int idx = m ? t : 0x7fffffff;
+        const int any_m = __syncthreads_or(m);
+        warp_argmax(v, idx);
+        if ((t & 31) == 0) {
+            s_v[t >> 5] = v;
+            s_i[t >> 5] = idx;
+        }
+        __syncthreads();
+        if (t < 32) {
+            v = t < kThreads / 32 ? s_v[t] : -INFINITY;
+            idx = t < kThreads / 32 ? s_i[t] : 0x7fffffff;
+            warp_argmax(v, idx);
+            if (t == 0) {
+                if (any_m) sel[idx] = 1;
+                a.n_selected[b] = any_m ? 1 : 0;
+            }
+        }
+        return;
+    }
+    const int W = (n + 31) >> 5;
+    for (int k = t; k < n * W; k += blockDim.x) {
+        const int s = k / W, w = k - s * W;
+        s_adj[s * W + w] = a.adj[((int64_t)b * a.p_max + s) * a.words + w];
+    }
+    if (t < n) s_tier[t] = a.high_tier_unconditional && a.conf[(int64_t)b * a.blk + pool[t]] >= a.tau_high;
+    __syncthreads();
+    if (t < 32) {
+        uint32_t kept = 0;  // lane w holds word w of the kept set
+        if (a.high_tier_unconditional) {
+            for (int j = 0; j < 32; ++j) {
+                const int s = t * 32 + j;
+                if (t < W && s < n && s_tier[s]) kept |= 1u << j;
+            }
+        }
+        for (int s = 0; s < n; ++s) {
+            if (s_tier[s]) continue;  // already kept (unconditional tier)
+            const uint32_t hit = t < W ? (s_adj[s * W + t] & kept) : 0u;
+            if (!__any_sync(DLM_FULL_MASK, hit != 0u) && t == (s >> 5)) kept |= 1u << (s & 31);
+        }
+        if (t < W) s_kept[t] = kept;
+    }
+    __syncthreads();
+    int mine = 0;
+    if (t < n && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
+        sel[pool[t]] = 1;
+        mine = 1;
+    }
+    const int total = __syncthreads_count(mine);
+    if (t == 0) a.n_selected[b] = total;
+}
+
+}  // namespace
+
+size_t cap_workspace_bytes(int batch, int p_max) {
+    const size_t words = (size_t)((p_max + 31) / 32);
+    size_t pool = ((size_t)batch * p_max * 4 + 255) & ~(size_t)255;
+    size_t pn = ((size_t)batch * 4 + 255) & ~(size_t)255;
+    size_t adj = (size_t)batch * p_max * words * 4;
+    return pool + pn + adj;
+}
+
+void cap_carve(CapArgs& a, void* ws) {
+    char* p = static_cast<char*>(ws);
+    a.words = (a.p_max + 31) / 32;
+    a.pool = reinterpret_cast<int32_t*>(p);
+    p += ((size_t)a.batch * a.p_max * 4 + 255) & ~(size_t)255;
+    a.pool_n = reinterpret_cast<int32_t*>(p);
+    p += ((size_t)a.batch * 4 + 255) & ~(size_t)255;
+    a.adj = reinterpret_cast<uint32_t*>(p);
+}
+
+cudaError_t launch_cap(const CapArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.gridDim = dim3((unsigned)a.batch);
+    cfg.blockDim = dim3(kThreads);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, cap_pool_kernel, a);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)((a.p_max + kConflictWarps - 1) / kConflictWarps), (unsigned)a.batch);
+    cfg.blockDim = dim3(kConflictWarps * 32);
+    e = cudaLaunchKernelEx(&cfg, cap_conflict_kernel, a);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)a.batch);
+    cfg.blockDim = dim3(kThreads);
+    return cudaLaunchKernelEx(&cfg, cap_greedy_kernel, a);
+}
+
+}  // namespace dlm

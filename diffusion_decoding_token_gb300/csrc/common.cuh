@@ -1,0 +1,120 @@
+// common.cuh -- device helpers shared by the libdlm kernels (sm_103a only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "dlm.h"
+
+#define DLM_FULL_MASK 0xffffffffu
+
+namespace dlm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// 2^x on the SFU (PTX ex2.approx, flush-to-zero): relative error ~2^-22.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// NaN-propagating max (PTX max.NaN).
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// ---- packed fp32x2 arithmetic (sm_100+ f32x2 forms) --------------------
+struct f2 {
+    uint64_t v;
+};
+
+__device__ __forceinline__ f2 pack2(float a, float b) {
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void unpack2(f2 r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r.v));
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    f2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+    f2 d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+    f2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d.v) : "l"(a.v), "l"(b.v));
+    return d;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+    f2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return d;
+}
+__device__ __forceinline__ f2 ex2x2(f2 a) {
+    float x, y;
+    unpack2(a, x, y);
+    return pack2(ex2(x), ex2(y));
+}
+__device__ __forceinline__ float hsum2(f2 a) {
+    float x, y;
+    unpack2(a, x, y);
+    return x + y;
+}
+
+// ---- 16-bit storage -> fp32 (exact widening) ----------------------------
+// bf16 pair in one 32-bit word: element 0 in the low half.
+__device__ __forceinline__ f2 bf16x2_to_f2(uint32_t w) {
+    return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ f2 f16x2_to_f2(uint32_t w) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    float2 f = __half22float2(h);
+    return pack2(f.x, f.y);
+}
+
+// ---- reductions -----------------------------------------------------------
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(DLM_FULL_MASK, v, o);
+    return v;
+}
+__device__ __forceinline__ long long warp_sum_ll(long long v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(DLM_FULL_MASK, v, o);
+    return v;
+}
+
+// (value, index) arg-max with ties to the lower index; NaN never wins.
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
+    bool take = (v2 > v) || (v2 == v && i2 < i) || (v != v && v2 == v2);
+    if (take) {
+        v = v2;
+        i = i2;
+    }
+}
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        float v2 = __shfl_xor_sync(DLM_FULL_MASK, v, o);
+        int i2 = __shfl_xor_sync(DLM_FULL_MASK, i, o);
+        argmax_merge(v, i, v2, i2);
+    }
+}
+
+__device__ __forceinline__ void raise_status(uint32_t* st, uint32_t bits) {
+    if (st) atomicOr(st, bits);
+}
+
+}  // namespace dlm

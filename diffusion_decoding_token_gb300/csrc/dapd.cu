@@ -1,0 +1,486 @@
+// dapd.cu -- DAPD: attention -> tau-graph -> Welsh-Powell greedy independent
+// set, with the late-phase confidence rule (DAPD, "整体框架", "关键设计 1-3").
+//
+// Three launches on the caller's stream:
+//   dapd_accum   the HBM-bound part: for every masked row i of the block and
+//                every column j, the sum over the given layers and heads of
+//                attention[i][j].  Grid = sequences x row tiles x split, the
+//                split CTAs of one tile forming a thread-block cluster that
+//                divides the layer*head range and merges through distributed
+//                shared memory.  Loads are 16-byte vectors; the sums are exact:
+//                each value x is split as hi = (x + 256) - 256 (a multiple of
+//                2^-15) and lo = x - hi (a multiple of 2^-24 for f16 input,
+//                |lo| <= 2^-16), hi and lo are summed separately in fp32 --
+//                both sums stay exactly representable for f16 values in
+//                [0, 256) whose total stays below 512 -- and the pair is
+//                stored as a 64-bit fixed-point number in units of 2^-32.
+//   dapd_graph   one warp per masked row: I_ij = A_ij + A_ji (= 2 L H 2^32 s_ij),
+//                the edge test I_ij > floor(2 L H 2^32 tau) (exact), the
+//                adjacency words by ballot, the row sum D_i (= 2 L H 2^32 d~_i)
+//                and the edge degree.
+//   dapd_select  one CTA per sequence: the 50% switch, then either the
+//                late-phase rule or the exact ordering of key_i = d~_i conf_i
+//                (compared as 128-bit integer mantissas with a shared exponent)
+//                and the greedy scan over the shared-memory adjacency bitmask.
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace dlm {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxWords = DLM_MAX_BLK / 32;
+constexpr int kSliceUnroll = 4;
+
+__device__ __forceinline__ bool late_phase(const DapdArgs& a, int b, int* count_out) {
+    const bool m = threadIdx.x < (unsigned)a.blk && a.masked[(int64_t)b * a.blk + threadIdx.x] != 0;
+    const int M = __syncthreads_count(m);
+    if (count_out) *count_out = M;
+    return (float)M < a.bulk_frac * (float)a.blk;
+}
+
+template <int DT>
+struct AFmt;
+template <>
+struct AFmt<DLM_F16> {
+    static constexpr int EPV = 8;
+    static constexpr int ESZ = 2;
+    static __device__ __forceinline__ void to_f2(uint4 w, f2 (&x)[4]) {
+        x[0] = f16x2_to_f2(w.x);
+        x[1] = f16x2_to_f2(w.y);
+        x[2] = f16x2_to_f2(w.z);
+        x[3] = f16x2_to_f2(w.w);
+    }
+    static __device__ __forceinline__ float scalar(const void* p) { return __half2float(*static_cast<const __half*>(p)); }
+};
+template <>
+struct AFmt<DLM_BF16> {
+    static constexpr int EPV = 8;
+    static constexpr int ESZ = 2;
+    static __device__ __forceinline__ void to_f2(uint4 w, f2 (&x)[4]) {
+        x[0] = bf16x2_to_f2(w.x);
+        x[1] = bf16x2_to_f2(w.y);
+        x[2] = bf16x2_to_f2(w.z);
+        x[3] = bf16x2_to_f2(w.w);
+    }
+    static __device__ __forceinline__ float scalar(const void* p) {
+        return __uint_as_float((uint32_t) * static_cast<const uint16_t*>(p) << 16);
+    }
+};
+template <>
+struct AFmt<DLM_F32> {
+    static constexpr int EPV = 4;
+    static constexpr int ESZ = 4;
+    static __device__ __forceinline__ void to_f2(uint4 w, f2 (&x)[2]) {
+        x[0] = pack2(__uint_as_float(w.x), __uint_as_float(w.y));
+        x[1] = pack2(__uint_as_float(w.z), __uint_as_float(w.w));
+    }
+    static __device__ __forceinline__ float scalar(const void* p) { return *static_cast<const float*>(p); }
+};
+
+__device__ __forceinline__ uint4 ld_nc(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// exact split accumulate: x = hi + lo, hi multiple of 2^-15 when 0 <= x < 256
+template <int NP>
+__device__ __forceinline__ void split_acc(const f2 (&x)[NP], f2 (&H)[NP], f2 (&L)[NP]) {
+    const f2 c = pack2(256.f, 256.f);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        f2 hi = sub2(add2(x[p], c), c);
+        f2 lo = sub2(x[p], hi);
+        H[p] = add2(H[p], hi);
+        L[p] = add2(L[p], lo);
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
+    constexpr int EPV = AFmt<DT>::EPV;
+    constexpr int ESZ = AFmt<DT>::ESZ;
+    constexpr int NP = EPV / 2;
+    // per thread: NP pairs of (H, L) -> 2*EPV floats
+    __shared__ float s_red[kThreads * 2 * EPV];
+    __shared__ int s_rows[kThreads];
+    __shared__ int s_nm;
+
+    const int split = a.split;
+    const int g = blockIdx.x % split;
+    const int tb = blockIdx.x / split;
+    const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
+    const int tile = tb % tiles;
+    const int b = tb / tiles;
+    if (late_phase(a, b, nullptr)) return;  // the whole cluster takes the same branch
+
+    const int r0 = tile * a.row_tile, r1 = min(a.blk, r0 + a.row_tile);
+    if (threadIdx.x == 0) {
+        int nm = 0;
+        for (int r = r0; r < r1; ++r)
+            if (a.masked[(int64_t)b * a.blk + r]) s_rows[nm++] = r;
+        s_nm = nm;
+    }
+    __syncthreads();
+    const int nm = s_nm;
+    const int vpr = (a.blk + EPV - 1) / EPV;  // vectors per row
+    const int Q = nm * vpr;                   // slots per slice (<= kThreads by construction)
+    const int LH = a.n_layers * a.n_heads;
+    const int chunk = (LH + split - 1) / split;
+    const int s0 = g * chunk, s1 = min(LH, s0 + chunk);
+    const int G2 = Q > 0 ? max(1, kThreads / Q) : 1;  // slice groups inside the CTA
+    const int t = threadIdx.x;
+    const bool active = Q > 0 && t < G2 * Q;
+    const int slot = active ? t % Q : 0;
+    const int grp = active ? t / Q : 0;
+    const int row = active ? s_rows[slot / vpr] : 0;
+    const int vec = slot % vpr;
+    const int col0 = vec * EPV;
+    const bool full = col0 + EPV <= a.blk;
+
+    f2 H[NP], L[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) H[p] = L[p] = pack2(0.f, 0.f);
+
+    if (active) {
+        const char* base = static_cast<const char*>(a.attn) +
+                           ((int64_t)b * a.sb + (int64_t)(a.block_start + row) * a.sr + a.block_start + col0) * ESZ;
+        auto addr = [&](int s) {
+            const int l = s / a.n_heads, h = s - l * a.n_heads;
+            return base + ((int64_t)l * a.sl + (int64_t)h * a.sh) * ESZ;
+        };
+        int s = s0 + grp;
+        if (full) {
+            for (; s + (kSliceUnroll - 1) * G2 < s1; s += kSliceUnroll * G2) {
+                uint4 w[kSliceUnroll];
+#pragma unroll
+                for (int u = 0; u < kSliceUnroll; ++u) w[u] = ld_nc(addr(s + u * G2));
+#pragma unroll
+                for (int u = 0; u < kSliceUnroll; ++u) {
+                    f2 x[NP];
+                    AFmt<DT>::to_f2(w[u], x);
+                    split_acc<NP>(x, H, L);
+                }
+            }
+            for (; s < s1; s += G2) {
+                f2 x[NP];
+                AFmt<DT>::to_f2(ld_nc(addr(s)), x);
+                split_acc<NP>(x, H, L);
+            }
+        } else {
+            // ragged last vector of the row: element loads of the valid columns
+            for (; s < s1; s += G2) {
+                const char* p = addr(s);
+                float v[EPV];
+#pragma unroll
+                for (int k = 0; k < EPV; ++k) v[k] = (col0 + k < a.blk) ? AFmt<DT>::scalar(p + k * ESZ) : 0.f;
+                f2 x[NP];
+#pragma unroll
+                for (int q = 0; q < NP; ++q) x[q] = pack2(v[2 * q], v[2 * q + 1]);
+                split_acc<NP>(x, H, L);
+            }
+        }
+    }
+
+    // merge the slice groups of this CTA in group order
+    float* mine = s_red + (size_t)t * 2 * EPV;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        unpack2(H[p], mine[4 * p + 0], mine[4 * p + 1]);
+        unpack2(L[p], mine[4 * p + 2], mine[4 * p + 3]);
+    }
+    __syncthreads();
+    if (active && grp == 0) {
+        for (int gg = 1; gg < G2; ++gg) {
+            const float* o = s_red + (size_t)(gg * Q + slot) * 2 * EPV;
+#pragma unroll
+            for (int k = 0; k < 2 * EPV; ++k) mine[k] += o[k];
+        }
+    }
+    if (split > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (g == 0 && active && grp == 0) {
+            for (int rr = 1; rr < split; ++rr) {
+                const float* o = cluster.map_shared_rank(mine, rr);
+#pragma unroll
+                for (int k = 0; k < 2 * EPV; ++k) mine[k] += o[k];
+            }
+        }
+        cluster.sync();
+    } else {
+        __syncthreads();
+    }
+    if (g != 0 || !active || grp != 0) return;
+    long long* A = a.A + ((int64_t)b * a.blk + row) * a.blk;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int col = col0 + 2 * p + k;
+            if (col < a.blk) {
+                const float hi = mine[4 * p + k], lo = mine[4 * p + 2 + k];
+                A[col] = __float2ll_rn(hi * 32768.f) * 131072LL + __float2ll_rn(lo * 4294967296.f);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
+    const int b = blockIdx.y;
+    if (late_phase(a, b, nullptr)) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i = blockIdx.x * (kThreads / 32) + warp;
+    if (i >= a.blk) return;
+    const uint8_t* mk = a.masked + (int64_t)b * a.blk;
+    if (!mk[i]) return;
+    const long long* A = a.A + (int64_t)b * a.blk * a.blk;
+    long long D = 0;
+    int deg = 0;
+    uint32_t* adj = a.adj + ((int64_t)b * a.blk + i) * kMaxWords;
+    const int nw = (a.blk + 31) >> 5;
+    for (int c = 0; c < kMaxWords; ++c) {
+        bool edge = false;
+        if (c < nw) {
+            const int j = c * 32 + lane;
+            if (j < a.blk && mk[j]) {
+                const long long I = A[(int64_t)i * a.blk + j] + A[(int64_t)j * a.blk + i];
+                if (a.s_out) a.s_out[((int64_t)b * a.blk + i) * a.blk + j] = __ll2float_rn(I) * a.s_scale;
+                if (j != i) {
+                    D += I;
+                    edge = I > a.edge_thresh;
+                    deg += edge;
+                }
+            }
+        }
+        const uint32_t w = __ballot_sync(DLM_FULL_MASK, edge);
+        if (lane == 0) adj[c] = w;
+    }
+    D = warp_sum_ll(D);
+    deg = warp_sum_i(deg);
+    if (lane == 0) {
+        a.Dsum[(int64_t)b * a.blk + i] = D;
+        if (a.dtilde_out) a.dtilde_out[(int64_t)b * a.blk + i] = __ll2float_rn(D) * a.s_scale;
+        if (a.deg_out) a.deg_out[(int64_t)b * a.blk + i] = deg;
+    }
+}
+
+// key = sign * mant * 2^exp with a 128-bit mantissa normalised to bit 127
+struct Key {
+    int sign;
+    int exp;
+    unsigned long long hi, lo;
+};
+
+__device__ __forceinline__ Key make_key(long long D, float c, int order_mode) {
+    Key k;
+    unsigned long long mag;
+    int sign = D > 0 ? 1 : (D < 0 ? -1 : 0);
+    mag = D < 0 ? (unsigned long long)(-D) : (unsigned long long)D;
+    unsigned long long phi = 0, plo = mag;
+    int e = 0;
+    if (order_mode == 0) {
+        const uint32_t u = __float_as_uint(c);
+        const int ce = (u >> 23) & 0xff;
+        uint32_t cm = u & 0x7fffff;
+        if (!(c > 0.f) || ce == 0xff) {  // zero, negative, NaN or inf confidence: key 0
+            sign = 0;
+            cm = 0;
+        }
+        if (ce != 0) cm |= 0x800000u;
+        e = ce == 0 ? -149 : ce - 150;
+        plo = mag * (unsigned long long)cm;
+        phi = __umul64hi(mag, (unsigned long long)cm);
+    }
+    if (sign == 0 || (phi == 0 && plo == 0)) {
+        k.sign = 0;
+        k.exp = 0;
+        k.hi = k.lo = 0;
+        return k;
+    }
+    const int lz = phi ? __clzll(phi) : 64 + __clzll(plo);
+    if (lz >= 64) {
+        phi = plo << (lz - 64);
+        plo = 0;
+    } else if (lz > 0) {
+        phi = (phi << lz) | (plo >> (64 - lz));
+        plo <<= lz;
+    }
+    k.sign = sign;
+    k.exp = e - lz;
+    k.hi = phi;
+    k.lo = plo;
+    return k;
+}
+
+// +1 if a > b, -1 if a < b, 0 if equal
+__device__ __forceinline__ int key_cmp(const Key& a, const Key& b) {
+    if (a.sign != b.sign) return a.sign > b.sign ? 1 : -1;
+    if (a.sign == 0) return 0;
+    int r;
+    if (a.exp != b.exp)
+        r = a.exp > b.exp ? 1 : -1;
+    else if (a.hi != b.hi)
+        r = a.hi > b.hi ? 1 : -1;
+    else if (a.lo != b.lo)
+        r = a.lo > b.lo ? 1 : -1;
+    else
+        r = 0;
+    return a.sign > 0 ? r : -r;
+}
+
+__global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
+    __shared__ Key s_key[DLM_MAX_BLK];
+    __shared__ int s_order[DLM_MAX_BLK];
+    __shared__ uint32_t s_adj[DLM_MAX_BLK * kMaxWords];
+    __shared__ uint32_t s_kept[kMaxWords];
+    __shared__ unsigned char s_m[DLM_MAX_BLK];
+    __shared__ float s_v[kThreads / 32];
+    __shared__ int s_i[kThreads / 32];
+    const int b = blockIdx.x, t = threadIdx.x;
+    int M;
+    const bool late = late_phase(a, b, &M);
+    const int64_t o = (int64_t)b * a.blk + t;
+    const bool m = t < a.blk && a.masked[o] != 0;
+    uint8_t* sel = a.selected + (int64_t)b * a.blk;
+    if (late) {
+        const float c = m ? a.conf[o] : 0.f;
+        bool s = m && c > a.bulk_conf;
+        int n = __syncthreads_count(s);
+        if (n == 0 && M > 0) {
+            float v = m ? c : -INFINITY;
+            int idx = m ? t : 0x7fffffff;
+            warp_argmax(v, idx);
+            if ((t & 31) == 0) {
+                s_v[t >> 5] = v;
+                s_i[t >> 5] = idx;
+            }
+            __syncthreads();
+            if (t < 32) {
+                v = t < kThreads / 32 ? s_v[t] : -INFINITY;
+                idx = t < kThreads / 32 ? s_i[t] : 0x7fffffff;
+                warp_argmax(v, idx);
+                if (t == 0) s_i[0] = idx;
+            }
+            __syncthreads();
+            s = (t == s_i[0]);
+            n = 1;
+        }
+        if (t < a.blk) sel[t] = s ? 1 : 0;
+        if (t == 0) a.n_selected[b] = n;
+        return;
+    }
+    if (t < a.blk) {
+        s_m[t] = m;
+        sel[t] = 0;
+        if (m) s_key[t] = make_key(a.Dsum[o], a.conf[o], a.order_mode);
+    }
+    const int nw = (a.blk + 31) >> 5;
+    for (int k = t; k < a.blk * nw; k += blockDim.x) {
+        const int r = k / nw, w = k - r * nw;
+        s_adj[r * kMaxWords + w] = a.adj[((int64_t)b * a.blk + r) * kMaxWords + w];
+    }
+    __syncthreads();
+    if (m) {
+        const Key ki = s_key[t];
+        int rank = 0;
+        for (int j = 0; j < a.blk; ++j) {
+            if (!s_m[j] || j == t) continue;
+            const int c = key_cmp(s_key[j], ki);
+            rank += (c > 0) || (c == 0 && j < t);
+        }
+        s_order[rank] = t;
+    }
+    __syncthreads();
+    if (t < 32) {
+        uint32_t kept = 0;
+        for (int k = 0; k < M; ++k) {
+            const int v = s_order[k];
+            const uint32_t hit = t < nw ? (s_adj[v * kMaxWords + t] & kept) : 0u;
+            if (!__any_sync(DLM_FULL_MASK, hit != 0u) && t == (v >> 5)) kept |= 1u << (v & 31);
+        }
+        if (t < kMaxWords) s_kept[t] = kept;
+    }
+    __syncthreads();
+    int mine = 0;
+    if (m && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
+        sel[t] = 1;
+        mine = 1;
+    }
+    const int total = __syncthreads_count(mine);
+    if (t == 0) a.n_selected[b] = total;
+}
+
+template <int DT>
+cudaError_t launch_accum(const DapdArgs& a, cudaStream_t s) {
+    const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.batch * tiles * a.split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (a.split > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = a.split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, dapd_accum_kernel<DT>, a);
+}
+
+}  // namespace
+
+size_t dapd_workspace_bytes(int batch, int blk) {
+    size_t A = ((size_t)batch * blk * blk * 8 + 255) & ~(size_t)255;
+    size_t Ds = ((size_t)batch * blk * 8 + 255) & ~(size_t)255;
+    size_t adj = (size_t)batch * blk * kMaxWords * 4;
+    return A + Ds + adj;
+}
+
+void dapd_carve(DapdArgs& a, void* ws) {
+    char* p = static_cast<char*>(ws);
+    a.A = reinterpret_cast<long long*>(p);
+    p += ((size_t)a.batch * a.blk * a.blk * 8 + 255) & ~(size_t)255;
+    a.Dsum = reinterpret_cast<long long*>(p);
+    p += ((size_t)a.batch * a.blk * 8 + 255) & ~(size_t)255;
+    a.adj = reinterpret_cast<uint32_t*>(p);
+}
+
+cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
+    const int epv = a.dtype == DLM_F32 ? 4 : 8;
+    const int vpr = (a.blk + epv - 1) / epv;
+    a.row_tile = max(1, min(a.blk, kThreads / vpr));
+    const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
+    const int LH = a.n_layers * a.n_heads;
+    const long long base = (long long)a.batch * tiles;
+    int split = (int)((2LL * num_sms + base - 1) / base);
+    split = max(1, min(8, min(split, LH)));
+    a.split = split;
+    cudaError_t e;
+    switch (a.dtype) {
+    case DLM_F16: e = launch_accum<DLM_F16>(a, s); break;
+    case DLM_BF16: e = launch_accum<DLM_BF16>(a, s); break;
+    default: e = launch_accum<DLM_F32>(a, s); break;
+    }
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.gridDim = dim3((unsigned)((a.blk + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.batch);
+    cfg.blockDim = dim3(kThreads);
+    e = cudaLaunchKernelEx(&cfg, dapd_graph_kernel, a);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)a.batch);
+    return cudaLaunchKernelEx(&cfg, dapd_select_kernel, a);
+}
+
+}  // namespace dlm

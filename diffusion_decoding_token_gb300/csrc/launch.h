@@ -1,0 +1,107 @@
+// launch.h -- internal kernel launchers of libdlm (host side, not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dlm.h"
+
+namespace dlm {
+
+struct RowStatsArgs {
+    const void* cur;
+    const void* prev;
+    int64_t n_rows, vocab, row_stride;
+    const int32_t* row_index;
+    int32_t* argmax;
+    float* conf;
+    float* lse;
+    float* entropy;
+    float* kl;
+    float* lse_prev;
+    uint32_t* dev_status;
+    int split;  // CTAs per row (thread-block cluster size), 1..8
+};
+cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s);
+int row_stats_elems_per_vector(int dtype);
+int row_stats_threads();
+
+struct ThresholdArgs {
+    const float* conf;
+    const uint8_t* masked;
+    int batch, blk;
+    float tau;
+    uint8_t* selected;
+    int32_t* n_selected;
+};
+cudaError_t launch_threshold(const ThresholdArgs& a, cudaStream_t s);
+
+struct BoundaryArgs {
+    const float* kl;
+    const float* entropy;
+    int batch, L_window;
+    const uint8_t* cold_start;
+    float lambda;
+    int L_min, smooth_w, norm_mode;
+    int32_t* block_len;
+    float* score;
+};
+cudaError_t launch_boundary(const BoundaryArgs& a, cudaStream_t s);
+
+struct CapArgs {
+    const void* logits;
+    int dtype;
+    int64_t row_stride;
+    const int32_t* argmax;
+    const float* conf;
+    const float* lse;
+    const uint8_t* masked;
+    const int32_t* scope_len;
+    int batch, blk;
+    float tau_low, tau_high, gamma;
+    int p_max, high_tier_unconditional;
+    uint8_t* selected;
+    int32_t* n_selected;
+    float* D_out;
+    uint32_t* dev_status;
+    // workspace carve-up
+    int32_t* pool;     // [batch][p_max] block positions in pool order
+    int32_t* pool_n;   // [batch]
+    uint32_t* adj;     // [batch][p_max][words] conflict bits over pool slots
+    int words;         // ceil(p_max / 32)
+};
+size_t cap_workspace_bytes(int batch, int p_max);
+void cap_carve(CapArgs& a, void* ws);
+cudaError_t launch_cap(const CapArgs& a, cudaStream_t s);
+
+struct DapdArgs {
+    const void* attn;
+    int dtype;
+    int batch, n_layers, n_heads;
+    int64_t sb, sl, sh, sr;  // element strides
+    int block_start, blk;
+    const uint8_t* masked;
+    const float* conf;
+    float tau_edge, bulk_conf, bulk_frac;
+    int order_mode;
+    long long edge_thresh;   // floor(tau * 2 * L * H * 2^32): edge <=> 2LH 2^32 s > this
+    float s_scale;           // 1 / (2 * L * H * 2^32)
+    uint8_t* selected;
+    int32_t* n_selected;
+    float* s_out;
+    float* dtilde_out;
+    int32_t* deg_out;
+    uint32_t* dev_status;
+    // workspace carve-up
+    long long* A;      // [batch][blk][blk] fixed-point sums (units 2^-32)
+    long long* Dsum;   // [batch][blk]
+    uint32_t* adj;     // [batch][blk][8]
+    int split;         // CTAs per cluster over the layer*head range
+    int row_tile;      // rows per CTA
+};
+size_t dapd_workspace_bytes(int batch, int blk);
+void dapd_carve(DapdArgs& a, void* ws);
+cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);
+
+}  // namespace dlm

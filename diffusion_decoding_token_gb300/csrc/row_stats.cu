@@ -1,0 +1,446 @@
+// row_stats.cu -- fused streaming pass over vocab-wide logit rows.
+//
+// Per row (DepCap "Methodology": I_k = KL(p_curr || p_prev), H_k = H(p_curr),
+// c = max_v p(v); Fast-dLLM review "Method": max-softmax confidence) one pass
+// over the current row and, optionally, the previous step's row produces
+// argmax, confidence, log-sum-exp, entropy, KL(cur || prev) and the previous
+// row's log-sum-exp.
+//
+// Design (HBM-bound, ~1 flop per byte):
+//  * one CTA (or a cluster of `split` CTAs when there are too few rows to
+//    fill 152 SMs) streams a row with coalesced 16-byte loads that bypass L1;
+//  * each thread keeps an online softmax state relative to a lazily moved
+//    reference (moved only when a value exceeds it by more than kRebase, so
+//    the common path has no rescale), in base-2 units so every element costs
+//    one FMA and one ex2 on the SFU; the arithmetic is done on packed f32x2;
+//  * the exact maximum is tracked per 8-element vector and the argmax position
+//    is recovered at the end by re-reading the winning vector, ties to the
+//    lowest index everywhere;
+//  * partial states merge through warp shuffles, shared memory and, for split
+//    rows, distributed shared memory inside the cluster; the merge order is
+//    fixed, so results are deterministic.
+// Every quantity is independent of the reference r:
+//   S = sum 2^{a_v}, a_v = (z_v - r) log2 e,  T = sum 2^{a_v} a_v,
+//   K = sum 2^{a_v} (z_v - z'_v):
+//   lse = r + ln S, conf = exp(max z - lse), H = ln S - ln2 T/S,
+//   KL = K/S - (r - r') - (ln S - ln S').
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace cg = cooperative_groups;
+
+namespace dlm {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kUnroll = 4;
+constexpr float kRebase = 8.0f;    // e^8 of headroom before the reference moves
+constexpr float kFloorLog2 = -256.0f;
+constexpr float kClampLo = -1e30f;                 // lower clamp of bf16 / f32 logits
+constexpr unsigned short kClampBf16 = 0xf14a;        // -1e30 rounded to bf16
+constexpr float kDegenerate = -1e29f;              // a row whose max is below this held only -inf
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// partial state of a slice of one row
+struct Part {
+    float mx;   // exact max of the (clamped) stored values
+    int idx;    // first position holding mx
+    float ref;  // softmax reference
+    float S, T, K;
+    float refp, Sp;
+};
+
+__device__ __forceinline__ void part_empty(Part& p) {
+    p.mx = -INFINITY;
+    p.idx = 0x7fffffff;
+    p.ref = -FLT_MAX;
+    p.S = p.T = p.K = 0.f;
+    p.refp = -FLT_MAX;
+    p.Sp = 0.f;
+}
+
+__device__ __forceinline__ void part_merge(Part& a, const Part& b) {
+    if (b.mx > a.mx || (b.mx == a.mx && b.idx < a.idx)) {
+        a.mx = b.mx;
+        a.idx = b.idx;
+    }
+    float r = fmaxf(a.ref, b.ref);
+    float da = fmaxf((a.ref - r) * kLog2e, kFloorLog2);
+    float db = fmaxf((b.ref - r) * kLog2e, kFloorLog2);
+    float ea = ex2(da), eb = ex2(db);
+    a.T = ea * fmaf(da, a.S, a.T) + eb * fmaf(db, b.S, b.T);
+    a.S = ea * a.S + eb * b.S;
+    a.K = ea * a.K + eb * b.K;
+    a.ref = r;
+    float rp = fmaxf(a.refp, b.refp);
+    float dpa = fmaxf((a.refp - rp) * kLog2e, kFloorLog2);
+    float dpb = fmaxf((b.refp - rp) * kLog2e, kFloorLog2);
+    a.Sp = ex2(dpa) * a.Sp + ex2(dpb) * b.Sp;
+    a.refp = rp;
+}
+
+__device__ __forceinline__ Part part_shfl(const Part& p, int o) {
+    Part q;
+    q.mx = __shfl_xor_sync(DLM_FULL_MASK, p.mx, o);
+    q.idx = __shfl_xor_sync(DLM_FULL_MASK, p.idx, o);
+    q.ref = __shfl_xor_sync(DLM_FULL_MASK, p.ref, o);
+    q.S = __shfl_xor_sync(DLM_FULL_MASK, p.S, o);
+    q.T = __shfl_xor_sync(DLM_FULL_MASK, p.T, o);
+    q.K = __shfl_xor_sync(DLM_FULL_MASK, p.K, o);
+    q.refp = __shfl_xor_sync(DLM_FULL_MASK, p.refp, o);
+    q.Sp = __shfl_xor_sync(DLM_FULL_MASK, p.Sp, o);
+    return q;
+}
+
+__device__ __forceinline__ void warp_merge(Part& p) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        Part q = part_shfl(p, o);
+        // combine in a fixed (lower lane first) order so every lane agrees
+        if (threadIdx.x & o) {
+            Part lo = q;
+            part_merge(lo, p);
+            p = lo;
+        } else {
+            part_merge(p, q);
+        }
+    }
+}
+
+// ---- storage formats --------------------------------------------------
+// A 16-byte vector is unpacked into NP packed pairs of fp32 and its max.
+// Values are clamped from below (NaN is kept) so that -inf logits become a
+// large finite negative number: its exponential is exactly 0 and its product
+// with the base-2 scaling stays finite, so 0 * (z - r) terms stay 0.  The
+// clamp is -1e30 for bf16/f32 storage and the f16 minimum for f16.
+template <int DT>
+struct Fmt;
+
+template <>
+struct Fmt<DLM_BF16> {
+    static constexpr int EPV = 8;
+    static constexpr int ESZ = 2;
+    static __device__ __forceinline__ float scalar(const void* base, int64_t i) {
+        uint32_t b = static_cast<const uint16_t*>(base)[i];
+        return max_nan(__uint_as_float(b << 16), __uint_as_float((uint32_t)kClampBf16 << 16));
+    }
+    static __device__ __forceinline__ float unpack(uint4 w, f2 (&z)[4]) {
+        const __nv_bfloat162 lo = __halves2bfloat162(__ushort_as_bfloat16(kClampBf16), __ushort_as_bfloat16(kClampBf16));
+        uint32_t r[4] = {w.x, w.y, w.z, w.w};
+        __nv_bfloat162 m;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&r[k]);
+            h = __hmax2_nan(h, lo);
+            m = k ? __hmax2(m, h) : h;
+            r[k] = *reinterpret_cast<uint32_t*>(&h);
+            z[k] = bf16x2_to_f2(r[k]);
+        }
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+};
+
+template <>
+struct Fmt<DLM_F16> {
+    static constexpr int EPV = 8;
+    static constexpr int ESZ = 2;
+    static __device__ __forceinline__ float scalar(const void* base, int64_t i) {
+        return max_nan(__half2float(static_cast<const __half*>(base)[i]), -65504.f);
+    }
+    static __device__ __forceinline__ float unpack(uint4 w, f2 (&z)[4]) {
+        const __half2 lo = __halves2half2(__ushort_as_half(0xfbff), __ushort_as_half(0xfbff));
+        uint32_t r[4] = {w.x, w.y, w.z, w.w};
+        __half2 m;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            __half2 h = *reinterpret_cast<__half2*>(&r[k]);
+            h = __hmax2_nan(h, lo);
+            m = k ? __hmax2(m, h) : h;
+            r[k] = *reinterpret_cast<uint32_t*>(&h);
+            z[k] = f16x2_to_f2(r[k]);
+        }
+        return fmaxf(__low2float(m), __high2float(m));
+    }
+};
+
+template <>
+struct Fmt<DLM_F32> {
+    static constexpr int EPV = 4;
+    static constexpr int ESZ = 4;
+    static __device__ __forceinline__ float scalar(const void* base, int64_t i) {
+        return max_nan(static_cast<const float*>(base)[i], kClampLo);
+    }
+    static __device__ __forceinline__ float unpack(uint4 w, f2 (&z)[2]) {
+        float a = max_nan(__uint_as_float(w.x), kClampLo);
+        float b = max_nan(__uint_as_float(w.y), kClampLo);
+        float c = max_nan(__uint_as_float(w.z), kClampLo);
+        float d = max_nan(__uint_as_float(w.w), kClampLo);
+        z[0] = pack2(a, b);
+        z[1] = pack2(c, d);
+        return fmaxf(fmaxf(a, b), fmaxf(c, d));
+    }
+};
+
+// per-thread accumulator
+struct Acc {
+    float mx;
+    int bv;     // vector holding mx (first), or -1 when it came from the tail
+    int bidx;   // position when it came from the tail
+    float ref, refL;
+    f2 S, T, K;
+    float refp, refpL;
+    f2 Sp;
+};
+
+__device__ __forceinline__ void rebase(Acc& a, float nref) {
+    float d = fmaxf((a.ref - nref) * kLog2e, kFloorLog2);
+    float al = ex2(d);
+    f2 d2 = pack2(d, d), al2 = pack2(al, al);
+    a.T = mul2(al2, fma2(d2, a.S, a.T));
+    a.S = mul2(al2, a.S);
+    a.K = mul2(al2, a.K);
+    a.ref = nref;
+    a.refL = nref * kLog2e;
+}
+
+__device__ __forceinline__ void rebase_p(Acc& a, float nref) {
+    float d = fmaxf((a.refp - nref) * kLog2e, kFloorLog2);
+    float al = ex2(d);
+    a.Sp = mul2(pack2(al, al), a.Sp);
+    a.refp = nref;
+    a.refpL = nref * kLog2e;
+}
+
+template <int NP, bool PREV>
+__device__ __forceinline__ void accum(Acc& a, const f2 (&z)[NP], const f2 (&zp)[NP]) {
+    const f2 l2e = pack2(kLog2e, kLog2e);
+    const f2 nr = pack2(-a.refL, -a.refL);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        f2 x = fma2(z[p], l2e, nr);
+        f2 e = ex2x2(x);
+        a.S = add2(a.S, e);
+        a.T = fma2(e, x, a.T);
+        if (PREV) a.K = fma2(e, sub2(z[p], zp[p]), a.K);
+    }
+    if (PREV) {
+        const f2 nrp = pack2(-a.refpL, -a.refpL);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+            f2 x = fma2(zp[p], l2e, nrp);
+            a.Sp = add2(a.Sp, ex2x2(x));
+        }
+    }
+}
+
+template <int DT, bool PREV>
+__device__ __forceinline__ void process_vec(Acc& a, uint4 cw, uint4 pw, int v) {
+    constexpr int NP = Fmt<DT>::EPV / 2;
+    f2 z[NP], zp[NP];
+    float vmax = Fmt<DT>::unpack(cw, z);
+    float vmaxp = 0.f;
+    if (PREV) vmaxp = Fmt<DT>::unpack(pw, zp);
+    if (vmax > a.mx) {
+        a.mx = vmax;
+        a.bv = v;
+    }
+    if (vmax > a.ref + kRebase) rebase(a, vmax);
+    if (PREV && vmaxp > a.refp + kRebase) rebase_p(a, vmaxp);
+    accum<NP, PREV>(a, z, zp);
+}
+
+template <bool PREV>
+__device__ __forceinline__ void process_scalar(Acc& a, float z, float zp, int pos) {
+    if (z > a.mx) {
+        a.mx = z;
+        a.bv = -1;
+        a.bidx = pos;
+    }
+    if (z > a.ref + kRebase) rebase(a, z);
+    if (PREV && zp > a.refp + kRebase) rebase_p(a, zp);
+    // scalar form of accum (keeps the pair layout: only the low lane is used)
+    float x = fmaf(z, kLog2e, -a.refL);
+    float e = ex2(x);
+    a.S = add2(a.S, pack2(e, 0.f));
+    a.T = fma2(pack2(e, 0.f), pack2(x, 0.f), a.T);
+    if (PREV) {
+        a.K = fma2(pack2(e, 0.f), pack2(z - zp, 0.f), a.K);
+        float xp = fmaf(zp, kLog2e, -a.refpL);
+        a.Sp = add2(a.Sp, pack2(ex2(xp), 0.f));
+    }
+}
+
+template <int DT, bool PREV>
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) {
+    constexpr int EPV = Fmt<DT>::EPV;
+    constexpr int ESZ = Fmt<DT>::ESZ;
+    __shared__ Part s_warp[kWarps];
+    __shared__ Part s_cta;
+
+    const int split = args.split;
+    const int64_t r = blockIdx.x / split;
+    const int rank = blockIdx.x - (int)(r * split);
+    if (r >= args.n_rows) return;  // never taken: grid = n_rows * split
+    const int64_t q = args.row_index ? (int64_t)args.row_index[r] : r;
+    const char* cur_row = static_cast<const char*>(args.cur) + q * args.row_stride * ESZ;
+    const char* prev_row = PREV ? static_cast<const char*>(args.prev) + q * args.row_stride * ESZ : nullptr;
+    const uint4* cv = reinterpret_cast<const uint4*>(cur_row);
+    const uint4* pv = reinterpret_cast<const uint4*>(prev_row);
+
+    const int nvec = (int)(args.vocab / EPV);
+    const int chunk = (nvec + split - 1) / split;
+    const int v0 = rank * chunk;
+    const int v1 = min(nvec, v0 + chunk);
+
+    Acc a;
+    a.mx = -INFINITY;
+    a.bv = -1;
+    a.bidx = 0x7fffffff;
+    a.ref = -FLT_MAX;
+    a.refL = -FLT_MAX;
+    a.S = a.T = a.K = pack2(0.f, 0.f);
+    a.refp = -FLT_MAX;
+    a.refpL = -FLT_MAX;
+    a.Sp = pack2(0.f, 0.f);
+
+    int v = v0 + threadIdx.x;
+    for (; v + (kUnroll - 1) * kThreads < v1; v += kUnroll * kThreads) {
+        uint4 c[kUnroll], p[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            c[u] = ld_stream(cv + v + u * kThreads);
+            if (PREV) p[u] = ld_stream(pv + v + u * kThreads);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) process_vec<DT, PREV>(a, c[u], PREV ? p[u] : c[u], v + u * kThreads);
+    }
+    for (; v < v1; v += kThreads) {
+        uint4 c = ld_stream(cv + v);
+        uint4 p = PREV ? ld_stream(pv + v) : c;
+        process_vec<DT, PREV>(a, c, p, v);
+    }
+    // ragged tail (vocab not a multiple of the vector width): last CTA of the row
+    if (rank == split - 1) {
+        const int64_t t0 = (int64_t)nvec * EPV;
+        for (int64_t i = t0 + threadIdx.x; i < args.vocab; i += kThreads) {
+            float z = Fmt<DT>::scalar(cur_row, i);
+            float zp = PREV ? Fmt<DT>::scalar(prev_row, i) : 0.f;
+            process_scalar<PREV>(a, z, zp, (int)i);
+        }
+    }
+
+    Part p;
+    p.mx = a.mx;
+    p.idx = a.bidx;
+    if (a.bv >= 0) {
+        // recover the first position of the maximum inside the winning vector
+        constexpr int NP = EPV / 2;
+        f2 z[NP];
+        Fmt<DT>::unpack(ld_stream(cv + a.bv), z);
+        int k = EPV;
+#pragma unroll
+        for (int j = NP - 1; j >= 0; --j) {
+            float x, y;
+            unpack2(z[j], x, y);
+            if (y == a.mx) k = 2 * j + 1;
+            if (x == a.mx) k = 2 * j;
+        }
+        p.idx = a.bv * EPV + k;
+    }
+    p.ref = a.ref;
+    p.S = hsum2(a.S);
+    p.T = hsum2(a.T);
+    p.K = hsum2(a.K);
+    p.refp = a.refp;
+    p.Sp = hsum2(a.Sp);
+
+    warp_merge(p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) s_warp[warp] = p;
+    __syncthreads();
+    if (warp == 0) {
+        if (lane < kWarps)
+            p = s_warp[lane];
+        else
+            part_empty(p);
+        warp_merge(p);
+        if (lane == 0) s_cta = p;
+    }
+    if (split > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (rank == 0 && warp == 0) {
+            if (lane < split) {
+                Part* rp = cluster.map_shared_rank(&s_cta, lane);
+                p = *rp;
+            } else {
+                part_empty(p);
+            }
+            warp_merge(p);
+        }
+        cluster.sync();
+    }
+    if (rank != 0 || threadIdx.x != 0) return;
+
+    const float lnS = logf(p.S);
+    const float lse = p.ref + lnS;
+    args.argmax[q] = p.idx;
+    args.lse[q] = lse;
+    args.conf[q] = expf((p.mx - p.ref) - lnS);
+    args.entropy[q] = lnS - kLn2 * (p.T / p.S);
+    bool ok = isfinite(p.S) && p.S > 0.f && isfinite(p.T) && isfinite(p.mx) && p.mx > kDegenerate;
+    if (PREV) {
+        const float lnSp = logf(p.Sp);
+        if (args.kl) args.kl[q] = p.K / p.S - (p.ref - p.refp) - (lnS - lnSp);
+        if (args.lse_prev) args.lse_prev[q] = p.refp + lnSp;
+        ok = ok && isfinite(p.Sp) && p.Sp > 0.f && isfinite(p.K);
+    }
+    if (!ok) raise_status(args.dev_status, DLM_DEV_NONFINITE);
+}
+
+template <int DT, bool PREV>
+cudaError_t launch_typed(const RowStatsArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.n_rows * a.split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (a.split > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = a.split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, row_stats_kernel<DT, PREV>, a);
+}
+
+}  // namespace
+
+int row_stats_elems_per_vector(int dtype) { return dtype == DLM_F32 ? 4 : 8; }
+
+cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s) {
+    const bool prev = a.prev != nullptr;
+    switch (dtype) {
+    case DLM_BF16: return prev ? launch_typed<DLM_BF16, true>(a, s) : launch_typed<DLM_BF16, false>(a, s);
+    case DLM_F16: return prev ? launch_typed<DLM_F16, true>(a, s) : launch_typed<DLM_F16, false>(a, s);
+    default: return prev ? launch_typed<DLM_F32, true>(a, s) : launch_typed<DLM_F32, false>(a, s);
+    }
+}
+
+int row_stats_threads() { return kThreads; }
+
+}  // namespace dlm

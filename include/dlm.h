@@ -1,0 +1,258 @@
+/*
+ * dlm.h -- C ABI of the per-step unmask-decision library (libdlm.so).
+ *
+ * After every forward pass of a masked diffusion LM, the positions still
+ * masked in the active block have a vocab-wide logit row each.  This library
+ * turns those rows (and, for DAPD, the model's attention maps) into the set of
+ * positions to unmask in this step.  Committing the tokens and updating the
+ * mask stay with the caller; the token for a selected position is the argmax
+ * returned by dlm_row_stats.
+ *
+ * Conventions shared by every entry point
+ *  - Every data pointer is DEVICE memory owned by the caller.  The library
+ *    never allocates, frees or synchronises; all work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream) and runs on the
+ *    current CUDA device.
+ *  - Argument errors are reported synchronously, before anything is launched:
+ *    DLM_ERR_INVALID_ARG (null required pointer, negative or oversized size,
+ *    bad parameter), DLM_ERR_ALIGNMENT (a base address or row stride that is
+ *    not 16-byte aligned where the call says it must be), DLM_ERR_UNSUPPORTED
+ *    (dtype not accepted by the call), DLM_ERR_WORKSPACE (workspace too
+ *    small).  A failed launch returns DLM_ERR_CUDA.
+ *  - Conditions found on the device never trap: they OR DLM_DEV_* bits into
+ *    the caller's `dev_status` word (nullable: then they are not reported).
+ *  - Positions are "block positions": sequence b, position i of its active
+ *    block is row b*blk + i of every [batch][blk] array, and row b*blk + i of
+ *    the logits.
+ *  - Float decisions (threshold tests, orderings) are taken in fp32 on the
+ *    values the caller passes; DAPD's graph decisions are exact (see there).
+ *  - Sizes: 1 <= blk <= 256 for the selection calls; a batch of 0 is a no-op.
+ */
+#ifndef DLM_H
+#define DLM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without the CUDA headers */
+typedef struct CUstream_st* dlm_stream_t;
+
+typedef enum dlm_status {
+    DLM_OK = 0,
+    DLM_ERR_INVALID_ARG = 1,
+    DLM_ERR_ALIGNMENT = 2,
+    DLM_ERR_UNSUPPORTED = 3,
+    DLM_ERR_WORKSPACE = 4,
+    DLM_ERR_CUDA = 5
+} dlm_status;
+
+typedef enum dlm_dtype { DLM_F32 = 0, DLM_BF16 = 1, DLM_F16 = 2 } dlm_dtype;
+
+/* device status bits (OR-ed into *dev_status by the kernels) */
+#define DLM_DEV_NONFINITE 1u    /* a logit row held NaN or +inf, or only -inf   */
+#define DLM_DEV_POOL_CLIPPED 2u /* a CAP pool had more than p_max candidates    */
+
+/* Maximum block size accepted by the selection calls. */
+#define DLM_MAX_BLK 256
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dlm_status_string(dlm_status s);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int dlm_version(void);
+
+/*
+ * dlm_row_stats -- one fused streaming pass over each vocab-wide logit row.
+ *
+ * Defines (DepCap, "Methodology": I_k = KL(p_curr^k || p_prev^k),
+ * H_k = H(p_curr^k), c_i = max_v p_i(v); Fast-dLLM review, "Method":
+ * max-softmax confidence), with p = softmax(z) at temperature 1 and natural
+ * logarithms:
+ *   argmax[q]   = smallest v with z_v = max_v z_v (exact on stored values)
+ *   conf[q]     = max_v p_v
+ *   lse[q]      = log sum_v exp z_v
+ *   entropy[q]  = -sum_v p_v log p_v
+ *   kl[q]       = sum_v p_v (log p_v - log p'_v)   p' = softmax(prev row)
+ *   lse_prev[q] = log sum_v exp z'_v
+ *
+ * cur, prev   : logit rows, element (q, v) at base + q*row_stride + v, dtype
+ *               DLM_F32, DLM_BF16 or DLM_F16.  Base 16-byte aligned and
+ *               row_stride*sizeof(dtype) a multiple of 16 (DLM_ERR_ALIGNMENT
+ *               otherwise).  prev is nullable: then kl / lse_prev are not
+ *               written.  -inf logits are allowed and carry probability 0.
+ * n_rows      : number of rows to process (0 = nothing).
+ * vocab       : row length V, 1 <= V <= row_stride, V < 2^31.
+ * row_index   : nullable int32[n_rows]; row r processed is q = row_index[r]
+ *               (else q = r).  Results are stored at index q, so the output
+ *               arrays must hold max(q)+1 entries; entries of rows not
+ *               processed are left unchanged.
+ * argmax      : int32 output; conf, lse, entropy: float outputs (required).
+ * kl, lse_prev: float outputs, nullable (ignored when prev is NULL).
+ * dev_status  : nullable; DLM_DEV_NONFINITE is set for a row holding NaN or
+ *               +inf (its outputs are then unspecified).
+ */
+dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
+                         int64_t vocab, int64_t row_stride, const int32_t* row_index,
+                         int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
+                         float* lse_prev, uint32_t* dev_status, dlm_stream_t stream);
+
+/*
+ * dlm_select_threshold -- Fast-dLLM confidence-threshold decoding.
+ *
+ * Fast-dLLM review, "Method"; Fast-dLLM notes, "Key ideas" (safety valve):
+ * selected[b][i] = masked[b][i] && conf[b][i] > tau; if that is empty for a
+ * sequence with at least one masked position, the single masked position of
+ * highest confidence is selected (ties to the lower position).
+ *
+ * conf [batch][blk] float, masked [batch][blk] uint8 (nonzero = masked),
+ * selected [batch][blk] uint8 output (0/1), n_selected [batch] int32 output.
+ */
+dlm_status dlm_select_threshold(const float* conf, const uint8_t* masked, int32_t batch,
+                                int32_t blk, float tau, uint8_t* selected, int32_t* n_selected,
+                                dlm_stream_t stream);
+
+/*
+ * dlm_depcap_boundary -- DepGA-Block: length of the next block.
+ *
+ * DepCap, "Methodology" and "Technical Contribution": over a window of
+ * L_window future positions with KL influence I_k and entropy H_k,
+ * smooth and locally normalise both, form S_k = I~_k - lambda H~_k, stop
+ * before the first S_k < 0 and clip the length to [L_min, L_window]; a cold
+ * start uses L_min.  Readings of the unstated operators:
+ *   smooth_w  : centred moving average of odd width (1 = none); at the
+ *               window edges the neighbours that exist are averaged.
+ *   norm_mode : 0 = divide by the window mean (floored at 1e-12),
+ *               1 = rescale by window min/max to [0,1], 2 = none.
+ *   length    = min(max(k*, L_min), L_window), k* = first k with S_k < 0
+ *               (fp32 test) or L_window if none; cold start: min(L_min, L_window).
+ * L_window = min(L_max, L_remain) is the caller's choice.
+ *
+ * kl, entropy : float [batch][L_window] (k-th future position of sequence b
+ *               at b*L_window + k), 1 <= L_window <= 1024.
+ * cold_start  : nullable uint8 [batch].
+ * block_len   : int32 [batch] output.
+ * score       : nullable float [batch][L_window] output (S_k).
+ */
+typedef struct dlm_depcap_params {
+    float lambda;
+    int32_t L_min;     /* >= 1 */
+    int32_t smooth_w;  /* odd, 1..63 */
+    int32_t norm_mode; /* 0, 1 or 2 */
+} dlm_depcap_params;
+
+dlm_status dlm_depcap_boundary(const float* kl, const float* entropy, int32_t batch,
+                               int32_t L_window, const uint8_t* cold_start,
+                               const dlm_depcap_params* params, int32_t* block_len,
+                               float* score, dlm_stream_t stream);
+
+/*
+ * dlm_cap_select -- DepCap CAP-Decoding (conflict-aware parallel decoding).
+ *
+ * DepCap, "Methodology"; defaults in "Experiments" (tau_low 0.8, tau_high
+ * 0.95, gamma -16).  Within the first scope_len[b] positions of the block:
+ *   pool  = masked positions with conf >= tau_low, ordered by confidence
+ *           (descending, ties to the lower position), at most p_max kept
+ *           (DLM_DEV_POOL_CLIPPED when more qualified); the tau_high tier is
+ *           the head of this order.
+ *   D_ij  = log p_i(yhat_j) + log p_j(yhat_i),  log p_i(v) = z_i[v] - lse_i
+ *   i, j conflict  <=>  D_ij > gamma
+ *   greedy: scan the pool in order, keep a position iff it conflicts with no
+ *   kept one.  high_tier_unconditional = 1 keeps every tier member first,
+ *   then scans the rest.  Empty pool: the highest-confidence masked position
+ *   of the scope ("if no safe set exists").
+ *
+ * logits      : the current logit rows (as given to dlm_row_stats), row
+ *               b*blk + i, stride row_stride elements; 16-byte alignment is
+ *               not required (scattered 2-byte reads).
+ * argmax, conf, lse : [batch][blk] from dlm_row_stats.
+ * masked      : uint8 [batch][blk].
+ * scope_len   : nullable int32 [batch] (e.g. dlm_depcap_boundary's block_len);
+ *               NULL = the whole block.
+ * selected, n_selected : outputs as in dlm_select_threshold.
+ * D_out       : nullable float [batch][blk][blk]; D_ij is written at [b][i][j]
+ *               for every ordered pair of pool members; other entries are left
+ *               unchanged.
+ * workspace   : device scratch of at least dlm_cap_workspace_size(batch, p_max)
+ *               bytes, 16-byte aligned, owned by the caller; its contents on
+ *               entry do not matter.  Calls sharing a workspace must not
+ *               overlap on the GPU.
+ */
+typedef struct dlm_cap_params {
+    float tau_low;
+    float tau_high;
+    float gamma;
+    int32_t p_max;                   /* 1..256 */
+    int32_t high_tier_unconditional; /* 0 or 1 */
+} dlm_cap_params;
+
+size_t dlm_cap_workspace_size(int32_t batch, int32_t p_max);
+
+dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
+                          const int32_t* argmax, const float* conf, const float* lse,
+                          const uint8_t* masked, const int32_t* scope_len, int32_t batch,
+                          int32_t blk, const dlm_cap_params* params, uint8_t* selected,
+                          int32_t* n_selected, float* D_out, void* workspace, size_t ws_bytes,
+                          uint32_t* dev_status, dlm_stream_t stream);
+
+/*
+ * dlm_dapd_graph_mis -- DAPD: attention graph and Welsh-Powell selection.
+ *
+ * DAPD, "整体框架" and "关键设计 1-3".  V_t = masked positions of the block,
+ * r = |V_t| / blk.
+ *   r >= bulk_frac (fp32): a_ij = mean over the given layers and heads of
+ *       attention[i][j]; s_ij = (a_ij + a_ji)/2; edge (i,j) <=> s_ij > tau_edge;
+ *       d~_i = sum over j in V_t, j != i, of s_ij; key_i = d~_i * conf_i
+ *       (order_mode 1: d~_i); scan V_t by key descending (ties to the lower
+ *       position) keeping every node with no kept neighbour.
+ *   r <  bulk_frac: select masked positions with conf > bulk_conf; if none,
+ *       the highest-confidence masked one.
+ * The "last ~30% of layers" choice is the caller's: pass exactly the layers
+ * to average.  The per-pair sums are accumulated exactly in fixed point, so
+ * the edge test and the key order are exact decisions when every attention
+ * value is an f16 in [0, 256) and the sum over layers*heads of each entry
+ * stays below 512 (true for softmax rows with layers*heads <= 511); other
+ * inputs are summed with fp32-level accuracy.
+ *
+ * attn        : element (b, l, h, row, col) at
+ *               attn + b*stride_b + l*stride_l + h*stride_h + row*stride_row + col
+ *               (element strides); the block is rows and columns
+ *               [block_start, block_start + blk).  dtype F16, BF16 or F32;
+ *               the address of (b,l,h,block_start,block_start) and every
+ *               stride must be 16-byte aligned.  Only masked rows are read.
+ * masked, conf: [batch][blk].
+ * selected, n_selected : outputs as in dlm_select_threshold.
+ * s_out       : nullable float [batch][blk][blk]; s_ij for i, j in V_t.
+ * dtilde_out  : nullable float [batch][blk]; d~_i for i in V_t.
+ * deg_out     : nullable int32 [batch][blk]; number of tau-edges of i in V_t.
+ *               (The three are written only for sequences on the graph path;
+ *               other entries are left unchanged.)
+ * workspace   : device scratch, at least dlm_dapd_workspace_size(batch, blk)
+ *               bytes, 16-byte aligned; calls sharing it must not overlap.
+ */
+typedef struct dlm_dapd_params {
+    float tau_edge;
+    float bulk_conf;  /* 0.9 on the page */
+    float bulk_frac;  /* 0.5 on the page */
+    int32_t order_mode; /* 0: d~ * conf, 1: d~ */
+} dlm_dapd_params;
+
+size_t dlm_dapd_workspace_size(int32_t batch, int32_t blk);
+
+dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
+                              int32_t n_heads, int64_t stride_b, int64_t stride_l,
+                              int64_t stride_h, int64_t stride_row, int32_t block_start,
+                              int32_t blk, const uint8_t* masked, const float* conf,
+                              const dlm_dapd_params* params, uint8_t* selected,
+                              int32_t* n_selected, float* s_out, float* dtilde_out,
+                              int32_t* deg_out, void* workspace, size_t ws_bytes,
+                              uint32_t* dev_status, dlm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLM_H */

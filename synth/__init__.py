@@ -31,6 +31,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass, field, replace
 import math
+import os
 
 import numpy as np
 
@@ -106,7 +107,7 @@ CONFIGS: dict[str, Config] = {
         name="stress_bulk", batch=8, blk=256, vocab=126464, logit_dtype=BF16, sigma=2.0,
         boost_lo=4.0, boost_hi=12.0, boost_frac=0.6, prev_sigma=0.3,
         n_layers=10, n_heads=32, seq_len=1024, block_start=768, band=2, p_link=0.02,
-        masked_count=100, p_max=256),
+        masked_count=100, p_max=256, rules=("threshold", "cap", "dapd")),
 }
 
 # the pages' five workloads in order (the last one has two phases)
@@ -273,6 +274,14 @@ def make(cfg: Config | str, seed: int, attempts=None) -> Workload:
         attn = np.empty((B, cfg.n_layers, cfg.n_heads, blk, blk), at)
         links = np.empty((B, blk, blk), bool)
     w = Workload(cfg, seed, cur, prev, masked, attn, links, att)
-    for b in range(B):
-        w.replace_sequence(b, int(att[b]))
+    # sequences are independent streams: draw them on a few threads (numpy
+    # releases the GIL in its bulk kernels); the result does not depend on it
+    from concurrent.futures import ThreadPoolExecutor
+    workers = max(1, min(B, os.cpu_count() or 1, 16))
+    if workers == 1:
+        for b in range(B):
+            w.replace_sequence(b, int(att[b]))
+    else:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(lambda b: w.replace_sequence(b, int(att[b])), range(B)))
     return w

@@ -1,0 +1,113 @@
+"""The C-ABI library loads and exports every entry point declared in
+include/dlm.h; host-side argument checks return their status codes before
+anything touches a GPU (no device needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dlm.h")
+
+
+@pytest.fixture(scope="module")
+def libdlm():
+    from diffusion_decoding_token_gb300 import build
+    build.build()
+    import diffusion_decoding_token_gb300 as d
+    return d.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dlm_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
+              "dlm_dapd_graph_mis"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(libdlm):
+    for name in declared_functions():
+        assert hasattr(libdlm, name), f"{name} not exported"
+
+
+def test_status_strings_and_version(libdlm):
+    for code in range(6):
+        assert libdlm.dlm_status_string(code)
+    assert libdlm.dlm_version() >= 100
+
+
+def test_workspace_queries(libdlm):
+    assert libdlm.dlm_cap_workspace_size(64, 32) >= 64 * 32 * 4
+    assert libdlm.dlm_cap_workspace_size(1, 0) == 0
+    assert libdlm.dlm_cap_workspace_size(1, 257) == 0
+    assert libdlm.dlm_dapd_workspace_size(8, 256) >= 8 * 256 * 256 * 8
+    assert libdlm.dlm_dapd_workspace_size(1, 300) == 0
+
+
+INVALID, ALIGN, UNSUP, WS = 1, 2, 3, 4
+P = ctypes.c_void_p
+
+
+def test_row_stats_argument_errors(libdlm):
+    f = libdlm.dlm_row_stats
+    fake = P(0x10000)
+    outs = [fake] * 4
+    assert f(fake, None, 7, 4, 16, 16, None, *outs, None, None, None, None) == UNSUP
+    assert f(fake, None, 1, -1, 16, 16, None, *outs, None, None, None, None) == INVALID
+    assert f(fake, None, 1, 4, 0, 16, None, *outs, None, None, None, None) == INVALID
+    assert f(fake, None, 1, 4, 32, 16, None, *outs, None, None, None, None) == INVALID   # vocab > stride
+    assert f(None, None, 1, 4, 16, 16, None, *outs, None, None, None, None) == INVALID
+    assert f(fake, None, 1, 4, 16, 16, None, None, fake, fake, fake, None, None, None, None) == INVALID
+    assert f(P(0x10002), None, 1, 4, 16, 16, None, *outs, None, None, None, None) == ALIGN
+    assert f(fake, None, 1, 4, 12, 12, None, *outs, None, None, None, None) == ALIGN      # 24-byte rows
+    assert f(fake, P(0x10008), 1, 4, 16, 16, None, *outs, None, None, None, None) == ALIGN
+    assert f(fake, None, 1, 0, 16, 16, None, *outs, None, None, None, None) == 0           # empty: no launch
+
+
+def test_selection_argument_errors(libdlm):
+    fake = P(0x10000)
+    assert libdlm.dlm_select_threshold(fake, fake, 1, 0, ctypes.c_float(0.9), fake, fake, None) == INVALID
+    assert libdlm.dlm_select_threshold(fake, fake, 1, 257, ctypes.c_float(0.9), fake, fake, None) == INVALID
+    assert libdlm.dlm_select_threshold(None, fake, 1, 32, ctypes.c_float(0.9), fake, fake, None) == INVALID
+    assert libdlm.dlm_select_threshold(fake, fake, 0, 32, ctypes.c_float(0.9), fake, fake, None) == 0
+
+    from diffusion_decoding_token_gb300._binding import CapParams, DapdParams, DepcapParams
+    dp = DepcapParams(1.0, 8, 2, 0)  # even smoothing width
+    assert libdlm.dlm_depcap_boundary(fake, fake, 1, 32, None, ctypes.byref(dp), fake, None, None) == INVALID
+    dp = DepcapParams(1.0, 8, 1, 3)
+    assert libdlm.dlm_depcap_boundary(fake, fake, 1, 32, None, ctypes.byref(dp), fake, None, None) == INVALID
+    dp = DepcapParams(1.0, 8, 1, 0)
+    assert libdlm.dlm_depcap_boundary(fake, fake, 1, 2000, None, ctypes.byref(dp), fake, None, None) == INVALID
+
+    cp = CapParams(0.8, 0.95, -16.0, 32, 0)
+    args = (fake, 1, 100, 100, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
+    assert libdlm.dlm_cap_select(*args, None, 0, None, None) == WS
+    assert libdlm.dlm_cap_select(*args, fake, 16, None, None) == WS
+    assert libdlm.dlm_cap_select(*args, P(0x10004), 1 << 20, None, None) == ALIGN
+    cp = CapParams(0.8, 0.95, -16.0, 300, 0)
+    args = (fake, 1, 100, 100, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
+    assert libdlm.dlm_cap_select(*args, fake, 1 << 20, None, None) == INVALID
+
+    pp = DapdParams(0.01, 0.9, 0.5, 0)
+    base = (fake, 2, 2, 10, 32, 10 * 32 * 512 * 512, 32 * 512 * 512, 512 * 512, 512)
+    ok_tail = (fake, fake, ctypes.byref(pp), fake, fake, None, None, None)
+    assert libdlm.dlm_dapd_graph_mis(*base, 256, 32, *ok_tail, fake, 16, None, None) == WS
+    assert libdlm.dlm_dapd_graph_mis(*base, 255, 32, *ok_tail, fake, 1 << 30, None, None) == ALIGN
+    assert libdlm.dlm_dapd_graph_mis(*base, 256, 300, *ok_tail, fake, 1 << 30, None, None) == INVALID
+    pp = DapdParams(0.01, 0.9, 0.5, 2)
+    bad = (fake, fake, ctypes.byref(pp), fake, fake, None, None, None)
+    assert libdlm.dlm_dapd_graph_mis(*base, 256, 32, *bad, fake, 1 << 30, None, None) == INVALID
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import diffusion_decoding_token_gb300 as d
+    with pytest.raises(ValueError):
+        d.row_stats(torch.zeros(2, 8))

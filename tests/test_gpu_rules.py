@@ -1,0 +1,347 @@
+"""GPU parity of the four selection rules against the oracle (through the C ABI).
+
+Two levels:
+* unit parity -- each rule gets the SAME fp32 inputs on both sides (the
+  oracle's statistics rounded to fp32), so the decisions must agree bit for
+  bit: selections, counts, boundary lengths, pool order, degrees.  Float side
+  outputs (S_k, D_ij, s_ij, d~_i) agree within 1e-4 abs + 1e-4 rel.  DAPD's
+  graph is exact on f16 attention, so its unit parity needs no margin.
+* pipeline parity -- GPU statistics feed GPU rules, oracle statistics feed
+  oracle rules.  Sequences whose oracle decisions clear the margins of
+  ``parity.py`` must match exactly; the others must be valid results.
+Workloads are the pages' five (six with the late phase of the stress case) at
+full size, plus edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import (DeviceWorkload, boundary_margin_ok, cap_margin_ok, close, dapd_margin_ok, gpu_stats,
+                    greedy_valid, oracle_stats, threshold_margin_ok, to_torch)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dlm():
+    import diffusion_decoding_token_gb300 as d
+    d.lib()
+    return d
+
+
+_CACHE = {}
+
+
+def workload(name):
+    if name not in _CACHE:
+        w = synth.make(name, seed=1000 + synth.ORDER.index(name))
+        _CACHE.clear()
+        _CACHE[name] = (w, DeviceWorkload(w), oracle_stats(w))
+    return _CACHE[name]
+
+
+def f32(x):
+    return np.nan_to_num(np.asarray(x, np.float64), nan=0.0).astype(np.float32)
+
+
+def cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+# ------------------------------------------------------------------ unit
+def run_unit_threshold(dlm, cfg, w, o):
+    B, blk = cfg.batch, cfg.blk
+    c32 = f32(o["conf"]).reshape(B, blk)
+    gs, gn = dlm.select_threshold(cuda(c32), cuda(w.masked), cfg.tau)
+    os_, on = oracle.select_threshold(c32.astype(np.float64), w.masked, cfg.tau)
+    np.testing.assert_array_equal(gs.cpu().numpy(), os_)
+    np.testing.assert_array_equal(gn.cpu().numpy(), on)
+
+
+def run_unit_boundary(dlm, cfg, w, o):
+    B, blk = cfg.batch, cfg.blk
+    kl32, en32 = f32(o["kl"]).reshape(B, blk), f32(o["entropy"]).reshape(B, blk)
+    gl, gsc = dlm.depcap_boundary(cuda(kl32), cuda(en32), cfg.lam, cfg.L_min)
+    ol, osc = oracle.depcap_boundary(kl32.astype(np.float64), en32.astype(np.float64), cfg.lam, cfg.L_min)
+    assert close(gsc.cpu().numpy(), osc).all()
+    gl = gl.cpu().numpy()
+    for b in range(B):
+        if boundary_margin_ok(osc[b]):
+            assert gl[b] == ol[b]
+        else:
+            assert min(cfg.L_min, blk) <= gl[b] <= blk
+
+
+def run_unit_cap(dlm, cfg, w, dw, o, scope=None):
+    B, blk = cfg.batch, cfg.blk
+    am = np.nan_to_num(o["argmax"]).astype(np.int32).reshape(B, blk)
+    am[am < 0] = 0
+    c32, l32 = f32(o["conf"]).reshape(B, blk), f32(o["lse"]).reshape(B, blk)
+    D = torch.full((B, blk, blk), float("nan"), device="cuda")
+    st = dlm.new_status()
+    gs, gn = dlm.cap_select(dw.cur, cuda(am), cuda(c32), cuda(l32), dw.masked, cfg.tau_low, cfg.tau_high,
+                            cfg.gamma, cfg.p_max, scope_len=None if scope is None else cuda(scope), D_out=D,
+                            status=st)
+    code = None if cfg.logit_dtype == synth.F32 else cfg.logit_dtype
+    r = oracle.cap_select(w.cur, am, c32.astype(np.float64), l32.astype(np.float64), w.masked, cfg.tau_low,
+                          cfg.tau_high, cfg.gamma, cfg.p_max, scope_len=scope, dtype=code)
+    gs, gn, D = gs.cpu().numpy(), gn.cpu().numpy(), D.cpu().numpy()
+    for b in range(B):
+        pn = r["pool_n"][b]
+        pool = r["pool"][b][:pn]
+        if pn:
+            Dg = D[b][np.ix_(pool, pool)]
+            Do = r["D"][b][np.ix_(pool, pool)]
+            off = ~np.eye(pn, dtype=bool)
+            assert close(Dg[off], Do[off]).all()
+        sc = blk if scope is None else int(scope[b])
+        if cap_margin_ok(cfg, c32[b].astype(np.float64), w.masked[b], r["D"][b], r["pool"][b], pn, sc):
+            np.testing.assert_array_equal(gs[b], r["selected"][b])
+            assert gn[b] == r["n_selected"][b]
+        else:
+            adj = (D[b] > np.float32(cfg.gamma))
+            sel = set(np.nonzero(gs[b])[0].tolist())
+            if pn:
+                assert greedy_valid(adj, sel, c32[b], list(pool), 1e-6)
+    assert bool(int(st.item()) & dlm.DEV_POOL_CLIPPED) == r["clipped"]
+
+
+def run_unit_dapd(dlm, cfg, w, dw, o, order_mode=0):
+    B, blk = cfg.batch, cfg.blk
+    c32 = f32(o["conf"]).reshape(B, blk)
+    s = torch.full((B, blk, blk), float("nan"), device="cuda")
+    dt = torch.full((B, blk), float("nan"), device="cuda")
+    deg = torch.full((B, blk), -1, dtype=torch.int32, device="cuda")
+    gs, gn = dlm.dapd_graph_mis(dw.attn, dw.masked, cuda(c32), cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac,
+                                order_mode, dw.block_start, s_out=s, dtilde_out=dt, deg_out=deg)
+    code = None if cfg.attn_dtype == synth.F32 else cfg.attn_dtype
+    r = oracle.dapd(w.attn, w.masked, c32.astype(np.float64), cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac,
+                    order_mode, dtype=code)
+    gs, gn, s, dt, deg = (t.cpu().numpy() for t in (gs, gn, s, dt, deg))
+    exact_arith = cfg.attn_dtype == synth.F16
+    for b in range(B):
+        m = w.masked[b].astype(bool)
+        if r["path"][b] == 0:
+            nodes = np.nonzero(m)[0]
+            assert close(s[b][np.ix_(nodes, nodes)], r["s"][b][np.ix_(nodes, nodes)]).all()
+            assert close(dt[b][nodes], r["dtilde"][b][nodes]).all()
+            np.testing.assert_array_equal(deg[b][nodes], r["deg"][b][nodes])
+        tol = 1e-12 if exact_arith else 1e-5
+        if dapd_margin_ok(cfg, c32[b].astype(np.float64), w.masked[b], r["s"][b], r["dtilde"][b], order_mode, tol):
+            np.testing.assert_array_equal(gs[b], r["selected"][b])
+            assert gn[b] == r["n_selected"][b]
+        else:
+            assert not exact_arith, "exact DAPD arithmetic must not need a margin"
+
+
+@pytest.mark.parametrize("name", synth.ORDER)
+def test_unit_rules(dlm, name):
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    if "threshold" in cfg.rules:
+        run_unit_threshold(dlm, cfg, w, o)
+    scope = None
+    if "boundary" in cfg.rules:
+        run_unit_boundary(dlm, cfg, w, o)
+        if name == "depcap_window":
+            kl32, en32 = f32(o["kl"]).reshape(1, -1), f32(o["entropy"]).reshape(1, -1)
+            scope, _ = oracle.depcap_boundary(kl32.astype(np.float64), en32.astype(np.float64), cfg.lam,
+                                              cfg.L_min)
+    if "cap" in cfg.rules:
+        run_unit_cap(dlm, cfg, w, dw, o, scope)
+    if "dapd" in cfg.rules:
+        run_unit_dapd(dlm, cfg, w, dw, o)
+        run_unit_dapd(dlm, cfg, w, dw, o, order_mode=1)
+
+
+# -------------------------------------------------------------- pipeline
+@pytest.mark.parametrize("name", synth.ORDER)
+def test_pipeline(dlm, name):
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    B, blk = cfg.batch, cfg.blk
+    st = dlm.new_status()
+    g = gpu_stats(dw, status=st)
+    gconf, glse = g.conf.view(B, blk), g.lse.view(B, blk)
+    oconf = o["conf"].reshape(B, blk)
+    exact = valid = 0
+    if "threshold" in cfg.rules:
+        gs, _ = dlm.select_threshold(gconf, dw.masked, cfg.tau)
+        os_, _ = oracle.select_threshold(oconf, w.masked, cfg.tau)
+        gs = gs.cpu().numpy()
+        for b in range(B):
+            if threshold_margin_ok(oconf[b], w.masked[b], cfg.tau):
+                np.testing.assert_array_equal(gs[b], os_[b])
+                exact += 1
+            else:
+                valid += 1
+    scope_g = scope_o = None
+    if "boundary" in cfg.rules:
+        gl, _ = dlm.depcap_boundary(g.kl.view(B, blk), g.entropy.view(B, blk), cfg.lam, cfg.L_min)
+        ol, osc = oracle.depcap_boundary(o["kl"].reshape(B, blk), o["entropy"].reshape(B, blk), cfg.lam, cfg.L_min)
+        gl_np = gl.cpu().numpy()
+        for b in range(B):
+            if boundary_margin_ok(osc[b]):
+                assert gl_np[b] == ol[b]
+                exact += 1
+            else:
+                valid += 1
+        if name == "depcap_window":
+            scope_g, scope_o = gl, ol
+    if "cap" in cfg.rules:
+        gs, _ = dlm.cap_select(dw.cur, g.argmax.view(B, blk), gconf, glse, dw.masked, cfg.tau_low, cfg.tau_high,
+                               cfg.gamma, cfg.p_max, scope_len=scope_g)
+        code = None if cfg.logit_dtype == synth.F32 else cfg.logit_dtype
+        am = np.where(o["argmax"] < 0, 0, o["argmax"]).reshape(B, blk)
+        r = oracle.cap_select(w.cur, am, oconf, o["lse"].reshape(B, blk), w.masked, cfg.tau_low, cfg.tau_high,
+                              cfg.gamma, cfg.p_max, scope_len=scope_o, dtype=code)
+        gs = gs.cpu().numpy()
+        for b in range(B):
+            sc = blk if scope_o is None else int(scope_o[b])
+            if cap_margin_ok(cfg, oconf[b], w.masked[b], r["D"][b], r["pool"][b], r["pool_n"][b], sc):
+                np.testing.assert_array_equal(gs[b], r["selected"][b])
+                exact += 1
+            else:
+                pool = list(r["pool"][b][:r["pool_n"][b]])
+                adj = np.nan_to_num(r["D"][b], nan=-np.inf) > cfg.gamma
+                assert not pool or greedy_valid(adj, set(np.nonzero(gs[b])[0].tolist()), oconf[b], pool, 1e-4)
+                valid += 1
+    if "dapd" in cfg.rules:
+        gs, _ = dlm.dapd_graph_mis(dw.attn, dw.masked, gconf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0,
+                                   dw.block_start)
+        code = None if cfg.attn_dtype == synth.F32 else cfg.attn_dtype
+        r = oracle.dapd(w.attn, w.masked, oconf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0, dtype=code)
+        gs = gs.cpu().numpy()
+        for b in range(B):
+            if dapd_margin_ok(cfg, oconf[b], w.masked[b], r["s"][b], r["dtilde"][b]):
+                np.testing.assert_array_equal(gs[b], r["selected"][b])
+                exact += 1
+            else:
+                nodes = np.nonzero(w.masked[b])[0]
+                if r["path"][b] == 0:
+                    S = r["s"][b][np.ix_(nodes, nodes)]
+                    adj = (S > cfg.tau_edge) & ~np.eye(len(nodes), dtype=bool)
+                    key = r["dtilde"][b][nodes] * oconf[b][nodes]
+                    loc = {int(v): k for k, v in enumerate(nodes)}
+                    sel = {loc[int(v)] for v in np.nonzero(gs[b])[0]}
+                    assert greedy_valid(adj, sel, key, range(len(nodes)), 1e-4)
+                valid += 1
+    assert int(st.item()) == 0
+    print(f"{name}: {exact} exact, {valid} validity-checked decisions")
+    assert exact >= 3 * valid
+
+
+# ------------------------------------------------------------- edge cases
+def test_threshold_edges(dlm):
+    conf = np.array([[0.3, 0.5, 0.5, 0.1], [0.95, 0.2, 0.99, 0.3], [0.91, 0.2, 0.1, 0.95]], np.float32)
+    masked = np.array([[1, 1, 1, 1], [0, 0, 0, 0], [1, 0, 0, 0]], np.uint8)
+    gs, gn = dlm.select_threshold(cuda(conf), cuda(masked), 0.9)
+    os_, on = oracle.select_threshold(conf.astype(np.float64), masked, 0.9)
+    np.testing.assert_array_equal(gs.cpu().numpy(), os_)
+    np.testing.assert_array_equal(gn.cpu().numpy(), on)
+    assert gn.cpu().tolist() == [1, 0, 1]
+
+
+@pytest.mark.parametrize("blk", [1, 5, 256])
+def test_threshold_random_sizes(dlm, blk):
+    rng = np.random.default_rng(blk)
+    conf = rng.random((33, blk)).astype(np.float32)
+    masked = (rng.random((33, blk)) < 0.6).astype(np.uint8)
+    gs, gn = dlm.select_threshold(cuda(conf), cuda(masked), 0.9)
+    os_, on = oracle.select_threshold(conf.astype(np.float64), masked, 0.9)
+    np.testing.assert_array_equal(gs.cpu().numpy(), os_)
+    np.testing.assert_array_equal(gn.cpu().numpy(), on)
+
+
+@pytest.mark.parametrize("w_,mode", [(1, 0), (3, 0), (5, 1), (1, 2), (7, 2)])
+def test_boundary_modes(dlm, w_, mode):
+    rng = np.random.default_rng(w_ * 10 + mode)
+    B, L = 17, 77
+    I = rng.gamma(1.0, 1.0, (B, L)).astype(np.float32)
+    H = rng.gamma(1.0, 1.0, (B, L)).astype(np.float32)
+    cold = (rng.random(B) < 0.2).astype(np.uint8)
+    gl, gsc = dlm.depcap_boundary(cuda(I), cuda(H), 1.2, 8, w_, mode, cold_start=cuda(cold))
+    ol, osc = oracle.depcap_boundary(I.astype(np.float64), H.astype(np.float64), 1.2, 8, w_, mode, cold)
+    assert close(gsc.cpu().numpy(), osc).all()
+    gl = gl.cpu().numpy()
+    for b in range(B):
+        if cold[b] or boundary_margin_ok(osc[b]):
+            assert gl[b] == ol[b]
+
+
+def test_cap_edges(dlm):
+    """Pool clipping, an empty pool, scope limits, the unconditional tier and
+    a ragged block, on a tiny fp32 case."""
+    rng = np.random.default_rng(21)
+    B, blk, V = 4, 37, 300
+    z = (rng.standard_normal((B * blk, V)) * 1.0).astype(np.float32)
+    tok = rng.integers(0, V, B * blk)
+    for r in range(B * blk):
+        if r % 5:
+            z[r, tok[r]] = 10 + rng.uniform(0, 4)
+    for r in range(0, B * blk - 1, 3):
+        z[r, tok[r + 1]] = z[r, tok[r]] - 3
+        z[r + 1, tok[r]] = z[r + 1, tok[r + 1]] - 3
+    z[blk:2 * blk, :] = rng.standard_normal((blk, V)).astype(np.float32)  # sequence 1: no candidate
+    o = oracle.row_stats(z)
+    masked = (rng.random((B, blk)) < 0.9).astype(np.uint8)
+    scope = np.array([blk, blk, 11, 0], np.int32)
+    am = o["argmax"].reshape(B, blk)
+    c32, l32 = f32(o["conf"]).reshape(B, blk), f32(o["lse"]).reshape(B, blk)
+    for p_max, htu in [(8, False), (37, False), (37, True)]:
+        st = dlm.new_status()
+        gs, gn = dlm.cap_select(cuda(z), cuda(am), cuda(c32), cuda(l32), cuda(masked), 0.8, 0.95, -16.0, p_max,
+                                high_tier_unconditional=htu, scope_len=cuda(scope), status=st)
+        r = oracle.cap_select(z, am, c32.astype(np.float64), l32.astype(np.float64), masked, 0.8, 0.95, -16.0,
+                              p_max, high_tier_unconditional=htu, scope_len=scope)
+        np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+        np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+        assert bool(int(st.item()) & dlm.DEV_POOL_CLIPPED) == r["clipped"]
+
+
+@pytest.mark.parametrize("blk,M", [(30, 30), (30, 15), (30, 14), (256, 256), (9, 9), (64, 40)])
+def test_dapd_edges(dlm, blk, M):
+    """Ragged block (partial last vector), the 50% switch on both sides,
+    the maximum block, and the page's 9-node MRF size."""
+    rng = np.random.default_rng(blk * 100 + M)
+    B, L, H = 3, 2, 3
+    N = (blk + 24 + 7) // 8 * 8   # 16-byte aligned f16 rows
+    bs = 8
+    sub = rng.random((B, L, H, blk, blk)) ** 6 * 0.3
+    sub = (sub / (sub.sum(-1, keepdims=True) + 1.0)).astype(np.float32)
+    sub16 = synth.to_f16_bits(sub)
+    full = torch.zeros((B, L, H, N, N), dtype=torch.float16, device="cuda")
+    full[:, :, :, bs:bs + blk, bs:bs + blk] = to_torch(sub16, synth.F16, "cuda")
+    masked = np.zeros((B, blk), np.uint8)
+    for b in range(B):
+        masked[b, rng.choice(blk, M, replace=False)] = 1
+    conf = rng.random((B, blk)).astype(np.float32)
+    tau = 0.02
+    for om in (0, 1):
+        s = torch.full((B, blk, blk), float("nan"), device="cuda")
+        deg = torch.full((B, blk), -1, dtype=torch.int32, device="cuda")
+        gs, gn = dlm.dapd_graph_mis(full, cuda(masked), cuda(conf), tau, 0.9, 0.5, om, bs, s_out=s, deg_out=deg)
+        r = oracle.dapd(sub16, masked, conf.astype(np.float64), tau, 0.9, 0.5, om, dtype=synth.F16)
+        np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+        np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+        for b in range(B):
+            if r["path"][b] == 0:
+                nodes = np.nonzero(masked[b])[0]
+                np.testing.assert_array_equal(deg.cpu().numpy()[b][nodes], r["deg"][b][nodes])
+
+
+def test_dapd_key_ties_break_to_lower_position(dlm):
+    """Equal keys (identical rows and confidences) order by position."""
+    blk = 16
+    A = np.full((blk, blk), 0.001, np.float32)
+    for i in range(0, blk - 1, 2):
+        A[i, i + 1] = A[i + 1, i] = 0.25
+    sub16 = synth.to_f16_bits(A[None, None, None])
+    conf = np.full((1, blk), 0.5, np.float32)
+    masked = np.ones((1, blk), np.uint8)
+    gs, _ = dlm.dapd_graph_mis(to_torch(sub16, synth.F16, "cuda"), cuda(masked), cuda(conf), 0.1)
+    r = oracle.dapd(sub16, masked, conf.astype(np.float64), 0.1, dtype=synth.F16)
+    np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+    assert np.nonzero(r["selected"][0])[0].tolist() == list(range(0, blk, 2))
