@@ -143,6 +143,25 @@ class ClockSampler:
                 "samples": len(sm), "window": used}
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The maximum of a per-rank scalar over all ranks (identity at N=1).
+    Only a timing scalar crosses ranks: the decision path has no collective."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as td
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(decisions_per_rank_step: int, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job decisions/s: every rank decides its own batch each step
+    (weak scaling), timed by the slowest rank."""
+    return decisions_per_rank_step * world * steps / (max_ms / 1000.0)
+
+
 # ------------------------------------------------------------------ native
 def run_native(args, rank, world, local):
     import torch
@@ -358,15 +377,10 @@ def main():
     import torch
     r = run_native(args, rank, world, local)
     cfg = r["cfg"]
-    total_ms = r["total_ms"]
-    if world > 1:
-        t = torch.tensor([total_ms], device=f"cuda:{local}")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(r["total_ms"], world, f"cuda:{local}")
     if rank != 0:
         return
-    decisions = cfg.batch * cfg.blk * world * args.steps
-    value = decisions / (total_ms / 1000.0)
+    value = job_throughput(cfg.batch * cfg.blk, world, args.steps, total_ms)
     ms_step = total_ms / args.steps
     k1_ms = statistics.mean(r["k1"])
     k1_bytes = 2 * cfg.batch * cfg.blk * cfg.vocab * 2  # cur + prev bf16 rows

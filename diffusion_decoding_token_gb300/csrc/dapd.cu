@@ -35,7 +35,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kMaxWords = DLM_MAX_BLK / 32;
-constexpr int kSliceUnroll = 4;
+constexpr int kSliceUnroll = 8;
 
 __device__ __forceinline__ bool late_phase(const DapdArgs& a, int b, int* count_out) {
     const bool m = threadIdx.x < (unsigned)a.blk && a.masked[(int64_t)b * a.blk + threadIdx.x] != 0;
@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     constexpr int ESZ = AFmt<DT>::ESZ;
     constexpr int NP = EPV / 2;
     // per thread: NP pairs of (H, L) -> 2*EPV floats
-    __shared__ float s_red[kThreads * 2 * EPV];
+    __shared__ __align__(16) float s_red[kThreads * 2 * EPV];
     __shared__ int s_rows[kThreads];
     __shared__ int s_nm;
 
@@ -123,11 +123,23 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     if (late_phase(a, b, nullptr)) return;  // the whole cluster takes the same branch
 
     const int r0 = tile * a.row_tile, r1 = min(a.blk, r0 + a.row_tile);
-    if (threadIdx.x == 0) {
-        int nm = 0;
-        for (int r = r0; r < r1; ++r)
-            if (a.masked[(int64_t)b * a.blk + r]) s_rows[nm++] = r;
-        s_nm = nm;
+    {
+        // compact the masked rows of the tile, in order (ballot prefix sums)
+        __shared__ int s_wcount[kThreads / 32];
+        const int r = r0 + (int)threadIdx.x;
+        const bool mr = r < r1 && a.masked[(int64_t)b * a.blk + r] != 0;
+        const unsigned bal = __ballot_sync(DLM_FULL_MASK, mr);
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        if (lane == 0) s_wcount[wid] = __popc(bal);
+        __syncthreads();
+        int off = 0;
+        for (int k = 0; k < wid; ++k) off += s_wcount[k];
+        if (mr) s_rows[off + __popc(bal & ((1u << lane) - 1u))] = r;
+        if (threadIdx.x == 0) {
+            int tot = 0;
+            for (int k = 0; k < kThreads / 32; ++k) tot += s_wcount[k];
+            s_nm = tot;
+        }
     }
     __syncthreads();
     const int nm = s_nm;
@@ -153,16 +165,31 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     if (active) {
         const char* base = static_cast<const char*>(a.attn) +
                            ((int64_t)b * a.sb + (int64_t)(a.block_start + row) * a.sr + a.block_start + col0) * ESZ;
-        auto addr = [&](int s) {
-            const int l = s / a.n_heads, h = s - l * a.n_heads;
-            return base + ((int64_t)l * a.sl + (int64_t)h * a.sh) * ESZ;
-        };
+        // walk the (layer, head) slices s0+grp, s0+grp+G2, ... with running
+        // element offsets instead of a division per load
+        const int nh = a.n_heads;
         int s = s0 + grp;
+        int h = s % nh;
+        int64_t off = (int64_t)(s / nh) * a.sl + (int64_t)h * a.sh;
+        const int dh = G2 % nh;
+        const int64_t doff = (int64_t)(G2 / nh) * a.sl + (int64_t)dh * a.sh;
+        const int64_t wrap = a.sl - (int64_t)nh * a.sh;
+        auto next = [&]() {
+            off += doff;
+            h += dh;
+            if (h >= nh) {
+                h -= nh;
+                off += wrap;
+            }
+        };
         if (full) {
             for (; s + (kSliceUnroll - 1) * G2 < s1; s += kSliceUnroll * G2) {
                 uint4 w[kSliceUnroll];
 #pragma unroll
-                for (int u = 0; u < kSliceUnroll; ++u) w[u] = ld_nc(addr(s + u * G2));
+                for (int u = 0; u < kSliceUnroll; ++u) {
+                    w[u] = ld_nc(base + off * ESZ);
+                    next();
+                }
 #pragma unroll
                 for (int u = 0; u < kSliceUnroll; ++u) {
                     f2 x[NP];
@@ -172,13 +199,15 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
             }
             for (; s < s1; s += G2) {
                 f2 x[NP];
-                AFmt<DT>::to_f2(ld_nc(addr(s)), x);
+                AFmt<DT>::to_f2(ld_nc(base + off * ESZ), x);
+                next();
                 split_acc<NP>(x, H, L);
             }
         } else {
             // ragged last vector of the row: element loads of the valid columns
             for (; s < s1; s += G2) {
-                const char* p = addr(s);
+                const char* p = base + off * ESZ;
+                next();
                 float v[EPV];
 #pragma unroll
                 for (int k = 0; k < EPV; ++k) v[k] = (col0 + k < a.blk) ? AFmt<DT>::scalar(p + k * ESZ) : 0.f;
@@ -190,7 +219,9 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
         }
     }
 
-    // merge the slice groups of this CTA in group order
+    // merge the slice groups of this CTA in group order, then the CTAs of the
+    // cluster in rank order; partial sums are gathered into registers first so
+    // the remote loads of one rank are all in flight together
     float* mine = s_red + (size_t)t * 2 * EPV;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
@@ -198,26 +229,48 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
         unpack2(L[p], mine[4 * p + 2], mine[4 * p + 3]);
     }
     __syncthreads();
+    float acc[2 * EPV];
+#pragma unroll
+    for (int k = 0; k < 2 * EPV; ++k) acc[k] = mine[k];
     if (active && grp == 0) {
         for (int gg = 1; gg < G2; ++gg) {
-            const float* o = s_red + (size_t)(gg * Q + slot) * 2 * EPV;
+            const float4* o = reinterpret_cast<const float4*>(s_red + (size_t)(gg * Q + slot) * 2 * EPV);
+            float4 v[EPV / 2];
 #pragma unroll
-            for (int k = 0; k < 2 * EPV; ++k) mine[k] += o[k];
+            for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
+#pragma unroll
+            for (int k = 0; k < EPV / 2; ++k) {
+                acc[4 * k + 0] += v[k].x;
+                acc[4 * k + 1] += v[k].y;
+                acc[4 * k + 2] += v[k].z;
+                acc[4 * k + 3] += v[k].w;
+            }
         }
     }
     if (split > 1) {
         cg::cluster_group cluster = cg::this_cluster();
+        __syncthreads();
+        if (active && grp == 0) {
+#pragma unroll
+            for (int k = 0; k < 2 * EPV; ++k) mine[k] = acc[k];
+        }
         cluster.sync();
         if (g == 0 && active && grp == 0) {
             for (int rr = 1; rr < split; ++rr) {
-                const float* o = cluster.map_shared_rank(mine, rr);
+                const float4* o = reinterpret_cast<const float4*>(cluster.map_shared_rank(mine, rr));
+                float4 v[EPV / 2];
 #pragma unroll
-                for (int k = 0; k < 2 * EPV; ++k) mine[k] += o[k];
+                for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
+#pragma unroll
+                for (int k = 0; k < EPV / 2; ++k) {
+                    acc[4 * k + 0] += v[k].x;
+                    acc[4 * k + 1] += v[k].y;
+                    acc[4 * k + 2] += v[k].z;
+                    acc[4 * k + 3] += v[k].w;
+                }
             }
         }
         cluster.sync();
-    } else {
-        __syncthreads();
     }
     if (g != 0 || !active || grp != 0) return;
     long long* A = a.A + ((int64_t)b * a.blk + row) * a.blk;
@@ -227,7 +280,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
         for (int k = 0; k < 2; ++k) {
             const int col = col0 + 2 * p + k;
             if (col < a.blk) {
-                const float hi = mine[4 * p + k], lo = mine[4 * p + 2 + k];
+                const float hi = acc[4 * p + k], lo = acc[4 * p + 2 + k];
                 A[col] = __float2ll_rn(hi * 32768.f) * 131072LL + __float2ll_rn(lo * 4294967296.f);
             }
         }

@@ -12,7 +12,8 @@
 //  * each thread keeps an online softmax state relative to a lazily moved
 //    reference (moved only when a value exceeds it by more than kRebase, so
 //    the common path has no rescale), in base-2 units so every element costs
-//    one FMA and one ex2 on the SFU; the arithmetic is done on packed f32x2;
+//    a subtract, a multiply and one ex2 on the SFU; the arithmetic is done on
+//    packed f32x2;
 //  * the exact maximum is tracked per 8-element vector and the argmax position
 //    is recovered at the end by re-reading the winning vector, ties to the
 //    lowest index everywhere;
@@ -197,9 +198,9 @@ struct Acc {
     float mx;
     int bv;     // vector holding mx (first), or -1 when it came from the tail
     int bidx;   // position when it came from the tail
-    float ref, refL;
+    float ref;
     f2 S, T, K;
-    float refp, refpL;
+    float refp;
     f2 Sp;
 };
 
@@ -211,7 +212,6 @@ __device__ __forceinline__ void rebase(Acc& a, float nref) {
     a.S = mul2(al2, a.S);
     a.K = mul2(al2, a.K);
     a.ref = nref;
-    a.refL = nref * kLog2e;
 }
 
 __device__ __forceinline__ void rebase_p(Acc& a, float nref) {
@@ -219,26 +219,27 @@ __device__ __forceinline__ void rebase_p(Acc& a, float nref) {
     float al = ex2(d);
     a.Sp = mul2(pack2(al, al), a.Sp);
     a.refp = nref;
-    a.refpL = nref * kLog2e;
 }
 
 template <int NP, bool PREV>
 __device__ __forceinline__ void accum(Acc& a, const f2 (&z)[NP], const f2 (&zp)[NP]) {
+    // x = (z - r) log2 e: the subtraction is exact for nearby values, so x
+    // carries one rounding whatever the magnitude of r
     const f2 l2e = pack2(kLog2e, kLog2e);
-    const f2 nr = pack2(-a.refL, -a.refL);
+    const f2 r = pack2(a.ref, a.ref);
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        f2 x = fma2(z[p], l2e, nr);
+        f2 x = mul2(sub2(z[p], r), l2e);
         f2 e = ex2x2(x);
         a.S = add2(a.S, e);
         a.T = fma2(e, x, a.T);
         if (PREV) a.K = fma2(e, sub2(z[p], zp[p]), a.K);
     }
     if (PREV) {
-        const f2 nrp = pack2(-a.refpL, -a.refpL);
+        const f2 rp = pack2(a.refp, a.refp);
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-            f2 x = fma2(zp[p], l2e, nrp);
+            f2 x = mul2(sub2(zp[p], rp), l2e);
             a.Sp = add2(a.Sp, ex2x2(x));
         }
     }
@@ -270,13 +271,13 @@ __device__ __forceinline__ void process_scalar(Acc& a, float z, float zp, int po
     if (z > a.ref + kRebase) rebase(a, z);
     if (PREV && zp > a.refp + kRebase) rebase_p(a, zp);
     // scalar form of accum (keeps the pair layout: only the low lane is used)
-    float x = fmaf(z, kLog2e, -a.refL);
+    float x = (z - a.ref) * kLog2e;
     float e = ex2(x);
     a.S = add2(a.S, pack2(e, 0.f));
     a.T = fma2(pack2(e, 0.f), pack2(x, 0.f), a.T);
     if (PREV) {
         a.K = fma2(pack2(e, 0.f), pack2(z - zp, 0.f), a.K);
-        float xp = fmaf(zp, kLog2e, -a.refpL);
+        float xp = (zp - a.refp) * kLog2e;
         a.Sp = add2(a.Sp, pack2(ex2(xp), 0.f));
     }
 }
@@ -308,10 +309,8 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) 
     a.bv = -1;
     a.bidx = 0x7fffffff;
     a.ref = -FLT_MAX;
-    a.refL = -FLT_MAX;
     a.S = a.T = a.K = pack2(0.f, 0.f);
     a.refp = -FLT_MAX;
-    a.refpL = -FLT_MAX;
     a.Sp = pack2(0.f, 0.f);
 
     int v = v0 + threadIdx.x;
