@@ -199,6 +199,38 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
                           uint32_t* dev_status, dlm_stream_t stream);
 
 /*
+ * dlm_cap_select_noalloc -- dlm_cap_select for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call: it is a deployment variant of
+ * dlm_cap_select.  Some callers cannot call cudaMalloc (a serving runtime whose
+ * allocator reserved all device memory up front, a plug-in inside a framework
+ * that owns every allocation, a decode loop that cannot afford cudaMalloc's
+ * implicit synchronisation), so they cannot pass the CAP workspace.  This call
+ * takes the same arguments as dlm_cap_select minus the workspace, computes the
+ * same results, and keeps its scratch in an array inside libdlm.
+ *
+ * Limit: the scratch holds DLM_CAP_NOALLOC_MAX_BYTES (1 MiB); a call whose
+ * dlm_cap_workspace_size(batch, params->p_max) is larger returns
+ * DLM_ERR_WORKSPACE (e.g. batch 64 with p_max 256 fits, batch 128 does not).
+ * The array exists on every GPU that loads the library until the process
+ * exits.  The first call on a device looks up the array's device address with
+ * that device current (an internal runtime query); make that first call before
+ * any stream capture.  Every call shares the one array and leaves its contents
+ * behind: calls that can overlap on the GPU (other streams, other host threads)
+ * race on it and must be ordered by the caller.  The kernels rewrite every
+ * scratch entry they read, so nothing needs clearing between calls.  No
+ * cudaMalloc, cudaFree or allocating routine is called.
+ */
+#define DLM_CAP_NOALLOC_MAX_BYTES (1u << 20)
+
+dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
+                                  const int32_t* argmax, const float* conf, const float* lse,
+                                  const uint8_t* masked, const int32_t* scope_len, int32_t batch,
+                                  int32_t blk, const dlm_cap_params* params, uint8_t* selected,
+                                  int32_t* n_selected, float* D_out, uint32_t* dev_status,
+                                  dlm_stream_t stream);
+
+/*
  * dlm_dapd_graph_mis -- DAPD: attention graph and Welsh-Powell selection.
  *
  * DAPD, "整体框架" and "关键设计 1-3".  V_t = masked positions of the block,
