@@ -34,7 +34,6 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "masked-position decisions/sec per decode step; logit-read GB/s vs HBM peak"
-WORKLOAD = "batched"
 
 
 def parse():
@@ -46,6 +45,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=1004)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--workload", default="batched",
+                    help="batched (default, the headline), tiny, llada_step, depcap_window, stress_graph, stress_bulk")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
     ap.add_argument("--compact-attn", action="store_true",
                     help="hold only the attention block [B, L, H, blk, blk] on the device (small profiling cases)")
@@ -60,9 +61,31 @@ def dist_env():
 
 
 def workload_desc(cfg):
-    return (f"batched serving: B={cfg.batch} sequences x {cfg.blk} masked positions, V={cfg.vocab} bf16 "
-            f"current+previous logits, fp16 attention {cfg.n_layers}x{cfg.n_heads} over {cfg.seq_len} "
-            f"positions; all four rules per sequence")
+    dt = {0: "f32", 1: "bf16", 2: "f16"}
+    m = cfg.blk if cfg.masked_count < 0 else cfg.masked_count
+    att = (f", {dt[cfg.attn_dtype]} attention {cfg.n_layers}x{cfg.n_heads} over {cfg.seq_len} positions"
+           if cfg.n_layers else "")
+    return (f"{cfg.name}: B={cfg.batch} sequences x {m} masked of {cfg.blk} positions, V={cfg.vocab} "
+            f"{dt[cfg.logit_dtype]} current+previous logits{att}; rules: {', '.join(cfg.rules)}")
+
+
+def recorded_traffic():
+    """DRAM bytes per row-pass launch from the committed ncu summary, valid
+    only while the kernel source still matches the one that was profiled."""
+    import hashlib
+    summary = os.path.join(ROOT, "profiles", "row_stats_batched.md")
+    src = os.path.join(ROOT, "diffusion_decoding_token_gb300", "csrc", "row_stats.cu")
+    if not (os.path.exists(summary) and os.path.exists(src)):
+        return None
+    kv = {}
+    for line in open(summary):
+        if ":" in line and line.split(":")[0].strip() in ("traffic_bytes_per_launch", "kernel_source_sha256_16"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if kv.get("kernel_source_sha256_16") != h or "traffic_bytes_per_launch" not in kv:
+        return None
+    return int(kv["traffic_bytes_per_launch"])
 
 
 def load_peaks():
@@ -171,31 +194,39 @@ def run_native(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = synth.CONFIGS[WORKLOAD]
+    cfg = synth.CONFIGS[args.workload]
     if args.batch:
         cfg = synth.scaled(cfg, batch=args.batch)
     B, blk, V = cfg.batch, cfg.blk, cfg.vocab
     w = synth.make(cfg, seed=args.seed + 100 * rank)
+    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}
 
-    def dev16(a, dt):
-        return torch.from_numpy(a.view(np.int16)).to(dev).view(dt)
+    def dev_of(a, code):
+        if code == synth.F32:
+            return torch.from_numpy(a).to(dev)
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(tdt[code])
 
-    cur = dev16(w.cur, torch.bfloat16)
-    prev = dev16(w.prev, torch.bfloat16)
+    cur = dev_of(w.cur, cfg.logit_dtype)
+    prev = dev_of(w.prev, cfg.logit_dtype)
     masked = torch.from_numpy(w.masked).to(dev)
+    row_index = None
+    if cfg.masked_count >= 0:
+        row_index = torch.from_numpy(np.nonzero(w.masked.reshape(-1))[0].astype(np.int32)).to(dev)
     N, bs = cfg.seq_len, cfg.block_start
-    if args.compact_attn:
-        attn, bs = dev16(w.attn, torch.float16), 0
-    else:
-        attn = torch.zeros((B, cfg.n_layers, cfg.n_heads, N, N), dtype=torch.float16, device=dev)
-        attn[:, :, :, bs:bs + blk, bs:bs + blk] = dev16(w.attn, torch.float16)
+    attn = None
+    if cfg.n_layers and args.compact_attn:
+        attn, bs = dev_of(w.attn, cfg.attn_dtype), 0
+    elif cfg.n_layers:
+        attn = torch.zeros((B, cfg.n_layers, cfg.n_heads, N, N), dtype=tdt[cfg.attn_dtype], device=dev)
+        attn[:, :, :, bs:bs + blk, bs:bs + blk] = dev_of(w.attn, cfg.attn_dtype)
 
     status = dlm.new_status(dev)
     stream = torch.cuda.current_stream(dev)
     common = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
                   gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
                   bulk_frac=cfg.bulk_frac, status=status)
-    plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, **common)
+    common.update(rules=cfg.rules, cap_scope_from_boundary=(cfg.name == "depcap_window"))
+    plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 
     for _ in range(args.warmup):
         plan.run(stream)
@@ -250,30 +281,34 @@ def run_native(args, rank, world, local):
     # --- end to end through host buffers (pinned), same public API
     e2e = None
     if args.e2e_steps > 0:
-        cur_h = torch.from_numpy(w.cur.view(np.int16)).view(torch.bfloat16).pin_memory()
-        prev_h = torch.from_numpy(w.prev.view(np.int16)).view(torch.bfloat16).pin_memory()
-        attn_h = torch.from_numpy(w.attn.view(np.int16)).view(torch.float16).pin_memory()
+        cur_h = cur.cpu().pin_memory()
+        prev_h = prev.cpu().pin_memory()
+        attn_h = None if w.attn is None else (torch.from_numpy(w.attn) if cfg.attn_dtype == synth.F32 else
+                                              torch.from_numpy(w.attn.view(np.int16)).view(tdt[cfg.attn_dtype]))
+        attn_h = None if attn_h is None else attn_h.pin_memory()
         masked_h = torch.from_numpy(w.masked).pin_memory()
         cur_d2 = torch.empty_like(cur)
         prev_d2 = torch.empty_like(prev)
-        attn_c = torch.empty(attn_h.shape, dtype=torch.float16, device=dev)
+        attn_c = None if attn_h is None else torch.empty(attn_h.shape, dtype=attn_h.dtype, device=dev)
         masked_d2 = torch.empty_like(masked)
-        outs_h = [torch.empty((B, blk), dtype=torch.uint8).pin_memory() for _ in range(3)]
-        nsel_h = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(3)]
         blen_h = torch.empty(B, dtype=torch.int32).pin_memory()
 
-        plan2 = dlm.StepPlan(cur_d2, prev_d2, masked_d2, attn=attn_c, block_start=0, **common)
+        plan2 = dlm.StepPlan(cur_d2, prev_d2, masked_d2, attn=attn_c, block_start=0, row_index=row_index, **common)
+        outs_h = {k: torch.empty((B, blk), dtype=torch.uint8).pin_memory() for k in plan2.out}
+        nsel_h = {k: torch.empty(B, dtype=torch.int32).pin_memory() for k in plan2.out}
 
         def e2e_step():
             cur_d2.copy_(cur_h, non_blocking=True)
             prev_d2.copy_(prev_h, non_blocking=True)
-            attn_c.copy_(attn_h, non_blocking=True)
+            if attn_c is not None:
+                attn_c.copy_(attn_h, non_blocking=True)
             masked_d2.copy_(masked_h, non_blocking=True)
             plan2.run(stream)
-            for i, k in enumerate(("threshold", "cap", "dapd")):
-                outs_h[i].copy_(plan2.out[k][0], non_blocking=True)
-                nsel_h[i].copy_(plan2.out[k][1], non_blocking=True)
-            blen_h.copy_(plan2.block_len, non_blocking=True)
+            for k in plan2.out:
+                outs_h[k].copy_(plan2.out[k][0], non_blocking=True)
+                nsel_h[k].copy_(plan2.out[k][1], non_blocking=True)
+            if plan2.block_len is not None:
+                blen_h.copy_(plan2.block_len, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -286,17 +321,21 @@ def run_native(args, rank, world, local):
         a1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a0.elapsed_time(a1) / args.e2e_steps
-        h2d = (cur_h.numel() + prev_h.numel() + attn_h.numel()) * 2 + masked_h.numel()
-        d2h = sum(t.numel() for t in outs_h) + sum(t.numel() * 4 for t in nsel_h) + blen_h.numel() * 4
+        h2d = (cur_h.numel() * cur_h.element_size() + prev_h.numel() * prev_h.element_size() + masked_h.numel()
+               + (0 if attn_h is None else attn_h.numel() * attn_h.element_size()))
+        d2h = (sum(t.numel() for t in outs_h.values()) + sum(t.numel() * 4 for t in nsel_h.values())
+               + (blen_h.numel() * 4 if plan2.block_len is not None else 0))
         e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, clocks=clocks, e2e=e2e, host_ms=host_ms,
-                cfg=cfg, launches=plan.n_launches * args.steps, w=w)
+                cfg=cfg, launches=plan.n_launches * args.steps, w=w, decisions=int(w.masked.sum()),
+                rows=int(w.masked.sum()))
 
 
 # ------------------------------------------------------------------ oracle
 def oracle_sample(w, n_seq):
-    """The oracle's whole path (stats + four rules) on the first n_seq sequences."""
+    """The oracle's whole path (statistics + the workload's rules) on the
+    first n_seq sequences; returns (seconds, decisions)."""
     import oracle
     import synth
 
@@ -306,15 +345,29 @@ def oracle_sample(w, n_seq):
     cur = np.ascontiguousarray(w.cur[:rows])
     prev = np.ascontiguousarray(w.prev[:rows])
     masked = np.ascontiguousarray(w.masked[:n_seq])
+    code = None if cfg.logit_dtype == synth.F32 else cfg.logit_dtype
+    ri = None
+    if cfg.masked_count >= 0:
+        ri = np.nonzero(masked.reshape(-1))[0].astype(np.int32)
     t = time.perf_counter()
-    o = oracle.row_stats(cur, prev, dtype=synth.BF16)
+    o = oracle.row_stats(cur, prev, dtype=code, row_index=ri, n_out=rows)
     conf = o["conf"].reshape(n_seq, blk)
-    oracle.select_threshold(conf, masked, cfg.tau)
-    oracle.depcap_boundary(o["kl"].reshape(n_seq, blk), o["entropy"].reshape(n_seq, blk), cfg.lam, cfg.L_min)
-    oracle.cap_select(cur, o["argmax"].reshape(n_seq, blk), conf, o["lse"].reshape(n_seq, blk), masked,
-                      cfg.tau_low, cfg.tau_high, cfg.gamma, cfg.p_max, dtype=synth.BF16)
-    oracle.dapd(np.ascontiguousarray(w.attn[:n_seq]), masked, conf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac,
-                dtype=synth.F16)
+    if "threshold" in cfg.rules:
+        oracle.select_threshold(conf, masked, cfg.tau)
+    scope = None
+    if "boundary" in cfg.rules:
+        bl, _ = oracle.depcap_boundary(o["kl"].reshape(n_seq, blk), o["entropy"].reshape(n_seq, blk), cfg.lam,
+                                       cfg.L_min)
+        if cfg.name == "depcap_window":
+            scope = bl
+    if "cap" in cfg.rules:
+        am = np.where(o["argmax"] < 0, 0, o["argmax"]).reshape(n_seq, blk)
+        oracle.cap_select(cur, am, conf, o["lse"].reshape(n_seq, blk), masked, cfg.tau_low, cfg.tau_high,
+                          cfg.gamma, cfg.p_max, scope_len=scope, dtype=code)
+    if "dapd" in cfg.rules:
+        acode = None if cfg.attn_dtype == synth.F32 else cfg.attn_dtype
+        oracle.dapd(np.ascontiguousarray(w.attn[:n_seq]), masked, conf, cfg.tau_edge, cfg.bulk_conf,
+                    cfg.bulk_frac, dtype=acode)
     return time.perf_counter() - t, int(masked.sum())
 
 
@@ -340,7 +393,7 @@ def run_reference(args, rank, world):
     import synth
     if rank != 0:
         return
-    cfg = synth.CONFIGS[WORKLOAD]
+    cfg = synth.CONFIGS[args.workload]
     w = synth.make(cfg, seed=args.seed)
     import oracle
     oracle.build()
@@ -380,24 +433,28 @@ def main():
     total_ms = max_over_ranks(r["total_ms"], world, f"cuda:{local}")
     if rank != 0:
         return
-    value = job_throughput(cfg.batch * cfg.blk, world, args.steps, total_ms)
+    value = job_throughput(r["decisions"], world, args.steps, total_ms)
     ms_step = total_ms / args.steps
     k1_ms = statistics.mean(r["k1"])
-    k1_bytes = 2 * cfg.batch * cfg.blk * cfg.vocab * 2  # cur + prev bf16 rows
+    esz = 4 if cfg.logit_dtype == 0 else 2
+    k1_bytes = 2 * r["rows"] * cfg.vocab * esz  # current + previous rows actually read
     k1_gbs = k1_bytes / (k1_ms / 1000.0) / 1e9
     peak, peak_kind = load_peaks()
     line = {
         "metric": METRIC, "value": value, "unit": "decisions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "batch_per_gpu": cfg.batch, "masked_per_seq": cfg.blk,
-                   "vocab": cfg.vocab, "logits": "bf16", "attention": "f16",
-                   "l2": "no flush: 1.25 GB of logit rows per step, larger than L2", "parallelism": f"dp{world}"},
+        "config": {"workload": workload_desc(cfg), "batch_per_gpu": cfg.batch, "positions_per_seq": cfg.blk,
+                   "vocab": cfg.vocab,
+                   "l2": (f"no flush: {k1_bytes / 1e9:.3f} GB of logit rows per step, larger than L2"
+                          if k1_bytes > 129e6 else
+                          f"{k1_bytes / 1e6:.1f} MB of logit rows per step fit in L2 (no flush; warm-L2 number)"),
+                   "parallelism": f"dp{world}"},
         "logit_gbps": k1_gbs,
         "kernels_ms": {"row_stats": k1_ms, "four_rules": r["rules_ms"]},
         "host_enqueue_ms_per_step": r["host_ms"],
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
-                     "traffic": None, "kernel": "row_stats", "peak_kind": peak_kind,
+                     "traffic": recorded_traffic() if (cfg.batch == 64 and not args.compact_attn) else None, "kernel": "row_stats", "peak_kind": peak_kind,
                      "algorithmic_bytes": k1_bytes},
         "gpu_launches": r["launches"],
     }
@@ -405,11 +462,12 @@ def main():
         line["clocks"] = r["clocks"]
     if r["e2e"]:
         e = r["e2e"]
-        line["e2e"] = {"value": cfg.batch * cfg.blk * world / (e["ms_per_step"] / 1000.0), "unit": "decisions/s",
+        line["e2e"] = {"value": r["decisions"] * world / (e["ms_per_step"] / 1000.0), "unit": "decisions/s",
                        "h2d_bytes_per_step": e["h2d_bytes_per_step"], "d2h_bytes_per_step": e["d2h_bytes_per_step"],
                        "ms_per_step": e["ms_per_step"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(r["w"])
+    line["config"]["workload_name"] = cfg.name
     print(json.dumps(line), flush=True)
 
 

@@ -266,8 +266,9 @@ class StepPlan:
     def __init__(self, cur, prev, masked, *, tau=0.9, lam=1.0, L_min=8, smooth_w=1, norm_mode=0,
                  tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=None, high_tier_unconditional=False,
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
-                 bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None):
-        _need_cuda(cur, prev, masked, attn)
+                 bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
+                 row_index=None):
+        _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
         B, blk = masked.shape
@@ -278,10 +279,16 @@ class StepPlan:
         self.status = status if status is not None else new_status(dev)
         self.stats = alloc_row_stats(B * blk, dev, prev is not None)
         self.rules = tuple(rules)
-        self.keep = [cur, prev, attn, self.masked]
+        n_rows = B * blk
+        if row_index is not None:
+            row_index = row_index.to(torch.int32).contiguous()
+            n_rows = row_index.numel()
+            self.stats = RowStats(*[None if t is None else t.zero_() for t in self.stats])
+        self.keep = [cur, prev, attn, self.masked, row_index]
         st = self.stats
         self._calls = []
-        self._calls.append((L.dlm_row_stats, (_p(cur), _p(prev), _dt(cur), B * blk, cur.shape[1], cur.stride(0), None,
+        self._calls.append((L.dlm_row_stats, (_p(cur), _p(prev), _dt(cur), n_rows, cur.shape[1], cur.stride(0),
+                                               _p(row_index),
                                                _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
                                                _p(st.lse_prev), _p(self.status))))
         u8 = dict(dtype=torch.uint8, device=dev)

@@ -23,6 +23,9 @@
 //                (compared as 128-bit integer mantissas with a shared exponent)
 //                and the greedy scan over the shared-memory adjacency bitmask.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -287,6 +290,167 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     }
 }
 
+constexpr int kStages = 4;                       // bulk-copy ring depth
+constexpr long long kWaitLimit = 2000000000LL;   // ~1 s at 2 GHz
+
+// The same sums as dapd_accum_kernel, with the attention staged by the TMA
+// engine: one thread issues bulk tensor copies of [box_heads x rows x
+// box_cols] boxes (about 16 KB) into a kStages-deep shared-memory ring, so a
+// CTA keeps up to 64 KB in flight without spending registers on it; every
+// thread then sums its (row, 8-column vector) slots over the heads of each box.
+// Rows of the tile that are not masked are loaded but never stored.
+template <int DT>
+__global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                  DapdArgs a) {
+    constexpr int EPV = AFmt<DT>::EPV;
+    constexpr int ESZ = AFmt<DT>::ESZ;
+    constexpr int NP = EPV / 2;
+    extern __shared__ __align__(128) unsigned char s_ring[];
+    __shared__ __align__(16) float s_red[kThreads * 2 * EPV];
+    __shared__ __align__(8) uint64_t s_full[kStages];
+
+    const int split = a.split;
+    const int g = blockIdx.x % split;
+    const int tb = blockIdx.x / split;
+    const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
+    const int tile = tb % tiles;
+    const int b = tb / tiles;
+    if (late_phase(a, b, nullptr)) return;  // the whole cluster takes the same branch
+
+    const int RB = a.row_tile, CB = a.box_cols, HB = a.box_heads;
+    const int r0 = tile * RB;
+    const int vpr = CB / EPV;
+    const int Q = RB * vpr;
+    const int G2 = max(1, min(HB, kThreads / Q));
+    const int t = threadIdx.x;
+    const bool active = t < G2 * Q;
+    const int slot = active ? t % Q : 0;
+    const int grp = active ? t / Q : 0;
+    const int rr = slot / vpr, cv = slot % vpr;
+    const int nbox = a.n_layers * a.head_groups;
+    const int chunk = (nbox + split - 1) / split;
+    const int j0 = g * chunk;
+    const int n = max(0, min(nbox, j0 + chunk) - j0);
+    const int stage_stride = (a.box_bytes + 127) & ~127;  // 128-byte aligned ring slots
+
+    if (t == 0) {
+        for (int k = 0; k < kStages; ++k) mbar_init(&s_full[k], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    auto issue = [&](int j, int stage) {
+        const int bj = j0 + j;
+        const int l = bj / a.head_groups, hg = bj - l * a.head_groups;
+        mbar_expect_tx(&s_full[stage], (uint32_t)a.box_bytes);
+        tma_load_5d(s_ring + (size_t)stage * stage_stride, &tmap, &s_full[stage], a.block_start,
+                    a.block_start + r0, hg * HB, l, b);
+    };
+    if (t == 0)
+        for (int k = 0; k < min(kStages, n); ++k) issue(k, k);
+
+    f2 H[NP], L[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) H[p] = L[p] = pack2(0.f, 0.f);
+    int timed_out = 0, j_stop = n;
+    for (int j = 0; j < n; ++j) {
+        const int stage = j % kStages;
+        const uint32_t parity = (uint32_t)((j / kStages) & 1);
+        const int late = !mbar_wait_bounded(&s_full[stage], parity, kWaitLimit);
+        if (__syncthreads_or(late)) {
+            timed_out = 1;
+            j_stop = j;
+            break;
+        }
+        if (active) {
+            const unsigned char* box = s_ring + (size_t)stage * stage_stride;
+            for (int hh = grp; hh < HB; hh += G2) {
+                const uint4 w = *reinterpret_cast<const uint4*>(box + ((size_t)(hh * RB + rr) * CB + cv * EPV) * ESZ);
+                f2 x[NP];
+                AFmt<DT>::to_f2(w, x);
+                split_acc<NP>(x, H, L);
+            }
+        }
+        __syncthreads();  // the stage is free again
+        if (t == 0 && j + kStages < n) issue(j + kStages, stage);
+    }
+    if (timed_out) {
+        // give the copies already issued a bounded chance to land before the
+        // shared memory they target is released, then report and stop
+        if (t == 0) {
+            for (int j = j_stop; j < min(n, j_stop + kStages); ++j)
+                mbar_wait_bounded(&s_full[j % kStages], (uint32_t)((j / kStages) & 1), kWaitLimit);
+            raise_status(a.dev_status, DLM_DEV_TIMEOUT);
+        }
+    }
+
+    float* mine = s_red + (size_t)t * 2 * EPV;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        unpack2(H[p], mine[4 * p + 0], mine[4 * p + 1]);
+        unpack2(L[p], mine[4 * p + 2], mine[4 * p + 3]);
+    }
+    __syncthreads();
+    float acc[2 * EPV];
+#pragma unroll
+    for (int k = 0; k < 2 * EPV; ++k) acc[k] = mine[k];
+    if (active && grp == 0) {
+        for (int gg = 1; gg < G2; ++gg) {
+            const float4* o = reinterpret_cast<const float4*>(s_red + (size_t)(gg * Q + slot) * 2 * EPV);
+            float4 v[EPV / 2];
+#pragma unroll
+            for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
+#pragma unroll
+            for (int k = 0; k < EPV / 2; ++k) {
+                acc[4 * k + 0] += v[k].x;
+                acc[4 * k + 1] += v[k].y;
+                acc[4 * k + 2] += v[k].z;
+                acc[4 * k + 3] += v[k].w;
+            }
+        }
+    }
+    if (split > 1) {
+        cg::cluster_group cluster = cg::this_cluster();
+        __syncthreads();
+        if (active && grp == 0) {
+#pragma unroll
+            for (int k = 0; k < 2 * EPV; ++k) mine[k] = acc[k];
+        }
+        cluster.sync();
+        if (g == 0 && active && grp == 0) {
+            for (int r = 1; r < split; ++r) {
+                const float4* o = reinterpret_cast<const float4*>(cluster.map_shared_rank(mine, r));
+                float4 v[EPV / 2];
+#pragma unroll
+                for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
+#pragma unroll
+                for (int k = 0; k < EPV / 2; ++k) {
+                    acc[4 * k + 0] += v[k].x;
+                    acc[4 * k + 1] += v[k].y;
+                    acc[4 * k + 2] += v[k].z;
+                    acc[4 * k + 3] += v[k].w;
+                }
+            }
+        }
+        cluster.sync();
+    }
+    const int row = r0 + rr;
+    if (g != 0 || !active || grp != 0 || timed_out || row >= a.blk) return;
+    if (!a.masked[(int64_t)b * a.blk + row]) return;
+    long long* A = a.A + ((int64_t)b * a.blk + row) * a.blk;
+    const int col0 = cv * EPV;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int col = col0 + 2 * p + k;
+            if (col < a.blk) {
+                const float hi = acc[4 * p + k], lo = acc[4 * p + 2 + k];
+                A[col] = __float2ll_rn(hi * 32768.f) * 131072LL + __float2ll_rn(lo * 4294967296.f);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
     const int b = blockIdx.y;
     if (late_phase(a, b, nullptr)) return;
@@ -491,6 +655,99 @@ cudaError_t launch_accum(const DapdArgs& a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, dapd_accum_kernel<DT>, a);
 }
 
+// ---- bulk-tensor path: tensor map of the attention as a 5-d tensor ------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Describe [B][L][H][rows][cols] (element strides sb, sl, sh, sr, 1) to the
+// TMA engine, clipped to the block's rows and columns so reads past the block
+// fill with zeros.  Returns false when the tensor cannot be described (the
+// register-load kernel is used then).
+bool encode_attention_map(DapdArgs& a, CUtensorMap* map) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const int esz = a.dtype == DLM_F32 ? 4 : 2;
+    const int epv = 16 / esz;
+    const int CB = (a.blk + epv - 1) / epv * epv;
+    if (CB > 256 || a.row_tile > 256) return false;
+    if ((reinterpret_cast<uintptr_t>(a.attn) & 15u) != 0 || ((int64_t)a.block_start * esz) % 16 != 0) return false;
+    const int64_t strides[4] = {a.sr, a.sh, a.sl, a.sb};
+    for (int k = 0; k < 4; ++k)
+        if (strides[k] <= 0 || (strides[k] * esz) % 16 != 0 || strides[k] * esz >= (1LL << 40)) return false;
+    int HB = 16384 / (CB * a.row_tile * esz);
+    HB = std::max(1, std::min(HB, std::min(a.n_heads, 256)));
+    const cuuint64_t dims[5] = {(cuuint64_t)(a.block_start + a.blk), (cuuint64_t)(a.block_start + a.blk),
+                                (cuuint64_t)a.n_heads, (cuuint64_t)a.n_layers, (cuuint64_t)a.batch};
+    const cuuint64_t gstr[4] = {(cuuint64_t)(a.sr * esz), (cuuint64_t)(a.sh * esz), (cuuint64_t)(a.sl * esz),
+                                (cuuint64_t)(a.sb * esz)};
+    const cuuint32_t box[5] = {(cuuint32_t)CB, (cuuint32_t)a.row_tile, (cuuint32_t)HB, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUtensorMapDataType dt = a.dtype == DLM_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                   : a.dtype == DLM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUresult r = enc(map, dt, 5, const_cast<void*>(a.attn), dims, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    a.box_cols = CB;
+    a.box_heads = HB;
+    a.head_groups = (a.n_heads + HB - 1) / HB;
+    a.box_bytes = CB * a.row_tile * HB * esz;
+    return true;
+}
+
+constexpr int kMaxDev = 64;
+
+template <int DT>
+cudaError_t launch_accum_tma(const DapdArgs& a, const CUtensorMap& map, cudaStream_t s) {
+    static std::mutex mu;
+    static bool smem_set[kMaxDev] = {false};
+    const size_t dyn = (size_t)kStages * (size_t)((a.box_bytes + 127) & ~127);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < kMaxDev && !smem_set[dev]) {
+            e = cudaFuncSetAttribute(dapd_accum_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)(kStages * 16384));
+            if (e != cudaSuccess) return e;
+            smem_set[dev] = true;
+        }
+    }
+    const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.batch * tiles * a.split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = dyn;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    if (a.split > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = a.split;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, dapd_accum_tma_kernel<DT>, map, a);
+}
+
 }  // namespace
 
 size_t dapd_workspace_bytes(int batch, int blk) {
@@ -516,14 +773,17 @@ cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
     const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
     const int LH = a.n_layers * a.n_heads;
     const long long base = (long long)a.batch * tiles;
+    CUtensorMap map;
+    const bool tma = encode_attention_map(a, &map);
+    const int units = tma ? a.n_layers * a.head_groups : LH;  // work items split over a cluster
     int split = (int)((2LL * num_sms + base - 1) / base);
-    split = max(1, min(8, min(split, LH)));
+    split = max(1, min(8, min(split, units)));
     a.split = split;
     cudaError_t e;
     switch (a.dtype) {
-    case DLM_F16: e = launch_accum<DLM_F16>(a, s); break;
-    case DLM_BF16: e = launch_accum<DLM_BF16>(a, s); break;
-    default: e = launch_accum<DLM_F32>(a, s); break;
+    case DLM_F16: e = tma ? launch_accum_tma<DLM_F16>(a, map, s) : launch_accum<DLM_F16>(a, s); break;
+    case DLM_BF16: e = tma ? launch_accum_tma<DLM_BF16>(a, map, s) : launch_accum<DLM_BF16>(a, s); break;
+    default: e = tma ? launch_accum_tma<DLM_F32>(a, map, s) : launch_accum<DLM_F32>(a, s); break;
     }
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -99,6 +99,8 @@ struct DapdArgs {
     uint32_t* adj;     // [batch][blk][8]
     int split;         // CTAs per cluster over the layer*head range
     int row_tile;      // rows per CTA
+    // bulk-tensor (TMA) path: box = [box_cols x row_tile rows x box_heads]
+    int box_cols, box_heads, head_groups, box_bytes;
 };
 size_t dapd_workspace_bytes(int batch, int blk);
 void dapd_carve(DapdArgs& a, void* ws);

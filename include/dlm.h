@@ -55,6 +55,8 @@ typedef enum dlm_dtype { DLM_F32 = 0, DLM_BF16 = 1, DLM_F16 = 2 } dlm_dtype;
 /* device status bits (OR-ed into *dev_status by the kernels) */
 #define DLM_DEV_NONFINITE 1u    /* a logit row held NaN or +inf, or only -inf   */
 #define DLM_DEV_POOL_CLIPPED 2u /* a CAP pool had more than p_max candidates    */
+#define DLM_DEV_TIMEOUT 4u      /* a kernel's bounded wait for its own copies gave
+                                   up (~1 s); that call's outputs are unspecified */
 
 /* Maximum block size accepted by the selection calls. */
 #define DLM_MAX_BLK 256

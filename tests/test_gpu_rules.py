@@ -345,3 +345,24 @@ def test_dapd_key_ties_break_to_lower_position(dlm):
     r = oracle.dapd(sub16, masked, conf.astype(np.float64), 0.1, dtype=synth.F16)
     np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
     assert np.nonzero(r["selected"][0])[0].tolist() == list(range(0, blk, 2))
+
+
+def test_dapd_broadcast_heads_uses_register_path(dlm):
+    """A head-broadcast view (head stride 0) cannot be described to the bulk
+    tensor engine; the register-load kernel must give the same answer."""
+    rng = np.random.default_rng(77)
+    B, L, H, blk, N, bs = 2, 3, 5, 40, 64, 16
+    sub = (rng.random((B, L, 1, blk, blk)) ** 4 * 0.2).astype(np.float32)
+    sub16 = synth.to_f16_bits(sub)
+    full = torch.zeros((B, L, 1, N, N), dtype=torch.float16, device="cuda")
+    full[:, :, :, bs:bs + blk, bs:bs + blk] = to_torch(sub16, synth.F16, "cuda")
+    view = full.expand(B, L, H, N, N)
+    assert view.stride(2) == 0
+    masked = np.ones((B, blk), np.uint8)
+    masked[1, ::3] = 0
+    conf = rng.random((B, blk)).astype(np.float32)
+    gs, gn = dlm.dapd_graph_mis(view, cuda(masked), cuda(conf), 0.05, block_start=bs)
+    r = oracle.dapd(np.ascontiguousarray(np.broadcast_to(sub16, (B, L, H, blk, blk))), masked,
+                    conf.astype(np.float64), 0.05, dtype=synth.F16)
+    np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+    np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
