@@ -134,18 +134,9 @@ __global__ void __launch_bounds__(kThreads) cap_greedy_kernel(CapArgs a) {
     if (t < n) s_tier[t] = a.high_tier_unconditional && a.conf[(int64_t)b * a.blk + pool[t]] >= a.tau_high;
     __syncthreads();
     if (t < 32) {
-        uint32_t kept = 0;  // lane w holds word w of the kept set
-        if (a.high_tier_unconditional) {
-            for (int j = 0; j < 32; ++j) {
-                const int s = t * 32 + j;
-                if (t < W && s < n && s_tier[s]) kept |= 1u << j;
-            }
-        }
-        for (int s = 0; s < n; ++s) {
-            if (s_tier[s]) continue;  // already kept (unconditional tier)
-            const uint32_t hit = t < W ? (s_adj[s * W + t] & kept) : 0u;
-            if (!__any_sync(DLM_FULL_MASK, hit != 0u) && t == (s >> 5)) kept |= 1u << (s & 31);
-        }
+        // lane w holds word w of the kept set; tier members are forced in when
+        // the tier is unconditional (s_tier is all zero otherwise)
+        const uint32_t kept = greedy_scan(s_adj, W, nullptr, s_tier, n, W);
         if (t < W) s_kept[t] = kept;
     }
     __syncthreads();

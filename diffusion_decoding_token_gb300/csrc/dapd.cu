@@ -305,8 +305,10 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
     constexpr int EPV = AFmt<DT>::EPV;
     constexpr int ESZ = AFmt<DT>::ESZ;
     constexpr int NP = EPV / 2;
+    // the ring holds the boxes while streaming; once the stream is done the
+    // same bytes hold the per-thread partial sums for the merges
     extern __shared__ __align__(128) unsigned char s_ring[];
-    __shared__ __align__(16) float s_red[kThreads * 2 * EPV];
+    float* const s_red = reinterpret_cast<float*>(s_ring);
     __shared__ __align__(8) uint64_t s_full[kStages];
 
     const int split = a.split;
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
             raise_status(a.dev_status, DLM_DEV_TIMEOUT);
         }
     }
+    __syncthreads();  // every read of the ring is done before it is reused
 
     float* mine = s_red + (size_t)t * 2 * EPV;
 #pragma unroll
@@ -490,76 +493,77 @@ __global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
     }
 }
 
-// key = sign * mant * 2^exp with a 128-bit mantissa normalised to bit 127
-struct Key {
-    int sign;
-    int exp;
+// Sortable exact key.  key = D * c (order_mode 0) or D (order_mode 1), with D
+// an integer of at most 51 bits and c an fp32 confidence: the product has at
+// most 75 significant bits.  It is written as sign, an 11-bit biased binary
+// exponent and the 127 bits below the leading one of the normalised 128-bit
+// mantissa, of which the top 115 are kept (bits below those are zero for
+// every such product).  Two unsigned 64-bit words then compare exactly like
+// the keys: (hi, lo) larger <=> key larger.  Zero keys sit between the
+// negatives and the positives; unused slots are (0, 0).
+struct SortKey {
     unsigned long long hi, lo;
 };
 
-__device__ __forceinline__ Key make_key(long long D, float c, int order_mode) {
-    Key k;
-    unsigned long long mag;
+__device__ __forceinline__ SortKey make_sort_key(long long D, float c, int order_mode) {
     int sign = D > 0 ? 1 : (D < 0 ? -1 : 0);
-    mag = D < 0 ? (unsigned long long)(-D) : (unsigned long long)D;
-    unsigned long long phi = 0, plo = mag;
+    const unsigned long long mag = D < 0 ? (unsigned long long)(-D) : (unsigned long long)D;
+    unsigned long long mhi = 0, mlo = mag;
     int e = 0;
     if (order_mode == 0) {
         const uint32_t u = __float_as_uint(c);
         const int ce = (u >> 23) & 0xff;
         uint32_t cm = u & 0x7fffff;
-        if (!(c > 0.f) || ce == 0xff) {  // zero, negative, NaN or inf confidence: key 0
-            sign = 0;
-            cm = 0;
-        }
+        if (!(c > 0.f) || ce == 0xff) sign = 0;  // zero, negative, NaN or inf confidence: key 0
         if (ce != 0) cm |= 0x800000u;
         e = ce == 0 ? -149 : ce - 150;
-        plo = mag * (unsigned long long)cm;
-        phi = __umul64hi(mag, (unsigned long long)cm);
+        mlo = mag * (unsigned long long)cm;
+        mhi = __umul64hi(mag, (unsigned long long)cm);
     }
-    if (sign == 0 || (phi == 0 && plo == 0)) {
-        k.sign = 0;
-        k.exp = 0;
-        k.hi = k.lo = 0;
+    SortKey k;
+    if (sign == 0 || (mhi == 0 && mlo == 0)) {
+        k.hi = 1ULL << 63;
+        k.lo = 0;
         return k;
     }
-    const int lz = phi ? __clzll(phi) : 64 + __clzll(plo);
+    // normalise: leading one to bit 127
+    const int lz = mhi ? __clzll(mhi) : 64 + __clzll(mlo);
     if (lz >= 64) {
-        phi = plo << (lz - 64);
-        plo = 0;
+        mhi = mlo << (lz - 64);
+        mlo = 0;
     } else if (lz > 0) {
-        phi = (phi << lz) | (plo >> (64 - lz));
-        plo <<= lz;
+        mhi = (mhi << lz) | (mlo >> (64 - lz));
+        mlo <<= lz;
     }
-    k.sign = sign;
-    k.exp = e - lz;
-    k.hi = phi;
-    k.lo = plo;
+    const unsigned long long ex = (unsigned long long)(e - lz + 512) & 0x7ffULL;  // biased exponent
+    // fraction bits 126..76 -> 51 bits, 75..12 -> 64 bits
+    const unsigned long long f1 = (mhi << 1) >> 13;
+    const unsigned long long f2 = (mhi << 52) | (mlo >> 12);
+    unsigned long long hi = (ex << 51) | f1, lo = f2;
+    if (sign > 0) {
+        hi |= 1ULL << 63;
+    } else {  // mirror below zero: 2^127 - magnitude
+        hi = (0x8000000000000000ULL - hi) - (lo != 0 ? 1 : 0);
+        lo = ~lo + 1;
+    }
+    k.hi = hi;
+    k.lo = lo;
     return k;
 }
 
-// +1 if a > b, -1 if a < b, 0 if equal
-__device__ __forceinline__ int key_cmp(const Key& a, const Key& b) {
-    if (a.sign != b.sign) return a.sign > b.sign ? 1 : -1;
-    if (a.sign == 0) return 0;
-    int r;
-    if (a.exp != b.exp)
-        r = a.exp > b.exp ? 1 : -1;
-    else if (a.hi != b.hi)
-        r = a.hi > b.hi ? 1 : -1;
-    else if (a.lo != b.lo)
-        r = a.lo > b.lo ? 1 : -1;
-    else
-        r = 0;
-    return a.sign > 0 ? r : -r;
+// a goes before b: larger key first, then the lower position
+__device__ __forceinline__ bool key_before(unsigned long long ah, unsigned long long al, int ai, unsigned long long bh,
+                                           unsigned long long bl, int bi) {
+    if (ah != bh) return ah > bh;
+    if (al != bl) return al > bl;
+    return ai < bi;
 }
 
 __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
-    __shared__ Key s_key[DLM_MAX_BLK];
-    __shared__ int s_order[DLM_MAX_BLK];
+    __shared__ unsigned long long s_kh[DLM_MAX_BLK], s_kl[DLM_MAX_BLK];
+    __shared__ int s_ix[DLM_MAX_BLK];
     __shared__ uint32_t s_adj[DLM_MAX_BLK * kMaxWords];
     __shared__ uint32_t s_kept[kMaxWords];
-    __shared__ unsigned char s_m[DLM_MAX_BLK];
     __shared__ float s_v[kThreads / 32];
     __shared__ int s_i[kThreads / 32];
     const int b = blockIdx.x, t = threadIdx.x;
@@ -595,35 +599,53 @@ __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
         if (t == 0) a.n_selected[b] = n;
         return;
     }
-    if (t < a.blk) {
-        s_m[t] = m;
-        sel[t] = 0;
-        if (m) s_key[t] = make_key(a.Dsum[o], a.conf[o], a.order_mode);
+    // keys of the masked nodes; unused slots sort last
+    int n2 = 1;
+    while (n2 < a.blk) n2 <<= 1;
+    if (t < n2) {
+        if (m) {
+            const SortKey k = make_sort_key(a.Dsum[o], a.conf[o], a.order_mode);
+            s_kh[t] = k.hi;
+            s_kl[t] = k.lo;
+            s_ix[t] = t;
+        } else {
+            s_kh[t] = 0;
+            s_kl[t] = 0;
+            s_ix[t] = 0x7fffffff;
+        }
     }
-    const int nw = (a.blk + 31) >> 5;
-    for (int k = t; k < a.blk * nw; k += blockDim.x) {
-        const int r = k / nw, w = k - r * nw;
-        s_adj[r * kMaxWords + w] = a.adj[((int64_t)b * a.blk + r) * kMaxWords + w];
+    if (t < a.blk) sel[t] = 0;
+    // bitonic sort into "goes before" order
+    for (int k = 2; k <= n2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            __syncthreads();
+            const int l = t ^ j;
+            if (t < n2 && l > t) {
+                const bool asc = (t & k) == 0;
+                const unsigned long long ah = s_kh[t], al = s_kl[t], bh = s_kh[l], bl = s_kl[l];
+                const int ai = s_ix[t], bi = s_ix[l];
+                const bool ab = key_before(ah, al, ai, bh, bl, bi);
+                if (asc ? !ab : ab) {
+                    s_kh[t] = bh;
+                    s_kl[t] = bl;
+                    s_ix[t] = bi;
+                    s_kh[l] = ah;
+                    s_kl[l] = al;
+                    s_ix[l] = ai;
+                }
+            }
+        }
     }
     __syncthreads();
-    if (m) {
-        const Key ki = s_key[t];
-        int rank = 0;
-        for (int j = 0; j < a.blk; ++j) {
-            if (!s_m[j] || j == t) continue;
-            const int c = key_cmp(s_key[j], ki);
-            rank += (c > 0) || (c == 0 && j < t);
-        }
-        s_order[rank] = t;
+    // adjacency rows in visiting order
+    const int nw = (a.blk + 31) >> 5;
+    for (int k = t; k < M * nw; k += blockDim.x) {
+        const int r = k / nw, w = k - r * nw;
+        s_adj[r * kMaxWords + w] = a.adj[((int64_t)b * a.blk + s_ix[r]) * kMaxWords + w];
     }
     __syncthreads();
     if (t < 32) {
-        uint32_t kept = 0;
-        for (int k = 0; k < M; ++k) {
-            const int v = s_order[k];
-            const uint32_t hit = t < nw ? (s_adj[v * kMaxWords + t] & kept) : 0u;
-            if (!__any_sync(DLM_FULL_MASK, hit != 0u) && t == (v >> 5)) kept |= 1u << (v & 31);
-        }
+        const uint32_t kept = greedy_scan(s_adj, kMaxWords, s_ix, nullptr, M, nw);
         if (t < kMaxWords) s_kept[t] = kept;
     }
     __syncthreads();
@@ -713,23 +735,37 @@ bool encode_attention_map(DapdArgs& a, CUtensorMap* map) {
 
 constexpr int kMaxDev = 64;
 
+// ring of kStages boxes, large enough to hold the per-thread partials later
+size_t tma_dyn_smem(const DapdArgs& a) {
+    const int epv = a.dtype == DLM_F32 ? 4 : 8;
+    const size_t ring = (size_t)kStages * (size_t)((a.box_bytes + 127) & ~127);
+    const size_t red = (size_t)kThreads * 2 * epv * sizeof(float);
+    return ring > red ? ring : red;
+}
+
+// allow the ring's dynamic shared memory (once per device)
 template <int DT>
-cudaError_t launch_accum_tma(const DapdArgs& a, const CUtensorMap& map, cudaStream_t s) {
+cudaError_t tma_smem_attribute() {
     static std::mutex mu;
     static bool smem_set[kMaxDev] = {false};
-    const size_t dyn = (size_t)kStages * (size_t)((a.box_bytes + 127) & ~127);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (dev >= 0 && dev < kMaxDev && !smem_set[dev]) {
-            e = cudaFuncSetAttribute(dapd_accum_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)(kStages * 16384));
-            if (e != cudaSuccess) return e;
-            smem_set[dev] = true;
-        }
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < kMaxDev && !smem_set[dev]) {
+        e = cudaFuncSetAttribute(dapd_accum_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kStages * 16384 + 16384));
+        if (e != cudaSuccess) return e;
+        smem_set[dev] = true;
     }
+    return cudaSuccess;
+}
+
+template <int DT>
+cudaError_t launch_accum_tma(const DapdArgs& a, const CUtensorMap& map, cudaStream_t s) {
+    const size_t dyn = tma_dyn_smem(a);
+    cudaError_t e = tma_smem_attribute<DT>();
+    if (e != cudaSuccess) return e;
     const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.batch * tiles * a.split));
@@ -776,7 +812,11 @@ cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
     CUtensorMap map;
     const bool tma = encode_attention_map(a, &map);
     const int units = tma ? a.n_layers * a.head_groups : LH;  // work items split over a cluster
-    int split = (int)((2LL * num_sms + base - 1) / base);
+    // cluster size over the layer*head range: the register-load kernel wants
+    // about two CTAs per SM; the bulk-copy kernel keeps 64 KB in flight per CTA
+    // and is fastest with fewer, longer CTAs (~1.5 per SM; measured on the
+    // 64 x 32 and 8 x 256 blocks: 33.5 us at split 4, 102 us at split 1)
+    int split = tma ? (int)((3LL * num_sms + base) / (2 * base)) : (int)((2LL * num_sms + base - 1) / base);
     split = max(1, min(8, min(split, units)));
     a.split = split;
     cudaError_t e;
