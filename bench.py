@@ -45,6 +45,9 @@ def parse():
     ap.add_argument("--seed", type=int, default=1004)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--serial-dapd", action="store_true",
+                    help="run the DAPD chain on the main stream after the other rules (default: on a side stream "
+                         "after the row pass, concurrently with the threshold, boundary and CAP kernels)")
     ap.add_argument("--workload", default="batched",
                     help="batched (default, the headline), tiny, llada_step, depcap_window, stress_graph, stress_bulk")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
@@ -225,7 +228,8 @@ def run_native(args, rank, world, local):
     common = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
                   gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
                   bulk_frac=cfg.bulk_frac, status=status)
-    common.update(rules=cfg.rules, cap_scope_from_boundary=(cfg.name == "depcap_window"))
+    common.update(rules=cfg.rules, cap_scope_from_boundary=(cfg.name == "depcap_window"),
+                  concurrent_dapd=not args.serial_dapd)
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 
     for _ in range(args.warmup):

@@ -25,7 +25,9 @@ from ._binding import (  # noqa: F401
     alloc_row_stats,
     cap_select,
     cap_workspace,
+    dapd_graph,
     dapd_graph_mis,
+    dapd_select,
     dapd_workspace,
     depcap_boundary,
     lib,
@@ -35,6 +37,6 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = [
-    "row_stats", "select_threshold", "depcap_boundary", "cap_select", "dapd_graph_mis",
+    "row_stats", "select_threshold", "depcap_boundary", "cap_select", "dapd_graph_mis", "dapd_graph", "dapd_select",
     "StepPlan", "alloc_row_stats", "cap_workspace", "dapd_workspace", "new_status", "RowStats", "DlmError", "lib",
 ]

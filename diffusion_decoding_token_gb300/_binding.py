@@ -67,8 +67,11 @@ def lib():
         L.dlm_dapd_workspace_size.argtypes = [I32, I32]
         L.dlm_dapd_graph_mis.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
+        L.dlm_dapd_graph.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
+                                     P, ctypes.POINTER(DapdParams), P, P, P, P, Z, P, P]
+        L.dlm_dapd_select.argtypes = [P, P, I32, I32, ctypes.POINTER(DapdParams), P, P, P, Z, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
-                  "dlm_dapd_graph_mis"):
+                  "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -254,20 +257,61 @@ def dapd_graph_mis(attn: torch.Tensor, masked: torch.Tensor, conf: torch.Tensor,
     return selected, n_selected
 
 
+def dapd_graph(attn: torch.Tensor, masked: torch.Tensor, tau_edge: float = 0.01, bulk_conf: float = 0.9,
+               bulk_frac: float = 0.5, order_mode: int = 0, block_start: int = 0, *, workspace=None, s_out=None,
+               dtilde_out=None, deg_out=None, status=None):
+    """dlm_dapd_graph: the attention half of DAPD (graph left in ``workspace``)."""
+    _need_cuda(attn, masked, s_out, dtilde_out, deg_out)
+    if attn.dim() != 5 or attn.stride(4) != 1:
+        raise ValueError("attn must be [B, L, H, N, N] with unit column stride")
+    B, L, H = attn.shape[:3]
+    blk = masked.shape[1]
+    masked = _u8(masked)
+    if workspace is None:
+        workspace = dapd_workspace(B, blk, attn.device)
+    sb, sl, sh, sr, _ = attn.stride()
+    prm = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
+    _check(lib().dlm_dapd_graph(_p(attn), _dt(attn), B, L, H, sb, sl, sh, sr, int(block_start), blk, _p(masked),
+                                ctypes.byref(prm), _p(s_out), _p(dtilde_out), _p(deg_out), _p(workspace),
+                                workspace.numel(), _p(status), _stream(attn.device)))
+    return workspace
+
+
+def dapd_select(workspace: torch.Tensor, masked: torch.Tensor, conf: torch.Tensor, tau_edge: float = 0.01,
+                bulk_conf: float = 0.9, bulk_frac: float = 0.5, order_mode: int = 0, *, selected=None,
+                n_selected=None):
+    """dlm_dapd_select: the selection half of DAPD from a graph built by dapd_graph."""
+    _need_cuda(workspace, masked, conf)
+    B, blk = masked.shape
+    masked = _u8(masked)
+    dev = masked.device
+    if selected is None:
+        selected = torch.empty((B, blk), dtype=torch.uint8, device=dev)
+    if n_selected is None:
+        n_selected = torch.empty(B, dtype=torch.int32, device=dev)
+    prm = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
+    _check(lib().dlm_dapd_select(_p(masked), _p(conf.reshape(B, blk).contiguous()), B, blk, ctypes.byref(prm),
+                                 _p(selected), _p(n_selected), _p(workspace), workspace.numel(), _stream(dev)))
+    return selected, n_selected
+
+
 class StepPlan:
     """One decode step's five C-ABI calls with every argument marshalled once.
 
     Built from preallocated CUDA tensors; :meth:`run` only issues the calls
     (row statistics, then the four rules) on the current stream, so the host
     cost per step is a handful of ctypes calls.  Any rule can be left out.
-    The tensors must stay alive and keep their storage while the plan is used.
+    With ``concurrent_dapd`` the DAPD chain runs on a side stream after the row
+    pass, concurrently with the threshold, boundary and CAP kernels (events
+    fork and join it inside the step).  The tensors must stay alive and keep
+    their storage while the plan is used.
     """
 
     def __init__(self, cur, prev, masked, *, tau=0.9, lam=1.0, L_min=8, smooth_w=1, norm_mode=0,
                  tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=None, high_tier_unconditional=False,
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
-                 row_index=None):
+                 row_index=None, concurrent_dapd=False):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -321,6 +365,8 @@ class StepPlan:
                                                     _p(st.conf), _p(st.lse), _p(self.masked), _p(scope), B, blk,
                                                     ctypes.byref(self._cap), _p(s), _p(n), None, _p(self.cap_ws),
                                                     self.cap_ws.numel(), _p(self.status))))
+        self.side = None
+        self._side_calls = []
         if "dapd" in rules:
             if attn is None or attn.dim() != 5 or attn.stride(4) != 1:
                 raise ValueError("the DAPD rule needs attn [B, L, H, N, N] with unit column stride")
@@ -329,10 +375,22 @@ class StepPlan:
             self.dapd_ws = dapd_workspace(B, blk, dev)
             self._dapd = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
             sb, sl, sh, sr, _ = attn.stride()
-            self._calls.append((L.dlm_dapd_graph_mis, (_p(attn), _dt(attn), B, attn.shape[1], attn.shape[2], sb, sl,
-                                                        sh, sr, int(block_start), blk, _p(self.masked), _p(st.conf),
-                                                        ctypes.byref(self._dapd), _p(s), _p(n), None, None, None,
-                                                        _p(self.dapd_ws), self.dapd_ws.numel(), _p(self.status))))
+            attn_args = (_p(attn), _dt(attn), B, attn.shape[1], attn.shape[2], sb, sl, sh, sr, int(block_start), blk,
+                         _p(self.masked))
+            call = (L.dlm_dapd_graph_mis, attn_args + (_p(st.conf), ctypes.byref(self._dapd), _p(s), _p(n), None,
+                                                        None, None, _p(self.dapd_ws), self.dapd_ws.numel(),
+                                                        _p(self.status)))
+            if concurrent_dapd:
+                # after the row pass, run the whole DAPD chain on a side stream
+                # while the main stream runs the latency-bound threshold,
+                # boundary and CAP kernels; the row pass keeps the memory
+                # system to itself
+                self.side = torch.cuda.Stream(device=dev)
+                self._ev_rows = torch.cuda.Event()
+                self._ev_side = torch.cuda.Event()
+                self._side_calls.append(call)
+            else:
+                self._calls.append(call)
 
     @property
     def n_launches(self) -> int:
@@ -343,15 +401,29 @@ class StepPlan:
     def run(self, stream=None, events=None, rules_only=False):
         """Issue the step on ``stream`` (default: the current stream).  With
         ``events`` = (e0, e1), e0/e1 are recorded around the row pass.
-        ``rules_only`` re-runs the four rules on the statistics already in
-        the plan's buffers (for timing them apart)."""
+        ``rules_only`` re-runs the rules on the statistics already in the
+        plan's buffers (for timing them apart)."""
         st = stream or torch.cuda.current_stream(self.dev)
         s = ctypes.c_void_p(st.cuda_stream)
         for k, (fn, args) in enumerate(self._calls):
-            if rules_only and k == 0:
+            if k > 0:
+                _check(fn(*args, s))
                 continue
-            if events is not None and k == 0:
-                events[0].record(st)
-            _check(fn(*args, s))
-            if events is not None and k == 0:
-                events[1].record(st)
+            if not rules_only:
+                if events is not None:
+                    events[0].record(st)
+                _check(fn(*args, s))
+                if events is not None:
+                    events[1].record(st)
+            if self.side is not None:
+                # statistics are ready: fork the DAPD chain onto the side stream
+                self._ev_rows.record(st)
+                self.side.wait_event(self._ev_rows)
+                side = ctypes.c_void_p(self.side.cuda_stream)
+                for fn2, args2 in self._side_calls:
+                    _check(fn2(*args2, side))
+                self._ev_side.record(self.side)
+        if self.side is not None:
+            # join: the next step's row pass must not overwrite statistics the
+            # side stream still reads
+            st.wait_event(self._ev_side)

@@ -162,6 +162,64 @@ size_t dlm_dapd_workspace_size(int32_t batch, int32_t blk) {
     return dlm::dapd_workspace_bytes(batch, blk);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Shared argument checks and set-up of the DAPD calls; selection outputs and
+// conf are checked by the callers that need them.
+dlm_status dapd_prepare(dlm::DapdArgs& a, const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
+                        int32_t n_heads, int64_t stride_b, int64_t stride_l, int64_t stride_h, int64_t stride_row,
+                        int32_t block_start, int32_t blk, const uint8_t* masked, const dlm_dapd_params* params,
+                        void* workspace, size_t ws_bytes, bool need_attn) {
+    if (need_attn && !dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
+    if (!params || batch < 0 || blk < 1 || blk > DLM_MAX_BLK || (params->order_mode != 0 && params->order_mode != 1) ||
+        !isfinite(params->tau_edge))
+        return DLM_ERR_INVALID_ARG;
+    if (need_attn && (n_layers < 1 || n_heads < 1 || (int64_t)n_layers * n_heads > (1 << 20) || block_start < 0 ||
+                      stride_b < 0 || stride_l < 0 || stride_h < 0 || stride_row < blk))
+        return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!masked || (need_attn && !attn)) return DLM_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < dlm::dapd_workspace_bytes(batch, blk)) return DLM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DLM_ERR_ALIGNMENT;
+    a = dlm::DapdArgs{};
+    if (need_attn) {
+        const int esz = dtype_size(dtype);
+        const char* first = static_cast<const char*>(attn) + ((int64_t)block_start * stride_row + block_start) * esz;
+        if (!aligned16(first) || (stride_b * esz) % 16 || (stride_l * esz) % 16 || (stride_h * esz) % 16 ||
+            (stride_row * esz) % 16)
+            return DLM_ERR_ALIGNMENT;
+        const double LH = (double)n_layers * (double)n_heads;
+        const double unit = 2.0 * LH * 4294967296.0;        // 2 L H 2^32: s = I / unit
+        const double t = floor((double)params->tau_edge * unit);  // exact: tau is fp32, unit < 2^53
+        a.edge_thresh = t >= 9.2e18 ? 0x7fffffffffffffffLL : (t <= -9.2e18 ? -0x7fffffffffffffffLL - 1 : (long long)t);
+        a.s_scale = (float)(1.0 / unit);
+        a.attn = attn;
+        a.dtype = dtype;
+        a.n_layers = n_layers;
+        a.n_heads = n_heads;
+        a.sb = stride_b;
+        a.sl = stride_l;
+        a.sh = stride_h;
+        a.sr = stride_row;
+        a.block_start = block_start;
+    }
+    a.batch = batch;
+    a.blk = blk;
+    a.masked = masked;
+    a.tau_edge = params->tau_edge;
+    a.bulk_conf = params->bulk_conf;
+    a.bulk_frac = params->bulk_frac;
+    a.order_mode = params->order_mode;
+    dlm::dapd_carve(a, workspace);
+    return DLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
                               int32_t n_heads, int64_t stride_b, int64_t stride_l,
                               int64_t stride_h, int64_t stride_row, int32_t block_start,
@@ -170,57 +228,49 @@ dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, 
                               int32_t* n_selected, float* s_out, float* dtilde_out,
                               int32_t* deg_out, void* workspace, size_t ws_bytes,
                               uint32_t* dev_status, dlm_stream_t stream) {
-    if (!dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
-    if (!params || batch < 0 || n_layers < 1 || n_heads < 1 || (int64_t)n_layers * n_heads > (1 << 20) ||
-        blk < 1 || blk > DLM_MAX_BLK || block_start < 0 || stride_b < 0 || stride_l < 0 || stride_h < 0 ||
-        stride_row < blk || (params->order_mode != 0 && params->order_mode != 1) || !isfinite(params->tau_edge))
-        return DLM_ERR_INVALID_ARG;
-    if (batch == 0) return DLM_OK;
-    if (!attn || !masked || !conf || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
-    if (!workspace || ws_bytes < dlm::dapd_workspace_bytes(batch, blk)) return DLM_ERR_WORKSPACE;
-    const int esz = dtype_size(dtype);
-    const char* first = static_cast<const char*>(attn) + ((int64_t)block_start * stride_row + block_start) * esz;
-    if (!aligned16(first) || !aligned16(workspace) || (stride_b * esz) % 16 || (stride_l * esz) % 16 ||
-        (stride_h * esz) % 16 || (stride_row * esz) % 16)
-        return DLM_ERR_ALIGNMENT;
-    const double LH = (double)n_layers * (double)n_heads;
-    const double unit = 2.0 * LH * 4294967296.0;   // 2 L H 2^32: s = I / unit
-    double t = floor((double)params->tau_edge * unit);  // exact: tau is fp32, unit < 2^53
-    long long thr;
-    if (t >= 9.2e18)
-        thr = 0x7fffffffffffffffLL;
-    else if (t <= -9.2e18)
-        thr = -0x7fffffffffffffffLL - 1;
-    else
-        thr = (long long)t;
     dlm::DapdArgs a{};
-    a.attn = attn;
-    a.dtype = dtype;
-    a.batch = batch;
-    a.n_layers = n_layers;
-    a.n_heads = n_heads;
-    a.sb = stride_b;
-    a.sl = stride_l;
-    a.sh = stride_h;
-    a.sr = stride_row;
-    a.block_start = block_start;
-    a.blk = blk;
-    a.masked = masked;
+    const dlm_status st = dapd_prepare(a, attn, dtype, batch, n_layers, n_heads, stride_b, stride_l, stride_h,
+                                       stride_row, block_start, blk, masked, params, workspace, ws_bytes, true);
+    if (st != DLM_OK || batch == 0) return st;
+    if (!conf || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
     a.conf = conf;
-    a.tau_edge = params->tau_edge;
-    a.bulk_conf = params->bulk_conf;
-    a.bulk_frac = params->bulk_frac;
-    a.order_mode = params->order_mode;
-    a.edge_thresh = thr;
-    a.s_scale = (float)(1.0 / unit);
     a.selected = selected;
     a.n_selected = n_selected;
     a.s_out = s_out;
     a.dtilde_out = dtilde_out;
     a.deg_out = deg_out;
     a.dev_status = dev_status;
-    dlm::dapd_carve(a, workspace);
     return from_cuda(dlm::launch_dapd(a, sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_dapd_graph(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers, int32_t n_heads,
+                          int64_t stride_b, int64_t stride_l, int64_t stride_h, int64_t stride_row,
+                          int32_t block_start, int32_t blk, const uint8_t* masked, const dlm_dapd_params* params,
+                          float* s_out, float* dtilde_out, int32_t* deg_out, void* workspace, size_t ws_bytes,
+                          uint32_t* dev_status, dlm_stream_t stream) {
+    dlm::DapdArgs a{};
+    const dlm_status st = dapd_prepare(a, attn, dtype, batch, n_layers, n_heads, stride_b, stride_l, stride_h,
+                                       stride_row, block_start, blk, masked, params, workspace, ws_bytes, true);
+    if (st != DLM_OK || batch == 0) return st;
+    a.s_out = s_out;
+    a.dtilde_out = dtilde_out;
+    a.deg_out = deg_out;
+    a.dev_status = dev_status;
+    return from_cuda(dlm::launch_dapd_graph(a, sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t batch, int32_t blk,
+                           const dlm_dapd_params* params, uint8_t* selected, int32_t* n_selected,
+                           void* workspace, size_t ws_bytes, dlm_stream_t stream) {
+    dlm::DapdArgs a{};
+    const dlm_status st = dapd_prepare(a, nullptr, DLM_F16, batch, 0, 0, 0, 0, 0, 0, 0, blk, masked, params,
+                                       workspace, ws_bytes, false);
+    if (st != DLM_OK || batch == 0) return st;
+    if (!conf || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
+    a.conf = conf;
+    a.selected = selected;
+    a.n_selected = n_selected;
+    return from_cuda(dlm::launch_dapd_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -802,7 +802,7 @@ void dapd_carve(DapdArgs& a, void* ws) {
     a.adj = reinterpret_cast<uint32_t*>(p);
 }
 
-cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s) {
     const int epv = a.dtype == DLM_F32 ? 4 : 8;
     const int vpr = (a.blk + epv - 1) / epv;
     a.row_tile = max(1, min(a.blk, kThreads / vpr));
@@ -830,10 +830,21 @@ cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
     cfg.stream = s;
     cfg.gridDim = dim3((unsigned)((a.blk + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.batch);
     cfg.blockDim = dim3(kThreads);
-    e = cudaLaunchKernelEx(&cfg, dapd_graph_kernel, a);
-    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, dapd_graph_kernel, a);
+}
+
+cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
     cfg.gridDim = dim3((unsigned)a.batch);
+    cfg.blockDim = dim3(kThreads);
     return cudaLaunchKernelEx(&cfg, dapd_select_kernel, a);
+}
+
+cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
+    cudaError_t e = launch_dapd_graph(a, num_sms, s);
+    if (e != cudaSuccess) return e;
+    return launch_dapd_select(a, s);
 }
 
 }  // namespace dlm

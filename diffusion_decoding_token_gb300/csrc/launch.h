@@ -104,6 +104,8 @@ struct DapdArgs {
 };
 size_t dapd_workspace_bytes(int batch, int blk);
 void dapd_carve(DapdArgs& a, void* ws);
-cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);
+cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);         // graph + select
+cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s);   // attention -> graph
+cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s);         // graph + conf -> selection
 
 }  // namespace dlm

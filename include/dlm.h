@@ -285,6 +285,30 @@ dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, 
                               int32_t* deg_out, void* workspace, size_t ws_bytes,
                               uint32_t* dev_status, dlm_stream_t stream);
 
+/*
+ * dlm_dapd_graph / dlm_dapd_select -- dlm_dapd_graph_mis in two halves.
+ *
+ * The DAPD graph (a_ij, s_ij, tau-edges, d~, degrees) needs only the attention
+ * and the mask, not the confidences, so it can be built on another stream
+ * while dlm_row_stats reads the logits; the selection then needs conf.
+ * dlm_dapd_graph takes the arguments of dlm_dapd_graph_mis except conf and the
+ * selection outputs, and leaves the graph of every sequence on the graph path
+ * in `workspace` (also writing s_out / dtilde_out / deg_out when given).
+ * dlm_dapd_select reads that graph and conf and writes the selection exactly
+ * as dlm_dapd_graph_mis does (late-phase sequences are decided from conf
+ * alone).  The two calls must see the same batch, blk, masked, params and
+ * workspace, and the caller orders them (same stream, or an event).
+ */
+dlm_status dlm_dapd_graph(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers, int32_t n_heads,
+                          int64_t stride_b, int64_t stride_l, int64_t stride_h, int64_t stride_row,
+                          int32_t block_start, int32_t blk, const uint8_t* masked, const dlm_dapd_params* params,
+                          float* s_out, float* dtilde_out, int32_t* deg_out, void* workspace, size_t ws_bytes,
+                          uint32_t* dev_status, dlm_stream_t stream);
+
+dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t batch, int32_t blk,
+                           const dlm_dapd_params* params, uint8_t* selected, int32_t* n_selected,
+                           void* workspace, size_t ws_bytes, dlm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -366,3 +366,37 @@ def test_dapd_broadcast_heads_uses_register_path(dlm):
                     conf.astype(np.float64), 0.05, dtype=synth.F16)
     np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
     np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+
+
+@pytest.mark.parametrize("name", ["llada_step", "stress_graph", "stress_bulk"])
+def test_dapd_split_calls_match(dlm, name):
+    """dlm_dapd_graph + dlm_dapd_select give exactly dlm_dapd_graph_mis."""
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    B, blk = cfg.batch, cfg.blk
+    c32 = cuda(f32(o["conf"]).reshape(B, blk))
+    ga, na = dlm.dapd_graph_mis(dw.attn, dw.masked, c32, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0,
+                                dw.block_start)
+    ws = dlm.dapd_graph(dw.attn, dw.masked, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0, dw.block_start)
+    gb, nb = dlm.dapd_select(ws, dw.masked, c32, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0)
+    np.testing.assert_array_equal(ga.cpu().numpy(), gb.cpu().numpy())
+    np.testing.assert_array_equal(na.cpu().numpy(), nb.cpu().numpy())
+
+
+def test_step_plan_concurrent_matches_serial(dlm):
+    """The step plan with the DAPD graph on a side stream gives the same
+    selections as the single-stream plan, over several steps."""
+    w, dw, o = workload("llada_step")
+    cfg = w.cfg
+    kw = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
+              gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, attn=dw.attn, block_start=dw.block_start)
+    serial = dlm.StepPlan(dw.cur, dw.prev, dw.masked, **kw)
+    conc = dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, **kw)
+    for _ in range(3):
+        serial.run()
+        conc.run()
+    torch.cuda.synchronize()
+    for k in serial.out:
+        np.testing.assert_array_equal(serial.out[k][0].cpu().numpy(), conc.out[k][0].cpu().numpy())
+        np.testing.assert_array_equal(serial.out[k][1].cpu().numpy(), conc.out[k][1].cpu().numpy())
+    np.testing.assert_array_equal(serial.block_len.cpu().numpy(), conc.block_len.cpu().numpy())
