@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--serial-dapd", action="store_true",
                     help="run the DAPD chain on the main stream after the other rules (default: on a side stream "
                          "after the row pass, concurrently with the threshold, boundary and CAP kernels)")
+    ap.add_argument("--early-dapd-fork", action="store_true",
+                    help="start the DAPD attention graph at the beginning of the step on the low-priority side "
+                         "stream (it then shares the row pass's last wave; default: fork after the row pass)")
     ap.add_argument("--workload", default="batched",
                     help="batched (default, the headline), tiny, llada_step, depcap_window, stress_graph, stress_bulk")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
@@ -224,12 +227,17 @@ def run_native(args, rank, world, local):
         attn[:, :, :, bs:bs + blk, bs:bs + blk] = dev_of(w.attn, cfg.attn_dtype)
 
     status = dlm.new_status(dev)
+    # the step runs on a high-priority stream so the DAPD side stream (lowest
+    # priority) only takes SMs the row pass leaves free
+    torch.cuda.synchronize()
+    _, hi = torch.cuda.Stream.priority_range()
+    torch.cuda.set_stream(torch.cuda.Stream(device=dev, priority=hi))
     stream = torch.cuda.current_stream(dev)
     common = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
                   gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
                   bulk_frac=cfg.bulk_frac, status=status)
     common.update(rules=cfg.rules, cap_scope_from_boundary=(cfg.name == "depcap_window"),
-                  concurrent_dapd=not args.serial_dapd)
+                  concurrent_dapd=not args.serial_dapd, dapd_early=args.early_dapd_fork)
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 
     for _ in range(args.warmup):

@@ -311,7 +311,7 @@ class StepPlan:
                  tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=None, high_tier_unconditional=False,
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
-                 row_index=None, concurrent_dapd=False):
+                 row_index=None, concurrent_dapd=False, dapd_early=False):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -380,15 +380,30 @@ class StepPlan:
             call = (L.dlm_dapd_graph_mis, attn_args + (_p(st.conf), ctypes.byref(self._dapd), _p(s), _p(n), None,
                                                         None, None, _p(self.dapd_ws), self.dapd_ws.numel(),
                                                         _p(self.status)))
+            self.dapd_early = bool(concurrent_dapd and dapd_early)
             if concurrent_dapd:
-                # after the row pass, run the whole DAPD chain on a side stream
-                # while the main stream runs the latency-bound threshold,
-                # boundary and CAP kernels; the row pass keeps the memory
-                # system to itself
-                self.side = torch.cuda.Stream(device=dev)
+                # the DAPD chain runs on a side stream of the lowest priority.
+                # By default it forks after the row pass and overlaps the
+                # latency-bound threshold, boundary and CAP kernels.  With
+                # dapd_early the attention graph (which needs no statistics)
+                # forks at the start of the step: as a lower-priority kernel
+                # its CTAs take SMs only as the row pass's last wave drains;
+                # the selection then waits for the statistics.  Run the plan on
+                # a higher-priority stream for that to hold.
+                lo, _ = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, 0)
+                self.side = torch.cuda.Stream(device=dev, priority=lo)
+                self._ev_start = torch.cuda.Event()
                 self._ev_rows = torch.cuda.Event()
                 self._ev_side = torch.cuda.Event()
-                self._side_calls.append(call)
+                if self.dapd_early:
+                    self._graph_calls = [(L.dlm_dapd_graph, attn_args + (ctypes.byref(self._dapd), None, None, None,
+                                                                         _p(self.dapd_ws), self.dapd_ws.numel(),
+                                                                         _p(self.status)))]
+                    self._side_calls = [(L.dlm_dapd_select, (_p(self.masked), _p(st.conf), B, blk,
+                                                             ctypes.byref(self._dapd), _p(s), _p(n), _p(self.dapd_ws),
+                                                             self.dapd_ws.numel()))]
+                else:
+                    self._side_calls.append(call)
             else:
                 self._calls.append(call)
 
@@ -405,10 +420,13 @@ class StepPlan:
         plan's buffers (for timing them apart)."""
         st = stream or torch.cuda.current_stream(self.dev)
         s = ctypes.c_void_p(st.cuda_stream)
+        side = ctypes.c_void_p(self.side.cuda_stream) if self.side is not None else None
         for k, (fn, args) in enumerate(self._calls):
             if k > 0:
                 _check(fn(*args, s))
                 continue
+            if self.side is not None and self.dapd_early:
+                self._ev_start.record(st)
             if not rules_only:
                 if events is not None:
                     events[0].record(st)
@@ -416,10 +434,15 @@ class StepPlan:
                 if events is not None:
                     events[1].record(st)
             if self.side is not None:
-                # statistics are ready: fork the DAPD chain onto the side stream
+                if self.dapd_early:
+                    # issued after the row pass on the host, so the row pass
+                    # reaches the GPU first; waits only for the step start
+                    self.side.wait_event(self._ev_start)
+                    for fn2, args2 in self._graph_calls:
+                        _check(fn2(*args2, side))
+                # statistics are ready: the rest of the DAPD chain
                 self._ev_rows.record(st)
                 self.side.wait_event(self._ev_rows)
-                side = ctypes.c_void_p(self.side.cuda_stream)
                 for fn2, args2 in self._side_calls:
                     _check(fn2(*args2, side))
                 self._ev_side.record(self.side)

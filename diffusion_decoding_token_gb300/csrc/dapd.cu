@@ -223,31 +223,28 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     }
 
     // merge the slice groups of this CTA in group order, then the CTAs of the
-    // cluster in rank order; partial sums are gathered into registers first so
-    // the remote loads of one rank are all in flight together
-    float* mine = s_red + (size_t)t * 2 * EPV;
+    // cluster in rank order.  Partial sums are stored component-major,
+    // s_red[k * kThreads + thread], so stores and loads are bank-conflict free,
+    // and each rank's values are loaded into registers before they are added.
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        unpack2(H[p], mine[4 * p + 0], mine[4 * p + 1]);
-        unpack2(L[p], mine[4 * p + 2], mine[4 * p + 3]);
+        float h0, h1, l0, l1;
+        unpack2(H[p], h0, h1);
+        unpack2(L[p], l0, l1);
+        s_red[(4 * p + 0) * kThreads + t] = h0;
+        s_red[(4 * p + 1) * kThreads + t] = h1;
+        s_red[(4 * p + 2) * kThreads + t] = l0;
+        s_red[(4 * p + 3) * kThreads + t] = l1;
     }
     __syncthreads();
     float acc[2 * EPV];
 #pragma unroll
-    for (int k = 0; k < 2 * EPV; ++k) acc[k] = mine[k];
+    for (int k = 0; k < 2 * EPV; ++k) acc[k] = s_red[k * kThreads + t];
     if (active && grp == 0) {
         for (int gg = 1; gg < G2; ++gg) {
-            const float4* o = reinterpret_cast<const float4*>(s_red + (size_t)(gg * Q + slot) * 2 * EPV);
-            float4 v[EPV / 2];
+            const int src = gg * Q + slot;
 #pragma unroll
-            for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
-#pragma unroll
-            for (int k = 0; k < EPV / 2; ++k) {
-                acc[4 * k + 0] += v[k].x;
-                acc[4 * k + 1] += v[k].y;
-                acc[4 * k + 2] += v[k].z;
-                acc[4 * k + 3] += v[k].w;
-            }
+            for (int k = 0; k < 2 * EPV; ++k) acc[k] += s_red[k * kThreads + src];
         }
     }
     if (split > 1) {
@@ -255,22 +252,17 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
         __syncthreads();
         if (active && grp == 0) {
 #pragma unroll
-            for (int k = 0; k < 2 * EPV; ++k) mine[k] = acc[k];
+            for (int k = 0; k < 2 * EPV; ++k) s_red[k * kThreads + t] = acc[k];
         }
         cluster.sync();
         if (g == 0 && active && grp == 0) {
-            for (int rr = 1; rr < split; ++rr) {
-                const float4* o = reinterpret_cast<const float4*>(cluster.map_shared_rank(mine, rr));
-                float4 v[EPV / 2];
+            for (int r = 1; r < split; ++r) {
+                const float* o = cluster.map_shared_rank(s_red, r);
+                float v[2 * EPV];
 #pragma unroll
-                for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
+                for (int k = 0; k < 2 * EPV; ++k) v[k] = o[k * kThreads + t];
 #pragma unroll
-                for (int k = 0; k < EPV / 2; ++k) {
-                    acc[4 * k + 0] += v[k].x;
-                    acc[4 * k + 1] += v[k].y;
-                    acc[4 * k + 2] += v[k].z;
-                    acc[4 * k + 3] += v[k].w;
-                }
+                for (int k = 0; k < 2 * EPV; ++k) acc[k] += v[k];
             }
         }
         cluster.sync();
@@ -386,29 +378,27 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
     }
     __syncthreads();  // every read of the ring is done before it is reused
 
-    float* mine = s_red + (size_t)t * 2 * EPV;
+    // partial sums, component-major: s_red[k * kThreads + thread], so stores
+    // and loads are bank-conflict free; merged by group, then by cluster rank
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
-        unpack2(H[p], mine[4 * p + 0], mine[4 * p + 1]);
-        unpack2(L[p], mine[4 * p + 2], mine[4 * p + 3]);
+        float h0, h1, l0, l1;
+        unpack2(H[p], h0, h1);
+        unpack2(L[p], l0, l1);
+        s_red[(4 * p + 0) * kThreads + t] = h0;
+        s_red[(4 * p + 1) * kThreads + t] = h1;
+        s_red[(4 * p + 2) * kThreads + t] = l0;
+        s_red[(4 * p + 3) * kThreads + t] = l1;
     }
     __syncthreads();
     float acc[2 * EPV];
 #pragma unroll
-    for (int k = 0; k < 2 * EPV; ++k) acc[k] = mine[k];
+    for (int k = 0; k < 2 * EPV; ++k) acc[k] = s_red[k * kThreads + t];
     if (active && grp == 0) {
         for (int gg = 1; gg < G2; ++gg) {
-            const float4* o = reinterpret_cast<const float4*>(s_red + (size_t)(gg * Q + slot) * 2 * EPV);
-            float4 v[EPV / 2];
+            const int src = gg * Q + slot;
 #pragma unroll
-            for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
-#pragma unroll
-            for (int k = 0; k < EPV / 2; ++k) {
-                acc[4 * k + 0] += v[k].x;
-                acc[4 * k + 1] += v[k].y;
-                acc[4 * k + 2] += v[k].z;
-                acc[4 * k + 3] += v[k].w;
-            }
+            for (int k = 0; k < 2 * EPV; ++k) acc[k] += s_red[k * kThreads + src];
         }
     }
     if (split > 1) {
@@ -416,22 +406,17 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
         __syncthreads();
         if (active && grp == 0) {
 #pragma unroll
-            for (int k = 0; k < 2 * EPV; ++k) mine[k] = acc[k];
+            for (int k = 0; k < 2 * EPV; ++k) s_red[k * kThreads + t] = acc[k];
         }
         cluster.sync();
         if (g == 0 && active && grp == 0) {
             for (int r = 1; r < split; ++r) {
-                const float4* o = reinterpret_cast<const float4*>(cluster.map_shared_rank(mine, r));
-                float4 v[EPV / 2];
+                const float* o = cluster.map_shared_rank(s_red, r);
+                float v[2 * EPV];
 #pragma unroll
-                for (int k = 0; k < EPV / 2; ++k) v[k] = o[k];
+                for (int k = 0; k < 2 * EPV; ++k) v[k] = o[k * kThreads + t];
 #pragma unroll
-                for (int k = 0; k < EPV / 2; ++k) {
-                    acc[4 * k + 0] += v[k].x;
-                    acc[4 * k + 1] += v[k].y;
-                    acc[4 * k + 2] += v[k].z;
-                    acc[4 * k + 3] += v[k].w;
-                }
+                for (int k = 0; k < 2 * EPV; ++k) acc[k] += v[k];
             }
         }
         cluster.sync();

@@ -391,12 +391,19 @@ def test_step_plan_concurrent_matches_serial(dlm):
     kw = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
               gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, attn=dw.attn, block_start=dw.block_start)
     serial = dlm.StepPlan(dw.cur, dw.prev, dw.masked, **kw)
-    conc = dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, **kw)
-    for _ in range(3):
-        serial.run()
-        conc.run()
+    plans = [dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, **kw),
+             dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, dapd_early=True, **kw)]
+    _, hi = torch.cuda.Stream.priority_range()
+    main = torch.cuda.Stream(priority=hi)
     torch.cuda.synchronize()
-    for k in serial.out:
-        np.testing.assert_array_equal(serial.out[k][0].cpu().numpy(), conc.out[k][0].cpu().numpy())
-        np.testing.assert_array_equal(serial.out[k][1].cpu().numpy(), conc.out[k][1].cpu().numpy())
-    np.testing.assert_array_equal(serial.block_len.cpu().numpy(), conc.block_len.cpu().numpy())
+    with torch.cuda.stream(main):
+        for _ in range(3):
+            serial.run()
+            for p in plans:
+                p.run()
+    torch.cuda.synchronize()
+    for conc in plans:
+        for k in serial.out:
+            np.testing.assert_array_equal(serial.out[k][0].cpu().numpy(), conc.out[k][0].cpu().numpy())
+            np.testing.assert_array_equal(serial.out[k][1].cpu().numpy(), conc.out[k][1].cpu().numpy())
+        np.testing.assert_array_equal(serial.block_len.cpu().numpy(), conc.block_len.cpu().numpy())
