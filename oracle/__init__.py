@@ -57,6 +57,9 @@ def _load():
             lib.oracle_dapd.argtypes = [_P, _I32, _I32, _I32, _I32, _I64, _I64, _I64, _I64, _I32, _I32,
                                         _P, _P, _F, _F, _F, _I32, _P, _P, _P, _P, _P, _P]
             lib.oracle_greedy_mis.argtypes = [_I32, _P, _P, _P]
+            lib.oracle_select_topk.argtypes = [_P, _P, _I32, _I32, _I32, _P, _P]
+            lib.oracle_select_factor.argtypes = [_P, _P, _I32, _I32, _F, _P, _P]
+            lib.oracle_parallel_certificate.argtypes = [_P, _P, _I32, _I32, _P]
             lib.oracle_set_threads.argtypes = [_I32]
             lib.oracle_get_threads.restype = _I32
             _lib = lib
@@ -211,3 +214,38 @@ def greedy_mis(adj, order):
     kept = np.zeros(n, np.uint8)
     lib.oracle_greedy_mis(n, _ptr(adj), _ptr(order), _ptr(kept))
     return kept
+
+
+def select_topk(conf, masked, k):
+    """Fixed top-K per step (Fast-dLLM review, Prior limitations)."""
+    lib = _load()
+    conf = np.ascontiguousarray(conf, dtype=np.float64)
+    masked = np.ascontiguousarray(masked, dtype=np.uint8)
+    B, blk = masked.shape
+    sel = np.zeros((B, blk), np.uint8)
+    n = np.zeros(B, np.int32)
+    lib.oracle_select_topk(_ptr(conf), _ptr(masked), B, blk, int(k), _ptr(sel), _ptr(n))
+    return sel, n
+
+
+def select_factor(conf, masked, f):
+    """Fast-dLLM factor decoding (Fast-dLLM review, Method, appendix variant)."""
+    lib = _load()
+    conf = np.ascontiguousarray(conf, dtype=np.float64)
+    masked = np.ascontiguousarray(masked, dtype=np.uint8)
+    B, blk = masked.shape
+    sel = np.zeros((B, blk), np.uint8)
+    n = np.zeros(B, np.int32)
+    lib.oracle_select_factor(_ptr(conf), _ptr(masked), B, blk, float(f), _ptr(sel), _ptr(n))
+    return sel, n
+
+
+def parallel_certificate(conf, selected):
+    """Theorem-1 certificate of a selection (Fast-dLLM review, Key idea)."""
+    lib = _load()
+    conf = np.ascontiguousarray(conf, dtype=np.float64)
+    selected = np.ascontiguousarray(selected, dtype=np.uint8)
+    B, blk = selected.shape
+    out = np.zeros(B, np.uint8)
+    lib.oracle_parallel_certificate(_ptr(conf), _ptr(selected), B, blk, _ptr(out))
+    return out

@@ -505,3 +505,83 @@ void oracle_greedy_mis(int n, const uint8_t* adj, const int32_t* order, uint8_t*
         if (ok) kept[x] = 1;
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Confidence order of the masked positions of one block: (conf desc,
+ * position asc), compared in fp32.  Returns the count m; order[0..m).
+ * ------------------------------------------------------------------------ */
+static int masked_by_conf(const double* c, const uint8_t* mk, int blk, int* order) {
+    int m = 0;
+    for (int i = 0; i < blk; ++i)
+        if (mk[i]) order[m++] = i;
+    for (int a = 1; a < m; ++a) {
+        int x = order[a], k = a - 1;
+        while (k >= 0 && conf_before(c, x, order[k])) { order[k + 1] = order[k]; --k; }
+        order[k + 1] = x;
+    }
+    return m;
+}
+
+/* Fixed top-K per step (Fast-dLLM review, Prior limitations: LLaDA's default
+ * commits K tokens per step whatever their confidence): the min(K, masked)
+ * masked positions of highest confidence, ties to the lower position. */
+void oracle_select_topk(const double* conf, const uint8_t* masked, int batch, int blk, int k,
+                        uint8_t* selected, int32_t* n_selected) {
+    int* order = (int*)malloc(sizeof(int) * (size_t)(blk > 0 ? blk : 1));
+    for (int b = 0; b < batch; ++b) {
+        const double* c = conf + (int64_t)b * blk;
+        uint8_t* sel = selected + (int64_t)b * blk;
+        int m = masked_by_conf(c, masked + (int64_t)b * blk, blk, order);
+        int n = k < m ? k : m;
+        for (int i = 0; i < blk; ++i) sel[i] = 0;
+        for (int r = 0; r < n; ++r) sel[order[r]] = 1;
+        n_selected[b] = n;
+    }
+    free(order);
+}
+
+/* Factor decoding (Fast-dLLM review, Method, appendix variant): with
+ * c^(1) >= c^(2) >= ... the masked confidences in decreasing order, commit
+ * the top n* positions, n* = the largest n with (n + 1)(1 - c^(n)) < f,
+ * evaluated in fp32.  The left side grows with n, so the qualifying n form a
+ * prefix.  If no n qualifies, the top position alone is committed (the
+ * threshold rule's progress guarantee). */
+void oracle_select_factor(const double* conf, const uint8_t* masked, int batch, int blk, float f,
+                          uint8_t* selected, int32_t* n_selected) {
+    int* order = (int*)malloc(sizeof(int) * (size_t)(blk > 0 ? blk : 1));
+    for (int b = 0; b < batch; ++b) {
+        const double* c = conf + (int64_t)b * blk;
+        uint8_t* sel = selected + (int64_t)b * blk;
+        int m = masked_by_conf(c, masked + (int64_t)b * blk, blk, order);
+        int n = 0;
+        for (int r = 0; r < m; ++r) {
+            float cn = (float)c[order[r]];
+            float lhs = (float)(r + 2) * (1.0f - cn);
+            if (lhs < f) n = r + 1;
+        }
+        if (n == 0 && m > 0) n = 1;
+        for (int i = 0; i < blk; ++i) sel[i] = 0;
+        for (int r = 0; r < n; ++r) sel[order[r]] = 1;
+        n_selected[b] = n;
+    }
+    free(order);
+}
+
+/* Theorem-1 certificate (Fast-dLLM review, Key idea): committing the n
+ * selected positions in parallel gives the same tokens as committing them one
+ * by one greedily when every one of them has confidence above 1 - 1/(n+1).
+ * Tested in fp32; an empty selection is certified. */
+void oracle_parallel_certificate(const double* conf, const uint8_t* selected, int batch, int blk,
+                                 uint8_t* certified) {
+    for (int b = 0; b < batch; ++b) {
+        const double* c = conf + (int64_t)b * blk;
+        const uint8_t* sel = selected + (int64_t)b * blk;
+        int n = 0;
+        for (int i = 0; i < blk; ++i) n += sel[i] ? 1 : 0;
+        float bound = 1.0f - 1.0f / (float)(n + 1);
+        int ok = 1;
+        for (int i = 0; i < blk; ++i)
+            if (sel[i] && !((float)c[i] > bound)) ok = 0;
+        certified[b] = (uint8_t)ok;
+    }
+}
