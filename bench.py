@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--early-dapd-fork", action="store_true",
                     help="start the DAPD attention graph at the beginning of the step on the low-priority side "
                          "stream (it then shares the row pass's last wave; default: fork after the row pass)")
+    ap.add_argument("--extra-rules", default="",
+                    help="comma list of extra selection rules to run in every step: topk, factor")
     ap.add_argument("--workload", default="batched",
                     help="batched (default, the headline), tiny, llada_step, depcap_window, stress_graph, stress_bulk")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
@@ -236,7 +238,8 @@ def run_native(args, rank, world, local):
     common = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
                   gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
                   bulk_frac=cfg.bulk_frac, status=status)
-    common.update(rules=cfg.rules, cap_scope_from_boundary=(cfg.name == "depcap_window"),
+    extra = tuple(r for r in args.extra_rules.split(",") if r)
+    common.update(rules=tuple(cfg.rules) + extra, cap_scope_from_boundary=(cfg.name == "depcap_window"),
                   concurrent_dapd=not args.serial_dapd, dapd_early=args.early_dapd_fork)
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 

@@ -34,9 +34,12 @@ from ._binding import (  # noqa: F401
     new_status,
     row_stats,
     select_threshold,
+    select_topk,
+    select_factor,
+    parallel_certificate,
 )
 
 __all__ = [
-    "row_stats", "select_threshold", "depcap_boundary", "cap_select", "dapd_graph_mis", "dapd_graph", "dapd_select",
+    "row_stats", "select_threshold", "select_topk", "select_factor", "parallel_certificate", "depcap_boundary", "cap_select", "dapd_graph_mis", "dapd_graph", "dapd_select",
     "StepPlan", "alloc_row_stats", "cap_workspace", "dapd_workspace", "new_status", "RowStats", "DlmError", "lib",
 ]

@@ -67,11 +67,15 @@ def lib():
         L.dlm_dapd_workspace_size.argtypes = [I32, I32]
         L.dlm_dapd_graph_mis.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
+        L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
+        L.dlm_select_factor.argtypes = [P, P, I32, I32, F, P, P, P]
+        L.dlm_parallel_certificate.argtypes = [P, P, I32, I32, P, P]
         L.dlm_dapd_graph.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                      P, ctypes.POINTER(DapdParams), P, P, P, P, Z, P, P]
         L.dlm_dapd_select.argtypes = [P, P, I32, I32, ctypes.POINTER(DapdParams), P, P, P, Z, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
-                  "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select"):
+                  "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select", "dlm_select_topk",
+                  "dlm_select_factor", "dlm_parallel_certificate"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -166,6 +170,48 @@ def select_threshold(conf: torch.Tensor, masked: torch.Tensor, tau: float = 0.9,
     _check(lib().dlm_select_threshold(_p(conf), _p(masked), B, blk, float(tau), _p(selected), _p(n_selected),
                                       _stream(conf.device)))
     return selected, n_selected
+
+
+def select_topk(conf: torch.Tensor, masked: torch.Tensor, k: int, *, selected=None, n_selected=None):
+    """dlm_select_topk: the k most confident masked positions per sequence."""
+    _need_cuda(conf, masked)
+    B, blk = masked.shape
+    conf = conf.reshape(B, blk).contiguous()
+    masked = _u8(masked)
+    if selected is None:
+        selected = torch.empty((B, blk), dtype=torch.uint8, device=conf.device)
+    if n_selected is None:
+        n_selected = torch.empty(B, dtype=torch.int32, device=conf.device)
+    _check(lib().dlm_select_topk(_p(conf), _p(masked), B, blk, int(k), _p(selected), _p(n_selected),
+                                 _stream(conf.device)))
+    return selected, n_selected
+
+
+def select_factor(conf: torch.Tensor, masked: torch.Tensor, f: float, *, selected=None, n_selected=None):
+    """dlm_select_factor: Fast-dLLM factor decoding."""
+    _need_cuda(conf, masked)
+    B, blk = masked.shape
+    conf = conf.reshape(B, blk).contiguous()
+    masked = _u8(masked)
+    if selected is None:
+        selected = torch.empty((B, blk), dtype=torch.uint8, device=conf.device)
+    if n_selected is None:
+        n_selected = torch.empty(B, dtype=torch.int32, device=conf.device)
+    _check(lib().dlm_select_factor(_p(conf), _p(masked), B, blk, float(f), _p(selected), _p(n_selected),
+                                   _stream(conf.device)))
+    return selected, n_selected
+
+
+def parallel_certificate(conf: torch.Tensor, selected: torch.Tensor, *, out=None):
+    """dlm_parallel_certificate: Theorem-1 condition of each sequence's selection."""
+    _need_cuda(conf, selected)
+    B, blk = selected.shape
+    conf = conf.reshape(B, blk).contiguous()
+    selected = _u8(selected)
+    if out is None:
+        out = torch.empty(B, dtype=torch.uint8, device=conf.device)
+    _check(lib().dlm_parallel_certificate(_p(conf), _p(selected), B, blk, _p(out), _stream(conf.device)))
+    return out
 
 
 def depcap_boundary(kl: torch.Tensor, entropy: torch.Tensor, lam: float = 1.0, L_min: int = 8,
@@ -311,7 +357,7 @@ class StepPlan:
                  tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=None, high_tier_unconditional=False,
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
-                 row_index=None, concurrent_dapd=False, dapd_early=False):
+                 row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -343,6 +389,15 @@ class StepPlan:
             self.out["threshold"] = (s, n)
             self._calls.append((L.dlm_select_threshold, (_p(st.conf), _p(self.masked), B, blk, ctypes.c_float(tau),
                                                           _p(s), _p(n))))
+        if "topk" in rules:
+            s_, n_ = torch.zeros((B, blk), **u8), torch.zeros(B, **i32)
+            self.out["topk"] = (s_, n_)
+            self._calls.append((L.dlm_select_topk, (_p(st.conf), _p(self.masked), B, blk, int(topk_k), _p(s_), _p(n_))))
+        if "factor" in rules:
+            s_, n_ = torch.zeros((B, blk), **u8), torch.zeros(B, **i32)
+            self.out["factor"] = (s_, n_)
+            self._calls.append((L.dlm_select_factor, (_p(st.conf), _p(self.masked), B, blk, ctypes.c_float(factor_f),
+                                                       _p(s_), _p(n_))))
         self.block_len = None
         if "boundary" in rules:
             if prev is None:
@@ -410,7 +465,7 @@ class StepPlan:
     @property
     def n_launches(self) -> int:
         """Kernels launched per step: 1 row pass + 1 threshold + 1 boundary + 3 CAP + 3 DAPD."""
-        per = {"threshold": 1, "boundary": 1, "cap": 3, "dapd": 3}
+        per = {"threshold": 1, "boundary": 1, "cap": 3, "dapd": 3, "topk": 1, "factor": 1}
         return 1 + sum(per[r] for r in self.rules)
 
     def run(self, stream=None, events=None, rules_only=False):

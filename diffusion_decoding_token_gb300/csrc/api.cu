@@ -98,6 +98,33 @@ dlm_status dlm_select_threshold(const float* conf, const uint8_t* masked, int32_
     return from_cuda(dlm::launch_threshold(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dlm_status dlm_select_topk(const float* conf, const uint8_t* masked, int32_t batch, int32_t blk, int32_t k,
+                           uint8_t* selected, int32_t* n_selected, dlm_stream_t stream) {
+    if (batch < 0 || blk < 1 || blk > DLM_MAX_BLK || k < 0) return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!conf || !masked || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
+    dlm::RankSelectArgs a{conf, masked, batch, blk, 0, k, 0.f, selected, n_selected};
+    return from_cuda(dlm::launch_rank_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_select_factor(const float* conf, const uint8_t* masked, int32_t batch, int32_t blk, float f,
+                             uint8_t* selected, int32_t* n_selected, dlm_stream_t stream) {
+    if (batch < 0 || blk < 1 || blk > DLM_MAX_BLK || !isfinite(f)) return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!conf || !masked || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
+    dlm::RankSelectArgs a{conf, masked, batch, blk, 1, 0, f, selected, n_selected};
+    return from_cuda(dlm::launch_rank_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_parallel_certificate(const float* conf, const uint8_t* selected, int32_t batch, int32_t blk,
+                                    uint8_t* certified, dlm_stream_t stream) {
+    if (batch < 0 || blk < 1 || blk > DLM_MAX_BLK) return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!conf || !selected || !certified) return DLM_ERR_INVALID_ARG;
+    dlm::CertificateArgs a{conf, selected, batch, blk, certified};
+    return from_cuda(dlm::launch_certificate(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dlm_status dlm_depcap_boundary(const float* kl, const float* entropy, int32_t batch,
                                int32_t L_window, const uint8_t* cold_start,
                                const dlm_depcap_params* params, int32_t* block_len,

@@ -37,6 +37,26 @@ struct ThresholdArgs {
 };
 cudaError_t launch_threshold(const ThresholdArgs& a, cudaStream_t s);
 
+struct RankSelectArgs {
+    const float* conf;
+    const uint8_t* masked;
+    int batch, blk;
+    int mode;  // 0: top-K, 1: factor decoding
+    int k;
+    float f;
+    uint8_t* selected;
+    int32_t* n_selected;
+};
+cudaError_t launch_rank_select(const RankSelectArgs& a, cudaStream_t s);
+
+struct CertificateArgs {
+    const float* conf;
+    const uint8_t* selected;
+    int batch, blk;
+    uint8_t* certified;
+};
+cudaError_t launch_certificate(const CertificateArgs& a, cudaStream_t s);
+
 struct BoundaryArgs {
     const float* kl;
     const float* entropy;

@@ -1,6 +1,7 @@
-// select.cu -- Fast-dLLM threshold selection and the DepGA-Block boundary.
+// select.cu -- Fast-dLLM threshold selection, the DepGA-Block boundary, the
+// fixed top-K and factor-decoding rules and the Theorem-1 certificate.
 //
-// Both are per-sequence decisions over at most a few hundred values, so each
+// All are per-sequence decisions over at most a few hundred values, so each
 // sequence is one CTA working out of registers and shared memory; the cost is
 // launch latency, not bandwidth.
 #include "common.cuh"
@@ -158,6 +159,61 @@ __global__ void __launch_bounds__(kBndThreads) boundary_kernel(BoundaryArgs a) {
     }
 }
 
+// Rank of each masked position in (conf desc, position asc) order, counted
+// against all masked positions of the block (all-pairs in shared memory).
+__device__ __forceinline__ int conf_rank(const float* s_c, const unsigned char* s_m, int blk, int i) {
+    const float c = s_c[i];
+    int r = 0;
+    for (int j = 0; j < blk; ++j) {
+        if (!s_m[j]) continue;
+        const float cj = s_c[j];
+        r += (cj > c) || (cj == c && j < i);
+    }
+    return r;
+}
+
+// Fixed top-K (Fast-dLLM review, Prior limitations: LLaDA's default commits
+// K tokens per step whatever their confidence) and factor decoding (Fast-dLLM
+// review, Method, appendix variant: the largest n with (n+1)(1 - c^(n)) < f,
+// the top position alone when no n qualifies).  mode 0 = top-K, 1 = factor.
+__global__ void __launch_bounds__(kSelThreads) rank_select_kernel(RankSelectArgs a) {
+    __shared__ float s_c[kSelThreads];
+    __shared__ unsigned char s_m[kSelThreads];
+    const int b = blockIdx.x, i = threadIdx.x;
+    const bool valid = i < a.blk;
+    const int64_t o = (int64_t)b * a.blk + i;
+    const bool m = valid && a.masked[o] != 0;
+    s_c[i] = m ? a.conf[o] : 0.f;
+    s_m[i] = m;
+    const int M = __syncthreads_count(m);
+    const int r = m ? conf_rank(s_c, s_m, a.blk, i) : 0x7fffffff;
+    int n;
+    if (a.mode == 0) {
+        n = min(a.k, M);
+    } else {
+        const bool ok = m && __fmul_rn((float)(r + 2), __fsub_rn(1.0f, s_c[i])) < a.f;
+        n = __syncthreads_count(ok);  // the qualifying n form a prefix of the order
+        if (n == 0 && M > 0) n = 1;
+    }
+    if (valid) a.selected[o] = (m && r < n) ? 1 : 0;
+    if (i == 0) a.n_selected[b] = n;
+}
+
+// Theorem-1 certificate (Fast-dLLM review, Key idea): every one of the n
+// selected positions has confidence above 1 - 1/(n+1); an empty selection is
+// certified.
+__global__ void __launch_bounds__(kSelThreads) certificate_kernel(CertificateArgs a) {
+    const int b = blockIdx.x, i = threadIdx.x;
+    const bool valid = i < a.blk;
+    const int64_t o = (int64_t)b * a.blk + i;
+    const bool s = valid && a.selected[o] != 0;
+    const int n = __syncthreads_count(s);
+    const float bound = __fsub_rn(1.0f, __fdiv_rn(1.0f, (float)(n + 1)));
+    const bool bad = s && !(a.conf[o] > bound);
+    const int any_bad = __syncthreads_or(bad);
+    if (i == 0) a.certified[b] = any_bad ? 0 : 1;
+}
+
 }  // namespace
 
 cudaError_t launch_threshold(const ThresholdArgs& a, cudaStream_t s) {
@@ -166,6 +222,22 @@ cudaError_t launch_threshold(const ThresholdArgs& a, cudaStream_t s) {
     cfg.blockDim = dim3(kSelThreads);
     cfg.stream = s;
     return cudaLaunchKernelEx(&cfg, threshold_kernel, a);
+}
+
+cudaError_t launch_rank_select(const RankSelectArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.batch);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, rank_select_kernel, a);
+}
+
+cudaError_t launch_certificate(const CertificateArgs& a, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.batch);
+    cfg.blockDim = dim3(kSelThreads);
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, certificate_kernel, a);
 }
 
 cudaError_t launch_boundary(const BoundaryArgs& a, cudaStream_t s) {

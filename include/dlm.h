@@ -118,6 +118,40 @@ dlm_status dlm_select_threshold(const float* conf, const uint8_t* masked, int32_
                                 dlm_stream_t stream);
 
 /*
+ * dlm_select_topk -- fixed top-K per step (the LLaDA default that Fast-dLLM
+ * compares against; Fast-dLLM review, "Prior limitations": K tokens are
+ * committed every step whatever their confidence).  Selects the min(k, masked)
+ * masked positions of highest confidence, ties to the lower position.
+ * Arrays as in dlm_select_threshold; k >= 0.
+ */
+dlm_status dlm_select_topk(const float* conf, const uint8_t* masked, int32_t batch, int32_t blk, int32_t k,
+                           uint8_t* selected, int32_t* n_selected, dlm_stream_t stream);
+
+/*
+ * dlm_select_factor -- Fast-dLLM factor decoding (Fast-dLLM review,
+ * "Method", appendix variant).  With c^(1) >= c^(2) >= ... the confidences of
+ * the masked positions in decreasing order, the n* most confident positions
+ * are selected, n* the largest n with (n + 1)(1 - c^(n)) < f (evaluated in
+ * fp32; the qualifying n form a prefix).  If no n qualifies, the single most
+ * confident masked position is selected (reading: the threshold rule's
+ * progress guarantee).  Arrays as in dlm_select_threshold.
+ */
+dlm_status dlm_select_factor(const float* conf, const uint8_t* masked, int32_t batch, int32_t blk, float f,
+                             uint8_t* selected, int32_t* n_selected, dlm_stream_t stream);
+
+/*
+ * dlm_parallel_certificate -- the Theorem-1 condition of the Fast-dLLM review
+ * ("Key idea"): committing the n selected positions in parallel yields the
+ * same tokens as committing them one at a time greedily when each has
+ * confidence above 1 - 1/(n+1).  certified[b] = 1 when every selected position
+ * of sequence b satisfies conf > 1 - 1/(n+1) in fp32 (an empty selection is
+ * certified), else 0.  conf [batch][blk], selected [batch][blk] uint8,
+ * certified [batch] uint8 output.
+ */
+dlm_status dlm_parallel_certificate(const float* conf, const uint8_t* selected, int32_t batch, int32_t blk,
+                                    uint8_t* certified, dlm_stream_t stream);
+
+/*
  * dlm_depcap_boundary -- DepGA-Block: length of the next block.
  *
  * DepCap, "Methodology" and "Technical Contribution": over a window of
