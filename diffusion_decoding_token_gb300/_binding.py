@@ -37,7 +37,8 @@ class CapParams(ctypes.Structure):
 
 class DapdParams(ctypes.Structure):
     _fields_ = [("tau_edge", ctypes.c_float), ("bulk_conf", ctypes.c_float),
-                ("bulk_frac", ctypes.c_float), ("order_mode", ctypes.c_int32)]
+                ("bulk_frac", ctypes.c_float), ("order_mode", ctypes.c_int32),
+                ("preunmask_certain", ctypes.c_int32)]
 
 
 class DlmError(RuntimeError):
@@ -276,7 +277,7 @@ def dapd_workspace(batch: int, blk: int, device) -> torch.Tensor:
 def dapd_graph_mis(attn: torch.Tensor, masked: torch.Tensor, conf: torch.Tensor, tau_edge: float = 0.01,
                    bulk_conf: float = 0.9, bulk_frac: float = 0.5, order_mode: int = 0, block_start: int = 0, *,
                    s_out=None, dtilde_out=None, deg_out=None, workspace=None, status=None, selected=None,
-                   n_selected=None):
+                   n_selected=None, preunmask_certain: bool = False):
     """dlm_dapd_graph_mis on ``attn`` = [B, L, H, N, N] (any element strides with unit
     column stride).  The block is rows/cols [block_start, block_start+blk)."""
     _need_cuda(attn, masked, conf, s_out, dtilde_out, deg_out)
@@ -295,7 +296,7 @@ def dapd_graph_mis(attn: torch.Tensor, masked: torch.Tensor, conf: torch.Tensor,
     if n_selected is None:
         n_selected = torch.empty(B, dtype=torch.int32, device=dev)
     sb, sl, sh, sr, _ = attn.stride()
-    prm = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
+    prm = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode), int(bool(preunmask_certain)))
     _check(lib().dlm_dapd_graph_mis(_p(attn), _dt(attn), B, L, H, sb, sl, sh, sr, int(block_start), blk,
                                     _p(masked), _p(conf.reshape(B, blk).contiguous()), ctypes.byref(prm),
                                     _p(selected), _p(n_selected), _p(s_out), _p(dtilde_out), _p(deg_out),

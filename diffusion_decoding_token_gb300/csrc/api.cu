@@ -201,7 +201,7 @@ dlm_status dapd_prepare(dlm::DapdArgs& a, const void* attn, dlm_dtype dtype, int
                         void* workspace, size_t ws_bytes, bool need_attn) {
     if (need_attn && !dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
     if (!params || batch < 0 || blk < 1 || blk > DLM_MAX_BLK || (params->order_mode != 0 && params->order_mode != 1) ||
-        !isfinite(params->tau_edge))
+        (params->preunmask_certain != 0 && params->preunmask_certain != 1) || !isfinite(params->tau_edge))
         return DLM_ERR_INVALID_ARG;
     if (need_attn && (n_layers < 1 || n_heads < 1 || (int64_t)n_layers * n_heads > (1 << 20) || block_start < 0 ||
                       stride_b < 0 || stride_l < 0 || stride_h < 0 || stride_row < blk))
@@ -239,6 +239,7 @@ dlm_status dapd_prepare(dlm::DapdArgs& a, const void* attn, dlm_dtype dtype, int
     a.bulk_conf = params->bulk_conf;
     a.bulk_frac = params->bulk_frac;
     a.order_mode = params->order_mode;
+    a.preunmask_certain = params->preunmask_certain;
     dlm::dapd_carve(a, workspace);
     return DLM_OK;
 }

@@ -580,6 +580,8 @@ __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
             s = (t == s_i[0]);
             n = 1;
         }
+        if (a.preunmask_certain && m && !s && c == 1.0f) s = true;
+        n = __syncthreads_count(s);
         if (t < a.blk) sel[t] = s ? 1 : 0;
         if (t == 0) a.n_selected[b] = n;
         return;
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
     }
     __syncthreads();
     int mine = 0;
-    if (m && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
+    if (m && (((s_kept[t >> 5] >> (t & 31)) & 1u) || (a.preunmask_certain && a.conf[o] == 1.0f))) {
         sel[t] = 1;
         mine = 1;
     }

@@ -105,6 +105,7 @@ struct DapdArgs {
     const float* conf;
     float tau_edge, bulk_conf, bulk_frac;
     int order_mode;
+    int preunmask_certain;
     long long edge_thresh;   // floor(tau * 2 * L * H * 2^32): edge <=> 2LH 2^32 s > this
     float s_scale;           // 1 / (2 * L * H * 2^32)
     uint8_t* selected;

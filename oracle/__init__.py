@@ -55,7 +55,7 @@ def _load():
                                               _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P]
             lib.oracle_cap_select.restype = _I32
             lib.oracle_dapd.argtypes = [_P, _I32, _I32, _I32, _I32, _I64, _I64, _I64, _I64, _I32, _I32,
-                                        _P, _P, _F, _F, _F, _I32, _P, _P, _P, _P, _P, _P]
+                                        _P, _P, _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P, _P]
             lib.oracle_greedy_mis.argtypes = [_I32, _P, _P, _P]
             lib.oracle_select_topk.argtypes = [_P, _P, _I32, _I32, _I32, _P, _P]
             lib.oracle_select_factor.argtypes = [_P, _P, _I32, _I32, _F, _P, _P]
@@ -177,7 +177,7 @@ def cap_select(logits, argmax, conf, lse, masked, tau_low, tau_high, gamma, p_ma
 
 
 def dapd(attn, masked, conf, tau_edge, bulk_conf=0.9, bulk_frac=0.5, order_mode=0,
-         block_start=0, dtype=None):
+         block_start=0, dtype=None, preunmask_certain=False):
     """DAPD step (DAPD, 整体框架, 关键设计 1-3).
 
     ``attn`` is [B, L, H, N, N] (or the compact block [B, L, H, blk, blk] with
@@ -201,7 +201,7 @@ def dapd(attn, masked, conf, tau_edge, bulk_conf=0.9, bulk_frac=0.5, order_mode=
     sr, sh, sl, sb = N, N * N, H * N * N, L * H * N * N
     lib.oracle_dapd(_ptr(attn), code, B, L, H, sb, sl, sh, sr, int(block_start), blk, _ptr(masked),
                     _ptr(conf), float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode),
-                    _ptr(sel), _ptr(n), _ptr(s), _ptr(dt), _ptr(deg), _ptr(path))
+                    int(bool(preunmask_certain)), _ptr(sel), _ptr(n), _ptr(s), _ptr(dt), _ptr(deg), _ptr(path))
     return dict(selected=sel, n_selected=n, s=s, dtilde=dt, deg=deg, path=path)
 
 

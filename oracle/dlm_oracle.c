@@ -392,12 +392,17 @@ int oracle_cap_select(const void* logits, int dtype, int64_t row_stride,
  * row*sr + col]; the block occupies rows and columns
  * [block_start, block_start+blk).  Outputs s (NaN off V_t), d~, the edge
  * degree, and the path taken (0 graph, 1 late phase).
+ * preunmask_certain (DAPD, 关键设计 3, appendix remark: a position whose
+ * confidence is exactly 1.0 can be unmasked at any time): read as adding
+ * every masked position with conf == 1.0 (fp32) to the selection of either
+ * path; the graph itself is unchanged.
  * ------------------------------------------------------------------------ */
 void oracle_dapd(const void* attn, int dtype, int batch, int n_layers, int n_heads,
                  int64_t sb, int64_t sl, int64_t sh, int64_t sr, int block_start, int blk,
                  const uint8_t* masked, const double* conf, float tau_edge, float bulk_conf,
-                 float bulk_frac, int order_mode, uint8_t* selected, int32_t* n_selected,
-                 double* s_out, double* dtilde_out, int32_t* deg_out, int32_t* path_out) {
+                 float bulk_frac, int order_mode, int preunmask_certain, uint8_t* selected,
+                 int32_t* n_selected, double* s_out, double* dtilde_out, int32_t* deg_out,
+                 int32_t* path_out) {
     int b;
 #pragma omp parallel for schedule(dynamic, 1)
     for (b = 0; b < batch; ++b) {
@@ -426,6 +431,9 @@ void oracle_dapd(const void* attn, int dtype, int batch, int n_layers, int n_hea
                 int t = top_conf(c, mk, blk);
                 if (t >= 0) { sel[t] = 1; n = 1; }
             }
+            if (preunmask_certain)
+                for (int i = 0; i < blk; ++i)
+                    if (mk[i] && !sel[i] && (float)c[i] == 1.0f) { sel[i] = 1; ++n; }
             n_selected[b] = n;
             continue;
         }
@@ -482,6 +490,9 @@ void oracle_dapd(const void* attn, int dtype, int batch, int n_layers, int n_hea
                 if (kept[y] && adj[(int64_t)x * M + y]) { ok = 0; break; }
             if (ok) { kept[x] = 1; sel[node[x]] = 1; ++cnt; }
         }
+        if (preunmask_certain)
+            for (int i = 0; i < blk; ++i)
+                if (mk[i] && !sel[i] && (float)c[i] == 1.0f) { sel[i] = 1; ++cnt; }
         n_selected[b] = cnt;
         free(kept);
         free(ord);

@@ -407,3 +407,24 @@ def test_step_plan_concurrent_matches_serial(dlm):
             np.testing.assert_array_equal(serial.out[k][0].cpu().numpy(), conc.out[k][0].cpu().numpy())
             np.testing.assert_array_equal(serial.out[k][1].cpu().numpy(), conc.out[k][1].cpu().numpy())
         np.testing.assert_array_equal(serial.block_len.cpu().numpy(), conc.block_len.cpu().numpy())
+
+
+@pytest.mark.parametrize("n_masked", [48, 20])
+def test_dapd_preunmask_certain(dlm, n_masked):
+    """Masked positions whose confidence is exactly 1.0 join the selection
+    (graph path with 48/48 masked, late phase with 20/48)."""
+    rng = np.random.default_rng(n_masked)
+    B, L, H, blk = 3, 2, 4, 48
+    sub = (rng.random((B, L, H, blk, blk)) ** 5 * 0.3).astype(np.float32)
+    sub16 = synth.to_f16_bits(sub)
+    masked = np.zeros((B, blk), np.uint8)
+    for b in range(B):
+        masked[b, rng.choice(blk, n_masked, replace=False)] = 1
+    conf = rng.random((B, blk)).astype(np.float32)
+    conf[:, ::5] = 1.0
+    for flag in (False, True):
+        gs, gn = dlm.dapd_graph_mis(to_torch(sub16, synth.F16, "cuda"), cuda(masked), cuda(conf), 0.05,
+                                    preunmask_certain=flag)
+        r = oracle.dapd(sub16, masked, conf.astype(np.float64), 0.05, dtype=synth.F16, preunmask_certain=flag)
+        np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+        np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])

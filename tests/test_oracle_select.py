@@ -305,3 +305,26 @@ def test_dapd_on_generated_workload(oracle):
         assert (adj == w.links[b]).all()
         sel = np.nonzero(r["selected"][b])[0]
         assert is_independent(adj, sel) and is_maximal(adj, sel, nodes)
+
+
+def test_dapd_preunmask_certain(oracle):
+    """Positions of confidence exactly 1.0 join the selection on both paths."""
+    g = __import__("json").load(open(os.path.join(GOLDEN, "dapd_mrf9.json")))
+    n = len(g["nodes"])
+    A = np.full((n, n), 0.001, np.float32)
+    for a, b in g["edges"]:
+        A[a, b] = A[b, a] = 0.1
+    conf = np.array([[0.9, 0.8, 0.95, 0.7, 0.6, 0.99, 0.5, 0.85, 0.75]])
+    conf[0, 6] = 1.0  # Y2: key 0.206, shut out by the kept X3 (order X3, X2, X4, Y2, Y1, ...)
+    masked = np.ones((1, n), np.uint8)
+    plain = oracle.dapd(A[None, None, None], masked, conf, tau_edge=0.05)
+    pre = oracle.dapd(A[None, None, None], masked, conf, tau_edge=0.05, preunmask_certain=True)
+    assert np.nonzero(plain["selected"][0])[0].tolist() == [2, 5, 8]
+    assert np.nonzero(pre["selected"][0])[0].tolist() == [2, 5, 6, 8]
+    assert pre["n_selected"][0] == 4
+    # late phase: certain positions join the confidence rule's selection
+    masked2 = np.zeros((1, n), np.uint8)
+    masked2[0, [0, 1, 3]] = 1
+    conf2 = np.array([[0.95, 1.0, 0.2, 0.3, 0, 0, 0, 0, 0]])
+    r = oracle.dapd(A[None, None, None], masked2, conf2, tau_edge=0.05, preunmask_certain=True)
+    assert r["path"][0] == 1 and np.nonzero(r["selected"][0])[0].tolist() == [0, 1]
