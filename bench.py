@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--early-dapd-fork", action="store_true",
                     help="start the DAPD attention graph at the beginning of the step on the low-priority side "
                          "stream (it then shares the row pass's last wave; default: fork after the row pass)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the rules eagerly instead of replaying them as one captured CUDA graph")
     ap.add_argument("--extra-rules", default="",
                     help="comma list of extra selection rules to run in every step: topk, factor")
     ap.add_argument("--workload", default="batched",
@@ -246,6 +248,25 @@ def run_native(args, rank, world, local):
     for _ in range(args.warmup):
         plan.run(stream)
     torch.cuda.synchronize()
+    # the rules (everything after the row pass) as one CUDA graph; the row
+    # pass stays an eager launch so CUDA events can bracket it every step
+    rules_graph = None
+    if not args.no_graph:
+        rules_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(rules_graph, stream=stream):
+            plan.run(rules_only=True)
+        torch.cuda.synchronize()
+
+    def run_step(ev=None):
+        if rules_graph is None:
+            plan.run(stream, events=ev)
+            return
+        plan.run_rows(stream, events=ev)
+        rules_graph.replay()
+
+    for _ in range(args.warmup):
+        run_step()
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
 
@@ -258,7 +279,7 @@ def run_native(args, rank, world, local):
         t_end = time.time() + 1.0
         while time.time() < t_end:
             for _ in range(50):
-                plan.run(stream)
+                run_step()
             torch.cuda.synchronize()
     torch.cuda.synchronize()
     if world > 1:
@@ -268,7 +289,7 @@ def run_native(args, rank, world, local):
     w0 = time.time()
     t0.record(stream)
     for k in range(args.steps):
-        plan.run(stream, events=evs[k])
+        run_step(evs[k])
     t1.record(stream)
     host_ms = (time.time() - w0) * 1000.0 / args.steps
     torch.cuda.synchronize()
@@ -285,10 +306,10 @@ def run_native(args, rank, world, local):
     r0 = torch.cuda.Event(enable_timing=True)
     r1 = torch.cuda.Event(enable_timing=True)
     for _ in range(3):
-        plan.run(stream, rules_only=True)
+        rules_graph.replay() if rules_graph is not None else plan.run(stream, rules_only=True)
     r0.record(stream)
     for _ in range(100):
-        plan.run(stream, rules_only=True)
+        rules_graph.replay() if rules_graph is not None else plan.run(stream, rules_only=True)
     r1.record(stream)
     torch.cuda.synchronize()
     rules_ms = r0.elapsed_time(r1) / 100
@@ -468,6 +489,7 @@ def main():
         "logit_gbps": k1_gbs,
         "kernels_ms": {"row_stats": k1_ms, "four_rules": r["rules_ms"]},
         "host_enqueue_ms_per_step": r["host_ms"],
+        "rules_as_cuda_graph": not args.no_graph,
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
                      "traffic": recorded_traffic() if (cfg.batch == 64 and not args.compact_attn) else None, "kernel": "row_stats", "peak_kind": peak_kind,
                      "algorithmic_bytes": k1_bytes},

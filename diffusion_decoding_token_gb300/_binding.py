@@ -469,6 +469,17 @@ class StepPlan:
         per = {"threshold": 1, "boundary": 1, "cap": 3, "dapd": 3, "topk": 1, "factor": 1}
         return 1 + sum(per[r] for r in self.rules)
 
+    def run_rows(self, stream=None, events=None):
+        """Issue only the row pass (e.g. ahead of a captured graph of the
+        rules, see ``run(rules_only=True)``)."""
+        st = stream or torch.cuda.current_stream(self.dev)
+        fn, args = self._calls[0]
+        if events is not None:
+            events[0].record(st)
+        _check(fn(*args, ctypes.c_void_p(st.cuda_stream)))
+        if events is not None:
+            events[1].record(st)
+
     def run(self, stream=None, events=None, rules_only=False):
         """Issue the step on ``stream`` (default: the current stream).  With
         ``events`` = (e0, e1), e0/e1 are recorded around the row pass.
