@@ -282,13 +282,14 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     }
 }
 
-constexpr int kStages = 4;                       // bulk-copy ring depth
+constexpr int kStages = 3;                       // bulk-copy ring depth
+constexpr int kBoxBytes = 32768;                 // target bytes per bulk tensor copy
 constexpr long long kWaitLimit = 2000000000LL;   // ~1 s at 2 GHz
 
 // The same sums as dapd_accum_kernel, with the attention staged by the TMA
 // engine: one thread issues bulk tensor copies of [box_heads x rows x
-// box_cols] boxes (about 16 KB) into a kStages-deep shared-memory ring, so a
-// CTA keeps up to 64 KB in flight without spending registers on it; every
+// box_cols] boxes (about 32 KB) into a kStages-deep shared-memory ring, so a
+// CTA keeps up to 96 KB in flight without spending registers on it; every
 // thread then sums its (row, 8-column vector) slots over the heads of each box.
 // Rows of the tile that are not masked are loaded but never stored.
 template <int DT>
@@ -698,7 +699,7 @@ bool encode_attention_map(DapdArgs& a, CUtensorMap* map) {
     const int64_t strides[4] = {a.sr, a.sh, a.sl, a.sb};
     for (int k = 0; k < 4; ++k)
         if (strides[k] <= 0 || (strides[k] * esz) % 16 != 0 || strides[k] * esz >= (1LL << 40)) return false;
-    int HB = 16384 / (CB * a.row_tile * esz);
+    int HB = kBoxBytes / (CB * a.row_tile * esz);
     HB = std::max(1, std::min(HB, std::min(a.n_heads, 256)));
     const cuuint64_t dims[5] = {(cuuint64_t)(a.block_start + a.blk), (cuuint64_t)(a.block_start + a.blk),
                                 (cuuint64_t)a.n_heads, (cuuint64_t)a.n_layers, (cuuint64_t)a.batch};
@@ -710,7 +711,7 @@ bool encode_attention_map(DapdArgs& a, CUtensorMap* map) {
                                    : a.dtype == DLM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const CUresult r = enc(map, dt, 5, const_cast<void*>(a.attn), dims, gstr, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     a.box_cols = CB;
@@ -741,7 +742,7 @@ cudaError_t tma_smem_attribute() {
     std::lock_guard<std::mutex> lock(mu);
     if (dev >= 0 && dev < kMaxDev && !smem_set[dev]) {
         e = cudaFuncSetAttribute(dapd_accum_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kStages * 16384 + 16384));
+                                 (int)(kStages * kBoxBytes + 16384));
         if (e != cudaSuccess) return e;
         smem_set[dev] = true;
     }
