@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     select_factor,
     parallel_certificate,
 )
+from .driver import SyntheticDecoder  # noqa: F401
 
 __all__ = [
     "row_stats", "select_threshold", "select_topk", "select_factor", "parallel_certificate", "depcap_boundary", "cap_select", "dapd_graph_mis", "dapd_graph", "dapd_select",

@@ -285,3 +285,63 @@ def make(cfg: Config | str, seed: int, attempts=None) -> Workload:
         with ThreadPoolExecutor(workers) as ex:
             list(ex.map(lambda b: w.replace_sequence(b, int(att[b])), range(B)))
     return w
+
+
+# ---------------------------------------------------------------------------
+# Multi-step decoding problems (inputs of the synthetic decode driver).
+#
+# Per sequence of blk positions: a planted dependency graph (band + random
+# links, the same recipe as the attention), a target token t_i and a decoy
+# d_i per position, background logits N(0, sigma^2), a target margin
+# u_i ~ U(u_lo, u_hi) and a decoy strength v_i ~ U(0, v_hi).  The state-
+# dependent logits are formed by the driver (see
+# diffusion_decoding_token_gb300.driver): with s_i the fraction of i's
+# neighbours already decoded,
+#     z_i[t_i] = c0 + u_i + kappa * s_i,   z_i[d_i] = c0 + v_i * (1 - s_i),
+# c0 = ln(V - 1) + sigma^2 / 2 (the background's expected log-mass), so a
+# position whose neighbours are still masked may prefer its decoy.
+# ---------------------------------------------------------------------------
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str = "decode_small"
+    batch: int = 16
+    blk: int = 32
+    vocab: int = 4096
+    sigma: float = 1.0
+    u_lo: float = 0.0
+    u_hi: float = 6.0
+    v_hi: float = 5.0
+    kappa: float = 6.0
+    band: int = 1
+    p_link: float = 0.05
+    n_layers: int = 2
+    n_heads: int = 4
+    tau_edge: float = 0.05
+
+
+def decode_problem(cfg: DecodeConfig, seed: int) -> dict:
+    """Static inputs of one multi-step decoding problem (numpy arrays)."""
+    B, blk, V = cfg.batch, cfg.blk, cfg.vocab
+    base = np.empty((B * blk, V), np.float32)
+    target = np.empty((B, blk), np.int64)
+    decoy = np.empty((B, blk), np.int64)
+    u = np.empty((B, blk), np.float32)
+    v = np.empty((B, blk), np.float32)
+    links = np.empty((B, blk, blk), bool)
+    attn = np.empty((B, cfg.n_layers, cfg.n_heads, blk, blk), np.uint16)
+    acfg = Config(name="decode_attn", batch=1, blk=blk, vocab=1, logit_dtype=F32, sigma=1.0, boost_lo=0,
+                  boost_hi=0, boost_frac=0, prev_sigma=0, n_layers=cfg.n_layers, n_heads=cfg.n_heads,
+                  seq_len=blk, band=cfg.band, p_link=cfg.p_link, tau_edge=cfg.tau_edge, attn_sigma=0.25)
+    for b in range(B):
+        rng = _rng(seed, b, 0, 10)
+        base[b * blk:(b + 1) * blk] = rng.standard_normal((blk, V), dtype=np.float32) * np.float32(cfg.sigma)
+        t = rng.integers(0, V, blk)
+        d = (t + rng.integers(1, V, blk)) % V
+        target[b], decoy[b] = t, d
+        u[b] = rng.uniform(cfg.u_lo, cfg.u_hi, blk).astype(np.float32)
+        v[b] = rng.uniform(0.0, cfg.v_hi, blk).astype(np.float32)
+        a, P = sequence_attention(acfg, seed + 7919, b, 0)
+        attn[b] = a
+        links[b] = P
+    c0 = np.float32(math.log(V - 1) + cfg.sigma * cfg.sigma / 2.0)
+    return dict(cfg=cfg, base=base, target=target, decoy=decoy, u=u, v=v, links=links, attn=attn, c0=c0)
