@@ -59,6 +59,9 @@ def parse():
                     help="comma list of extra selection rules to run in every step: topk, factor")
     ap.add_argument("--workload", default="batched",
                     help="batched (default, the headline), tiny, llada_step, depcap_window, stress_graph, stress_bulk")
+    ap.add_argument("--driver", action="store_true",
+                    help="instead of the step benchmark: whole synthetic decodes per rule (steps/NFE, error rate, "
+                         "decode time as one CUDA graph)")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
     ap.add_argument("--compact-attn", action="store_true",
                     help="hold only the attention block [B, L, H, blk, blk] on the device (small profiling cases)")
@@ -471,8 +474,49 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_driver(args):
+    """Whole decodes of the synthetic problem, one per rule: steps per
+    sequence (NFE), wrong-token rate and the decode's device time when the
+    whole decode is replayed as one CUDA graph (the stand-in model's torch
+    ops included)."""
+    import torch
+
+    import synth
+    from diffusion_decoding_token_gb300.driver import RULES, SyntheticDecoder
+    cfg = synth.DecodeConfig(batch=args.batch or 64, blk=32, vocab=32768)
+    prob = synth.decode_problem(cfg, seed=args.seed)
+    dev = torch.device("cuda:0")
+    out = {}
+    for rule in RULES:
+        dec = SyntheticDecoder(prob, rule, dev)
+        dec.capture()
+        times = []
+        for _ in range(max(3, args.warmup) + 5):
+            dec.reset()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dec.graph.replay()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+        sm = dec.summary()
+        ms = statistics.median(times[max(3, args.warmup):])
+        out[rule] = {"mean_steps": sm["mean_steps"], "max_steps": int(sm["steps"].max()),
+                     "error_rate": sm["error_rate"], "tokens_per_step": sm["tokens_per_step"],
+                     "unfinished": sm["unfinished"], "graph_steps": dec.graph_steps, "ms_per_decode": ms,
+                     "tokens_per_s": cfg.batch * cfg.blk / (ms / 1000.0), "status": sm["status"]}
+    print(json.dumps({"mode": "decode_driver", "data": "synthetic",
+                      "config": {"batch": cfg.batch, "blk": cfg.blk, "vocab": cfg.vocab, "logits": "f32",
+                                 "attention": f"f16 {cfg.n_layers}x{cfg.n_heads} over the block"},
+                      "rules": out}), flush=True)
+
+
 def main():
     args = parse()
+    if args.driver:
+        run_driver(args)
+        return
     rank, world, local = dist_env()
     if world > 1:
         import torch.distributed as td

@@ -68,6 +68,7 @@ def lib():
         L.dlm_dapd_workspace_size.argtypes = [I32, I32]
         L.dlm_dapd_graph_mis.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
+        L.dlm_depcap_boundary_ragged.argtypes = [P, P, I32, I32, P, P, ctypes.POINTER(DepcapParams), P, P, P]
         L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
         L.dlm_select_factor.argtypes = [P, P, I32, I32, F, P, P, P]
         L.dlm_parallel_certificate.argtypes = [P, P, I32, I32, P, P]
@@ -76,7 +77,7 @@ def lib():
         L.dlm_dapd_select.argtypes = [P, P, I32, I32, ctypes.POINTER(DapdParams), P, P, P, Z, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
                   "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select", "dlm_select_topk",
-                  "dlm_select_factor", "dlm_parallel_certificate"):
+                  "dlm_select_factor", "dlm_parallel_certificate", "dlm_depcap_boundary_ragged"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -217,9 +218,11 @@ def parallel_certificate(conf: torch.Tensor, selected: torch.Tensor, *, out=None
 
 def depcap_boundary(kl: torch.Tensor, entropy: torch.Tensor, lam: float = 1.0, L_min: int = 8,
                     smooth_w: int = 1, norm_mode: int = 0, cold_start: torch.Tensor | None = None, *,
-                    block_len=None, score=None):
-    """dlm_depcap_boundary over [B, L_window] KL / entropy; returns (block_len, score)."""
-    _need_cuda(kl, entropy, cold_start)
+                    window_len: torch.Tensor | None = None, block_len=None, score=None):
+    """dlm_depcap_boundary over [B, L_window] KL / entropy; returns (block_len, score).
+    With ``window_len`` ([B] int32) it calls dlm_depcap_boundary_ragged:
+    sequence b uses the first window_len[b] entries of its row."""
+    _need_cuda(kl, entropy, cold_start, window_len)
     B, Lw = kl.shape
     kl = kl.contiguous()
     entropy = entropy.reshape(B, Lw).contiguous()
@@ -230,8 +233,13 @@ def depcap_boundary(kl: torch.Tensor, entropy: torch.Tensor, lam: float = 1.0, L
     if score is None:
         score = torch.empty((B, Lw), dtype=torch.float32, device=kl.device)
     prm = DepcapParams(float(lam), int(L_min), int(smooth_w), int(norm_mode))
-    _check(lib().dlm_depcap_boundary(_p(kl), _p(entropy), B, Lw, _p(cold_start), ctypes.byref(prm),
-                                     _p(block_len), _p(score), _stream(kl.device)))
+    if window_len is None:
+        _check(lib().dlm_depcap_boundary(_p(kl), _p(entropy), B, Lw, _p(cold_start), ctypes.byref(prm),
+                                         _p(block_len), _p(score), _stream(kl.device)))
+    else:
+        window_len = window_len.to(torch.int32).contiguous()
+        _check(lib().dlm_depcap_boundary_ragged(_p(kl), _p(entropy), B, Lw, _p(window_len), _p(cold_start),
+                                                ctypes.byref(prm), _p(block_len), _p(score), _stream(kl.device)))
     return block_len, score
 
 

@@ -135,7 +135,22 @@ dlm_status dlm_depcap_boundary(const float* kl, const float* entropy, int32_t ba
         return DLM_ERR_INVALID_ARG;
     if (batch == 0) return DLM_OK;
     if (!kl || !entropy || !block_len) return DLM_ERR_INVALID_ARG;
-    dlm::BoundaryArgs a{kl, entropy, batch, L_window, cold_start, params->lambda,
+    dlm::BoundaryArgs a{kl, entropy, batch, L_window, nullptr, cold_start, params->lambda,
+                        params->L_min, params->smooth_w, params->norm_mode, block_len, score};
+    return from_cuda(dlm::launch_boundary(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_depcap_boundary_ragged(const float* kl, const float* entropy, int32_t batch,
+                                      int32_t L_stride, const int32_t* window_len,
+                                      const uint8_t* cold_start, const dlm_depcap_params* params,
+                                      int32_t* block_len, float* score, dlm_stream_t stream) {
+    if (!params || batch < 0 || L_stride < 1 || L_stride > 1024) return DLM_ERR_INVALID_ARG;
+    if (params->L_min < 1 || params->smooth_w < 1 || params->smooth_w > 63 || (params->smooth_w % 2) == 0 ||
+        params->norm_mode < 0 || params->norm_mode > 2 || !isfinite(params->lambda))
+        return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!kl || !entropy || !block_len || !window_len) return DLM_ERR_INVALID_ARG;
+    dlm::BoundaryArgs a{kl, entropy, batch, L_stride, window_len, cold_start, params->lambda,
                         params->L_min, params->smooth_w, params->norm_mode, block_len, score};
     return from_cuda(dlm::launch_boundary(a, reinterpret_cast<cudaStream_t>(stream)));
 }

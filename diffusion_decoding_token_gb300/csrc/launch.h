@@ -60,7 +60,8 @@ cudaError_t launch_certificate(const CertificateArgs& a, cudaStream_t s);
 struct BoundaryArgs {
     const float* kl;
     const float* entropy;
-    int batch, L_window;
+    int batch, L_window;     // L_window: row stride (the longest window)
+    const int32_t* window_len;  // nullable: per-sequence window (<= L_window)
     const uint8_t* cold_start;
     float lambda;
     int L_min, smooth_w, norm_mode;

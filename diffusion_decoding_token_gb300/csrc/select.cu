@@ -81,12 +81,20 @@ constexpr int kMaxWindow = 1024;
 // the first negative, clip to [L_min, L_window], cold start -> L_min.
 // Smoothing: centred moving average of odd width, edge-truncated.
 // Normalisation: 0 window mean, 1 min-max, 2 none.
+// Ragged windows: with window_len, sequence b uses the first window_len[b]
+// entries of its row (row stride L_window); an empty window gives length 0.
 __global__ void __launch_bounds__(kBndThreads) boundary_kernel(BoundaryArgs a) {
     __shared__ float sI[kMaxWindow], sH[kMaxWindow], tI[kMaxWindow], tH[kMaxWindow];
     __shared__ float red[kBndThreads / 32];
-    const int b = blockIdx.x, L = a.L_window;
-    const float* I = a.kl + (int64_t)b * L;
-    const float* H = a.entropy + (int64_t)b * L;
+    const int b = blockIdx.x;
+    const int L = a.window_len ? min(max(a.window_len[b], 0), a.L_window) : a.L_window;
+    const int64_t row = (int64_t)b * a.L_window;
+    if (L == 0) {  // uniform over the CTA
+        if (threadIdx.x == 0) a.block_len[b] = 0;
+        return;
+    }
+    const float* I = a.kl + row;
+    const float* H = a.entropy + row;
     for (int k = threadIdx.x; k < L; k += blockDim.x) {
         sI[k] = I[k];
         sH[k] = H[k];
@@ -147,7 +155,7 @@ __global__ void __launch_bounds__(kBndThreads) boundary_kernel(BoundaryArgs a) {
             nh = tH[k];
         }
         const float s = ni - a.lambda * nh;
-        if (a.score) a.score[(int64_t)b * L + k] = s;
+        if (a.score) a.score[row + k] = s;
         if (s < 0.f) first = fminf(first, (float)k);
     }
     const float kstar = block_min(first, red);

@@ -19,8 +19,9 @@ stand-in for the model, so the rules can be compared by the number of steps
   here with torch indexing).  A sequence counts a step while it still has a
   masked position.
 
-The static inputs come from ``synth.decode_problem``.  One step can be
-captured in a CUDA graph and replayed (``run(graph=True)``).
+The static inputs come from ``synth.decode_problem``.  The whole decode
+(max_steps steps) can be captured as one CUDA graph and replayed
+(``run(graph=True)``).
 """
 from __future__ import annotations
 
@@ -73,6 +74,7 @@ class SyntheticDecoder:
         self.cap_ws = B.cap_workspace(Bn, blk, dev)
         self.dapd_ws = B.dapd_workspace(Bn, blk, dev)
         self.graph = None
+        self.graph_steps = 0
 
     # -- the stand-in model ------------------------------------------------
     def model(self):
@@ -110,8 +112,12 @@ class SyntheticDecoder:
         self.tok.copy_(torch.where(chosen, st.argmax.view(Bn, blk), self.tok))
         self.masked.mul_((~chosen).to(torch.uint8))
 
-    def capture(self):
-        """Capture one step as a CUDA graph (the buffers stay fixed)."""
+    def capture(self, n_steps: int | None = None):
+        """Capture ``n_steps`` decoding steps (default: the whole decode,
+        max_steps of them) as one CUDA graph.  A sequence with nothing masked
+        selects nothing and counts no step, so the surplus steps of a
+        finished sequence change nothing."""
+        n_steps = self.max_steps if n_steps is None else n_steps
         s = torch.cuda.Stream(device=self.dev)
         s.wait_stream(torch.cuda.current_stream(self.dev))
         saved = (self.tok.clone(), self.masked.clone(), self.steps.clone(), self.logits.clone())
@@ -120,30 +126,37 @@ class SyntheticDecoder:
         torch.cuda.current_stream(self.dev).wait_stream(s)
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
-            self.step()
+            for _ in range(n_steps):
+                self.step()
         torch.cuda.synchronize(self.dev)
-        self.tok.copy_(saved[0])
-        self.masked.copy_(saved[1])
-        self.steps.copy_(saved[2])
-        self.logits.copy_(saved[3])
+        self.graph_steps = n_steps
+        self.reset(saved)
 
-    def run(self, graph: bool = False, check_every: int = 4, log=None):
+    def reset(self, saved=None):
+        """Back to the initial state (everything masked, nothing committed)."""
+        if saved is None:
+            self.tok.fill_(-1)
+            self.masked.fill_(1)
+            self.steps.zero_()
+        else:
+            self.tok.copy_(saved[0])
+            self.masked.copy_(saved[1])
+            self.steps.copy_(saved[2])
+            self.logits.copy_(saved[3])
+
+    def run(self, graph: bool = False, log=None):
         """Decode until nothing is masked (or max_steps); returns a summary.
-        ``log``, a list, receives each step's selection (eager runs only)."""
-        if graph and self.graph is None:
-            self.capture()
-        done_steps = 0
-        while done_steps < self.max_steps:
-            for _ in range(check_every if graph else 1):
-                if graph:
-                    self.graph.replay()
-                else:
-                    self.step()
-                    if log is not None:
-                        log.append(self.sel.cpu().numpy().copy())
-                done_steps += 1
-                if done_steps >= self.max_steps:
-                    break
+        ``graph``: replay the captured whole-decode graph (captured on first
+        use).  ``log``, a list, receives each step's selection (eager runs)."""
+        if graph:
+            if self.graph is None:
+                self.capture()
+            self.graph.replay()
+            return self.summary()
+        for _ in range(self.max_steps):
+            self.step()
+            if log is not None:
+                log.append(self.sel.cpu().numpy().copy())
             if int(self.masked.sum().item()) == 0:
                 break
         return self.summary()
@@ -158,3 +171,187 @@ class SyntheticDecoder:
                     error_rate=float(wrong.sum() / max(1, committed.sum())),
                     tokens_per_step=float(committed.sum() / max(1, steps.sum())),
                     unfinished=int((~committed).sum()), status=int(self.status.item()))
+
+
+class DepCapDecoder:
+    """DepCap's block loop over a whole generation (DepCap, "Methodology"):
+    DepGA-Block picks each block's length from the KL shift that the last
+    decoded block caused in the window of future positions, against their
+    entropy; CAP-Decoding then unmasks a conflict-free subset of the block
+    per step until the block is done.
+
+    The problem's ``cfg.blk`` is the generation length N.  Per step, for every
+    sequence b with cursor_b (its first undecoded position):
+
+    1. model over all N positions (as in :class:`SyntheticDecoder`);
+    2. gather the window rows cursor_b + k, k < L_max (row b*L_max + k; rows
+       past the end repeat the last position and are never used);
+    3. ``dlm_row_stats`` on the gathered window rows against the same rows
+       of the snapshot -> ŷ, c, LSE, H, KL (row b*L_max + k);
+    4. sequences without a block: ``dlm_depcap_boundary_ragged`` with
+       L_window = min(L_max, N - cursor_b) (cold start for the first block)
+       sets the block length, and this forward pass becomes the sequence's
+       snapshot, the "before" of the next boundary's KL;
+    5. ``dlm_cap_select`` over the window rows with scope = the block length;
+    6. commit ŷ at the selected positions; a block with nothing masked left
+       advances the cursor.
+
+    Reading: p_prev of the KL is the model's distribution at the forward pass
+    where the last block began (before any of its tokens were committed),
+    p_curr the one after its last commit.
+    """
+
+    def __init__(self, problem: dict, device="cuda", *, L_max=32, lam=1.2, L_min=8, smooth_w=1, norm_mode=0,
+                 tau_low=0.8, tau_high=0.95, gamma=-16.0, max_steps=None):
+        cfg = problem["cfg"]
+        dev = torch.device(device)
+        Bn, N, V = cfg.batch, cfg.blk, cfg.vocab
+        if not 1 <= L_max <= min(N, B.MAX_BLK):
+            raise ValueError("L_max must be in [1, min(N, 256)]")
+        self.cfg, self.dev, self.B, self.N, self.V, self.L_max = cfg, dev, Bn, N, V, L_max
+        self.max_steps = max_steps or N
+        self.prm = dict(lam=lam, L_min=L_min, smooth_w=smooth_w, norm_mode=norm_mode, tau_low=tau_low,
+                        tau_high=tau_high, gamma=gamma)
+        f32 = dict(dtype=torch.float32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.logits = torch.from_numpy(problem["base"]).to(dev)               # [B*N, V]
+        self.snapshot = self.logits.clone()
+        self.rows = torch.arange(Bn * N, device=dev)
+        self.target = torch.from_numpy(problem["target"].reshape(-1)).to(dev)
+        self.decoy = torch.from_numpy(problem["decoy"].reshape(-1)).to(dev)
+        c0 = np.float32(problem["c0"])
+        self.zt0 = torch.from_numpy((c0 + problem["u"]).astype(np.float32).reshape(-1)).to(dev)
+        self.c0 = torch.tensor(c0, **f32)
+        self.v = torch.from_numpy(problem["v"].reshape(-1)).to(dev)
+        self.kappa = torch.tensor(np.float32(cfg.kappa), **f32)
+        self.one = torch.tensor(np.float32(1.0), **f32)
+        self.adj = torch.from_numpy(problem["links"].astype(np.int32)).to(dev)
+        self.deg = self.adj.sum(-1).clamp(min=1).to(torch.float32).reshape(-1)
+        self.k = torch.arange(L_max, **i32)
+        self.seq = torch.arange(Bn, device=dev)
+        self.tok = torch.full((Bn, N), -1, **i32)
+        self.masked = torch.ones((Bn, N), dtype=torch.uint8, device=dev)
+        self.cursor = torch.zeros(Bn, **i32)
+        self.blen = torch.zeros(Bn, **i32)           # 0: the next step picks a new block
+        self.cold = torch.ones(Bn, dtype=torch.uint8, device=dev)
+        self.steps = torch.zeros(Bn, **i32)
+        self.n_blocks = torch.zeros(Bn, **i32)
+        self.status = B.new_status(dev)
+        self.stats = B.alloc_row_stats(Bn * L_max, dev, with_prev=True)
+        self.win = torch.empty((Bn * L_max, V), **f32)         # window rows of this forward pass
+        self.win_prev = torch.empty((Bn * L_max, V), **f32)    # the same rows of the snapshot
+        self.new_len = torch.zeros(Bn, **i32)
+        self.score = torch.zeros((Bn, L_max), **f32)
+        self.sel = torch.zeros((Bn, L_max), dtype=torch.uint8, device=dev)
+        self.nsel = torch.zeros(Bn, **i32)
+        self.cap_ws = B.cap_workspace(Bn, L_max, dev)
+        self.graph = None
+        self.graph_steps = 0
+        self.trace = None
+
+    def model(self):
+        decoded = (self.masked == 0).to(torch.int32)
+        cnt = (self.adj * decoded[:, None, :]).sum(-1).reshape(-1)
+        s = cnt.to(torch.float32) / self.deg
+        zt = self.zt0 + self.kappa * s
+        zd = self.c0 + self.v * (self.one - s)
+        self.logits[self.rows, self.target] = zt
+        self.logits[self.rows, self.decoy] = zd
+
+    def step(self):
+        Bn, N, Lm = self.B, self.N, self.L_max
+        p = self.prm
+        active = self.cursor < N
+        self.steps += active.to(torch.int32)
+        self.model()
+        pos = (self.cursor[:, None] + self.k[None, :]).clamp(max=N - 1)               # [B, L_max]
+        row_index = (self.seq[:, None] * N + pos).reshape(-1).to(torch.int32)
+        window_len = (N - self.cursor).clamp(min=0, max=Lm)
+        torch.index_select(self.logits, 0, row_index, out=self.win)
+        torch.index_select(self.snapshot, 0, row_index, out=self.win_prev)
+        st = B.row_stats(self.win, self.win_prev, out=self.stats, status=self.status)
+        need = active & (self.blen == 0)
+        B.depcap_boundary(st.kl.view(Bn, Lm), st.entropy.view(Bn, Lm), p["lam"], p["L_min"], p["smooth_w"],
+                          p["norm_mode"], cold_start=self.cold, window_len=window_len, block_len=self.new_len,
+                          score=self.score)
+        self.blen.copy_(torch.where(need, self.new_len, self.blen))
+        self.n_blocks += need.to(torch.int32)
+        self.cold.mul_((~need).to(torch.uint8))
+        needv = need.repeat_interleave(N)[:, None]
+        self.snapshot.copy_(torch.where(needv, self.logits, self.snapshot))
+        in_block = self.k[None, :] < self.blen[:, None]
+        mwin = (torch.gather(self.masked, 1, pos.to(torch.int64)) * in_block.to(torch.uint8)).contiguous()
+        B.cap_select(self.win, st.argmax.view(Bn, Lm), st.conf.view(Bn, Lm), st.lse.view(Bn, Lm), mwin,
+                     p["tau_low"], p["tau_high"], p["gamma"], Lm, scope_len=self.blen, workspace=self.cap_ws,
+                     status=self.status, selected=self.sel, n_selected=self.nsel)
+        if self.trace is not None:
+            self.trace.append(dict(cursor=self.cursor.cpu().numpy(), need=need.cpu().numpy(),
+                                   blen=self.blen.cpu().numpy(), sel=self.sel.cpu().numpy(),
+                                   masked=self.masked.cpu().numpy()))
+        # commit: the selected positions are distinct (k < blen <= window), so
+        # accumulating into zeros writes each at most once
+        chosen = self.sel.to(torch.int32)
+        flat = (self.seq[:, None] * N + pos).reshape(-1)
+        dec = torch.zeros(Bn * N, dtype=torch.int32, device=self.dev)
+        dec.index_put_((flat,), chosen.reshape(-1), accumulate=True)
+        val = torch.zeros(Bn * N, dtype=torch.int32, device=self.dev)
+        val.index_put_((flat,), (chosen * st.argmax.view(Bn, Lm)).reshape(-1), accumulate=True)
+        dec = dec.view(Bn, N) > 0
+        self.tok.copy_(torch.where(dec, val.view(Bn, N), self.tok))
+        self.masked.mul_((~dec).to(torch.uint8))
+        left = (torch.gather(self.masked, 1, pos.to(torch.int64)) * in_block.to(torch.uint8)).sum(-1)
+        done = active & (self.blen > 0) & (left == 0)
+        self.cursor.copy_(torch.where(done, self.cursor + self.blen, self.cursor))
+        self.blen.copy_(torch.where(done, torch.zeros_like(self.blen), self.blen))
+
+    def capture(self, n_steps: int | None = None):
+        """Capture ``n_steps`` steps (default: max_steps, the whole decode) as
+        one CUDA graph; a finished sequence's surplus steps change nothing."""
+        n_steps = self.max_steps if n_steps is None else n_steps
+        s = torch.cuda.Stream(device=self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            self.step()
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            for _ in range(n_steps):
+                self.step()
+        torch.cuda.synchronize(self.dev)
+        self.graph_steps = n_steps
+        self.reset()
+
+    def reset(self):
+        self.tok.fill_(-1)
+        self.masked.fill_(1)
+        self.cursor.zero_()
+        self.blen.zero_()
+        self.cold.fill_(1)
+        self.steps.zero_()
+        self.n_blocks.zero_()
+
+    def run(self, graph: bool = False, trace: bool = False):
+        """Decode the whole generation; ``trace`` records every step's state
+        (eager runs only)."""
+        if graph:
+            if self.graph is None:
+                self.capture()
+            self.graph.replay()
+            return self.summary()
+        self.trace = [] if trace else None
+        for _ in range(self.max_steps):
+            self.step()
+            if bool((self.cursor >= self.N).all()):
+                break
+        return self.summary()
+
+    def summary(self) -> dict:
+        tok = self.tok.cpu().numpy()
+        target = self.target.view(self.B, self.N).cpu().numpy()
+        committed = tok >= 0
+        steps = self.steps.cpu().numpy()
+        return dict(rule="depcap", steps=steps, mean_steps=float(steps.mean()), tokens=tok,
+                    n_blocks=self.n_blocks.cpu().numpy(),
+                    error_rate=float((committed & (tok != target)).sum() / max(1, committed.sum())),
+                    tokens_per_step=float(committed.sum() / max(1, steps.sum())),
+                    unfinished=int((~committed).sum()), status=int(self.status.item()), trace=self.trace)

@@ -186,6 +186,26 @@ dlm_status dlm_depcap_boundary(const float* kl, const float* entropy, int32_t ba
                                float* score, dlm_stream_t stream);
 
 /*
+ * dlm_depcap_boundary_ragged -- dlm_depcap_boundary for a batch whose windows
+ * differ in length: L_window = min(L_max, L_remain) is per sequence (DepCap,
+ * "Methodology"), and sequences near the end of their generation have fewer
+ * future positions than L_max.
+ *
+ * kl, entropy : float [batch][L_stride]; sequence b uses its first
+ *               window_len[b] entries, exactly as dlm_depcap_boundary with
+ *               L_window = window_len[b] would.  1 <= L_stride <= 1024.
+ * window_len  : int32 [batch], required; values are clamped to [0, L_stride].
+ *               A window of 0 gives block_len[b] = 0 (nothing left).
+ * score       : nullable float [batch][L_stride]; entries at k >= window_len[b]
+ *               are not written.
+ * Other arguments and errors as dlm_depcap_boundary.
+ */
+dlm_status dlm_depcap_boundary_ragged(const float* kl, const float* entropy, int32_t batch, int32_t L_stride,
+                                      const int32_t* window_len, const uint8_t* cold_start,
+                                      const dlm_depcap_params* params, int32_t* block_len, float* score,
+                                      dlm_stream_t stream);
+
+/*
  * dlm_cap_select -- DepCap CAP-Decoding (conflict-aware parallel decoding).
  *
  * DepCap, "Methodology"; defaults in "Experiments" (tau_low 0.8, tau_high

@@ -50,7 +50,7 @@ def _load():
             lib = ctypes.CDLL(_LIB)
             lib.oracle_row_stats.argtypes = [_P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P]
             lib.oracle_select_threshold.argtypes = [_P, _P, _I32, _I32, _F, _P, _P]
-            lib.oracle_depcap_boundary.argtypes = [_P, _P, _I32, _I32, _P, _F, _I32, _I32, _I32, _P, _P]
+            lib.oracle_depcap_boundary.argtypes = [_P, _P, _I32, _I32, _P, _P, _F, _I32, _I32, _I32, _P, _P]
             lib.oracle_cap_select.argtypes = [_P, _I32, _I64, _P, _P, _P, _P, _P, _I32, _I32,
                                               _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P]
             lib.oracle_cap_select.restype = _I32
@@ -135,16 +135,21 @@ def select_threshold(conf, masked, tau):
     return sel, n
 
 
-def depcap_boundary(kl, entropy, lam, L_min, smooth_w=1, norm_mode=0, cold_start=None):
-    """DepGA-Block boundary (DepCap, Methodology).  Returns (block_len, score)."""
+def depcap_boundary(kl, entropy, lam, L_min, smooth_w=1, norm_mode=0, cold_start=None, window_len=None):
+    """DepGA-Block boundary (DepCap, Methodology).  Returns (block_len, score).
+
+    ``window_len`` (optional, [B]): sequence b uses the first window_len[b]
+    entries of its row, L_window = min(L_max, L_remain) per sequence; score
+    entries past it stay NaN."""
     lib = _load()
     kl = np.ascontiguousarray(kl, dtype=np.float64)
     entropy = np.ascontiguousarray(entropy, dtype=np.float64)
     B, Lw = kl.shape
     cs = None if cold_start is None else np.ascontiguousarray(cold_start, dtype=np.uint8)
+    wl = None if window_len is None else np.ascontiguousarray(window_len, dtype=np.int32)
     blen = np.zeros(B, np.int32)
-    score = np.zeros((B, Lw))
-    lib.oracle_depcap_boundary(_ptr(kl), _ptr(entropy), B, Lw, _ptr(cs), float(lam), int(L_min),
+    score = np.full((B, Lw), np.nan)
+    lib.oracle_depcap_boundary(_ptr(kl), _ptr(entropy), B, Lw, _ptr(wl), _ptr(cs), float(lam), int(L_min),
                                int(smooth_w), int(norm_mode), _ptr(blen), _ptr(score))
     return blen, score
 

@@ -240,24 +240,35 @@ static void smooth_norm(const double* x, int n, int w, int mode, double* out) {
 }
 
 void oracle_depcap_boundary(const double* kl, const double* entropy, int batch, int L_window,
-                            const uint8_t* cold_start, float lambda, int L_min, int smooth_w,
-                            int norm_mode, int32_t* block_len, double* score) {
+                            const int32_t* window_len, const uint8_t* cold_start, float lambda,
+                            int L_min, int smooth_w, int norm_mode, int32_t* block_len, double* score) {
     double* In = (double*)malloc(sizeof(double) * (size_t)L_window);
     double* Hn = (double*)malloc(sizeof(double) * (size_t)L_window);
     for (int b = 0; b < batch; ++b) {
+        /* L_window = min(L_max, L_remain) per sequence when window_len is given;
+         * the rows keep the stride L_window */
+        int L = L_window;
+        if (window_len) {
+            L = window_len[b] < 0 ? 0 : window_len[b];
+            if (L > L_window) L = L_window;
+        }
+        if (L == 0) {
+            block_len[b] = 0;
+            continue;
+        }
         const double* I = kl + (int64_t)b * L_window;
         const double* H = entropy + (int64_t)b * L_window;
-        smooth_norm(I, L_window, smooth_w, norm_mode, In);
-        smooth_norm(H, L_window, smooth_w, norm_mode, Hn);
-        int kstar = L_window;
-        for (int k = 0; k < L_window; ++k) {
+        smooth_norm(I, L, smooth_w, norm_mode, In);
+        smooth_norm(H, L, smooth_w, norm_mode, Hn);
+        int kstar = L;
+        for (int k = 0; k < L; ++k) {
             double s = In[k] - (double)lambda * Hn[k];
             if (score) score[(int64_t)b * L_window + k] = s;
-            if (kstar == L_window && (float)s < 0.0f) kstar = k;
+            if (kstar == L && (float)s < 0.0f) kstar = k;
         }
         int len = kstar < L_min ? L_min : kstar;
-        if (len > L_window) len = L_window;
-        if (cold_start && cold_start[b]) len = L_min < L_window ? L_min : L_window;
+        if (len > L) len = L;
+        if (cold_start && cold_start[b]) len = L_min < L ? L_min : L;
         block_len[b] = len;
     }
     free(In);

@@ -71,3 +71,105 @@ def oracle_decode(problem, rule, max_steps, prm):
         tok = np.where(sel > 0, o["argmax"].reshape(B, blk), tok)
         masked = masked * (1 - sel)
     return log, stats, tok
+
+
+# ---------------------------------------------------------------------------
+# DepCap block loop (DepCap, "Methodology"): the oracle side of
+# DepCapDecoder.  The problem's cfg.blk is the generation length N.
+# ---------------------------------------------------------------------------
+DEPCAP_DEFAULT = dict(L_max=32, lam=1.2, L_min=8, smooth_w=1, norm_mode=0, tau_low=0.8, tau_high=0.95, gamma=-16.0)
+
+
+def full_logits(problem, masked):
+    lg = problem["base"].copy()
+    model_logits(problem, lg, masked)
+    return lg
+
+
+def depcap_step(problem, state, prm, blen_override=None):
+    """One step of the block loop from ``state`` (masked [B,N], cursor [B],
+    blen [B] (0 = pick a block), cold [B], snap_masked [B,N]: the mask at the
+    forward pass that became the sequence's snapshot, or None before the
+    first).  ``blen_override`` replaces the block lengths CAP works on (the
+    other side's, to compare CAP from the same state).  Returns dict(need, new_len, score, blen, sel, pos, stats, cap)."""
+    cfg = problem["cfg"]
+    B, N, Lm = cfg.batch, cfg.blk, prm["L_max"]
+    masked, cursor = state["masked"], state["cursor"]
+    cur = full_logits(problem, masked)
+    pos = np.minimum(cursor[:, None] + np.arange(Lm)[None, :], N - 1)
+    rows = (np.arange(B)[:, None] * N + pos).reshape(-1)
+    prev = np.empty((B * Lm, cfg.vocab), np.float32)
+    snap_all = masked.copy()       # a sequence's rows depend on its own mask only
+    have = np.zeros(B, bool)
+    for b in range(B):
+        if state["snap_masked"][b] is not None:
+            snap_all[b], have[b] = state["snap_masked"][b], True
+    snap = full_logits(problem, snap_all) if have.any() else cur
+    for b in range(B):
+        src = snap if have[b] else cur
+        prev[b * Lm:(b + 1) * Lm] = src[rows[b * Lm:(b + 1) * Lm]]
+    win = cur[rows]
+    o = oracle.row_stats(win, prev)
+    window_len = np.clip(N - cursor, 0, Lm)
+    active = cursor < N
+    need = active & (state["blen"] == 0)
+    new_len, score = oracle.depcap_boundary(o["kl"].reshape(B, Lm), o["entropy"].reshape(B, Lm), prm["lam"],
+                                            prm["L_min"], prm["smooth_w"], prm["norm_mode"],
+                                            cold_start=state["cold"], window_len=window_len)
+    blen = np.where(need, new_len, state["blen"]) if blen_override is None else blen_override
+    in_block = np.arange(Lm)[None, :] < blen[:, None]
+    mwin = (np.take_along_axis(masked, pos, 1) * in_block).astype(np.uint8)
+    r = oracle.cap_select(win, o["argmax"].reshape(B, Lm), o["conf"].reshape(B, Lm), o["lse"].reshape(B, Lm),
+                          mwin, prm["tau_low"], prm["tau_high"], prm["gamma"], Lm, scope_len=blen)
+    return dict(need=need, new_len=new_len, score=score, blen=blen, sel=r["selected"], pos=pos, stats=o, cap=r,
+                mwin=mwin, window_len=window_len)
+
+
+def depcap_commit(state, out, tok):
+    """Commit a step's selection (given as ``out``'s sel/pos/blen/need) into
+    ``state`` and ``tok``; returns the new state."""
+    B = len(state["cursor"])
+    masked = state["masked"].copy()
+    snap = list(state["snap_masked"])
+    for b in range(B):
+        if out["need"][b]:
+            snap[b] = state["masked"][b].copy()
+        for k in np.nonzero(out["sel"][b])[0]:
+            p = out["pos"][b, k]
+            masked[b, p] = 0
+            tok[b, p] = out["argmax"][b, k]
+    cursor, blen = state["cursor"].copy(), out["blen"].copy()
+    for b in range(B):
+        if cursor[b] < masked.shape[1] and blen[b] > 0 and not masked[b, cursor[b]:cursor[b] + blen[b]].any():
+            cursor[b] += blen[b]
+            blen[b] = 0
+    cold = state["cold"] * (1 - out["need"].astype(np.uint8))
+    return dict(masked=masked, cursor=cursor, blen=blen, cold=cold, snap_masked=snap)
+
+
+def depcap_initial(problem):
+    cfg = problem["cfg"]
+    B, N = cfg.batch, cfg.blk
+    return dict(masked=np.ones((B, N), np.uint8), cursor=np.zeros(B, np.int64), blen=np.zeros(B, np.int64),
+                cold=np.ones(B, np.uint8), snap_masked=[None] * B)
+
+
+def depcap_decode(problem, prm=DEPCAP_DEFAULT, max_steps=None):
+    """The whole block loop on the oracle side.  Returns (steps [B], tok,
+    blocks: per sequence the list of (start, length))."""
+    cfg = problem["cfg"]
+    B, N = cfg.batch, cfg.blk
+    state = depcap_initial(problem)
+    tok = np.full((B, N), -1, np.int64)
+    steps = np.zeros(B, np.int64)
+    blocks = [[] for _ in range(B)]
+    for _ in range(max_steps or N):
+        if (state["cursor"] >= N).all():
+            break
+        out = depcap_step(problem, state, prm)
+        steps += state["cursor"] < N
+        for b in np.nonzero(out["need"])[0]:
+            blocks[b].append((int(state["cursor"][b]), int(out["blen"][b])))
+        out["argmax"] = out["stats"]["argmax"].reshape(B, prm["L_max"])
+        state = depcap_commit(state, out, tok)
+    return steps, tok, blocks

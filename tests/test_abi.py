@@ -85,6 +85,11 @@ def test_selection_argument_errors(libdlm):
     assert libdlm.dlm_depcap_boundary(fake, fake, 1, 32, None, ctypes.byref(dp), fake, None, None) == INVALID
     dp = DepcapParams(1.0, 8, 1, 0)
     assert libdlm.dlm_depcap_boundary(fake, fake, 1, 2000, None, ctypes.byref(dp), fake, None, None) == INVALID
+    # the ragged form needs its window lengths
+    assert libdlm.dlm_depcap_boundary_ragged(fake, fake, 1, 32, None, None, ctypes.byref(dp), fake, None,
+                                             None) == INVALID
+    assert libdlm.dlm_depcap_boundary_ragged(fake, fake, 0, 32, None, None, ctypes.byref(dp), fake, None,
+                                             None) == 0
 
     cp = CapParams(0.8, 0.95, -16.0, 32, 0)
     args = (fake, 1, 100, 100, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)

@@ -1,7 +1,8 @@
 """The multi-step synthetic decode driver on the GPU against its oracle twin:
-identical selections step by step for as long as every decision of the step
-clears the margins of parity.py; invariants (progress, termination, commits)
-on every rule; the CUDA-graph run equals the eager run."""
+every GPU step equals the oracle step taken from the same mask, sequence by
+sequence where the decisions clear the margins of parity.py; invariants (progress, termination, commits)
+on every rule; the whole decode replayed as one CUDA graph equals the eager
+run."""
 import numpy as np
 import pytest
 
@@ -76,10 +77,15 @@ def test_driver_matches_oracle_twin(rule):
           f"sequence-steps compared {compared}/{total}")
 
 
-def test_graph_run_equals_eager_run():
+@pytest.mark.parametrize("rule", ["threshold", "topk", "cap", "dapd"])
+def test_whole_decode_graph_equals_eager_run(rule):
     from diffusion_decoding_token_gb300.driver import SyntheticDecoder
     prob = synth.decode_problem(CFG, seed=23)
-    a = SyntheticDecoder(prob, "dapd", **PRM).run()
-    b = SyntheticDecoder(prob, "dapd", **PRM).run(graph=True)
+    a = SyntheticDecoder(prob, rule, **PRM).run()
+    dec = SyntheticDecoder(prob, rule, **PRM)
+    b = dec.run(graph=True)
     np.testing.assert_array_equal(a["tokens"], b["tokens"])
     np.testing.assert_array_equal(a["steps"], b["steps"])
+    dec.reset()
+    c = dec.run(graph=True)                      # a replay from the reset state repeats the decode
+    np.testing.assert_array_equal(c["tokens"], b["tokens"])

@@ -271,6 +271,32 @@ def test_boundary_modes(dlm, w_, mode):
             assert gl[b] == ol[b]
 
 
+@pytest.mark.parametrize("w_", [1, 3])
+def test_boundary_ragged_windows(dlm, w_):
+    """Per-sequence windows L_window = min(L_max, L_remain), including an
+    empty one and windows shorter than L_min and the smoothing width."""
+    rng = np.random.default_rng(40 + w_)
+    B, Ls = 24, 64
+    I = rng.gamma(1.0, 1.0, (B, Ls)).astype(np.float32)
+    H = rng.gamma(1.0, 1.0, (B, Ls)).astype(np.float32)
+    wl = rng.integers(0, Ls + 1, B).astype(np.int32)
+    wl[:4] = [0, 1, 2, Ls]
+    cold = (rng.random(B) < 0.2).astype(np.uint8)
+    score = torch.full((B, Ls), float("nan"), device="cuda")
+    gl, gsc = dlm.depcap_boundary(cuda(I), cuda(H), 1.2, 8, w_, 0, cold_start=cuda(cold), window_len=cuda(wl),
+                                  score=score)
+    ol, osc = oracle.depcap_boundary(I.astype(np.float64), H.astype(np.float64), 1.2, 8, w_, 0, cold,
+                                     window_len=wl)
+    gsc, gl = gsc.cpu().numpy(), gl.cpu().numpy()
+    for b in range(B):
+        n = wl[b]
+        assert np.isnan(gsc[b, n:]).all()                    # nothing written past the window
+        assert close(gsc[b, :n], osc[b, :n]).all()
+        if cold[b] or boundary_margin_ok(osc[b, :n]):
+            assert gl[b] == ol[b], b
+    assert gl[0] == 0
+
+
 def test_cap_edges(dlm):
     """Pool clipping, an empty pool, scope limits, the unconditional tier and
     a ragged block, on a tiny fp32 case."""

@@ -79,3 +79,21 @@ def test_decoys_hurt_parallel_rules_more():
         _, _, tok = oracle_decode(prob, rule, cfg.blk, prm)
         err[rule] = float((tok != prob["target"]).mean())
     assert err["topk"] < err["threshold"]
+
+
+def test_depcap_loop_invariants():
+    from decode_ref import DEPCAP_DEFAULT, depcap_decode
+    cfg = synth.DecodeConfig(name="depcap_loop", batch=3, blk=96, vocab=256, band=10, p_link=0.01)
+    prob = synth.decode_problem(cfg, seed=5)
+    prm = dict(DEPCAP_DEFAULT, L_max=32, L_min=4)
+    steps, tok, blocks = depcap_decode(prob, prm)
+    assert (tok >= 0).all()
+    for b in range(cfg.batch):
+        starts = [s for s, _ in blocks[b]]
+        ends = [s + n for s, n in blocks[b]]
+        assert starts[0] == 0 and ends[-1] == cfg.blk and starts[1:] == ends[:-1]     # contiguous tiling
+        assert blocks[b][0][1] == prm["L_min"]                                       # cold start
+        for s, n in blocks[b]:
+            assert min(prm["L_min"], cfg.blk - s) <= n <= min(prm["L_max"], cfg.blk - s)
+        assert len(blocks[b]) <= steps[b] <= cfg.blk
+    assert len({n for bl in blocks for _, n in bl}) > 2

@@ -106,6 +106,41 @@ def test_boundary_smoothing_and_norms_against_numpy(oracle):
         np.testing.assert_allclose(S2[0], Is - lam * Hs, rtol=1e-12)
 
 
+def test_boundary_ragged_windows(oracle):
+    # L_window = min(L_max, L_remain) per sequence: row stride 4, windows 4, 3, 2, 0.
+    I = np.ones((4, 4))
+    H = np.array([[0.5, 0.5, 2.0, 0.5]] * 4)
+    blen, S = oracle.depcap_boundary(I, H, lam=1.0, L_min=1, window_len=np.array([4, 3, 2, 0]))
+    # window 3: H/mean = [0.5, 0.5, 2] / 1 -> S = [0.5, 0.5, -1], first negative 2
+    np.testing.assert_allclose(S[1, :3], [0.5, 0.5, -1.0], rtol=1e-15)
+    # window 2: H/mean = [1, 1] -> S = [0, 0], none negative -> the whole window
+    np.testing.assert_allclose(S[2, :2], [0.0, 0.0], atol=1e-15)
+    assert blen.tolist() == [2, 2, 2, 0]
+    assert np.isnan(S[1, 3]) and np.isnan(S[2, 2:]).all() and np.isnan(S[3]).all()
+    blen, _ = oracle.depcap_boundary(I, H, lam=1.0, L_min=3, window_len=np.array([4, 3, 2, 0]),
+                                     cold_start=np.array([0, 0, 1, 1]))
+    assert blen.tolist() == [3, 3, 2, 0]      # clipped to the window; cold start min(L_min, window)
+
+
+def test_boundary_ragged_against_numpy(oracle):
+    rng = np.random.default_rng(4)
+    B, Ls = 6, 19
+    I = rng.gamma(2.0, 1.0, (B, Ls))
+    H = rng.gamma(2.0, 1.0, (B, Ls))
+    wl = np.array([19, 1, 7, 12, 2, 5])
+    lam = float(np.float32(0.9))
+    for w in (1, 3):
+        _, S = oracle.depcap_boundary(I, H, lam=0.9, L_min=1, smooth_w=w, norm_mode=0, window_len=wl)
+        for b in range(B):
+            n = wl[b]
+            k = np.ones(w)
+            sm = lambda x: np.convolve(x, k, "same")[:n] / np.convolve(np.ones(n), k, "same")[:n]
+            if n < w:   # np.convolve "same" needs len >= kernel: do it by hand
+                sm = lambda x: np.array([x[max(0, j - w // 2):min(n, j + w // 2 + 1)].mean() for j in range(n)])
+            Is, Hs = sm(I[b, :n]), sm(H[b, :n])
+            np.testing.assert_allclose(S[b, :n], Is / Is.mean() - lam * Hs / Hs.mean(), rtol=1e-12, atol=1e-14)
+
+
 # ---------------------------------------------------------------------- CAP
 def _cap_case(rng, blk, V, n_conf_pairs, dup_pairs=0):
     z = rng.standard_normal((blk, V)).astype(np.float32)
