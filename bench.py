@@ -506,6 +506,33 @@ def run_driver(args):
                      "error_rate": sm["error_rate"], "tokens_per_step": sm["tokens_per_step"],
                      "unfinished": sm["unfinished"], "graph_steps": dec.graph_steps, "ms_per_decode": ms,
                      "tokens_per_s": cfg.batch * cfg.blk / (ms / 1000.0), "status": sm["status"]}
+    # DepCap's block loop over a 256-token generation (page defaults L_max 128,
+    # L_min 8, lambda 1.2; banded dependencies reach 10 positions)
+    from diffusion_decoding_token_gb300.driver import DepCapDecoder
+    dcfg = synth.DecodeConfig(name="depcap_loop", batch=args.batch or 64, blk=256, vocab=16384, band=10,
+                              p_link=0.01)
+    dprob = synth.decode_problem(dcfg, seed=args.seed)
+    dec = DepCapDecoder(dprob, dev, L_max=128, L_min=8, lam=1.2)
+    dec.capture()
+    times = []
+    for _ in range(max(3, args.warmup) + 3):
+        dec.reset()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dec.graph.replay()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        times.append(e0.elapsed_time(e1))
+    sm = dec.summary()
+    ms = statistics.median(times[max(3, args.warmup):])
+    out["depcap_loop"] = {"mean_steps": sm["mean_steps"], "max_steps": int(sm["steps"].max()),
+                          "mean_blocks": float(sm["n_blocks"].mean()), "error_rate": sm["error_rate"],
+                          "tokens_per_step": sm["tokens_per_step"], "unfinished": sm["unfinished"],
+                          "graph_steps": dec.graph_steps, "ms_per_decode": ms,
+                          "tokens_per_s": dcfg.batch * dcfg.blk / (ms / 1000.0), "status": sm["status"],
+                          "config": {"batch": dcfg.batch, "gen_len": dcfg.blk, "vocab": dcfg.vocab, "L_max": 128,
+                                     "L_min": 8, "lambda": 1.2}}
     print(json.dumps({"mode": "decode_driver", "data": "synthetic",
                       "config": {"batch": cfg.batch, "blk": cfg.blk, "vocab": cfg.vocab, "logits": "f32",
                                  "attention": f"f16 {cfg.n_layers}x{cfg.n_heads} over the block"},
