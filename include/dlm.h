@@ -367,6 +367,75 @@ dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t bat
                            const dlm_dapd_params* params, uint8_t* selected, int32_t* n_selected,
                            void* workspace, size_t ws_bytes, dlm_stream_t stream);
 
+/*
+ * dlm_revocable_step -- one state update of revocable parallel decoding
+ * (COVER page: "Revocable Parallel Diffusion Decoding" for the step and its
+ * state update, "Method" for the three revision outcomes, stability-aware
+ * seed selection and the seed count |S_t| = ceil(sqrt(n_t) pi_t)).
+ *
+ * Per sequence b (one block of blk <= 256 positions), with yhat_i / c_i the
+ * model's prediction and confidence at position i this step (for a seed:
+ * its leave-one-out re-prediction), in this order:
+ *  0. a sequence with no masked position at the start of the step has
+ *     finished (the decode terminates when nothing is masked): nothing
+ *     changes, outcome 0, counts 0.
+ *  1. verify every seed (seed_i = 1 and decoded):
+ *       KEEP    (2) if yhat_i == tok_i;
+ *       REPLACE (3) if yhat_i != tok_i and c_i >= tau_replace: tok_i = yhat_i;
+ *       REMASK  (4) otherwise: masked_i = 1, last_tok_i = tok_i, tok_i = -1,
+ *                   remasks_i += 1.
+ *  2. draft among the positions masked at the start of the step: those with
+ *     c_i > tau_draft, most confident first (ties to the lower position), at
+ *     most draft_budget of them (<= 0: no cap); if none qualifies, the single
+ *     most confident one.  Drafted (1): tok_i = yhat_i, masked_i = 0; a
+ *     drafted token equal to last_tok_i is a flip-flop (flipflops[b] += 1).
+ *  3. choose the next step's seeds: eligible = decoded after 1-2, step -
+ *     last_seed_i > cooldown, remasks_i < remask_budget.  With n eligible,
+ *     k = min(n, ceil(sqrt(n) * pi)) (fp32); score_i = w_unc (1 - c_i) +
+ *     w_infl infl_i - w_drift drift_i (fp32, each product and sum rounded,
+ *     no fused multiply-add); the k best scores (ties to the lower position)
+ *     get seed_i = 1 and last_seed_i = step, all others seed_i = 0.
+ * Every comparison and the score are taken in fp32.
+ *
+ * Readings (the pages leave these open): KEEP / REPLACE / REMASK are decided
+ * by the prediction matching the token and a confidence threshold; the
+ * drafting rule is the confidence threshold with the top-1 fallback under an
+ * optional budget; uncertainty is 1 - c_i, downstream influence and cache
+ * drift are supplied by the caller (nullable: 0), the score is their linear
+ * combination with weights w_*; the revision rate pi_t is the constant pi and
+ * n_t the number of eligible positions.
+ *
+ * argmax, conf        : [batch][blk] int32 / float, this step's yhat, c.
+ * influence, drift    : nullable float [batch][blk].
+ * tok                 : int32 [batch][blk] in/out (-1 at masked positions).
+ * masked, seed        : uint8 [batch][blk] in/out.
+ * last_seed, remasks,
+ * last_tok            : int32 [batch][blk] in/out state; start a decode with
+ *                       last_seed = INT32_MIN / 2, remasks = 0, last_tok = -1.
+ * outcome             : nullable uint8 [batch][blk] output (0 none, 1 drafted,
+ *                       2 keep, 3 replace, 4 remask).
+ * n_drafted, n_revoked: nullable int32 [batch] outputs (net growth of the
+ *                       decoded set = drafted - revoked).
+ * flipflops           : nullable int32 [batch], accumulated.
+ * Errors: DLM_ERR_INVALID_ARG for a null required pointer, batch < 0,
+ * blk outside [1, 256], pi or a weight not finite, pi < 0.
+ */
+typedef struct dlm_revocable_params {
+    float tau_replace;     /* REPLACE threshold on c_i */
+    float tau_draft;       /* drafting threshold (strict) */
+    int32_t draft_budget;  /* <= 0: no cap */
+    float w_unc, w_infl, w_drift;
+    float pi;              /* seed rate: k = ceil(sqrt(n) * pi) */
+    int32_t cooldown;      /* eligible iff step - last_seed > cooldown */
+    int32_t remask_budget; /* eligible iff remasks < remask_budget */
+} dlm_revocable_params;
+
+dlm_status dlm_revocable_step(const int32_t* argmax, const float* conf, const float* influence, const float* drift,
+                              int32_t batch, int32_t blk, int32_t step, const dlm_revocable_params* params,
+                              int32_t* tok, uint8_t* masked, uint8_t* seed, int32_t* last_seed, int32_t* remasks,
+                              int32_t* last_tok, uint8_t* outcome, int32_t* n_drafted, int32_t* n_revoked,
+                              int32_t* flipflops, dlm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

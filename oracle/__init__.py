@@ -53,6 +53,8 @@ def _load():
             lib.oracle_depcap_boundary.argtypes = [_P, _P, _I32, _I32, _P, _P, _F, _I32, _I32, _I32, _P, _P]
             lib.oracle_cap_select.argtypes = [_P, _I32, _I64, _P, _P, _P, _P, _P, _I32, _I32,
                                               _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P]
+            lib.oracle_revocable_step.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _F, _F, _I32, _F, _F, _F,
+                                                  _F, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
             lib.oracle_cap_select.restype = _I32
             lib.oracle_dapd.argtypes = [_P, _I32, _I32, _I32, _I32, _I64, _I64, _I64, _I64, _I32, _I32,
                                         _P, _P, _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P, _P]
@@ -254,3 +256,38 @@ def parallel_certificate(conf, selected):
     out = np.zeros(B, np.uint8)
     lib.oracle_parallel_certificate(_ptr(conf), _ptr(selected), B, blk, _ptr(out))
     return out
+
+
+def revocable_init(B, blk):
+    """Initial state of a revocable decode: everything masked, no seeds."""
+    return dict(tok=np.full((B, blk), -1, np.int32), masked=np.ones((B, blk), np.uint8),
+                seed=np.zeros((B, blk), np.uint8), last_seed=np.full((B, blk), -(2 ** 30), np.int32),
+                remasks=np.zeros((B, blk), np.int32), last_tok=np.full((B, blk), -1, np.int32),
+                flipflops=np.zeros(B, np.int32))
+
+
+def revocable_step(argmax, conf, state, step, tau_replace=0.9, tau_draft=0.9, draft_budget=0, w_unc=1.0,
+                   w_infl=1.0, w_drift=1.0, pi=1.0, cooldown=1, remask_budget=2, influence=None, drift=None):
+    """One state update of revocable parallel decoding (COVER page,
+    Revocable Parallel Diffusion Decoding and Method).  ``state`` (a dict of
+    numpy arrays as revocable_init makes) is updated in place; returns dict
+    (outcome, n_drafted, n_revoked)."""
+    lib = _load()
+    argmax = np.ascontiguousarray(argmax, dtype=np.int32)
+    B, blk = argmax.shape
+    conf = np.ascontiguousarray(conf, dtype=np.float64).reshape(B, blk)
+    infl = None if influence is None else np.ascontiguousarray(influence, dtype=np.float64).reshape(B, blk)
+    dr = None if drift is None else np.ascontiguousarray(drift, dtype=np.float64).reshape(B, blk)
+    for k, dt in (("tok", np.int32), ("masked", np.uint8), ("seed", np.uint8), ("last_seed", np.int32),
+                  ("remasks", np.int32), ("last_tok", np.int32), ("flipflops", np.int32)):
+        assert state[k].dtype == dt and state[k].flags.c_contiguous, k
+    outcome = np.zeros((B, blk), np.uint8)
+    nd = np.zeros(B, np.int32)
+    nr = np.zeros(B, np.int32)
+    lib.oracle_revocable_step(_ptr(argmax), _ptr(conf), _ptr(infl), _ptr(dr), B, blk, int(step),
+                              float(tau_replace), float(tau_draft), int(draft_budget), float(w_unc), float(w_infl),
+                              float(w_drift), float(pi), int(cooldown), int(remask_budget), _ptr(state["tok"]),
+                              _ptr(state["masked"]), _ptr(state["seed"]), _ptr(state["last_seed"]),
+                              _ptr(state["remasks"]), _ptr(state["last_tok"]), _ptr(outcome), _ptr(nd), _ptr(nr),
+                              _ptr(state["flipflops"]))
+    return dict(outcome=outcome, n_drafted=nd, n_revoked=nr)

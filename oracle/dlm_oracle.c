@@ -607,3 +607,122 @@ void oracle_parallel_certificate(const double* conf, const uint8_t* selected, in
         certified[b] = (uint8_t)ok;
     }
 }
+
+/* ------------------------------------------------------------------------
+ * Revocable parallel decoding, one state update (COVER page: "Revocable
+ * Parallel Diffusion Decoding" -- draft masked positions, verify the seeds,
+ * remask some, net growth = drafted - revoked, stop when nothing is masked;
+ * "Method" -- KEEP / REPLACE / REMASK, stability-aware seed selection from
+ * uncertainty, downstream influence and cache drift, |S_t| = ceil(sqrt(n_t)
+ * pi_t), recently selected positions and those at their remask budget
+ * excluded).
+ * Readings: KEEP iff the re-prediction equals the token; REPLACE iff it
+ * differs and its confidence reaches tau_replace; REMASK otherwise.  Drafting
+ * is the confidence threshold (strict) with the top-1 fallback, at most
+ * draft_budget (<= 0: no cap).  score = w_unc (1 - c) + w_infl infl - w_drift
+ * drift; pi_t = pi; n_t = number of eligible positions.  Every decision is
+ * taken in fp32 (the score rounded after each operation).
+ * ------------------------------------------------------------------------ */
+static void sort_desc_f32(int* idx, const float* key, int n) {
+    /* insertion sort: larger key first, ties to the lower index */
+    for (int a = 1; a < n; ++a) {
+        int v = idx[a];
+        int p = a - 1;
+        while (p >= 0 && (key[idx[p]] < key[v] || (key[idx[p]] == key[v] && idx[p] > v))) {
+            idx[p + 1] = idx[p];
+            --p;
+        }
+        idx[p + 1] = v;
+    }
+}
+
+void oracle_revocable_step(const int32_t* argmax, const double* conf, const double* influence,
+                           const double* drift, int batch, int blk, int step, float tau_replace,
+                           float tau_draft, int draft_budget, float w_unc, float w_infl, float w_drift,
+                           float pi, int cooldown, int remask_budget, int32_t* tok, uint8_t* masked,
+                           uint8_t* seed, int32_t* last_seed, int32_t* remasks, int32_t* last_tok,
+                           uint8_t* outcome, int32_t* n_drafted, int32_t* n_revoked, int32_t* flipflops) {
+    int* idx = (int*)malloc(sizeof(int) * (size_t)blk);
+    float* key = (float*)malloc(sizeof(float) * (size_t)blk);
+    uint8_t* was_masked = (uint8_t*)malloc((size_t)blk);
+    for (int b = 0; b < batch; ++b) {
+        const int64_t o = (int64_t)b * blk;
+        int m0 = 0;
+        for (int i = 0; i < blk; ++i) {
+            was_masked[i] = masked[o + i] ? 1 : 0;
+            m0 += was_masked[i];
+            outcome[o + i] = 0;
+        }
+        n_drafted[b] = 0;
+        n_revoked[b] = 0;
+        if (m0 == 0) continue; /* finished: nothing changes */
+
+        /* 1. verification of the seeds */
+        for (int i = 0; i < blk; ++i) {
+            if (!seed[o + i] || was_masked[i]) continue;
+            if (argmax[o + i] == tok[o + i]) {
+                outcome[o + i] = 2;
+            } else if ((float)conf[o + i] >= tau_replace) {
+                outcome[o + i] = 3;
+                tok[o + i] = argmax[o + i];
+            } else {
+                outcome[o + i] = 4;
+                last_tok[o + i] = tok[o + i];
+                tok[o + i] = -1;
+                masked[o + i] = 1;
+                remasks[o + i] += 1;
+                n_revoked[b] += 1;
+            }
+        }
+
+        /* 2. drafting over the positions masked at the start */
+        int n = 0;
+        for (int i = 0; i < blk; ++i) {
+            key[i] = (float)conf[o + i];
+            if (was_masked[i] && key[i] > tau_draft) idx[n++] = i;
+        }
+        if (n == 0) {
+            for (int i = 0; i < blk; ++i)
+                if (was_masked[i]) idx[n++] = i;
+            sort_desc_f32(idx, key, n);
+            n = 1;
+        } else {
+            sort_desc_f32(idx, key, n);
+            if (draft_budget > 0 && n > draft_budget) n = draft_budget;
+        }
+        for (int r = 0; r < n; ++r) {
+            int i = idx[r];
+            outcome[o + i] = 1;
+            tok[o + i] = argmax[o + i];
+            masked[o + i] = 0;
+            if (last_tok[o + i] == argmax[o + i] && flipflops) flipflops[b] += 1;
+        }
+        n_drafted[b] = n;
+
+        /* 3. the next step's seeds */
+        int ne = 0;
+        for (int i = 0; i < blk; ++i) {
+            seed[o + i] = 0;
+            int eligible = !masked[o + i] && (step - last_seed[o + i] > cooldown) &&
+                           remasks[o + i] < remask_budget;
+            if (!eligible) continue;
+            float unc = 1.0f - (float)conf[o + i];
+            float a = w_unc * unc;
+            float c = w_infl * (influence ? (float)influence[o + i] : 0.0f);
+            float d = w_drift * (drift ? (float)drift[o + i] : 0.0f);
+            float s = a + c;
+            key[i] = s - d;
+            idx[ne++] = i;
+        }
+        float kf = ceilf(sqrtf((float)ne) * pi);
+        int k = kf < (float)ne ? (int)kf : ne;
+        sort_desc_f32(idx, key, ne);
+        for (int r = 0; r < k; ++r) {
+            seed[o + idx[r]] = 1;
+            last_seed[o + idx[r]] = step;
+        }
+    }
+    free(idx);
+    free(key);
+    free(was_masked);
+}
