@@ -37,6 +37,8 @@ from ._binding import (  # noqa: F401
     select_topk,
     select_factor,
     parallel_certificate,
+    revocable_state,
+    revocable_step,
 )
 from .driver import SyntheticDecoder  # noqa: F401
 

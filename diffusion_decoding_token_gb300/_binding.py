@@ -41,6 +41,12 @@ class DapdParams(ctypes.Structure):
                 ("preunmask_certain", ctypes.c_int32)]
 
 
+class RevocableParams(ctypes.Structure):
+    _fields_ = [("tau_replace", ctypes.c_float), ("tau_draft", ctypes.c_float), ("draft_budget", ctypes.c_int32),
+                ("w_unc", ctypes.c_float), ("w_infl", ctypes.c_float), ("w_drift", ctypes.c_float),
+                ("pi", ctypes.c_float), ("cooldown", ctypes.c_int32), ("remask_budget", ctypes.c_int32)]
+
+
 class DlmError(RuntimeError):
     pass
 
@@ -70,6 +76,8 @@ def lib():
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
         L.dlm_depcap_boundary_ragged.argtypes = [P, P, I32, I32, P, P, ctypes.POINTER(DepcapParams), P, P, P]
         L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
+        L.dlm_revocable_step.argtypes = [P, P, P, P, I32, I32, I32, ctypes.POINTER(RevocableParams), P, P, P, P, P,
+                                         P, P, P, P, P, P]
         L.dlm_select_factor.argtypes = [P, P, I32, I32, F, P, P, P]
         L.dlm_parallel_certificate.argtypes = [P, P, I32, I32, P, P]
         L.dlm_dapd_graph.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
@@ -77,7 +85,8 @@ def lib():
         L.dlm_dapd_select.argtypes = [P, P, I32, I32, ctypes.POINTER(DapdParams), P, P, P, Z, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
                   "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select", "dlm_select_topk",
-                  "dlm_select_factor", "dlm_parallel_certificate", "dlm_depcap_boundary_ragged"):
+                  "dlm_select_factor", "dlm_parallel_certificate", "dlm_depcap_boundary_ragged",
+                  "dlm_revocable_step"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -241,6 +250,48 @@ def depcap_boundary(kl: torch.Tensor, entropy: torch.Tensor, lam: float = 1.0, L
         _check(lib().dlm_depcap_boundary_ragged(_p(kl), _p(entropy), B, Lw, _p(window_len), _p(cold_start),
                                                 ctypes.byref(prm), _p(block_len), _p(score), _stream(kl.device)))
     return block_len, score
+
+
+def revocable_state(batch: int, blk: int, device) -> dict:
+    """Initial state of a revocable decode (everything masked, no seeds)."""
+    i32 = dict(dtype=torch.int32, device=device)
+    u8 = dict(dtype=torch.uint8, device=device)
+    return dict(tok=torch.full((batch, blk), -1, **i32), masked=torch.ones((batch, blk), **u8),
+                seed=torch.zeros((batch, blk), **u8), last_seed=torch.full((batch, blk), -(2 ** 30), **i32),
+                remasks=torch.zeros((batch, blk), **i32), last_tok=torch.full((batch, blk), -1, **i32),
+                flipflops=torch.zeros(batch, **i32))
+
+
+def revocable_step(argmax: torch.Tensor, conf: torch.Tensor, state: dict, step: int, *, tau_replace=0.9,
+                   tau_draft=0.9, draft_budget=0, w_unc=1.0, w_infl=1.0, w_drift=1.0, pi=1.0, cooldown=1,
+                   remask_budget=2, influence=None, drift=None, outcome=None, n_drafted=None, n_revoked=None):
+    """dlm_revocable_step: updates ``state`` (tensors as revocable_state makes)
+    in place; returns (outcome u8 [B, blk], n_drafted, n_revoked)."""
+    _need_cuda(argmax, conf, influence, drift)
+    B, blk = state["masked"].shape
+    dev = conf.device
+    for k, dt in (("tok", torch.int32), ("masked", torch.uint8), ("seed", torch.uint8),
+                  ("last_seed", torch.int32), ("remasks", torch.int32), ("last_tok", torch.int32),
+                  ("flipflops", torch.int32)):
+        t = state[k]
+        if t.dtype != dt or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"state[{k!r}] must be a contiguous {dt} tensor on {dev}")
+    if outcome is None:
+        outcome = torch.empty((B, blk), dtype=torch.uint8, device=dev)
+    if n_drafted is None:
+        n_drafted = torch.empty(B, dtype=torch.int32, device=dev)
+    if n_revoked is None:
+        n_revoked = torch.empty(B, dtype=torch.int32, device=dev)
+    prm = RevocableParams(float(tau_replace), float(tau_draft), int(draft_budget), float(w_unc), float(w_infl),
+                          float(w_drift), float(pi), int(cooldown), int(remask_budget))
+    _check(lib().dlm_revocable_step(_p(argmax.reshape(B, blk).contiguous()), _p(conf.reshape(B, blk).contiguous()),
+                                    _p(None if influence is None else influence.reshape(B, blk).contiguous()),
+                                    _p(None if drift is None else drift.reshape(B, blk).contiguous()), B, blk,
+                                    int(step), ctypes.byref(prm), _p(state["tok"]), _p(state["masked"]),
+                                    _p(state["seed"]), _p(state["last_seed"]), _p(state["remasks"]),
+                                    _p(state["last_tok"]), _p(outcome), _p(n_drafted), _p(n_revoked),
+                                    _p(state["flipflops"]), _stream(dev)))
+    return outcome, n_drafted, n_revoked
 
 
 def cap_workspace(batch: int, p_max: int, device) -> torch.Tensor:

@@ -155,6 +155,26 @@ dlm_status dlm_depcap_boundary_ragged(const float* kl, const float* entropy, int
     return from_cuda(dlm::launch_boundary(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dlm_status dlm_revocable_step(const int32_t* argmax, const float* conf, const float* influence,
+                              const float* drift, int32_t batch, int32_t blk, int32_t step,
+                              const dlm_revocable_params* p, int32_t* tok, uint8_t* masked, uint8_t* seed,
+                              int32_t* last_seed, int32_t* remasks, int32_t* last_tok, uint8_t* outcome,
+                              int32_t* n_drafted, int32_t* n_revoked, int32_t* flipflops,
+                              dlm_stream_t stream) {
+    if (!p || batch < 0 || blk < 1 || blk > DLM_MAX_BLK) return DLM_ERR_INVALID_ARG;
+    if (!isfinite(p->pi) || p->pi < 0.f || !isfinite(p->w_unc) || !isfinite(p->w_infl) ||
+        !isfinite(p->w_drift) || isnan(p->tau_replace) || isnan(p->tau_draft))
+        return DLM_ERR_INVALID_ARG;
+    if (batch == 0) return DLM_OK;
+    if (!argmax || !conf || !tok || !masked || !seed || !last_seed || !remasks || !last_tok)
+        return DLM_ERR_INVALID_ARG;
+    dlm::RevocableArgs a{argmax, conf, influence, drift, batch, blk, step, p->tau_replace, p->tau_draft,
+                         p->draft_budget, p->w_unc, p->w_infl, p->w_drift, p->pi, p->cooldown,
+                         p->remask_budget, tok, masked, seed, last_seed, remasks, last_tok, outcome,
+                         n_drafted, n_revoked, flipflops};
+    return from_cuda(dlm::launch_revocable(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t dlm_cap_workspace_size(int32_t batch, int32_t p_max) {
     if (batch < 0 || p_max < 1 || p_max > DLM_MAX_BLK) return 0;
     return dlm::cap_workspace_bytes(batch, p_max);

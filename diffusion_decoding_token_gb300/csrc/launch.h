@@ -57,6 +57,29 @@ struct CertificateArgs {
 };
 cudaError_t launch_certificate(const CertificateArgs& a, cudaStream_t s);
 
+struct RevocableArgs {
+    const int32_t* argmax;
+    const float* conf;
+    const float* influence;
+    const float* drift;
+    int batch, blk, step;
+    float tau_replace, tau_draft;
+    int draft_budget;
+    float w_unc, w_infl, w_drift, pi;
+    int cooldown, remask_budget;
+    int32_t* tok;
+    uint8_t* masked;
+    uint8_t* seed;
+    int32_t* last_seed;
+    int32_t* remasks;
+    int32_t* last_tok;
+    uint8_t* outcome;
+    int32_t* n_drafted;
+    int32_t* n_revoked;
+    int32_t* flipflops;
+};
+cudaError_t launch_revocable(const RevocableArgs& a, cudaStream_t s);
+
 struct BoundaryArgs {
     const float* kl;
     const float* entropy;

@@ -91,6 +91,16 @@ def test_selection_argument_errors(libdlm):
     assert libdlm.dlm_depcap_boundary_ragged(fake, fake, 0, 32, None, None, ctypes.byref(dp), fake, None,
                                              None) == 0
 
+    from diffusion_decoding_token_gb300._binding import RevocableParams
+    rp = RevocableParams(0.9, 0.9, 0, 1.0, 1.0, 1.0, float("nan"), 1, 2)   # pi must be finite
+    rargs = (fake, fake, None, None, 2, 32, 0)
+    state = (fake,) * 6 + (None, None, None, None, None)
+    assert libdlm.dlm_revocable_step(*rargs, ctypes.byref(rp), *state) == INVALID
+    rp = RevocableParams(0.9, 0.9, 0, 1.0, 1.0, 1.0, 1.0, 1, 2)
+    assert libdlm.dlm_revocable_step(fake, fake, None, None, 2, 300, 0, ctypes.byref(rp), *state) == INVALID
+    assert libdlm.dlm_revocable_step(None, fake, None, None, 2, 32, 0, ctypes.byref(rp), *state) == INVALID
+    assert libdlm.dlm_revocable_step(fake, fake, None, None, 0, 32, 0, ctypes.byref(rp), *state) == 0
+
     cp = CapParams(0.8, 0.95, -16.0, 32, 0)
     args = (fake, 1, 100, 100, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
     assert libdlm.dlm_cap_select(*args, None, 0, None, None) == WS
