@@ -18,6 +18,12 @@ stand-in for the model, so the rules can be compared by the number of steps
   token at every selected position (the caller's job in the library, done
   here with torch indexing).  A sequence counts a step while it still has a
   masked position.
+* rule "revocable" (COVER page, revocable parallel decoding): the step is
+  model -> dlm_row_stats (KL to the previous step = the seeds' drift) ->
+  dlm_revocable_step, which verifies last step's seeds (the stand-in's
+  prediction at a decoded position depends on its neighbours only, so it is
+  a leave-one-out re-prediction), drafts masked positions and picks the next
+  seeds (influence = attention received from masked queries).
 
 The static inputs come from ``synth.decode_problem``.  The whole decode
 (max_steps steps) can be captured as one CUDA graph and replayed
@@ -31,13 +37,17 @@ import torch
 from . import _binding as B
 
 
-RULES = ("threshold", "factor", "topk", "cap", "dapd")
+RULES = ("threshold", "factor", "topk", "cap", "dapd", "revocable")
+
+
+REVOCABLE_DEFAULT = dict(tau_replace=0.9, tau_draft=0.9, draft_budget=0, w_unc=1.0, w_infl=1.0, w_drift=1.0,
+                         pi=1.0, cooldown=1, remask_budget=2)
 
 
 class SyntheticDecoder:
     def __init__(self, problem: dict, rule: str, device="cuda", *, tau=0.9, factor_f=1.0, topk_k=2,
                  tau_low=0.8, tau_high=0.95, gamma=-16.0, tau_edge=None, bulk_conf=0.9, bulk_frac=0.5,
-                 max_steps=None):
+                 revocable=None, max_steps=None):
         if rule not in RULES:
             raise ValueError(f"rule must be one of {RULES}")
         cfg = problem["cfg"]
@@ -46,9 +56,10 @@ class SyntheticDecoder:
         self.dev = dev
         Bn, blk, V = cfg.batch, cfg.blk, cfg.vocab
         self.B, self.blk, self.V = Bn, blk, V
-        self.max_steps = max_steps or blk
+        self.max_steps = max_steps or (3 * blk if rule == "revocable" else blk)
         f32 = dict(dtype=torch.float32, device=dev)
         self.logits = torch.from_numpy(problem["base"]).to(dev)
+        self.base_logits = self.logits.clone() if rule == "revocable" else None
         self.rows = torch.arange(Bn * blk, device=dev)
         self.target = torch.from_numpy(problem["target"].reshape(-1)).to(dev)
         self.decoy = torch.from_numpy(problem["decoy"].reshape(-1)).to(dev)
@@ -75,6 +86,18 @@ class SyntheticDecoder:
         self.dapd_ws = B.dapd_workspace(Bn, blk, dev)
         self.graph = None
         self.graph_steps = 0
+        self.step_index = 0
+        if rule == "revocable":
+            # seeds' cache drift = KL to the previous step's distribution; downstream
+            # influence = attention received from masked queries, mean over layers x heads
+            self.rev = dict(REVOCABLE_DEFAULT, **(revocable or {}))
+            self.state = B.revocable_state(Bn, blk, dev)
+            self.tok, self.masked = self.state["tok"], self.state["masked"]
+            self.prev_logits = self.logits.clone()
+            self.stats = B.alloc_row_stats(Bn * blk, dev, with_prev=True)
+            self.attn_mean = self.attn.to(torch.float32).mean(dim=(1, 2))          # [B, q, i]
+            self.outcome = torch.zeros((Bn, blk), dtype=torch.uint8, device=dev)
+            self.n_revised = torch.zeros(Bn, dtype=torch.int32, device=dev)
 
     # -- the stand-in model ------------------------------------------------
     def model(self):
@@ -92,6 +115,9 @@ class SyntheticDecoder:
         active = (self.masked.sum(-1) > 0).to(torch.int32)
         self.steps += active
         self.model()
+        if self.rule == "revocable":
+            self._revocable_step()
+            return
         st = B.row_stats(self.logits, out=self.stats, status=self.status)
         conf = st.conf.view(Bn, blk)
         p = self.prm
@@ -112,6 +138,21 @@ class SyntheticDecoder:
         self.tok.copy_(torch.where(chosen, st.argmax.view(Bn, blk), self.tok))
         self.masked.mul_((~chosen).to(torch.uint8))
 
+    def _revocable_step(self):
+        Bn, blk = self.B, self.blk
+        st = B.row_stats(self.logits, self.prev_logits, out=self.stats, status=self.status)
+        self.prev_logits.copy_(self.logits)
+        infl = torch.bmm(self.masked.to(torch.float32)[:, None, :], self.attn_mean)[:, 0, :]
+        r = self.rev
+        B.revocable_step(st.argmax.view(Bn, blk), st.conf.view(Bn, blk), self.state, self.step_index,
+                         tau_replace=r["tau_replace"], tau_draft=r["tau_draft"], draft_budget=r["draft_budget"],
+                         w_unc=r["w_unc"], w_infl=r["w_infl"], w_drift=r["w_drift"], pi=r["pi"],
+                         cooldown=r["cooldown"], remask_budget=r["remask_budget"], influence=infl,
+                         drift=st.kl.view(Bn, blk), outcome=self.outcome, n_drafted=self.nsel)
+        self.sel.copy_(self.outcome)
+        self.n_revised += (self.outcome >= 3).sum(-1, dtype=torch.int32)
+        self.step_index += 1
+
     def capture(self, n_steps: int | None = None):
         """Capture ``n_steps`` decoding steps (default: the whole decode,
         max_steps of them) as one CUDA graph.  A sequence with nothing masked
@@ -124,6 +165,7 @@ class SyntheticDecoder:
         with torch.cuda.stream(s):
             self.step()  # warm-up outside the graph
         torch.cuda.current_stream(self.dev).wait_stream(s)
+        self.step_index = 0  # the captured steps carry step indices 0 .. n_steps-1
         self.graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.graph):
             for _ in range(n_steps):
@@ -143,6 +185,15 @@ class SyntheticDecoder:
             self.masked.copy_(saved[1])
             self.steps.copy_(saved[2])
             self.logits.copy_(saved[3])
+        self.step_index = 0
+        if self.rule == "revocable":
+            self.state["seed"].zero_()
+            self.state["last_seed"].fill_(-(2 ** 30))
+            self.state["remasks"].zero_()
+            self.state["last_tok"].fill_(-1)
+            self.state["flipflops"].zero_()
+            self.n_revised.zero_()
+            self.prev_logits.copy_(self.base_logits)
 
     def run(self, graph: bool = False, log=None):
         """Decode until nothing is masked (or max_steps); returns a summary.
@@ -167,10 +218,15 @@ class SyntheticDecoder:
         committed = tok >= 0
         wrong = committed & (tok != target)
         steps = self.steps.cpu().numpy()
-        return dict(rule=self.rule, steps=steps, mean_steps=float(steps.mean()), tokens=tok,
-                    error_rate=float(wrong.sum() / max(1, committed.sum())),
-                    tokens_per_step=float(committed.sum() / max(1, steps.sum())),
-                    unfinished=int((~committed).sum()), status=int(self.status.item()))
+        out = dict(rule=self.rule, steps=steps, mean_steps=float(steps.mean()), tokens=tok,
+                   error_rate=float(wrong.sum() / max(1, committed.sum())),
+                   tokens_per_step=float(committed.sum() / max(1, steps.sum())),
+                   unfinished=int((~committed).sum()), status=int(self.status.item()))
+        if self.rule == "revocable":
+            out["revisions"] = int(self.n_revised.sum().item())
+            out["remasks"] = int(self.state["remasks"].sum().item())
+            out["flipflops"] = int(self.state["flipflops"].sum().item())
+        return out
 
 
 class DepCapDecoder:

@@ -86,12 +86,11 @@ def full_logits(problem, masked):
     return lg
 
 
-def depcap_step(problem, state, prm, blen_override=None):
+def depcap_step(problem, state, prm):
     """One step of the block loop from ``state`` (masked [B,N], cursor [B],
     blen [B] (0 = pick a block), cold [B], snap_masked [B,N]: the mask at the
     forward pass that became the sequence's snapshot, or None before the
-    first).  ``blen_override`` replaces the block lengths CAP works on (the
-    other side's, to compare CAP from the same state).  Returns dict(need, new_len, score, blen, sel, pos, stats, cap)."""
+    first).  Returns dict(need, new_len, score, blen, sel, pos, stats, cap)."""
     cfg = problem["cfg"]
     B, N, Lm = cfg.batch, cfg.blk, prm["L_max"]
     masked, cursor = state["masked"], state["cursor"]
@@ -116,7 +115,7 @@ def depcap_step(problem, state, prm, blen_override=None):
     new_len, score = oracle.depcap_boundary(o["kl"].reshape(B, Lm), o["entropy"].reshape(B, Lm), prm["lam"],
                                             prm["L_min"], prm["smooth_w"], prm["norm_mode"],
                                             cold_start=state["cold"], window_len=window_len)
-    blen = np.where(need, new_len, state["blen"]) if blen_override is None else blen_override
+    blen = np.where(need, new_len, state["blen"])
     in_block = np.arange(Lm)[None, :] < blen[:, None]
     mwin = (np.take_along_axis(masked, pos, 1) * in_block).astype(np.uint8)
     r = oracle.cap_select(win, o["argmax"].reshape(B, Lm), o["conf"].reshape(B, Lm), o["lse"].reshape(B, Lm),
@@ -154,9 +153,10 @@ def depcap_initial(problem):
                 cold=np.ones(B, np.uint8), snap_masked=[None] * B)
 
 
-def depcap_decode(problem, prm=DEPCAP_DEFAULT, max_steps=None):
+def depcap_decode(problem, prm=DEPCAP_DEFAULT, max_steps=None, trace=None):
     """The whole block loop on the oracle side.  Returns (steps [B], tok,
-    blocks: per sequence the list of (start, length))."""
+    blocks: per sequence the list of (start, length)); ``trace``, a list,
+    receives (state before the step, the step's outputs) per step."""
     cfg = problem["cfg"]
     B, N = cfg.batch, cfg.blk
     state = depcap_initial(problem)
@@ -171,5 +171,43 @@ def depcap_decode(problem, prm=DEPCAP_DEFAULT, max_steps=None):
         for b in np.nonzero(out["need"])[0]:
             blocks[b].append((int(state["cursor"][b]), int(out["blen"][b])))
         out["argmax"] = out["stats"]["argmax"].reshape(B, prm["L_max"])
+        if trace is not None:
+            trace.append((state, out))
         state = depcap_commit(state, out, tok)
     return steps, tok, blocks
+
+
+# ---------------------------------------------------------------------------
+# Revocable decoding (COVER page): the oracle side of SyntheticDecoder's
+# "revocable" rule.
+# ---------------------------------------------------------------------------
+REVOCABLE_DEFAULT = dict(tau_replace=0.9, tau_draft=0.9, draft_budget=0, w_unc=1.0, w_infl=1.0, w_drift=1.0,
+                         pi=1.0, cooldown=1, remask_budget=2)
+
+
+def revocable_decode(problem, max_steps, prm=REVOCABLE_DEFAULT):
+    """Returns (trace, state): per step dict(masked, conf, argmax, kl, infl,
+    outcome, seed_before, last_seed_before, remasks_before, tok_before) and the
+    final state."""
+    cfg = problem["cfg"]
+    B, blk = cfg.batch, cfg.blk
+    attn = problem["attn"].view(np.float16).astype(np.float64).mean(axis=(1, 2))        # [B, q, i]
+    state = oracle.revocable_init(B, blk)
+    prev = problem["base"].copy()
+    trace = []
+    for t in range(max_steps):
+        if state["masked"].sum() == 0:
+            break
+        cur = full_logits(problem, state["masked"])
+        o = oracle.row_stats(cur, prev)
+        prev = cur
+        infl = np.einsum("bq,bqi->bi", state["masked"].astype(np.float64), attn)
+        rec = dict(masked=state["masked"].copy(), seed=state["seed"].copy(), last_seed=state["last_seed"].copy(),
+                   remasks=state["remasks"].copy(), tok=state["tok"].copy(), last_tok=state["last_tok"].copy(),
+                   conf=o["conf"].reshape(B, blk), argmax=o["argmax"].reshape(B, blk), kl=o["kl"].reshape(B, blk),
+                   infl=infl)
+        r = oracle.revocable_step(o["argmax"].reshape(B, blk), o["conf"].reshape(B, blk), state, t,
+                                  influence=infl, drift=o["kl"].reshape(B, blk), **prm)
+        rec["outcome"] = r["outcome"]
+        trace.append(rec)
+    return trace, state

@@ -116,11 +116,13 @@ def boundary_margin_ok(score):
     return not np.any(np.abs(upto) < THRESH_TOL)
 
 
-def cap_margin_ok(cfg, c, masked, D, pool, pool_n, scope):
+def cap_margin_ok(cfg, c, masked, D, pool, pool_n, scope, conf_tol=THRESH_TOL):
+    """``conf_tol``: margin of the tau_low test (f32 logits may use the
+    row-stats parity tolerance, 1e-4, instead of THRESH_TOL)."""
     m = masked.astype(bool).copy()
     m[scope:] = False
     for t in (cfg.tau_low,):
-        if np.any(np.abs(c[m] - t) < THRESH_TOL):
+        if np.any(np.abs(c[m] - t) < conf_tol):
             return False
     p = [int(x) for x in pool[:pool_n]]
     if not p:

@@ -1,13 +1,13 @@
 """DepCap's block loop on the GPU (DepCapDecoder: row stats against the
 snapshot, the ragged DepGA-Block boundary, CAP within the block) against the
-oracle's step from the same state, step by step, where the decisions clear
-the margins of parity.py; invariants of the loop; the whole decode replayed
-as one CUDA graph equals the eager run."""
+oracle's loop: the two run independently and each sequence agrees step by
+step up to its first decision inside the margins of parity.py; invariants of
+the loop; the whole decode replayed as one CUDA graph equals the eager run."""
 import numpy as np
 import pytest
 
 import synth
-from decode_ref import DEPCAP_DEFAULT, depcap_step
+from decode_ref import DEPCAP_DEFAULT, depcap_decode
 from parity import boundary_margin_ok, cap_margin_ok
 
 pytestmark = pytest.mark.gpu
@@ -21,55 +21,69 @@ def _decoder(prob):
     return DepCapDecoder(prob, **PRM)
 
 
-def test_depcap_loop_matches_oracle_steps():
+def _step_margin_ok(state, out, b, scfg):
+    """The boundary (when the sequence picks a block) and CAP decisions of
+    sequence b in this oracle step clear the margins."""
+    if out["need"][b] and state["snap_masked"][b] is not None:
+        wl = int(out["window_len"][b])
+        if not boundary_margin_ok(out["score"][b, :wl]):
+            return False
+    conf = out["stats"]["conf"].reshape(len(out["need"]), -1)
+    # f32 logits: GPU confidences are within the row-stats parity tolerance (1e-4) of the oracle's
+    return cap_margin_ok(scfg, conf[b], out["mwin"][b], out["cap"]["D"][b], out["cap"]["pool"][b],
+                         out["cap"]["pool_n"][b], int(out["blen"][b]), conf_tol=1e-4)
+
+
+def test_depcap_loop_matches_oracle():
+    """GPU and oracle run the loop independently; each sequence's steps
+    (cursor, block length, selection) agree up to its first step with a
+    decision inside the margins, and its tokens when it never had one."""
     prob = synth.decode_problem(CFG, seed=5)
     res = _decoder(prob).run(trace=True)
     assert res["status"] == 0 and res["unfinished"] == 0
+    otrace = []
+    osteps, otok, oblocks = depcap_decode(prob, PRM, trace=otrace)
     B, N, Lm = CFG.batch, CFG.blk, PRM["L_max"]
-    snap = [None] * B
-    seen = np.zeros(B, bool)
-    tok = np.full((B, N), -1, np.int64)
-    n_len = n_len_ok = n_cap = n_cap_ok = 0
-    lens = []
-    for k, t in enumerate(res["trace"]):
-        need = t["need"].astype(bool)
-        state = dict(masked=t["masked"], cursor=t["cursor"].astype(np.int64),
-                     blen=np.where(need, 0, t["blen"]).astype(np.int64), cold=(~seen).astype(np.uint8),
-                     snap_masked=snap)
-        out = depcap_step(prob, state, PRM, blen_override=t["blen"].astype(np.int64))
-        for b in np.nonzero(need)[0]:
-            n_len += 1
-            wl = int(out["window_len"][b])
-            assert min(PRM["L_min"], wl) <= t["blen"][b] <= wl, (k, b)
-            if not seen[b] or boundary_margin_ok(out["score"][b, :wl]):
-                assert t["blen"][b] == out["new_len"][b], (k, b)
-                n_len_ok += 1
-            lens.append(int(t["blen"][b]))
-        conf = out["stats"]["conf"].reshape(B, Lm)
-        scfg = synth.scaled(synth.CONFIGS["tiny"], tau_low=PRM["tau_low"], gamma=PRM["gamma"], p_max=Lm)
-        for b in range(B):
-            if t["cursor"][b] >= N:
-                assert not t["sel"][b].any()
+    scfg = synth.scaled(synth.CONFIGS["tiny"], tau_low=PRM["tau_low"], gamma=PRM["gamma"], p_max=Lm)
+    compared = total = whole = 0
+    for b in range(B):
+        clean = True
+        for k, (state, out) in enumerate(otrace):
+            if state["cursor"][b] >= N:
+                break
+            total += 1
+            if not clean or not _step_margin_ok(state, out, b, scfg):
+                clean = False
                 continue
-            n_cap += 1
-            if cap_margin_ok(scfg, conf[b], out["mwin"][b], out["cap"]["D"][b], out["cap"]["pool"][b],
-                             out["cap"]["pool_n"][b], int(t["blen"][b])):
-                np.testing.assert_array_equal(t["sel"][b], out["sel"][b], err_msg=f"step {k} sequence {b}")
-                n_cap_ok += 1
-            assert t["sel"][b].any()                                   # progress
-            am = out["stats"]["argmax"].reshape(B, Lm)[b]
-            for j in np.nonzero(t["sel"][b])[0]:
-                tok[b, out["pos"][b, j]] = am[j]
-        for b in np.nonzero(need)[0]:
-            snap[b] = t["masked"][b].copy()
-            seen[b] = True
-    np.testing.assert_array_equal(res["tokens"], tok)                  # every commit is the oracle's argmax
-    assert n_len_ok >= 0.8 * n_len and n_cap_ok >= 0.8 * n_cap
-    assert len(set(lens)) > 2                                          # the boundary really varies
-    assert (res["n_blocks"] >= N // Lm).all()
+            g = res["trace"][k]
+            assert g["cursor"][b] == state["cursor"][b] and bool(g["need"][b]) == bool(out["need"][b]), (b, k)
+            assert g["blen"][b] == out["blen"][b], (b, k)
+            np.testing.assert_array_equal(g["sel"][b], out["sel"][b], err_msg=f"sequence {b} step {k}")
+            compared += 1
+        if clean:
+            whole += 1
+            np.testing.assert_array_equal(res["tokens"][b], otok[b])
+            assert res["steps"][b] == osteps[b] and res["n_blocks"][b] == len(oblocks[b])
+    # the loop's invariants on the GPU trace alone
+    for b in range(B):
+        start, blen, lens = 0, 0, []
+        for k, t in enumerate(res["trace"]):
+            if t["cursor"][b] >= N:
+                assert start + blen == N
+                break
+            if t["need"][b]:                                            # a new block starts where the last ended
+                assert t["cursor"][b] == start + blen, (b, k)
+                start, blen = int(t["cursor"][b]), int(t["blen"][b])
+                wl = min(Lm, N - start)
+                assert min(PRM["L_min"], wl) <= blen <= wl
+                lens.append(blen)
+            else:
+                assert t["cursor"][b] == start and t["blen"][b] == blen, (b, k)
+            assert t["sel"][b].any() and not np.any(t["sel"][b][blen:])   # progress, inside the block
+        assert lens[0] == PRM["L_min"] and len(set(lens)) > 1
+    assert compared >= 0.6 * total and whole >= 1
     print(f"depcap loop: mean steps {res['mean_steps']:.1f}, blocks {res['n_blocks'].tolist()}, "
-          f"lengths compared {n_len_ok}/{n_len}, CAP steps compared {n_cap_ok}/{n_cap}, "
-          f"error rate {res['error_rate']:.3f}")
+          f"steps compared {compared}/{total}, whole sequences {whole}, error rate {res['error_rate']:.3f}")
 
 
 def test_depcap_whole_decode_graph_equals_eager():
