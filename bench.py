@@ -46,13 +46,15 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--serial-dapd", action="store_true",
-                    help="run the DAPD chain on the main stream after the other rules (default: on a side stream "
-                         "after the row pass, concurrently with the threshold, boundary and CAP kernels)")
-    ap.add_argument("--early-dapd-fork", action="store_true",
-                    help="start the DAPD attention graph at the beginning of the step on the low-priority side "
-                         "stream (it then shares the row pass's last wave; default: fork after the row pass)")
+                    help="run the DAPD chain on the main stream after the other rules (default: on a side stream)")
+    ap.add_argument("--late-dapd-fork", action="store_true",
+                    help="fork the DAPD chain after the row pass (default: the attention graph starts with the "
+                         "step on the low-priority side stream and takes the SMs the row pass's last wave leaves "
+                         "free; the selection waits for the statistics)")
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="write a 512 MB buffer between timed steps (auto: when a step reads less than twice L2)")
+    ap.add_argument("--serial-rules", action="store_true",
+                    help="run threshold, boundary and CAP one after another (default: parallel graph branches)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the rules eagerly instead of replaying them as one captured CUDA graph")
     ap.add_argument("--extra-rules", default="",
@@ -247,7 +249,8 @@ def run_native(args, rank, world, local):
                   bulk_frac=cfg.bulk_frac, status=status)
     extra = tuple(r for r in args.extra_rules.split(",") if r)
     common.update(rules=tuple(cfg.rules) + extra, cap_scope_from_boundary=(cfg.name == "depcap_window"),
-                  concurrent_dapd=not args.serial_dapd, dapd_early=args.early_dapd_fork)
+                  concurrent_dapd=not args.serial_dapd, dapd_early=not args.late_dapd_fork,
+                  parallel_rules=not args.serial_rules)
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 
     for _ in range(args.warmup):
@@ -268,6 +271,7 @@ def run_native(args, rank, world, local):
             return
         plan.run_rows(stream, events=ev)
         rules_graph.replay()
+        plan.join(stream)
 
     for _ in range(args.warmup):
         run_step()
@@ -575,7 +579,13 @@ def main():
                           f"no flush: {k1_bytes / 1e9:.3f} GB of logit rows per step, larger than L2"),
                    "parallelism": f"dp{world}"},
         "logit_gbps": k1_gbs,
-        "kernels_ms": {"row_stats": k1_ms, "four_rules": r["rules_ms"]},
+        "kernels_ms": {"row_stats": k1_ms, "rules_graph": r["rules_ms"]},
+        "step_structure": ("row pass on a high-priority stream; DAPD attention graph on a low-priority side stream "
+                           "from the step's start (" + ("after the row pass" if args.late_dapd_fork else
+                                                          "it shares the row pass's last wave") +
+                           "), DAPD selection after the row pass; threshold / boundary / CAP as " +
+                           ("one chain" if args.serial_rules else "parallel branches") +
+                           " of a captured CUDA graph (rules_graph = that graph alone)"),
         "host_enqueue_ms_per_step": r["host_ms"],
         "rules_as_cuda_graph": not args.no_graph,
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,

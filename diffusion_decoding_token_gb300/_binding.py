@@ -417,7 +417,8 @@ class StepPlan:
                  tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=None, high_tier_unconditional=False,
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
-                 row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0):
+                 row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0,
+                 parallel_rules=False):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -501,10 +502,11 @@ class StepPlan:
                 # By default it forks after the row pass and overlaps the
                 # latency-bound threshold, boundary and CAP kernels.  With
                 # dapd_early the attention graph (which needs no statistics)
-                # forks at the start of the step: as a lower-priority kernel
-                # its CTAs take SMs only as the row pass's last wave drains;
-                # the selection then waits for the statistics.  Run the plan on
-                # a higher-priority stream for that to hold.
+                # is issued with the row pass (run_rows) and forks at the start
+                # of the step: as a lower-priority kernel its CTAs take SMs
+                # only as the row pass's last wave drains; the selection then
+                # waits for the statistics.  Run the plan on a higher-priority
+                # stream for that to hold.
                 lo, _ = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, 0)
                 self.side = torch.cuda.Stream(device=dev, priority=lo)
                 self._ev_start = torch.cuda.Event()
@@ -522,6 +524,28 @@ class StepPlan:
             else:
                 self._calls.append(call)
 
+        # parallel_rules: the independent rules after the row pass run as
+        # parallel branches (streams forked and joined inside the step, so a
+        # captured graph gets parallel branches too); CAP scoped by the
+        # boundary's length stays behind the boundary on one branch
+        self._lanes = None
+        if parallel_rules and len(self._calls) > 2:
+            names = [n for n in ("threshold", "topk", "factor", "boundary", "cap") if n in rules]
+            if "dapd" in rules and self.side is None:
+                names.append("dapd")
+            assert len(names) == len(self._calls) - 1
+            by_name = dict(zip(names, self._calls[1:]))
+            lanes = [[by_name[n]] for n in ("dapd", "threshold", "topk", "factor") if n in by_name]
+            if cap_scope_from_boundary and "boundary" in by_name and "cap" in by_name:
+                lanes.append([by_name["boundary"], by_name["cap"]])
+            else:
+                lanes += [[by_name[n]] for n in ("boundary", "cap") if n in by_name]
+            _, hi = torch.cuda.Stream.priority_range()
+            self._lanes = [(torch.cuda.Stream(device=dev, priority=hi), lane, torch.cuda.Event())
+                           for lane in lanes[:-1]]
+            self._main_lane = lanes[-1]
+            self._ev_fork = torch.cuda.Event()
+
     @property
     def n_launches(self) -> int:
         """Kernels launched per step: 1 row pass + 1 threshold + 1 boundary + 3 CAP + 3 DAPD."""
@@ -529,50 +553,78 @@ class StepPlan:
         return 1 + sum(per[r] for r in self.rules)
 
     def run_rows(self, stream=None, events=None):
-        """Issue only the row pass (e.g. ahead of a captured graph of the
-        rules, see ``run(rules_only=True)``)."""
+        """Issue the row pass (e.g. ahead of a captured graph of the rules,
+        see ``run(rules_only=True)``).  With ``dapd_early`` it also issues the
+        whole DAPD chain on the side stream: the attention graph waits only
+        for the step's start (as a lower-priority kernel it takes the SMs the
+        row pass's last wave leaves free), the selection for the statistics.
+        Join it with :meth:`join` before the next step."""
         st = stream or torch.cuda.current_stream(self.dev)
+        early = self.side is not None and self.dapd_early
+        if early:
+            self._ev_start.record(st)
         fn, args = self._calls[0]
         if events is not None:
             events[0].record(st)
         _check(fn(*args, ctypes.c_void_p(st.cuda_stream)))
         if events is not None:
             events[1].record(st)
+        if early:
+            side = ctypes.c_void_p(self.side.cuda_stream)
+            self.side.wait_event(self._ev_start)
+            for fn2, args2 in self._graph_calls:
+                _check(fn2(*args2, side))
+            self._ev_rows.record(st)
+            self.side.wait_event(self._ev_rows)
+            for fn2, args2 in self._side_calls:
+                _check(fn2(*args2, side))
+            self._ev_side.record(self.side)
+
+    def join(self, stream=None):
+        """With ``dapd_early``: make ``stream`` wait for the side stream's DAPD
+        chain (the next step's row pass must not overwrite statistics it still
+        reads).  ``run`` joins by itself except for ``rules_only``; without
+        ``dapd_early`` the join is part of ``run`` and this does nothing."""
+        if self.side is not None and self.dapd_early:
+            (stream or torch.cuda.current_stream(self.dev)).wait_event(self._ev_side)
 
     def run(self, stream=None, events=None, rules_only=False):
         """Issue the step on ``stream`` (default: the current stream).  With
         ``events`` = (e0, e1), e0/e1 are recorded around the row pass.
-        ``rules_only`` re-runs the rules on the statistics already in the
-        plan's buffers (for timing them apart)."""
+        ``rules_only`` issues only what follows the row pass, on the
+        statistics already in the plan's buffers: the part that is captured
+        as a CUDA graph (with ``dapd_early`` the DAPD chain belongs to
+        :meth:`run_rows`, and the caller joins it with :meth:`join`)."""
         st = stream or torch.cuda.current_stream(self.dev)
         s = ctypes.c_void_p(st.cuda_stream)
-        side = ctypes.c_void_p(self.side.cuda_stream) if self.side is not None else None
-        for k, (fn, args) in enumerate(self._calls):
-            if k > 0:
+        if not rules_only:
+            self.run_rows(st, events)
+        late = self.side is not None and not self.dapd_early
+        if late:
+            # the statistics are ready: the DAPD chain on the side stream,
+            # concurrent with the other rules
+            side = ctypes.c_void_p(self.side.cuda_stream)
+            self._ev_rows.record(st)
+            self.side.wait_event(self._ev_rows)
+            for fn2, args2 in self._side_calls:
+                _check(fn2(*args2, side))
+            self._ev_side.record(self.side)
+        if self._lanes is None:
+            for fn, args in self._calls[1:]:
                 _check(fn(*args, s))
-                continue
-            if self.side is not None and self.dapd_early:
-                self._ev_start.record(st)
-            if not rules_only:
-                if events is not None:
-                    events[0].record(st)
+        else:
+            self._ev_fork.record(st)
+            for bs, lane, ev in self._lanes:
+                bs.wait_event(self._ev_fork)
+                b_s = ctypes.c_void_p(bs.cuda_stream)
+                for fn, args in lane:
+                    _check(fn(*args, b_s))
+                ev.record(bs)
+            for fn, args in self._main_lane:
                 _check(fn(*args, s))
-                if events is not None:
-                    events[1].record(st)
-            if self.side is not None:
-                if self.dapd_early:
-                    # issued after the row pass on the host, so the row pass
-                    # reaches the GPU first; waits only for the step start
-                    self.side.wait_event(self._ev_start)
-                    for fn2, args2 in self._graph_calls:
-                        _check(fn2(*args2, side))
-                # statistics are ready: the rest of the DAPD chain
-                self._ev_rows.record(st)
-                self.side.wait_event(self._ev_rows)
-                for fn2, args2 in self._side_calls:
-                    _check(fn2(*args2, side))
-                self._ev_side.record(self.side)
-        if self.side is not None:
-            # join: the next step's row pass must not overwrite statistics the
-            # side stream still reads
+            for _, _, ev in self._lanes:
+                st.wait_event(ev)
+        if late:
             st.wait_event(self._ev_side)
+        elif self.side is not None and not rules_only:
+            self.join(st)

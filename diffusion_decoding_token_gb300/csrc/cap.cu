@@ -2,7 +2,8 @@
 // greedy conflict-free selection (DepCap, "Methodology"; defaults in
 // "Experiments").
 //
-// Three launches on the caller's stream:
+// Pools of up to 64 candidates: one fused launch (cap_fused_kernel below).
+// Larger pools: three launches on the caller's stream:
 //   cap_pool     one CTA per sequence: candidates (masked, conf >= tau_low)
 //                ranked by (conf desc, position asc) with an all-pairs rank
 //                count, clipped to p_max;
@@ -149,6 +150,121 @@ __global__ void __launch_bounds__(kThreads) cap_greedy_kernel(CapArgs a) {
     if (t == 0) a.n_selected[b] = total;
 }
 
+// Small pools (p_max <= kFusedMaxPool): the three phases in one CTA per
+// sequence, the pool, its tokens / LSEs and the conflict bitmask in shared
+// memory.  D is symmetric (the two log-probabilities are added in either
+// order, and fp32 addition commutes), so each unordered pair is scored once
+// and both bits are set.
+constexpr int kFusedMaxPool = 64;
+constexpr int kFusedWords = kFusedMaxPool / 32;
+
+__global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
+    __shared__ float s_c[kThreads];
+    __shared__ int s_cand[kThreads];
+    __shared__ int s_pool[kFusedMaxPool];
+    __shared__ int s_y[kFusedMaxPool];
+    __shared__ float s_lse[kFusedMaxPool];
+    __shared__ uint32_t s_adj[kFusedMaxPool * kFusedWords];
+    __shared__ uint32_t s_kept[kFusedWords];
+    __shared__ unsigned char s_tier[kFusedMaxPool];
+    __shared__ float s_v[kThreads / 32];
+    __shared__ int s_i[kThreads / 32];
+    const int b = blockIdx.x, t = threadIdx.x;
+    const int scope = scope_of(a, b);
+    const int64_t o = (int64_t)b * a.blk + t;
+    uint8_t* sel = a.selected + (int64_t)b * a.blk;
+
+    // 1. pool: masked in scope with conf >= tau_low, by (conf desc, position asc)
+    const bool m = t < scope && a.masked[o] != 0;
+    const float c = t < a.blk ? a.conf[o] : 0.f;
+    const bool cand = m && c >= a.tau_low;
+    s_c[t] = cand ? c : 0.f;
+    s_cand[t] = cand;
+    if (t < kFusedMaxPool * kFusedWords) s_adj[t] = 0u;
+    const int n_cand = __syncthreads_count(cand);
+    const int n = min(n_cand, a.p_max);
+    if (cand) {
+        int rank = 0;
+        for (int j = 0; j < scope; ++j) {
+            if (!s_cand[j]) continue;
+            const float cj = s_c[j];
+            rank += (cj > c) || (cj == c && j < t);
+        }
+        if (rank < a.p_max) {
+            s_pool[rank] = t;
+            s_y[rank] = a.argmax[o];
+            s_lse[rank] = a.lse[o];
+            s_tier[rank] = a.high_tier_unconditional && c >= a.tau_high;
+        }
+    }
+    if (t < a.blk) sel[t] = 0;
+    if (t == 0 && n_cand > a.p_max) raise_status(a.dev_status, DLM_DEV_POOL_CLIPPED);
+    __syncthreads();
+
+    if (n == 0) {  // no candidate: the highest-confidence masked position of the scope
+        float v = m ? c : -INFINITY;
+        int idx = m ? t : 0x7fffffff;
+        const int any_m = __syncthreads_or(m);
+        warp_argmax(v, idx);
+        if ((t & 31) == 0) {
+            s_v[t >> 5] = v;
+            s_i[t >> 5] = idx;
+        }
+        __syncthreads();
+        if (t < 32) {
+            v = t < kThreads / 32 ? s_v[t] : -INFINITY;
+            idx = t < kThreads / 32 ? s_i[t] : 0x7fffffff;
+            warp_argmax(v, idx);
+            if (t == 0) {
+                if (any_m) sel[idx] = 1;
+                a.n_selected[b] = any_m ? 1 : 0;
+            }
+        }
+        return;
+    }
+
+    // 2. conflicts: one unordered pair (i < j) of pool slots per thread-step
+    const int pairs = n * (n - 1) / 2;
+    for (int q = t; q < pairs; q += kThreads) {
+        // row i holds the pairs (i, i+1 .. n-1); find i with start(i) <= q
+        int i = 0, start = 0;
+        while (start + (n - 1 - i) <= q) {
+            start += n - 1 - i;
+            ++i;
+        }
+        const int j = i + 1 + (q - start);
+        const int64_t ri = (int64_t)b * a.blk + s_pool[i];
+        const int64_t rj = (int64_t)b * a.blk + s_pool[j];
+        const float g1 = load_logit(a.logits, a.dtype, ri * a.row_stride + s_y[j]) - s_lse[i];
+        const float g2 = load_logit(a.logits, a.dtype, rj * a.row_stride + s_y[i]) - s_lse[j];
+        const float d = g1 + g2;
+        if (d > a.gamma) {
+            atomicOr(&s_adj[i * kFusedWords + (j >> 5)], 1u << (j & 31));
+            atomicOr(&s_adj[j * kFusedWords + (i >> 5)], 1u << (i & 31));
+        }
+        if (a.D_out) {
+            a.D_out[((int64_t)b * a.blk + s_pool[i]) * a.blk + s_pool[j]] = d;
+            a.D_out[((int64_t)b * a.blk + s_pool[j]) * a.blk + s_pool[i]] = d;
+        }
+    }
+    __syncthreads();
+
+    // 3. greedy over the pool order
+    const int W = (n + 31) >> 5;
+    if (t < 32) {
+        const uint32_t kept = greedy_scan(s_adj, kFusedWords, nullptr, s_tier, n, W);
+        if (t < W) s_kept[t] = kept;
+    }
+    __syncthreads();
+    int mine = 0;
+    if (t < n && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
+        sel[s_pool[t]] = 1;
+        mine = 1;
+    }
+    const int total = __syncthreads_count(mine);
+    if (t == 0) a.n_selected[b] = total;
+}
+
 }  // namespace
 
 size_t cap_workspace_bytes(int batch, int p_max) {
@@ -174,6 +290,7 @@ cudaError_t launch_cap(const CapArgs& a, cudaStream_t s) {
     cfg.stream = s;
     cfg.gridDim = dim3((unsigned)a.batch);
     cfg.blockDim = dim3(kThreads);
+    if (a.p_max <= kFusedMaxPool) return cudaLaunchKernelEx(&cfg, cap_fused_kernel, a);
     cudaError_t e = cudaLaunchKernelEx(&cfg, cap_pool_kernel, a);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3((unsigned)((a.p_max + kConflictWarps - 1) / kConflictWarps), (unsigned)a.batch);

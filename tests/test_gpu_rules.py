@@ -418,16 +418,35 @@ def test_step_plan_concurrent_matches_serial(dlm):
               gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, attn=dw.attn, block_start=dw.block_start)
     serial = dlm.StepPlan(dw.cur, dw.prev, dw.masked, **kw)
     plans = [dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, **kw),
-             dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, dapd_early=True, **kw)]
+             dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, dapd_early=True, **kw),
+             dlm.StepPlan(dw.cur, dw.prev, dw.masked, parallel_rules=True, **kw),
+             dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, parallel_rules=True, **kw),
+             dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, dapd_early=True, parallel_rules=True,
+                          **kw)]
+    graphed = [dlm.StepPlan(dw.cur, dw.prev, dw.masked, concurrent_dapd=True, dapd_early=early,
+                            parallel_rules=True, **kw) for early in (False, True)]
     _, hi = torch.cuda.Stream.priority_range()
     main = torch.cuda.Stream(priority=hi)
     torch.cuda.synchronize()
     with torch.cuda.stream(main):
+        graphs = []
+        for p in graphed:      # the rules captured as a CUDA graph, as the benchmark runs them
+            p.run()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                p.run(rules_only=True)
+            graphs.append(g)
         for _ in range(3):
             serial.run()
             for p in plans:
                 p.run()
+            for p, g in zip(graphed, graphs):
+                p.run_rows(main)
+                g.replay()
+                p.join(main)
     torch.cuda.synchronize()
+    plans += graphed
     for conc in plans:
         for k in serial.out:
             np.testing.assert_array_equal(serial.out[k][0].cpu().numpy(), conc.out[k][0].cpu().numpy())
