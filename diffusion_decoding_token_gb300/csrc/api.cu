@@ -198,6 +198,7 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
     dlm::CapArgs a{};
     a.logits = logits;
     a.dtype = dtype;
+    a.vocab = vocab;
     a.row_stride = row_stride;
     a.argmax = argmax;
     a.conf = conf;

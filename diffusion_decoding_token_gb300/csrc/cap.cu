@@ -29,6 +29,17 @@ __device__ __forceinline__ float load_logit(const void* base, int dtype, int64_t
     return static_cast<const float*>(base)[i];
 }
 
+// log p_i(token): the logit of `token` in row `row` minus the row's LSE.  A
+// token outside the vocabulary (an argmax of a row that held only NaN) is
+// not read: the value is NaN (never a conflict) and the status word says so.
+__device__ __forceinline__ float logp_at(const CapArgs& a, int64_t row, int token, float lse) {
+    if ((unsigned)token >= (unsigned long long)a.vocab) {
+        raise_status(a.dev_status, DLM_DEV_NONFINITE);
+        return __int_as_float(0x7fc00000);
+    }
+    return load_logit(a.logits, a.dtype, row * a.row_stride + token) - lse;
+}
+
 __device__ __forceinline__ int scope_of(const CapArgs& a, int b) {
     int sc = a.blk;
     if (a.scope_len) sc = min(sc, max(0, a.scope_len[b]));
@@ -80,8 +91,8 @@ __global__ void __launch_bounds__(kConflictWarps * 32) cap_conflict_kernel(CapAr
         if (e < n && e != slot) {
             const int pj = pool[e];
             const int64_t rj = (int64_t)b * a.blk + pj;
-            const float g1 = load_logit(a.logits, a.dtype, ri * a.row_stride + a.argmax[rj]) - li;
-            const float g2 = load_logit(a.logits, a.dtype, rj * a.row_stride + yi) - a.lse[rj];
+            const float g1 = logp_at(a, ri, a.argmax[rj], li);
+            const float g2 = logp_at(a, rj, yi, a.lse[rj]);
             const float d = g1 + g2;
             conflict = d > a.gamma;
             if (a.D_out) a.D_out[((int64_t)b * a.blk + pi) * a.blk + pj] = d;
@@ -157,6 +168,7 @@ __global__ void __launch_bounds__(kThreads) cap_greedy_kernel(CapArgs a) {
 // and both bits are set.
 constexpr int kFusedMaxPool = 64;
 constexpr int kFusedWords = kFusedMaxPool / 32;
+constexpr int kPairUnroll = 4;  // 64 * 63 / 2 pairs = 8 per thread at most
 
 __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     __shared__ float s_c[kThreads];
@@ -174,9 +186,13 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     const int64_t o = (int64_t)b * a.blk + t;
     uint8_t* sel = a.selected + (int64_t)b * a.blk;
 
-    // 1. pool: masked in scope with conf >= tau_low, by (conf desc, position asc)
+    // 1. pool: masked in scope with conf >= tau_low, by (conf desc, position asc);
+    // the token and LSE are loaded with the confidence (one round trip)
+    const bool in = t < a.blk;
     const bool m = t < scope && a.masked[o] != 0;
-    const float c = t < a.blk ? a.conf[o] : 0.f;
+    const float c = in ? a.conf[o] : 0.f;
+    const int y = in ? a.argmax[o] : 0;
+    const float l = in ? a.lse[o] : 0.f;
     const bool cand = m && c >= a.tau_low;
     s_c[t] = cand ? c : 0.f;
     s_cand[t] = cand;
@@ -192,8 +208,8 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
         }
         if (rank < a.p_max) {
             s_pool[rank] = t;
-            s_y[rank] = a.argmax[o];
-            s_lse[rank] = a.lse[o];
+            s_y[rank] = y;
+            s_lse[rank] = l;
             s_tier[rank] = a.high_tier_unconditional && c >= a.tau_high;
         }
     }
@@ -223,28 +239,46 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
         return;
     }
 
-    // 2. conflicts: one unordered pair (i < j) of pool slots per thread-step
+    // 2. conflicts: unordered pairs (i < j) of pool slots, kPairUnroll per
+    // thread at a time with all their scattered logit loads issued together
     const int pairs = n * (n - 1) / 2;
-    for (int q = t; q < pairs; q += kThreads) {
-        // row i holds the pairs (i, i+1 .. n-1); find i with start(i) <= q
-        int i = 0, start = 0;
-        while (start + (n - 1 - i) <= q) {
-            start += n - 1 - i;
-            ++i;
+    for (int q0 = t; q0 < pairs; q0 += kThreads * kPairUnroll) {
+        // an index past the last pair maps to the pair (0, 1), which exists
+        // (pairs >= 1), and its result is dropped
+        int pi[kPairUnroll], pj[kPairUnroll];
+        float z1[kPairUnroll], z2[kPairUnroll];
+#pragma unroll
+        for (int u = 0; u < kPairUnroll; ++u) {
+            const int q = min(q0 + u * kThreads, pairs - 1);
+            // row i holds the pairs (i, i+1 .. n-1); find i with start(i) <= q
+            int i = 0, start = 0;
+            while (start + (n - 1 - i) <= q) {
+                start += n - 1 - i;
+                ++i;
+            }
+            pi[u] = i;
+            pj[u] = i + 1 + (q - start);
         }
-        const int j = i + 1 + (q - start);
-        const int64_t ri = (int64_t)b * a.blk + s_pool[i];
-        const int64_t rj = (int64_t)b * a.blk + s_pool[j];
-        const float g1 = load_logit(a.logits, a.dtype, ri * a.row_stride + s_y[j]) - s_lse[i];
-        const float g2 = load_logit(a.logits, a.dtype, rj * a.row_stride + s_y[i]) - s_lse[j];
-        const float d = g1 + g2;
-        if (d > a.gamma) {
-            atomicOr(&s_adj[i * kFusedWords + (j >> 5)], 1u << (j & 31));
-            atomicOr(&s_adj[j * kFusedWords + (i >> 5)], 1u << (i & 31));
+#pragma unroll
+        for (int u = 0; u < kPairUnroll; ++u) {
+            const int64_t ri = (int64_t)b * a.blk + s_pool[pi[u]];
+            const int64_t rj = (int64_t)b * a.blk + s_pool[pj[u]];
+            z1[u] = logp_at(a, ri, s_y[pj[u]], s_lse[pi[u]]);
+            z2[u] = logp_at(a, rj, s_y[pi[u]], s_lse[pj[u]]);
         }
-        if (a.D_out) {
-            a.D_out[((int64_t)b * a.blk + s_pool[i]) * a.blk + s_pool[j]] = d;
-            a.D_out[((int64_t)b * a.blk + s_pool[j]) * a.blk + s_pool[i]] = d;
+#pragma unroll
+        for (int u = 0; u < kPairUnroll; ++u) {
+            if (q0 + u * kThreads >= pairs) break;
+            const int i = pi[u], j = pj[u];
+            const float d = z1[u] + z2[u];
+            if (d > a.gamma) {
+                atomicOr(&s_adj[i * kFusedWords + (j >> 5)], 1u << (j & 31));
+                atomicOr(&s_adj[j * kFusedWords + (i >> 5)], 1u << (i & 31));
+            }
+            if (a.D_out) {
+                a.D_out[((int64_t)b * a.blk + s_pool[i]) * a.blk + s_pool[j]] = d;
+                a.D_out[((int64_t)b * a.blk + s_pool[j]) * a.blk + s_pool[i]] = d;
+            }
         }
     }
     __syncthreads();

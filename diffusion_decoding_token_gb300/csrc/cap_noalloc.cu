@@ -67,6 +67,7 @@ extern "C" dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype
     dlm::CapArgs a{};
     a.logits = logits;
     a.dtype = dtype;
+    a.vocab = vocab;
     a.row_stride = row_stride;
     a.argmax = argmax;
     a.conf = conf;

@@ -96,6 +96,7 @@ cudaError_t launch_boundary(const BoundaryArgs& a, cudaStream_t s);
 struct CapArgs {
     const void* logits;
     int dtype;
+    int64_t vocab;  // a token outside [0, vocab) is never gathered
     int64_t row_stride;
     const int32_t* argmax;
     const float* conf;

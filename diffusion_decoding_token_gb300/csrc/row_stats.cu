@@ -394,7 +394,8 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) 
 
     const float lnS = logf(p.S);
     const float lse = p.ref + lnS;
-    args.argmax[q] = p.idx;
+    // a row of NaN only has no maximum: position 0 (the status flags the row)
+    args.argmax[q] = (int64_t)p.idx < args.vocab ? p.idx : 0;
     args.lse[q] = lse;
     args.conf[q] = expf((p.mx - p.ref) - lnS);
     args.entropy[q] = lnS - kLn2 * (p.T / p.S);

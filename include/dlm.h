@@ -92,7 +92,8 @@ int dlm_version(void);
  *               (else q = r).  Results are stored at index q, so the output
  *               arrays must hold max(q)+1 entries; entries of rows not
  *               processed are left unchanged.
- * argmax      : int32 output; conf, lse, entropy: float outputs (required).
+ * argmax      : int32 output (a row holding only NaN gets 0); conf, lse,
+ *               entropy: float outputs (required).
  * kl, lse_prev: float outputs, nullable (ignored when prev is NULL).
  * dev_status  : nullable; DLM_DEV_NONFINITE is set for a row holding NaN or
  *               +inf (its outputs are then unspecified).
@@ -224,7 +225,9 @@ dlm_status dlm_depcap_boundary_ragged(const float* kl, const float* entropy, int
  * logits      : the current logit rows (as given to dlm_row_stats), row
  *               b*blk + i, stride row_stride elements; 16-byte alignment is
  *               not required (scattered 2-byte reads).
- * argmax, conf, lse : [batch][blk] from dlm_row_stats.
+ * argmax, conf, lse : [batch][blk] from dlm_row_stats.  A token outside
+ *                     [0, vocab) is never read from the logits: its pairs
+ *                     score NaN (no conflict) and DLM_DEV_NONFINITE is set.
  * masked      : uint8 [batch][blk].
  * scope_len   : nullable int32 [batch] (e.g. dlm_depcap_boundary's block_len);
  *               NULL = the whole block.

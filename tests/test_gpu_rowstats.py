@@ -123,3 +123,16 @@ def test_split_and_unsplit_agree(dlm):
         a = getattr(few, k).cpu().numpy()
         b = getattr(many, k).cpu().numpy()[:8]
         assert close(a, b, atol=2e-5, rtol=2e-5).all()
+
+
+def test_all_nan_row_argmax_in_range(dlm):
+    # a row holding only NaN has no maximum: its argmax is position 0 and the
+    # status word flags it, so downstream gathers stay inside the row
+    x = np.zeros((2, 4096), np.float32)
+    x[0] = np.nan
+    x[1, 1234] = 3.0
+    st = dlm.new_status()
+    g = dlm.row_stats(to_torch(x, synth.F32, "cuda"), status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dlm.DEV_NONFINITE
+    assert int(g.argmax[0]) == 0 and int(g.argmax[1]) == 1234

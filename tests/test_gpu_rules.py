@@ -473,3 +473,26 @@ def test_dapd_preunmask_certain(dlm, n_masked):
         r = oracle.dapd(sub16, masked, conf.astype(np.float64), 0.05, dtype=synth.F16, preunmask_certain=flag)
         np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
         np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+
+
+@pytest.mark.parametrize("p_max", [4, 128])
+def test_cap_out_of_vocab_token_is_not_gathered(dlm, p_max):
+    """A caller-supplied token outside [0, V) scores NaN (no conflict) on both
+    CAP paths (fused for pools <= 64, three launches above) and sets the
+    status word; the valid pairs are still decided."""
+    V, blk = 16, 4
+    z = np.full((blk, V), -30.0, np.float32)
+    am = np.array([[3, 100000, 3, 1]], np.int32)
+    for i, t in enumerate(am[0]):
+        if t < V:
+            z[i, t] = 10.0
+    z[0, 3] = z[2, 3] = 10.0          # rows 0 and 2 share token 3: they conflict
+    lse = np.log(np.exp(z.astype(np.float64)).sum(-1)).astype(np.float32)
+    conf = np.array([[0.99, 0.98, 0.97, 0.96]], np.float32)
+    st = dlm.new_status()
+    sel, n = dlm.cap_select(cuda(z), cuda(am), cuda(conf), cuda(lse[None]), cuda(np.ones((1, blk), np.uint8)),
+                            0.8, 0.95, -16.0, p_max, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dlm.DEV_NONFINITE
+    s = sel.cpu().numpy()[0]
+    assert s[0] == 1 and s[2] == 0 and s[1] == 1 and s[3] == 1   # only the 0-2 conflict removes a position
