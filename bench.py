@@ -55,6 +55,9 @@ def parse():
                     help="write a 512 MB buffer between timed steps (auto: when a step reads less than twice L2)")
     ap.add_argument("--serial-rules", action="store_true",
                     help="run threshold, boundary and CAP one after another (default: parallel graph branches)")
+    ap.add_argument("--rules-graph", action="store_true",
+                    help="launch the row pass eagerly each step and only the rules as a captured graph (default: "
+                         "whole steps captured as CUDA graphs, events inside the graph bracket every row pass)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the rules eagerly instead of replaying them as one captured CUDA graph")
     ap.add_argument("--extra-rules", default="",
@@ -279,7 +282,43 @@ def run_native(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    esz = 4 if cfg.logit_dtype == synth.F32 else 2
+    step_bytes = 2 * int(w.masked.sum()) * cfg.vocab * esz
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and step_bytes < 2 * l2)
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if flush else None
+    whole = rules_graph is not None and not args.rules_graph
+    # timing events; inside a captured graph they are external event nodes
+    ev_kw = dict(enable_timing=True, external=True) if whole else dict(enable_timing=True)
+    evs = [[torch.cuda.Event(**ev_kw) for _ in range(2)] for _ in range(args.steps)]
+    s_ev = [(torch.cuda.Event(**ev_kw), torch.cuda.Event(**ev_kw)) for _ in range(args.steps)] if flush else None
+
+    def timed_step(k):
+        if flush:
+            # each step timed on its own, with a 512 MB write before it (not timed)
+            scrub.fill_(k & 0xff)
+            s_ev[k][0].record(stream)
+        if whole:
+            plan.run(stream, events=evs[k])
+        else:
+            run_step(evs[k])
+        if flush:
+            s_ev[k][1].record(stream)
+
+    step_graphs = []
+    if whole:
+        # the timed steps, captured back to back (at most 250 per graph):
+        # every kernel of every step runs, with no host launch between them
+        for c0 in range(0, args.steps, 250):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for k in range(c0, min(args.steps, c0 + 250)):
+                    timed_step(k)
+            step_graphs.append(g)
+        torch.cuda.synchronize()
+        step_graphs[0].replay()  # upload / warm-up (untimed)
+        torch.cuda.synchronize()
+
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -293,28 +332,17 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    esz = 4 if cfg.logit_dtype == synth.F32 else 2
-    step_bytes = 2 * int(w.masked.sum()) * cfg.vocab * esz
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and step_bytes < 2 * l2)
-    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if flush else None
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     w0 = time.time()
-    if flush:
-        # each step timed on its own, with a 512 MB write before it (not timed)
-        s_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
-        for k in range(args.steps):
-            scrub.fill_(k & 0xff)
-            s_ev[k][0].record(stream)
-            run_step(evs[k])
-            s_ev[k][1].record(stream)
+    t0.record(stream)
+    if whole:
+        for g in step_graphs:
+            g.replay()
     else:
-        t0.record(stream)
         for k in range(args.steps):
-            run_step(evs[k])
-        t1.record(stream)
+            timed_step(k)
+    t1.record(stream)
     host_ms = (time.time() - w0) * 1000.0 / args.steps
     torch.cuda.synchronize()
     w1 = time.time()
@@ -322,6 +350,7 @@ def run_native(args, rank, world, local):
         torch.distributed.barrier()
     clocks = sampler.stop((w0, w1)) if sampler else None
     total_ms = sum(a.elapsed_time(b) for a, b in s_ev) if flush else t0.elapsed_time(t1)
+    del step_graphs
     k1 = [e[0].elapsed_time(e[1]) for e in evs]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
@@ -584,10 +613,14 @@ def main():
                            "from the step's start (" + ("after the row pass" if args.late_dapd_fork else
                                                           "it shares the row pass's last wave") +
                            "), DAPD selection after the row pass; threshold / boundary / CAP as " +
-                           ("one chain" if args.serial_rules else "parallel branches") +
-                           " of a captured CUDA graph (rules_graph = that graph alone)"),
+                           ("one chain" if args.serial_rules else "parallel branches") + "; " +
+                           ("eager launches" if args.no_graph else
+                            "row pass eager, the rules replayed as a captured CUDA graph" if args.rules_graph else
+                            "every timed step captured in CUDA graphs (250 steps per graph, the row-pass timing "
+                            "events are event nodes inside them)") +
+                           " (rules_graph = the rules alone, replayed as one graph)"),
         "host_enqueue_ms_per_step": r["host_ms"],
-        "rules_as_cuda_graph": not args.no_graph,
+        "cuda_graphs": "none" if args.no_graph else ("rules" if args.rules_graph else "whole steps"),
         "roofline": {"bound": "hbm", "achieved": k1_gbs, "peak": peak, "unit": "GB/s", "frac": k1_gbs / peak,
                      "traffic": recorded_traffic() if (cfg.batch == 64 and not args.compact_attn) else None, "kernel": "row_stats", "peak_kind": peak_kind,
                      "algorithmic_bytes": k1_bytes},
