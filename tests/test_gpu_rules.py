@@ -297,11 +297,14 @@ def test_boundary_ragged_windows(dlm, w_):
     assert gl[0] == 0
 
 
-def test_cap_edges(dlm):
+@pytest.mark.parametrize("blk,p_maxes", [(37, (8, 37, 65)), (100, (64, 65, 100))])
+def test_cap_edges(dlm, blk, p_maxes):
     """Pool clipping, an empty pool, scope limits, the unconditional tier and
-    a ragged block, on a tiny fp32 case."""
-    rng = np.random.default_rng(21)
-    B, blk, V = 4, 37, 300
+    a ragged block, on a tiny fp32 case; pools up to 64 take the fused
+    single-CTA kernel, larger ones the three-launch path, and the pool is
+    clipped on both sides of that line."""
+    rng = np.random.default_rng(21 + blk)
+    B, V = 4, 300
     z = (rng.standard_normal((B * blk, V)) * 1.0).astype(np.float32)
     tok = rng.integers(0, V, B * blk)
     for r in range(B * blk):
@@ -316,7 +319,7 @@ def test_cap_edges(dlm):
     scope = np.array([blk, blk, 11, 0], np.int32)
     am = o["argmax"].reshape(B, blk)
     c32, l32 = f32(o["conf"]).reshape(B, blk), f32(o["lse"]).reshape(B, blk)
-    for p_max, htu in [(8, False), (37, False), (37, True)]:
+    for p_max, htu in [(p_maxes[0], False), (p_maxes[1], False), (p_maxes[1], True), (p_maxes[2], True)]:
         st = dlm.new_status()
         gs, gn = dlm.cap_select(cuda(z), cuda(am), cuda(c32), cuda(l32), cuda(masked), 0.8, 0.95, -16.0, p_max,
                                 high_tier_unconditional=htu, scope_len=cuda(scope), status=st)
