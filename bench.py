@@ -67,6 +67,9 @@ def parse():
     ap.add_argument("--driver", action="store_true",
                     help="instead of the step benchmark: whole synthetic decodes per rule (steps/NFE, error rate, "
                          "decode time as one CUDA graph)")
+    ap.add_argument("--boost-mode", default="relative", choices=["relative", "absolute"],
+                    help="logit boost reading of the input recipe (absolute = literal: no confidence reaches the "
+                         "thresholds; the bytes are the same)")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
     ap.add_argument("--compact-attn", action="store_true",
                     help="hold only the attention block [B, L, H, blk, blk] on the device (small profiling cases)")
@@ -206,6 +209,16 @@ def job_throughput(decisions_per_rank_step: int, world: int, steps: int, max_ms:
 
 
 # ------------------------------------------------------------------ native
+def bench_config(args):
+    import synth
+    cfg = synth.CONFIGS[args.workload]
+    if args.batch:
+        cfg = synth.scaled(cfg, batch=args.batch)
+    if args.boost_mode != cfg.boost_mode:
+        cfg = synth.scaled(cfg, boost_mode=args.boost_mode)
+    return cfg
+
+
 def run_native(args, rank, world, local):
     import torch
 
@@ -214,9 +227,7 @@ def run_native(args, rank, world, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cfg = synth.CONFIGS[args.workload]
-    if args.batch:
-        cfg = synth.scaled(cfg, batch=args.batch)
+    cfg = bench_config(args)
     B, blk, V = cfg.batch, cfg.blk, cfg.vocab
     w = synth.make(cfg, seed=args.seed + 100 * rank)
     tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}
@@ -262,7 +273,7 @@ def run_native(args, rank, world, local):
     # the rules (everything after the row pass) as one CUDA graph; the row
     # pass stays an eager launch so CUDA events can bracket it every step
     rules_graph = None
-    if not args.no_graph:
+    if not args.no_graph and plan.has_rules_after_rows:
         rules_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(rules_graph, stream=stream):
             plan.run(rules_only=True)
@@ -287,7 +298,7 @@ def run_native(args, rank, world, local):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = args.flush_l2 == "on" or (args.flush_l2 == "auto" and step_bytes < 2 * l2)
     scrub = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if flush else None
-    whole = rules_graph is not None and not args.rules_graph
+    whole = not args.no_graph and not args.rules_graph
     # timing events; inside a captured graph they are external event nodes
     ev_kw = dict(enable_timing=True, external=True) if whole else dict(enable_timing=True)
     evs = [[torch.cuda.Event(**ev_kw) for _ in range(2)] for _ in range(args.steps)]
@@ -367,6 +378,65 @@ def run_native(args, rank, world, local):
     torch.cuda.synchronize()
     rules_ms = r0.elapsed_time(r1) / 100
 
+    def time_steps(p, n):
+        """ms per step of plan p: eager row pass + its rules as one graph, each
+        step alone after the scrub write when the inputs fit in L2."""
+        p.run(stream)
+        torch.cuda.synchronize()
+        g = None
+        if p.has_rules_after_rows:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                p.run(rules_only=True)
+            torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for k in range(n + 3):
+            if flush:
+                scrub.fill_(k & 0xff)
+            if k >= 3:
+                ev[k - 3][0].record(stream)
+            p.run_rows(stream)
+            if g is not None:
+                g.replay()
+            p.join(stream)
+            if k >= 3:
+                ev[k - 3][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / n
+
+    # each rule with the row pass, and the row pass alone (decisions/s per rule)
+    per_rule = {}
+    n_rule = max(20, min(300, args.steps))
+    for rules in [()] + [(r,) for r in plan.rules]:
+        kw = dict(common, rules=rules, concurrent_dapd=("dapd" in rules) and not args.serial_dapd)
+        p = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **kw)
+        ms = time_steps(p, n_rule)
+        per_rule["+".join(rules) or "row_pass_only"] = {"decisions_per_s": int(w.masked.sum()) * world / (ms / 1e3),
+                                                         "ms_per_step": ms}
+        del p
+
+    # the DAPD attention graph alone (K6): attention GB/s
+    attention = None
+    if "dapd" in plan.rules:
+        ws = dlm.dapd_workspace(B, blk, dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(100)]
+        for k in range(103):
+            if flush:
+                scrub.fill_(k & 0xff)
+            if k >= 3:
+                ev[k - 3][0].record(stream)
+            dlm.dapd_graph(attn, masked, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0, bs, workspace=ws,
+                           status=status)
+            if k >= 3:
+                ev[k - 3][1].record(stream)
+        torch.cuda.synchronize()
+        a_ms = sum(x.elapsed_time(y) for x, y in ev) / 100
+        asz = 4 if cfg.attn_dtype == synth.F32 else 2
+        # only the masked rows of the block are read: L * H * M * blk elements per sequence
+        a_bytes = cfg.n_layers * cfg.n_heads * int(w.masked.sum()) * blk * asz
+        attention = {"gbps": a_bytes / (a_ms / 1e3) / 1e9, "ms": a_ms, "algorithmic_bytes": a_bytes,
+                     "kernels": "dapd_accum + dapd_graph, alone on the GPU"}
+
     # --- end to end through host buffers (pinned), same public API
     e2e = None
     if args.e2e_steps > 0:
@@ -416,7 +486,8 @@ def run_native(args, rank, world, local):
                + (blen_h.numel() * 4 if plan2.block_len is not None else 0))
         e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
-    return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, clocks=clocks, e2e=e2e, host_ms=host_ms, flush=flush,
+    return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, per_rule=per_rule, attention=attention, clocks=clocks,
+                e2e=e2e, host_ms=host_ms, flush=flush,
                 cfg=cfg, launches=plan.n_launches * args.steps, w=w, decisions=int(w.masked.sum()),
                 rows=int(w.masked.sum()))
 
@@ -482,7 +553,7 @@ def run_reference(args, rank, world):
     import synth
     if rank != 0:
         return
-    cfg = synth.CONFIGS[args.workload]
+    cfg = bench_config(args)
     w = synth.make(cfg, seed=args.seed)
     import oracle
     oracle.build()
@@ -625,7 +696,11 @@ def main():
                      "traffic": recorded_traffic() if (cfg.batch == 64 and not args.compact_attn) else None, "kernel": "row_stats", "peak_kind": peak_kind,
                      "algorithmic_bytes": k1_bytes},
         "gpu_launches": r["launches"],
+        "per_rule": r["per_rule"],
     }
+    if r["attention"]:
+        a = r["attention"]
+        line["attention"] = dict(a, peak=peak, frac=a["gbps"] / peak, unit="GB/s")
     if r["clocks"]:
         line["clocks"] = r["clocks"]
     if r["e2e"]:

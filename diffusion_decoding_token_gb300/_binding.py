@@ -548,6 +548,12 @@ class StepPlan:
             self._ev_fork = torch.cuda.Event()
 
     @property
+    def has_rules_after_rows(self) -> bool:
+        """Whether ``run(rules_only=True)`` issues anything (with dapd_early
+        and DAPD as the only rule, everything belongs to run_rows)."""
+        return len(self._calls) > 1 or (self.side is not None and not self.dapd_early)
+
+    @property
     def n_launches(self) -> int:
         """Kernels launched per step: 1 row pass + 1 per threshold / boundary /
         top-K / factor rule, CAP 1 (pools of up to 64) or 3, DAPD 3 (attention

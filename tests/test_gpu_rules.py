@@ -34,9 +34,17 @@ def dlm():
 _CACHE = {}
 
 
+LITERAL = ["tiny:absolute", "llada_step:absolute"]
+
+
 def workload(name):
+    """A workload by name; "<name>:absolute" is the literal reading of the
+    logit boost (u added to the token's own value, so confidences stay below
+    every threshold and the rules run on their fallbacks)."""
     if name not in _CACHE:
-        w = synth.make(name, seed=1000 + synth.ORDER.index(name))
+        base, _, mode = name.partition(":")
+        cfg = synth.CONFIGS[base] if not mode else synth.scaled(synth.CONFIGS[base], boost_mode=mode)
+        w = synth.make(cfg, seed=1000 + synth.ORDER.index(base))
         _CACHE.clear()
         _CACHE[name] = (w, DeviceWorkload(w), oracle_stats(w))
     return _CACHE[name]
@@ -157,7 +165,7 @@ def test_unit_rules(dlm, name):
 
 
 # -------------------------------------------------------------- pipeline
-@pytest.mark.parametrize("name", synth.ORDER)
+@pytest.mark.parametrize("name", synth.ORDER + LITERAL)
 def test_pipeline(dlm, name):
     w, dw, o = workload(name)
     cfg = w.cfg
@@ -188,7 +196,7 @@ def test_pipeline(dlm, name):
                 exact += 1
             else:
                 valid += 1
-        if name == "depcap_window":
+        if name.startswith("depcap_window"):
             scope_g, scope_o = gl, ol
     if "cap" in cfg.rules:
         gs, _ = dlm.cap_select(dw.cur, g.argmax.view(B, blk), gconf, glse, dw.masked, cfg.tau_low, cfg.tau_high,
