@@ -556,10 +556,10 @@ class StepPlan:
     @property
     def n_launches(self) -> int:
         """Kernels launched per step: 1 row pass + 1 per threshold / boundary /
-        top-K / factor rule, CAP 1 (pools of up to 64) or 3, DAPD 3 (attention
-        sum, graph, selection)."""
-        per = {"threshold": 1, "boundary": 1, "cap": 1 if self._cap_pmax <= 64 else 3, "dapd": 3, "topk": 1,
-               "factor": 1}
+        top-K / factor rule, CAP 1 (pools of up to 64) or 3, DAPD 2 (attention
+        sum, graph + selection; blocks of up to 64) or 3."""
+        per = {"threshold": 1, "boundary": 1, "cap": 1 if self._cap_pmax <= 64 else 3,
+               "dapd": 2 if self.blk <= 64 else 3, "topk": 1, "factor": 1}
         return 1 + sum(per[r] for r in self.rules)
 
     def run_rows(self, stream=None, events=None):

@@ -320,7 +320,10 @@ dlm_status dlm_dapd_graph(const void* attn, dlm_dtype dtype, int32_t batch, int3
     a.dtilde_out = dtilde_out;
     a.deg_out = deg_out;
     a.dev_status = dev_status;
-    return from_cuda(dlm::launch_dapd_graph(a, sm_count(), reinterpret_cast<cudaStream_t>(stream)));
+    // the graph kernel runs when the selection will not build the graph itself
+    // or when its float outputs are asked for
+    const bool graph_kernel = !dlm::dapd_select_builds_graph(blk) || s_out || dtilde_out || deg_out;
+    return from_cuda(dlm::launch_dapd_graph(a, sm_count(), reinterpret_cast<cudaStream_t>(stream), graph_kernel));
 }
 
 dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t batch, int32_t blk,
@@ -334,6 +337,7 @@ dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t bat
     a.conf = conf;
     a.selected = selected;
     a.n_selected = n_selected;
+    a.thresh_from_ws = 1;
     return from_cuda(dlm::launch_dapd_select(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

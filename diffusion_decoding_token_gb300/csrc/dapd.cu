@@ -109,6 +109,10 @@ __device__ __forceinline__ void split_acc(const f2 (&x)[NP], f2 (&H)[NP], f2 (&L
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {  // for a later dlm_dapd_select
+        a.hdr[0] = a.edge_thresh;
+        a.hdr[1] = (long long)__float_as_int(a.s_scale);
+    }
     constexpr int EPV = AFmt<DT>::EPV;
     constexpr int ESZ = AFmt<DT>::ESZ;
     constexpr int NP = EPV / 2;
@@ -295,6 +299,10 @@ constexpr long long kWaitLimit = 2000000000LL;   // ~1 s at 2 GHz
 template <int DT>
 __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                   DapdArgs a) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {  // for a later dlm_dapd_select
+        a.hdr[0] = a.edge_thresh;
+        a.hdr[1] = (long long)__float_as_int(a.s_scale);
+    }
     constexpr int EPV = AFmt<DT>::EPV;
     constexpr int ESZ = AFmt<DT>::ESZ;
     constexpr int NP = EPV / 2;
@@ -440,18 +448,18 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
     }
 }
 
-__global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
-    const int b = blockIdx.y;
-    if (late_phase(a, b, nullptr)) return;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int i = blockIdx.x * (kThreads / 32) + warp;
-    if (i >= a.blk) return;
+// One warp builds node i's graph row from the fixed-point sums A of sequence
+// b: the symmetrised score against every masked j, the tau-edges as a
+// bitmask (words of 32 neighbours, kMaxWords per row) and the proxy degree D
+// (sum over masked j != i); optional float outputs.  adj_row / D_out may point
+// to global or shared memory.
+__device__ __forceinline__ void graph_row(const DapdArgs& a, int b, int i, long long thresh, float scale,
+                                          uint32_t* adj_row, long long* D_out) {
+    const int lane = threadIdx.x & 31;
     const uint8_t* mk = a.masked + (int64_t)b * a.blk;
-    if (!mk[i]) return;
     const long long* A = a.A + (int64_t)b * a.blk * a.blk;
     long long D = 0;
     int deg = 0;
-    uint32_t* adj = a.adj + ((int64_t)b * a.blk + i) * kMaxWords;
     const int nw = (a.blk + 31) >> 5;
     for (int c = 0; c < kMaxWords; ++c) {
         bool edge = false;
@@ -459,24 +467,35 @@ __global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
             const int j = c * 32 + lane;
             if (j < a.blk && mk[j]) {
                 const long long I = A[(int64_t)i * a.blk + j] + A[(int64_t)j * a.blk + i];
-                if (a.s_out) a.s_out[((int64_t)b * a.blk + i) * a.blk + j] = __ll2float_rn(I) * a.s_scale;
+                if (a.s_out) a.s_out[((int64_t)b * a.blk + i) * a.blk + j] = __ll2float_rn(I) * scale;
                 if (j != i) {
                     D += I;
-                    edge = I > a.edge_thresh;
+                    edge = I > thresh;
                     deg += edge;
                 }
             }
         }
         const uint32_t w = __ballot_sync(DLM_FULL_MASK, edge);
-        if (lane == 0) adj[c] = w;
+        if (lane == 0) adj_row[c] = w;
     }
     D = warp_sum_ll(D);
     deg = warp_sum_i(deg);
     if (lane == 0) {
-        a.Dsum[(int64_t)b * a.blk + i] = D;
-        if (a.dtilde_out) a.dtilde_out[(int64_t)b * a.blk + i] = __ll2float_rn(D) * a.s_scale;
+        *D_out = D;
+        if (a.dtilde_out) a.dtilde_out[(int64_t)b * a.blk + i] = __ll2float_rn(D) * scale;
         if (a.deg_out) a.deg_out[(int64_t)b * a.blk + i] = deg;
     }
+}
+
+__global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
+    const int b = blockIdx.y;
+    if (late_phase(a, b, nullptr)) return;
+    const int warp = threadIdx.x >> 5;
+    const int i = blockIdx.x * (kThreads / 32) + warp;
+    if (i >= a.blk) return;
+    if (!a.masked[(int64_t)b * a.blk + i]) return;
+    graph_row(a, b, i, a.edge_thresh, a.s_scale, a.adj + ((int64_t)b * a.blk + i) * kMaxWords,
+              a.Dsum + (int64_t)b * a.blk + i);
 }
 
 // Sortable exact key.  key = D * c (order_mode 0) or D (order_mode 1), with D
@@ -545,16 +564,18 @@ __device__ __forceinline__ bool key_before(unsigned long long ah, unsigned long 
     return ai < bi;
 }
 
-__global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
+// The selection of sequence b (DAPD, key designs 2-3) from its graph: proxy
+// degrees D_b[i] and adjacency rows adj_b[i * kMaxWords ..] (global or shared
+// memory).  Every thread of the CTA calls it.
+__device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late, int M, const long long* D_b,
+                                            const uint32_t* adj_b) {
     __shared__ unsigned long long s_kh[DLM_MAX_BLK], s_kl[DLM_MAX_BLK];
     __shared__ int s_ix[DLM_MAX_BLK];
     __shared__ uint32_t s_adj[DLM_MAX_BLK * kMaxWords];
     __shared__ uint32_t s_kept[kMaxWords];
     __shared__ float s_v[kThreads / 32];
     __shared__ int s_i[kThreads / 32];
-    const int b = blockIdx.x, t = threadIdx.x;
-    int M;
-    const bool late = late_phase(a, b, &M);
+    const int t = threadIdx.x;
     const int64_t o = (int64_t)b * a.blk + t;
     const bool m = t < a.blk && a.masked[o] != 0;
     uint8_t* sel = a.selected + (int64_t)b * a.blk;
@@ -592,7 +613,7 @@ __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
     while (n2 < a.blk) n2 <<= 1;
     if (t < n2) {
         if (m) {
-            const SortKey k = make_sort_key(a.Dsum[o], a.conf[o], a.order_mode);
+            const SortKey k = make_sort_key(D_b[t], a.conf[o], a.order_mode);
             s_kh[t] = k.hi;
             s_kl[t] = k.lo;
             s_ix[t] = t;
@@ -629,7 +650,7 @@ __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
     const int nw = (a.blk + 31) >> 5;
     for (int k = t; k < M * nw; k += blockDim.x) {
         const int r = k / nw, w = k - r * nw;
-        s_adj[r * kMaxWords + w] = a.adj[((int64_t)b * a.blk + s_ix[r]) * kMaxWords + w];
+        s_adj[r * kMaxWords + w] = adj_b[(int64_t)s_ix[r] * kMaxWords + w];
     }
     __syncthreads();
     if (t < 32) {
@@ -644,6 +665,37 @@ __global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
     }
     const int total = __syncthreads_count(mine);
     if (t == 0) a.n_selected[b] = total;
+}
+
+__global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
+    const int b = blockIdx.x;
+    int M;
+    const bool late = late_phase(a, b, &M);
+    select_core(a, b, late, M, a.Dsum + (int64_t)b * a.blk, a.adj + (int64_t)b * a.blk * kMaxWords);
+}
+
+// Blocks of up to kDecideMaxBlk positions: the graph (from the sums A left by
+// the attention pass) and the selection in one CTA per sequence, the graph
+// kept in shared memory.
+constexpr int kDecideMaxBlk = 64;
+
+__global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
+    __shared__ uint32_t s_gadj[kDecideMaxBlk * kMaxWords];
+    __shared__ long long s_D[kDecideMaxBlk];
+    const int b = blockIdx.x;
+    int M;
+    const bool late = late_phase(a, b, &M);
+    if (!late) {
+        // called after a separate attention pass (dlm_dapd_select), the edge
+        // threshold and score scale come from the workspace header it wrote
+        const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
+        const float scale = a.thresh_from_ws ? __int_as_float((int)a.hdr[1]) : a.s_scale;
+        const uint8_t* mk = a.masked + (int64_t)b * a.blk;
+        for (int i = threadIdx.x >> 5; i < a.blk; i += kThreads / 32)
+            if (mk[i]) graph_row(a, b, i, thresh, scale, s_gadj + i * kMaxWords, s_D + i);
+        __syncthreads();
+    }
+    select_core(a, b, late, M, s_D, s_gadj);
 }
 
 template <int DT>
@@ -777,8 +829,8 @@ cudaError_t launch_accum_tma(const DapdArgs& a, const CUtensorMap& map, cudaStre
 size_t dapd_workspace_bytes(int batch, int blk) {
     size_t A = ((size_t)batch * blk * blk * 8 + 255) & ~(size_t)255;
     size_t Ds = ((size_t)batch * blk * 8 + 255) & ~(size_t)255;
-    size_t adj = (size_t)batch * blk * kMaxWords * 4;
-    return A + Ds + adj;
+    size_t adj = ((size_t)batch * blk * kMaxWords * 4 + 255) & ~(size_t)255;
+    return A + Ds + adj + 256;  // + header: edge threshold and score scale
 }
 
 void dapd_carve(DapdArgs& a, void* ws) {
@@ -788,9 +840,13 @@ void dapd_carve(DapdArgs& a, void* ws) {
     a.Dsum = reinterpret_cast<long long*>(p);
     p += ((size_t)a.batch * a.blk * 8 + 255) & ~(size_t)255;
     a.adj = reinterpret_cast<uint32_t*>(p);
+    p += ((size_t)a.batch * a.blk * kMaxWords * 4 + 255) & ~(size_t)255;
+    a.hdr = reinterpret_cast<long long*>(p);
 }
 
-cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s) {
+bool dapd_select_builds_graph(int blk) { return blk <= kDecideMaxBlk; }
+
+cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel) {
     const int epv = a.dtype == DLM_F32 ? 4 : 8;
     const int vpr = (a.blk + epv - 1) / epv;
     a.row_tile = max(1, min(a.blk, kThreads / vpr));
@@ -814,6 +870,7 @@ cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s) {
     default: e = tma ? launch_accum_tma<DLM_F32>(a, map, s) : launch_accum<DLM_F32>(a, s); break;
     }
     if (e != cudaSuccess) return e;
+    if (!graph_kernel) return cudaSuccess;  // the selection builds the graph (dapd_decide_kernel)
     cudaLaunchConfig_t cfg = {};
     cfg.stream = s;
     cfg.gridDim = dim3((unsigned)((a.blk + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.batch);
@@ -826,11 +883,14 @@ cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s) {
     cfg.stream = s;
     cfg.gridDim = dim3((unsigned)a.batch);
     cfg.blockDim = dim3(kThreads);
+    if (a.blk <= kDecideMaxBlk) return cudaLaunchKernelEx(&cfg, dapd_decide_kernel, a);
     return cudaLaunchKernelEx(&cfg, dapd_select_kernel, a);
 }
 
 cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
-    cudaError_t e = launch_dapd_graph(a, num_sms, s);
+    // small blocks: attention pass + one graph-and-selection kernel (which also
+    // writes the float outputs); larger ones: attention pass, graph, selection
+    cudaError_t e = launch_dapd_graph(a, num_sms, s, !dapd_select_builds_graph(a.blk));
     if (e != cudaSuccess) return e;
     return launch_dapd_select(a, s);
 }

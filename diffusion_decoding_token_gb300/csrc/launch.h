@@ -143,6 +143,8 @@ struct DapdArgs {
     long long* A;      // [batch][blk][blk] fixed-point sums (units 2^-32)
     long long* Dsum;   // [batch][blk]
     uint32_t* adj;     // [batch][blk][8]
+    long long* hdr;    // [2]: edge threshold, score scale bits (written by the attention pass)
+    int thresh_from_ws;  // the selection reads them from hdr (no attention arguments)
     int split;         // CTAs per cluster over the layer*head range
     int row_tile;      // rows per CTA
     // bulk-tensor (TMA) path: box = [box_cols x row_tile rows x box_heads]
@@ -150,8 +152,11 @@ struct DapdArgs {
 };
 size_t dapd_workspace_bytes(int batch, int blk);
 void dapd_carve(DapdArgs& a, void* ws);
-cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);         // graph + select
-cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s);   // attention -> graph
-cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s);         // graph + conf -> selection
+cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);  // attention -> selection
+// attention -> sums, and the graph when graph_kernel (always needed when the
+// selection does not build it itself, see dapd_select_builds_graph)
+cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel);
+bool dapd_select_builds_graph(int blk);
+cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s);  // (graph +) conf -> selection
 
 }  // namespace dlm
