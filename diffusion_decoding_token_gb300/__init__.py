@@ -39,6 +39,9 @@ from ._binding import (  # noqa: F401
     parallel_certificate,
     revocable_state,
     revocable_step,
+    row_stats_partial,
+    row_stats_merge,
+    allgather_row_partials,
 )
 from .driver import SyntheticDecoder  # noqa: F401
 

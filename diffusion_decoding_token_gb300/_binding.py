@@ -75,6 +75,8 @@ def lib():
         L.dlm_dapd_graph_mis.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
         L.dlm_depcap_boundary_ragged.argtypes = [P, P, I32, I32, P, P, ctypes.POINTER(DepcapParams), P, P, P]
+        L.dlm_row_stats_partial.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, I64, P, P]
+        L.dlm_row_stats_merge.argtypes = [P, I32, I64, I64, P, I32, P, P, P, P, P, P, P, P]
         L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
         L.dlm_revocable_step.argtypes = [P, P, P, P, I32, I32, I32, ctypes.POINTER(RevocableParams), P, P, P, P, P,
                                          P, P, P, P, P, P]
@@ -164,6 +166,63 @@ def row_stats(cur: torch.Tensor, prev: torch.Tensor | None = None, *, row_index:
                                _p(out.kl) if prev is not None else None,
                                _p(out.lse_prev) if prev is not None else None, _p(status),
                                _stream(cur.device)))
+    return out
+
+
+PARTIAL_FLOATS = 8  # dlm_row_partial: 8 four-byte fields
+
+
+def row_stats_partial(cur: torch.Tensor, prev: torch.Tensor | None = None, *, vocab_offset: int = 0,
+                      row_index: torch.Tensor | None = None, out: torch.Tensor | None = None) -> torch.Tensor:
+    """dlm_row_stats_partial over a vocabulary slice ``cur`` ([rows, V_slice],
+    unit column stride; the slice starts at global position ``vocab_offset``).
+    Returns the 32-byte states as a float32 [rows, 8] tensor (opaque)."""
+    _need_cuda(cur, prev, row_index)
+    if cur.dim() != 2 or cur.stride(1) != 1:
+        raise ValueError("cur must be [rows, V] with contiguous rows")
+    if prev is not None and (prev.shape != cur.shape or prev.stride() != cur.stride() or prev.dtype != cur.dtype):
+        raise ValueError("prev must match cur in shape, strides and dtype")
+    rows, V = cur.shape
+    if out is None:
+        out = torch.empty((rows, PARTIAL_FLOATS), dtype=torch.float32, device=cur.device)
+    n = rows
+    if row_index is not None:
+        row_index = row_index.to(torch.int32).contiguous()
+        n = row_index.numel()
+    _check(lib().dlm_row_stats_partial(_p(cur), _p(prev), _dt(cur), n, V, cur.stride(0), _p(row_index),
+                                       int(vocab_offset), _p(out), _stream(cur.device)))
+    return out
+
+
+def row_stats_merge(partials: torch.Tensor, has_prev: bool, *, row_index: torch.Tensor | None = None,
+                    out: RowStats | None = None, status: torch.Tensor | None = None) -> RowStats:
+    """dlm_row_stats_merge of [n_shards, rows, 8] partial states (slices in
+    vocabulary order) into the whole rows' statistics."""
+    _need_cuda(partials, row_index)
+    if partials.dim() != 3 or partials.shape[2] != PARTIAL_FLOATS or not partials.is_contiguous():
+        raise ValueError("partials must be a contiguous [n_shards, rows, 8] tensor")
+    n_shards, rows, _ = partials.shape
+    if out is None:
+        out = alloc_row_stats(rows, partials.device, has_prev)
+    n = rows
+    if row_index is not None:
+        row_index = row_index.to(torch.int32).contiguous()
+        n = row_index.numel()
+    _check(lib().dlm_row_stats_merge(_p(partials), n_shards, rows, n, _p(row_index), int(bool(has_prev)),
+                                     _p(out.argmax), _p(out.conf), _p(out.lse), _p(out.entropy),
+                                     _p(out.kl) if has_prev else None, _p(out.lse_prev) if has_prev else None,
+                                     _p(status), _stream(partials.device)))
+    return out
+
+
+def allgather_row_partials(partial: torch.Tensor, group=None) -> torch.Tensor:
+    """The exchange of a vocabulary-sharded row pass: every rank's [rows, 8]
+    partial states gathered into [world, rows, 8] in rank order (rank r holds
+    vocabulary slice r), ready for :func:`row_stats_merge`."""
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    out = torch.empty((world,) + tuple(partial.shape), dtype=partial.dtype, device=partial.device)
+    dist.all_gather(list(out.unbind(0)), partial.contiguous(), group=group)
     return out
 
 

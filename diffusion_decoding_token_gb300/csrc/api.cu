@@ -51,14 +51,13 @@ const char* dlm_status_string(dlm_status s) {
 
 int dlm_version(void) { return 100; }
 
-dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
-                         int64_t vocab, int64_t row_stride, const int32_t* row_index,
-                         int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
-                         float* lse_prev, uint32_t* dev_status, dlm_stream_t stream) {
+// Validation and launch shape shared by the whole-row and the slice calls.
+static dlm_status row_stats_prepare(dlm::RowStatsArgs& a, const void* cur, const void* prev, dlm_dtype dtype,
+                                    int64_t n_rows, int64_t vocab, int64_t row_stride, const int32_t* row_index) {
     if (!dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
     if (n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL || row_stride < vocab) return DLM_ERR_INVALID_ARG;
     if (n_rows == 0) return DLM_OK;
-    if (!cur || !argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    if (!cur) return DLM_ERR_INVALID_ARG;
     const int esz = dtype_size(dtype);
     if (!aligned16(cur) || (prev && !aligned16(prev)) || (row_stride * esz) % 16 != 0) return DLM_ERR_ALIGNMENT;
     const int epv = dlm::row_stats_elems_per_vector(dtype);
@@ -70,12 +69,58 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
     int split = 1;
     while (split < 8 && n_rows * split < target && nvec / (split * 2) >= 2LL * threads) split *= 2;
     if (n_rows * split > 0x7fffffffLL) return DLM_ERR_INVALID_ARG;
-    dlm::RowStatsArgs a;
+    a = dlm::RowStatsArgs{};
     a.cur = cur;
     a.prev = prev;
     a.n_rows = n_rows;
     a.vocab = vocab;
     a.row_stride = row_stride;
+    a.row_index = row_index;
+    a.split = split;
+    return DLM_OK;
+}
+
+dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
+                         int64_t vocab, int64_t row_stride, const int32_t* row_index,
+                         int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
+                         float* lse_prev, uint32_t* dev_status, dlm_stream_t stream) {
+    dlm::RowStatsArgs a{};
+    const dlm_status st = row_stats_prepare(a, cur, prev, dtype, n_rows, vocab, row_stride, row_index);
+    if (st != DLM_OK || n_rows == 0) return st;
+    if (!argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    a.argmax = argmax;
+    a.conf = conf;
+    a.lse = lse;
+    a.entropy = entropy;
+    a.kl = kl;
+    a.lse_prev = lse_prev;
+    a.dev_status = dev_status;
+    return from_cuda(dlm::launch_row_stats(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_row_stats_partial(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
+                                 int64_t vocab, int64_t row_stride, const int32_t* row_index,
+                                 int64_t vocab_offset, dlm_row_partial* partial, dlm_stream_t stream) {
+    dlm::RowStatsArgs a{};
+    const dlm_status st = row_stats_prepare(a, cur, prev, dtype, n_rows, vocab, row_stride, row_index);
+    if (st != DLM_OK || n_rows == 0) return st;
+    if (!partial || vocab_offset < 0 || vocab_offset + vocab > 0x7fffffffLL) return DLM_ERR_INVALID_ARG;
+    a.partial = partial;
+    a.vocab_offset = vocab_offset;
+    return from_cuda(dlm::launch_row_stats(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dlm_status dlm_row_stats_merge(const dlm_row_partial* partials, int32_t n_shards, int64_t shard_stride,
+                               int64_t n_rows, const int32_t* row_index, int32_t has_prev, int32_t* argmax,
+                               float* conf, float* lse, float* entropy, float* kl, float* lse_prev,
+                               uint32_t* dev_status, dlm_stream_t stream) {
+    if (n_shards < 1 || n_rows < 0 || shard_stride < 0 || (n_shards > 1 && shard_stride < 1) ||
+        (has_prev != 0 && has_prev != 1))
+        return DLM_ERR_INVALID_ARG;
+    if (n_rows == 0) return DLM_OK;
+    if (!partials || !argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    dlm::RowStatsArgs a{};
+    a.n_rows = n_rows;
     a.row_index = row_index;
     a.argmax = argmax;
     a.conf = conf;
@@ -84,8 +129,8 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
     a.kl = kl;
     a.lse_prev = lse_prev;
     a.dev_status = dev_status;
-    a.split = split;
-    return from_cuda(dlm::launch_row_stats(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+    return from_cuda(dlm::launch_row_merge(a, partials, n_shards, shard_stride, has_prev != 0,
+                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dlm_status dlm_select_threshold(const float* conf, const uint8_t* masked, int32_t batch,

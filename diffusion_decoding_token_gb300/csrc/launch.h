@@ -22,8 +22,13 @@ struct RowStatsArgs {
     float* lse_prev;
     uint32_t* dev_status;
     int split;  // CTAs per row (thread-block cluster size), 1..8
+    void* partial;         // non-null: write each row's dlm_row_partial state instead of outputs
+    int64_t vocab_offset;  // global position of the slice's first element
 };
 cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s);
+// merge of dlm_row_partial states: a gives n_rows, row_index and the outputs
+cudaError_t launch_row_merge(const RowStatsArgs& a, const void* partials, int n_shards, int64_t shard_stride,
+                             bool prev, cudaStream_t s);
 int row_stats_elems_per_vector(int dtype);
 int row_stats_threads();
 

@@ -27,6 +27,8 @@
 //   KL = K/S - (r - r') - (ln S - ln S').
 #include <cooperative_groups.h>
 
+#include <cstddef>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -61,6 +63,13 @@ struct Part {
     float S, T, K;
     float refp, Sp;
 };
+
+static_assert(sizeof(Part) == sizeof(dlm_row_partial), "Part mirrors dlm_row_partial");
+static_assert(offsetof(Part, idx) == offsetof(dlm_row_partial, idx) &&
+                  offsetof(Part, S) == offsetof(dlm_row_partial, S) &&
+                  offsetof(Part, refp) == offsetof(dlm_row_partial, ref_prev) &&
+                  offsetof(Part, Sp) == offsetof(dlm_row_partial, S_prev),
+              "Part mirrors dlm_row_partial");
 
 __device__ __forceinline__ void part_empty(Part& p) {
     p.mx = -INFINITY;
@@ -282,6 +291,26 @@ __device__ __forceinline__ void process_scalar(Acc& a, float z, float zp, int po
     }
 }
 
+// The outputs of a row from its merged state (one thread).
+template <bool PREV>
+__device__ __forceinline__ void write_outputs(const RowStatsArgs& args, const Part& p, int64_t q) {
+    const float lnS = logf(p.S);
+    const float lse = p.ref + lnS;
+    // a row of NaN only has no maximum: position 0 (the status flags the row)
+    args.argmax[q] = p.idx != 0x7fffffff ? p.idx : 0;
+    args.lse[q] = lse;
+    args.conf[q] = expf((p.mx - p.ref) - lnS);
+    args.entropy[q] = lnS - kLn2 * (p.T / p.S);
+    bool ok = isfinite(p.S) && p.S > 0.f && isfinite(p.T) && isfinite(p.mx) && p.mx > kDegenerate;
+    if (PREV) {
+        const float lnSp = logf(p.Sp);
+        if (args.kl) args.kl[q] = p.K / p.S - (p.ref - p.refp) - (lnS - lnSp);
+        if (args.lse_prev) args.lse_prev[q] = p.refp + lnSp;
+        ok = ok && isfinite(p.Sp) && p.Sp > 0.f && isfinite(p.K);
+    }
+    if (!ok) raise_status(args.dev_status, DLM_DEV_NONFINITE);
+}
+
 template <int DT, bool PREV>
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) {
     constexpr int EPV = Fmt<DT>::EPV;
@@ -391,22 +420,25 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) 
         cluster.sync();
     }
     if (rank != 0 || threadIdx.x != 0) return;
-
-    const float lnS = logf(p.S);
-    const float lse = p.ref + lnS;
-    // a row of NaN only has no maximum: position 0 (the status flags the row)
-    args.argmax[q] = (int64_t)p.idx < args.vocab ? p.idx : 0;
-    args.lse[q] = lse;
-    args.conf[q] = expf((p.mx - p.ref) - lnS);
-    args.entropy[q] = lnS - kLn2 * (p.T / p.S);
-    bool ok = isfinite(p.S) && p.S > 0.f && isfinite(p.T) && isfinite(p.mx) && p.mx > kDegenerate;
-    if (PREV) {
-        const float lnSp = logf(p.Sp);
-        if (args.kl) args.kl[q] = p.K / p.S - (p.ref - p.refp) - (lnS - lnSp);
-        if (args.lse_prev) args.lse_prev[q] = p.refp + lnSp;
-        ok = ok && isfinite(p.Sp) && p.Sp > 0.f && isfinite(p.K);
+    if (args.partial) {  // a slice of the row: its state, positions made global
+        if (p.idx != 0x7fffffff) p.idx += (int)args.vocab_offset;
+        static_cast<Part*>(args.partial)[q] = p;
+        return;
     }
-    if (!ok) raise_status(args.dev_status, DLM_DEV_NONFINITE);
+    write_outputs<PREV>(args, p, q);
+}
+
+// Merge the partial states of n_shards slices of each row (slice order fixed)
+// and write the row's outputs.  One thread per row.
+template <bool PREV>
+__global__ void __launch_bounds__(256) row_merge_kernel(RowStatsArgs args, const Part* parts, int n_shards,
+                                                        int64_t shard_stride) {
+    const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= args.n_rows) return;
+    const int64_t q = args.row_index ? (int64_t)args.row_index[r] : r;
+    Part p = parts[q];
+    for (int sh = 1; sh < n_shards; ++sh) part_merge(p, parts[(int64_t)sh * shard_stride + q]);
+    write_outputs<PREV>(args, p, q);
 }
 
 template <int DT, bool PREV>
@@ -431,6 +463,17 @@ cudaError_t launch_typed(const RowStatsArgs& a, cudaStream_t s) {
 }  // namespace
 
 int row_stats_elems_per_vector(int dtype) { return dtype == DLM_F32 ? 4 : 8; }
+
+cudaError_t launch_row_merge(const RowStatsArgs& a, const void* partials, int n_shards, int64_t shard_stride,
+                             bool prev, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((a.n_rows + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    const Part* parts = static_cast<const Part*>(partials);
+    return prev ? cudaLaunchKernelEx(&cfg, row_merge_kernel<true>, a, parts, n_shards, shard_stride)
+                : cudaLaunchKernelEx(&cfg, row_merge_kernel<false>, a, parts, n_shards, shard_stride);
+}
 
 cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s) {
     const bool prev = a.prev != nullptr;

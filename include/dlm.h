@@ -104,6 +104,42 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
                          float* lse_prev, uint32_t* dev_status, dlm_stream_t stream);
 
 /*
+ * dlm_row_stats_partial / dlm_row_stats_merge -- dlm_row_stats over a row
+ * whose vocabulary is split into slices (e.g. the vocab shards of a
+ * tensor-parallel model, one per GPU).
+ *
+ * dlm_row_stats_partial reads one slice of every row -- element (q, v) at
+ * cur + q*row_stride + v for 0 <= v < vocab, global position vocab_offset + v
+ * -- and writes its partial state to partial[q].  dlm_row_stats_merge merges
+ * the partial states of n_shards slices of the same rows (slice s of row q at
+ * partials[s*shard_stride + q], merged in slice order) and writes exactly the
+ * outputs dlm_row_stats writes for the whole row, with the same definitions
+ * (argmax: smallest global position of the maximum).  Exchanging the 32-byte
+ * states (an all-gather over the shards) is the only communication the split
+ * needs.  Alignment, row_index and dtype rules are those of dlm_row_stats (the
+ * slice's first element must be 16-byte aligned); a slice without a finite
+ * maximum is allowed (it contributes nothing), and the merge raises
+ * DLM_DEV_NONFINITE as dlm_row_stats does.  has_prev in the merge says whether
+ * the partial states were computed with prev (kl / lse_prev outputs).
+ */
+typedef struct dlm_row_partial {
+    float mx;                /* maximum of the slice's logits (-inf clamped) */
+    int32_t idx;             /* first global position of mx */
+    float ref;               /* softmax reference of the sums below */
+    float S, T, K;           /* sum 2^a, sum 2^a a, sum 2^a (z - z'); a = (z - ref) log2 e */
+    float ref_prev, S_prev;  /* the previous row's reference and sum */
+} dlm_row_partial;
+
+dlm_status dlm_row_stats_partial(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
+                                 int64_t vocab, int64_t row_stride, const int32_t* row_index,
+                                 int64_t vocab_offset, dlm_row_partial* partial, dlm_stream_t stream);
+
+dlm_status dlm_row_stats_merge(const dlm_row_partial* partials, int32_t n_shards, int64_t shard_stride,
+                               int64_t n_rows, const int32_t* row_index, int32_t has_prev, int32_t* argmax,
+                               float* conf, float* lse, float* entropy, float* kl, float* lse_prev,
+                               uint32_t* dev_status, dlm_stream_t stream);
+
+/*
  * dlm_select_threshold -- Fast-dLLM confidence-threshold decoding.
  *
  * Fast-dLLM review, "Method"; Fast-dLLM notes, "Key ideas" (safety valve):

@@ -136,3 +136,56 @@ def test_all_nan_row_argmax_in_range(dlm):
     torch.cuda.synchronize()
     assert int(st.item()) & dlm.DEV_NONFINITE
     assert int(g.argmax[0]) == 0 and int(g.argmax[1]) == 1234
+
+
+@pytest.mark.parametrize("name,cuts", [("llada_step", (0, 40000, 90000)), ("tiny", (0, 512)),
+                                       ("stress_bulk", (0, 8, 63232, 100000))])
+def test_vocab_split_partials_merge_to_whole_rows(dlm, name, cuts):
+    """Each vocabulary slice's partial states, merged in slice order, give the
+    whole rows' statistics (against the oracle on whole rows); argmax is a
+    global position."""
+    cfg = synth.CONFIGS[name]
+    w = synth.make(cfg, seed=77)
+    code = cfg.logit_dtype
+    cur = to_torch(w.cur, code, "cuda")
+    prev = to_torch(w.prev, code, "cuda")
+    V = cfg.vocab
+    bounds = list(cuts) + [V]
+    parts = torch.stack([dlm.row_stats_partial(cur[:, a:b], prev[:, a:b], vocab_offset=a)
+                         for a, b in zip(bounds[:-1], bounds[1:])]).contiguous()
+    st = dlm.new_status()
+    g = dlm.row_stats_merge(parts, True, status=st)
+    o = oracle.row_stats(w.cur, w.prev, dtype=None if code == synth.F32 else code)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _compare(g, o, np.arange(w.cur.shape[0]), with_prev=True)
+    # without prev rows, and with a row index
+    ri = torch.tensor([3, 0, 7], dtype=torch.int32, device="cuda")
+    parts = torch.stack([dlm.row_stats_partial(cur[:, a:b], vocab_offset=a, row_index=ri,
+                                               out=torch.zeros((cur.shape[0], 8), device="cuda"))
+                         for a, b in zip(bounds[:-1], bounds[1:])]).contiguous()
+    g2 = dlm.row_stats_merge(parts, False, row_index=ri)
+    torch.cuda.synchronize()
+    o2 = oracle.row_stats(w.cur[[3, 0, 7]], dtype=None if code == synth.F32 else code)
+    for k in ("argmax", "conf", "lse", "entropy"):
+        gv = getattr(g2, k).cpu().numpy()[[3, 0, 7]]
+        if k == "argmax":
+            np.testing.assert_array_equal(gv, o2[k])
+        else:
+            assert np.all(np.abs(gv - o2[k]) <= 1e-4 + 1e-4 * np.abs(o2[k])), k
+
+
+def test_vocab_split_with_empty_and_nan_slices(dlm):
+    # a slice of -inf only contributes nothing; a NaN slice flags the row
+    x = np.random.default_rng(5).standard_normal((3, 96)).astype(np.float32)
+    x[0, 32:64] = -np.inf
+    x[1, 64:] = np.nan
+    t = to_torch(x, synth.F32, "cuda")
+    parts = torch.stack([dlm.row_stats_partial(t[:, a:a + 32], vocab_offset=a) for a in (0, 32, 64)]).contiguous()
+    st = dlm.new_status()
+    g = dlm.row_stats_merge(parts, False, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & dlm.DEV_NONFINITE
+    o = oracle.row_stats(x[[0, 2]])
+    np.testing.assert_array_equal(g.argmax.cpu().numpy()[[0, 2]], o["argmax"])
+    assert np.all(np.abs(g.lse.cpu().numpy()[[0, 2]] - o["lse"]) <= 1e-4 + 1e-4 * np.abs(o["lse"]))
