@@ -6,23 +6,26 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "launch.h"
 
 namespace {
 
 constexpr int kMaxDevices = 64;
-int g_sm_count[kMaxDevices] = {0};
+std::atomic<int> g_sm_count[kMaxDevices];  // 0 = not read yet (static storage starts zeroed)
 
 int sm_count() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 152;
-    if (dev >= kMaxDevices) dev = kMaxDevices - 1;
-    if (g_sm_count[dev] <= 0) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
-        g_sm_count[dev] = n;
+    if (dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) return cached;
     }
-    return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -792,11 +792,12 @@ cudaError_t tma_smem_attribute() {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < kMaxDev && !smem_set[dev]) {
+    const bool cached = dev >= 0 && dev < kMaxDev;
+    if (!cached || !smem_set[dev]) {  // devices past the table are set on every call
         e = cudaFuncSetAttribute(dapd_accum_tma_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)(kStages * kBoxBytes + 16384));
         if (e != cudaSuccess) return e;
-        smem_set[dev] = true;
+        if (cached) smem_set[dev] = true;
     }
     return cudaSuccess;
 }
