@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kConflictWarps = 8;
+constexpr int kMaxPoolWords = DLM_MAX_BLK / 32;  // p_max <= 256
 
 __device__ __forceinline__ float load_logit(const void* base, int dtype, int64_t i) {
     if (dtype == DLM_BF16) return __uint_as_float((uint32_t) static_cast<const uint16_t*>(base)[i] << 16);
@@ -85,18 +86,25 @@ __global__ void __launch_bounds__(kConflictWarps * 32) cap_conflict_kernel(CapAr
     const float li = a.lse[ri];
     uint32_t* adj = a.adj + ((int64_t)b * a.p_max + slot) * a.words;
     const int nw = (n + 31) >> 5;
-    for (int c = 0; c < nw; ++c) {
+    // every partner's scattered loads are issued before any is used (one
+    // round trip for the row instead of one per 32 partners)
+    float g[kMaxPoolWords];
+#pragma unroll
+    for (int c = 0; c < kMaxPoolWords; ++c) {
         const int e = c * 32 + lane;
-        bool conflict = false;
-        if (e < n && e != slot) {
+        g[c] = __int_as_float(0x7fc00000);
+        if (c < nw && e < n && e != slot) {
             const int pj = pool[e];
             const int64_t rj = (int64_t)b * a.blk + pj;
-            const float g1 = logp_at(a, ri, a.argmax[rj], li);
-            const float g2 = logp_at(a, rj, yi, a.lse[rj]);
-            const float d = g1 + g2;
-            conflict = d > a.gamma;
-            if (a.D_out) a.D_out[((int64_t)b * a.blk + pi) * a.blk + pj] = d;
+            g[c] = logp_at(a, ri, a.argmax[rj], li) + logp_at(a, rj, yi, a.lse[rj]);
         }
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxPoolWords; ++c) {
+        if (c >= nw) break;
+        const int e = c * 32 + lane;
+        const bool conflict = g[c] > a.gamma;  // NaN (no partner) is never a conflict
+        if (a.D_out && e < n && e != slot) a.D_out[((int64_t)b * a.blk + pi) * a.blk + pool[e]] = g[c];
         const uint32_t word = __ballot_sync(DLM_FULL_MASK, conflict);
         if (lane == 0) adj[c] = word;
     }

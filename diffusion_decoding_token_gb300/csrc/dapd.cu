@@ -461,18 +461,27 @@ __device__ __forceinline__ void graph_row(const DapdArgs& a, int b, int i, long 
     long long D = 0;
     int deg = 0;
     const int nw = (a.blk + 31) >> 5;
+    // all of the row's loads first (one round trip), then the decisions
+    long long Iv[kMaxWords];
+    bool in[kMaxWords];
+#pragma unroll
     for (int c = 0; c < kMaxWords; ++c) {
+        const int j = c * 32 + lane;
+        in[c] = c < nw && j < a.blk && mk[j];
+        Iv[c] = in[c] ? A[(int64_t)i * a.blk + j] + A[(int64_t)j * a.blk + i] : 0;
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxWords; ++c) {
+        if (c >= nw) break;
+        const int j = c * 32 + lane;
         bool edge = false;
-        if (c < nw) {
-            const int j = c * 32 + lane;
-            if (j < a.blk && mk[j]) {
-                const long long I = A[(int64_t)i * a.blk + j] + A[(int64_t)j * a.blk + i];
-                if (a.s_out) a.s_out[((int64_t)b * a.blk + i) * a.blk + j] = __ll2float_rn(I) * scale;
-                if (j != i) {
-                    D += I;
-                    edge = I > thresh;
-                    deg += edge;
-                }
+        if (in[c]) {
+            const long long I = Iv[c];
+            if (a.s_out) a.s_out[((int64_t)b * a.blk + i) * a.blk + j] = __ll2float_rn(I) * scale;
+            if (j != i) {
+                D += I;
+                edge = I > thresh;
+                deg += edge;
             }
         }
         const uint32_t w = __ballot_sync(DLM_FULL_MASK, edge);
