@@ -528,7 +528,6 @@ class StepPlan:
             self._calls.append((L.dlm_depcap_boundary, (_p(st.kl), _p(st.entropy), B, blk, None,
                                                          ctypes.byref(self._dep), _p(self.block_len),
                                                          _p(self.score))))
-        self._cap_pmax = blk if p_max is None else int(p_max)
         if "cap" in rules:
             p_max = blk if p_max is None else int(p_max)
             s, n = torch.zeros((B, blk), **u8), torch.zeros(B, **i32)
@@ -615,10 +614,10 @@ class StepPlan:
     @property
     def n_launches(self) -> int:
         """Kernels launched per step: 1 row pass + 1 per threshold / boundary /
-        top-K / factor rule, CAP 1 (pools of up to 64) or 3, DAPD 2 (attention
-        sum, graph + selection; blocks of up to 64) or 3."""
-        per = {"threshold": 1, "boundary": 1, "cap": 1 if self._cap_pmax <= 64 else 3,
-               "dapd": 2 if self.blk <= 64 else 3, "topk": 1, "factor": 1}
+        top-K / factor / CAP rule, DAPD 2 (attention sum, graph + selection;
+        blocks of up to 64) or 3."""
+        per = {"threshold": 1, "boundary": 1, "cap": 1, "dapd": 2 if self.blk <= 64 else 3, "topk": 1,
+               "factor": 1}
         return 1 + sum(per[r] for r in self.rules)
 
     def run_rows(self, stream=None, events=None):

@@ -2,19 +2,23 @@
 // greedy conflict-free selection (DepCap, "Methodology"; defaults in
 // "Experiments").
 //
-// Pools of up to 64 candidates: one fused launch (cap_fused_kernel below).
-// Larger pools: three launches on the caller's stream:
-//   cap_pool     one CTA per sequence: candidates (masked, conf >= tau_low)
-//                ranked by (conf desc, position asc) with an all-pairs rank
-//                count, clipped to p_max;
-//   cap_conflict one warp per pool row: D_ij = log p_i(yhat_j) + log p_j(yhat_i)
-//                from two scattered logit reads per pair, conflict bits packed
-//                with a warp ballot (one 32-bit word per 32 partners);
-//   cap_greedy   one CTA per sequence: the greedy scan over the pool order on
-//                the shared-memory bitmask, or the top-confidence fallback.
-// The pool order and the two bitmask passes live in the caller's workspace.
+// One launch per call:
+//   pools of up to 64 candidates: cap_fused_kernel, one CTA per sequence;
+//   larger pools: cap_cluster_kernel, a thread-block cluster per sequence.
+// Both rank the candidates (masked, conf >= tau_low) by (conf desc, position
+// asc) with an all-pairs count, clip to p_max, score every unordered pool
+// pair once (D_ij = log p_i(yhat_j) + log p_j(yhat_i), two scattered logit
+// reads), keep the conflict bits in shared memory and run the greedy scan
+// over the pool order, or the top-confidence fallback on an empty pool.  The
+// caller's workspace is validated but not used by these kernels (their
+// scratch is shared memory); it stays in the interface as the scratch of any
+// later variant that needs global memory.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch.h"
+
+namespace cg = cooperative_groups;
 
 namespace dlm {
 
@@ -41,132 +45,23 @@ __device__ __forceinline__ float logp_at(const CapArgs& a, int64_t row, int toke
     return load_logit(a.logits, a.dtype, row * a.row_stride + token) - lse;
 }
 
+// The q-th unordered pair (i < j) of n items in row-major order (row i holds
+// (i, i+1) .. (i, n-1)), in closed form: counted from the end, k = T-1-q falls
+// in the block of the last r+1 rows with r(r+1)/2 <= k < (r+1)(r+2)/2.
+__device__ __forceinline__ void pair_of(int q, int n, int& i, int& j) {
+    const int T = n * (n - 1) / 2;
+    const int k = T - 1 - q;
+    int r = (int)((sqrtf(8.0f * (float)k + 1.0f) - 1.0f) * 0.5f);
+    while ((r + 1) * (r + 2) / 2 <= k) ++r;  // correct a rounding of the root
+    while (r * (r + 1) / 2 > k) --r;
+    i = n - 2 - r;
+    j = n - 1 - (k - r * (r + 1) / 2);
+}
+
 __device__ __forceinline__ int scope_of(const CapArgs& a, int b) {
     int sc = a.blk;
     if (a.scope_len) sc = min(sc, max(0, a.scope_len[b]));
     return sc;
-}
-
-__global__ void __launch_bounds__(kThreads) cap_pool_kernel(CapArgs a) {
-    __shared__ float s_c[kThreads];
-    __shared__ int s_cand[kThreads];
-    const int b = blockIdx.x, i = threadIdx.x;
-    const int scope = scope_of(a, b);
-    const int64_t o = (int64_t)b * a.blk + i;
-    const bool cand = i < scope && a.masked[o] != 0 && a.conf[o] >= a.tau_low;
-    s_c[i] = cand ? a.conf[o] : 0.f;
-    s_cand[i] = cand;
-    const int n = __syncthreads_count(cand);
-    if (cand) {
-        const float c = s_c[i];
-        int rank = 0;
-        for (int j = 0; j < scope; ++j) {
-            if (!s_cand[j]) continue;
-            const float cj = s_c[j];
-            rank += (cj > c) || (cj == c && j < i);
-        }
-        if (rank < a.p_max) a.pool[(int64_t)b * a.p_max + rank] = i;
-    }
-    if (i == 0) {
-        a.pool_n[b] = min(n, a.p_max);
-        if (n > a.p_max) raise_status(a.dev_status, DLM_DEV_POOL_CLIPPED);
-    }
-}
-
-__global__ void __launch_bounds__(kConflictWarps * 32) cap_conflict_kernel(CapArgs a) {
-    const int b = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int slot = blockIdx.x * kConflictWarps + warp;
-    const int n = a.pool_n[b];
-    if (slot >= n) return;
-    const int32_t* pool = a.pool + (int64_t)b * a.p_max;
-    const int pi = pool[slot];
-    const int64_t ri = (int64_t)b * a.blk + pi;
-    const int yi = a.argmax[ri];
-    const float li = a.lse[ri];
-    uint32_t* adj = a.adj + ((int64_t)b * a.p_max + slot) * a.words;
-    const int nw = (n + 31) >> 5;
-    // every partner's scattered loads are issued before any is used (one
-    // round trip for the row instead of one per 32 partners)
-    float g[kMaxPoolWords];
-#pragma unroll
-    for (int c = 0; c < kMaxPoolWords; ++c) {
-        const int e = c * 32 + lane;
-        g[c] = __int_as_float(0x7fc00000);
-        if (c < nw && e < n && e != slot) {
-            const int pj = pool[e];
-            const int64_t rj = (int64_t)b * a.blk + pj;
-            g[c] = logp_at(a, ri, a.argmax[rj], li) + logp_at(a, rj, yi, a.lse[rj]);
-        }
-    }
-#pragma unroll
-    for (int c = 0; c < kMaxPoolWords; ++c) {
-        if (c >= nw) break;
-        const int e = c * 32 + lane;
-        const bool conflict = g[c] > a.gamma;  // NaN (no partner) is never a conflict
-        if (a.D_out && e < n && e != slot) a.D_out[((int64_t)b * a.blk + pi) * a.blk + pool[e]] = g[c];
-        const uint32_t word = __ballot_sync(DLM_FULL_MASK, conflict);
-        if (lane == 0) adj[c] = word;
-    }
-}
-
-__global__ void __launch_bounds__(kThreads) cap_greedy_kernel(CapArgs a) {
-    __shared__ uint32_t s_adj[DLM_MAX_BLK * (DLM_MAX_BLK / 32)];
-    __shared__ uint32_t s_kept[DLM_MAX_BLK / 32];
-    __shared__ unsigned char s_tier[DLM_MAX_BLK];
-    __shared__ float s_v[kThreads / 32];
-    __shared__ int s_i[kThreads / 32];
-    const int b = blockIdx.x, t = threadIdx.x;
-    const int n = a.pool_n[b];
-    const int scope = scope_of(a, b);
-    uint8_t* sel = a.selected + (int64_t)b * a.blk;
-    const int32_t* pool = a.pool + (int64_t)b * a.p_max;
-    if (t < a.blk) sel[t] = 0;
-    if (n == 0) {
-        // no candidate: the highest-confidence masked position of the scope
-        const int64_t o = (int64_t)b * a.blk + t;
-        const bool m = t < scope && a.masked[o] != 0;
-        float v = m ? a.conf[o] : -INFINITY;
-        int idx = m ? t : 0x7fffffff;
-        const int any_m = __syncthreads_or(m);
-        warp_argmax(v, idx);
-        if ((t & 31) == 0) {
-            s_v[t >> 5] = v;
-            s_i[t >> 5] = idx;
-        }
-        __syncthreads();
-        if (t < 32) {
-            v = t < kThreads / 32 ? s_v[t] : -INFINITY;
-            idx = t < kThreads / 32 ? s_i[t] : 0x7fffffff;
-            warp_argmax(v, idx);
-            if (t == 0) {
-                if (any_m) sel[idx] = 1;
-                a.n_selected[b] = any_m ? 1 : 0;
-            }
-        }
-        return;
-    }
-    const int W = (n + 31) >> 5;
-    for (int k = t; k < n * W; k += blockDim.x) {
-        const int s = k / W, w = k - s * W;
-        s_adj[s * W + w] = a.adj[((int64_t)b * a.p_max + s) * a.words + w];
-    }
-    if (t < n) s_tier[t] = a.high_tier_unconditional && a.conf[(int64_t)b * a.blk + pool[t]] >= a.tau_high;
-    __syncthreads();
-    if (t < 32) {
-        // lane w holds word w of the kept set; tier members are forced in when
-        // the tier is unconditional (s_tier is all zero otherwise)
-        const uint32_t kept = greedy_scan(s_adj, W, nullptr, s_tier, n, W);
-        if (t < W) s_kept[t] = kept;
-    }
-    __syncthreads();
-    int mine = 0;
-    if (t < n && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
-        sel[pool[t]] = 1;
-        mine = 1;
-    }
-    const int total = __syncthreads_count(mine);
-    if (t == 0) a.n_selected[b] = total;
 }
 
 // Small pools (p_max <= kFusedMaxPool): the three phases in one CTA per
@@ -257,15 +152,7 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
         float z1[kPairUnroll], z2[kPairUnroll];
 #pragma unroll
         for (int u = 0; u < kPairUnroll; ++u) {
-            const int q = min(q0 + u * kThreads, pairs - 1);
-            // row i holds the pairs (i, i+1 .. n-1); find i with start(i) <= q
-            int i = 0, start = 0;
-            while (start + (n - 1 - i) <= q) {
-                start += n - 1 - i;
-                ++i;
-            }
-            pi[u] = i;
-            pj[u] = i + 1 + (q - start);
+            pair_of(min(q0 + u * kThreads, pairs - 1), n, pi[u], pj[u]);
         }
 #pragma unroll
         for (int u = 0; u < kPairUnroll; ++u) {
@@ -307,6 +194,138 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     if (t == 0) a.n_selected[b] = total;
 }
 
+// Large pools (p_max > kFusedMaxPool): one thread-block cluster of kCapCluster
+// CTAs per sequence.  Every CTA ranks the pool (cheap, redundant), the CTAs
+// split the unordered pairs between them and set the conflict bits with
+// atomics in the leader CTA's shared bitmask (distributed shared memory), and
+// the leader runs the greedy scan: one launch instead of three, and the
+// scattered logit loads spread over kCapCluster x 256 threads.
+constexpr int kCapCluster = 8;
+constexpr int kClusterPairUnroll = 8;
+
+__global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
+    __shared__ float s_c[kThreads];
+    __shared__ int s_cand[kThreads];
+    __shared__ int s_pool[DLM_MAX_BLK];
+    __shared__ int s_y[DLM_MAX_BLK];
+    __shared__ float s_lse[DLM_MAX_BLK];
+    __shared__ uint32_t s_adj[DLM_MAX_BLK * kMaxPoolWords];
+    __shared__ uint32_t s_kept[kMaxPoolWords];
+    __shared__ unsigned char s_tier[DLM_MAX_BLK];
+    __shared__ float s_v[kThreads / 32];
+    __shared__ int s_i[kThreads / 32];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int crank = (int)cluster.block_rank();
+    const int b = blockIdx.x / kCapCluster;
+    const int t = threadIdx.x;
+    const int scope = scope_of(a, b);
+    const int64_t o = (int64_t)b * a.blk + t;
+
+    // 1. the pool, in every CTA of the cluster
+    const bool in = t < a.blk;
+    const bool m = t < scope && a.masked[o] != 0;
+    const float c = in ? a.conf[o] : 0.f;
+    const int y = in ? a.argmax[o] : 0;
+    const float l = in ? a.lse[o] : 0.f;
+    const bool cand = m && c >= a.tau_low;
+    s_c[t] = cand ? c : 0.f;
+    s_cand[t] = cand;
+    for (int k = t; k < DLM_MAX_BLK * kMaxPoolWords; k += kThreads) s_adj[k] = 0u;
+    const int n_cand = __syncthreads_count(cand);
+    const int n = min(n_cand, a.p_max);
+    if (cand) {
+        int rank = 0;
+        for (int j = 0; j < scope; ++j) {
+            if (!s_cand[j]) continue;
+            const float cj = s_c[j];
+            rank += (cj > c) || (cj == c && j < t);
+        }
+        if (rank < a.p_max) {
+            s_pool[rank] = t;
+            s_y[rank] = y;
+            s_lse[rank] = l;
+            s_tier[rank] = a.high_tier_unconditional && c >= a.tau_high;
+        }
+    }
+    cluster.sync();  // pools ranked and the leader's bitmask zeroed, cluster-wide
+
+    // 2. the pairs, split over the cluster; bits land in the leader's bitmask
+    uint32_t* adj0 = cluster.map_shared_rank(s_adj, 0);
+    const int pairs = n * (n - 1) / 2;
+    const int stride = kThreads * kCapCluster;
+    for (int q0 = crank * kThreads + t; q0 < pairs; q0 += stride * kClusterPairUnroll) {
+        int pi[kClusterPairUnroll], pj[kClusterPairUnroll];
+        float dv[kClusterPairUnroll];
+#pragma unroll
+        for (int u = 0; u < kClusterPairUnroll; ++u) {
+            // an index past the last pair maps to the pair (0, 1), which
+            // exists (pairs >= 1); its result is dropped
+            pair_of(min(q0 + u * stride, pairs - 1), n, pi[u], pj[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kClusterPairUnroll; ++u) {
+            const int64_t ri = (int64_t)b * a.blk + s_pool[pi[u]];
+            const int64_t rj = (int64_t)b * a.blk + s_pool[pj[u]];
+            dv[u] = logp_at(a, ri, s_y[pj[u]], s_lse[pi[u]]) + logp_at(a, rj, s_y[pi[u]], s_lse[pj[u]]);
+        }
+#pragma unroll
+        for (int u = 0; u < kClusterPairUnroll; ++u) {
+            if (q0 + u * stride >= pairs) break;
+            const int i = pi[u], j = pj[u];
+            if (dv[u] > a.gamma) {
+                atomicOr(adj0 + i * kMaxPoolWords + (j >> 5), 1u << (j & 31));
+                atomicOr(adj0 + j * kMaxPoolWords + (i >> 5), 1u << (i & 31));
+            }
+            if (a.D_out) {
+                a.D_out[((int64_t)b * a.blk + s_pool[i]) * a.blk + s_pool[j]] = dv[u];
+                a.D_out[((int64_t)b * a.blk + s_pool[j]) * a.blk + s_pool[i]] = dv[u];
+            }
+        }
+    }
+    cluster.sync();  // every conflict bit is in the leader's bitmask
+    if (crank != 0) return;
+
+    // 3. the leader: greedy scan, or the fallback when the pool is empty
+    uint8_t* sel = a.selected + (int64_t)b * a.blk;
+    if (in) sel[t] = 0;
+    if (t == 0 && n_cand > a.p_max) raise_status(a.dev_status, DLM_DEV_POOL_CLIPPED);
+    __syncthreads();
+    if (n == 0) {
+        float v = m ? c : -INFINITY;
+        int idx = m ? t : 0x7fffffff;
+        const int any_m = __syncthreads_or(m);
+        warp_argmax(v, idx);
+        if ((t & 31) == 0) {
+            s_v[t >> 5] = v;
+            s_i[t >> 5] = idx;
+        }
+        __syncthreads();
+        if (t < 32) {
+            v = t < kThreads / 32 ? s_v[t] : -INFINITY;
+            idx = t < kThreads / 32 ? s_i[t] : 0x7fffffff;
+            warp_argmax(v, idx);
+            if (t == 0) {
+                if (any_m) sel[idx] = 1;
+                a.n_selected[b] = any_m ? 1 : 0;
+            }
+        }
+        return;
+    }
+    const int W = (n + 31) >> 5;
+    if (t < 32) {
+        const uint32_t kept = greedy_scan(s_adj, kMaxPoolWords, nullptr, s_tier, n, W);
+        if (t < W) s_kept[t] = kept;
+    }
+    __syncthreads();
+    int mine = 0;
+    if (t < n && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
+        sel[s_pool[t]] = 1;
+        mine = 1;
+    }
+    const int total = __syncthreads_count(mine);
+    if (t == 0) a.n_selected[b] = total;
+}
+
 }  // namespace
 
 size_t cap_workspace_bytes(int batch, int p_max) {
@@ -333,15 +352,15 @@ cudaError_t launch_cap(const CapArgs& a, cudaStream_t s) {
     cfg.gridDim = dim3((unsigned)a.batch);
     cfg.blockDim = dim3(kThreads);
     if (a.p_max <= kFusedMaxPool) return cudaLaunchKernelEx(&cfg, cap_fused_kernel, a);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, cap_pool_kernel, a);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3((unsigned)((a.p_max + kConflictWarps - 1) / kConflictWarps), (unsigned)a.batch);
-    cfg.blockDim = dim3(kConflictWarps * 32);
-    e = cudaLaunchKernelEx(&cfg, cap_conflict_kernel, a);
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3((unsigned)a.batch);
-    cfg.blockDim = dim3(kThreads);
-    return cudaLaunchKernelEx(&cfg, cap_greedy_kernel, a);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCapCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(a.batch * kCapCluster));
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, cap_cluster_kernel, a);
 }
 
 }  // namespace dlm
