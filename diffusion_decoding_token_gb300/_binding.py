@@ -76,6 +76,8 @@ def lib():
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
         L.dlm_depcap_boundary_ragged.argtypes = [P, P, I32, I32, P, P, ctypes.POINTER(DepcapParams), P, P, P]
         L.dlm_row_stats_partial.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, I64, P, P]
+        L.dlm_row_stats_launches.argtypes = [ctypes.c_int, I32, I64, I64]
+        L.dlm_row_stats_launches.restype = I32
         L.dlm_row_stats_merge.argtypes = [P, I32, I64, I64, P, I32, P, P, P, P, P, P, P, P]
         L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
         L.dlm_revocable_step.argtypes = [P, P, P, P, I32, I32, I32, ctypes.POINTER(RevocableParams), P, P, P, P, P,
@@ -495,6 +497,7 @@ class StepPlan:
             n_rows = row_index.numel()
             self.stats = RowStats(*[None if t is None else t.zero_() for t in self.stats])
         self.keep = [cur, prev, attn, self.masked, row_index]
+        self._row_shape = (_dt(cur), int(prev is not None), n_rows, cur.shape[1])
         st = self.stats
         self._calls = []
         self._calls.append((L.dlm_row_stats, (_p(cur), _p(prev), _dt(cur), n_rows, cur.shape[1], cur.stride(0),
@@ -613,12 +616,14 @@ class StepPlan:
 
     @property
     def n_launches(self) -> int:
-        """Kernels launched per step: 1 row pass + 1 per threshold / boundary /
-        top-K / factor / CAP rule, DAPD 2 (attention sum, graph + selection;
-        blocks of up to 64) or 3."""
+        """Kernels launched per step: the row pass (1, or 2 with a tail grid of
+        half rows, as dlm_row_stats_launches reports) + 1 per threshold /
+        boundary / top-K / factor / CAP rule, DAPD 2 (attention sum, graph +
+        selection; blocks of up to 64) or 3."""
         per = {"threshold": 1, "boundary": 1, "cap": 1, "dapd": 2 if self.blk <= 64 else 3, "topk": 1,
                "factor": 1}
-        return 1 + sum(per[r] for r in self.rules)
+        rows = max(0, lib().dlm_row_stats_launches(*self._row_shape))
+        return rows + sum(per[r] for r in self.rules)
 
     def run_rows(self, stream=None, events=None):
         """Issue the row pass (e.g. ahead of a captured graph of the rules,

@@ -80,6 +80,7 @@ static dlm_status row_stats_prepare(dlm::RowStatsArgs& a, const void* cur, const
     a.row_stride = row_stride;
     a.row_index = row_index;
     a.split = split;
+    a.num_sms = (int)(target / 2);
     return DLM_OK;
 }
 
@@ -99,6 +100,19 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
     a.lse_prev = lse_prev;
     a.dev_status = dev_status;
     return from_cuda(dlm::launch_row_stats(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab) {
+    if (!dtype_ok(dtype) || n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL) return -1;
+    if (n_rows == 0) return 0;
+    dlm::RowStatsArgs a{};
+    // alignment does not change the launch shape: use a dummy aligned pointer
+    static const uint4 dummy = {0, 0, 0, 0};
+    const int esz = dtype_size(dtype);
+    const int64_t stride = (vocab * esz + 15) / 16 * 16 / esz;
+    if (row_stats_prepare(a, &dummy, has_prev ? &dummy : nullptr, dtype, n_rows, vocab, stride, nullptr) != DLM_OK)
+        return -1;
+    return dlm::row_stats_grids(a, dtype);
 }
 
 dlm_status dlm_row_stats_partial(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,

@@ -24,8 +24,12 @@ struct RowStatsArgs {
     int split;  // CTAs per row (thread-block cluster size), 1..8
     void* partial;         // non-null: write each row's dlm_row_partial state instead of outputs
     int64_t vocab_offset;  // global position of the slice's first element
+    int64_t row_base;      // first row of this grid (a tail grid after whole waves)
+    int wait_prior;        // complete only after the previous grid on the stream
+    int num_sms;
 };
 cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s);
+int row_stats_grids(const RowStatsArgs& a, int dtype);  // kernel launches launch_row_stats makes
 // merge of dlm_row_partial states: a gives n_rows, row_index and the outputs
 cudaError_t launch_row_merge(const RowStatsArgs& a, const void* partials, int n_shards, int64_t shard_stride,
                              bool prev, cudaStream_t s);

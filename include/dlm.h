@@ -104,6 +104,15 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
                          float* lse_prev, uint32_t* dev_status, dlm_stream_t stream);
 
 /*
+ * dlm_row_stats_launches -- how many kernel launches dlm_row_stats makes for
+ * these sizes (1, or 2 when the rows left over after whole waves of the GPU
+ * run as half rows in a second grid that overlaps the first one's last
+ * wave); 0 for no rows, -1 for arguments dlm_row_stats would reject.  Reads
+ * device attributes of the current device; launches nothing.
+ */
+int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab);
+
+/*
  * dlm_row_stats_partial / dlm_row_stats_merge -- dlm_row_stats over a row
  * whose vocabulary is split into slices (e.g. the vocab shards of a
  * tensor-parallel model, one per GPU).

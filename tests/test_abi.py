@@ -78,6 +78,14 @@ def test_selection_argument_errors(libdlm):
     assert libdlm.dlm_select_threshold(None, fake, 1, 32, ctypes.c_float(0.9), fake, fake, None) == INVALID
     assert libdlm.dlm_select_threshold(fake, fake, 0, 32, ctypes.c_float(0.9), fake, fake, None) == 0
 
+    # the launch-count query launches nothing and rejects what dlm_row_stats rejects
+    from diffusion_decoding_token_gb300 import _binding as B
+    B.lib()
+    assert libdlm.dlm_row_stats_launches(1, 1, 0, 1000) == 0
+    assert libdlm.dlm_row_stats_launches(7, 1, 10, 1000) == -1
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 0) == -1
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000) in (1, 2)
+
     from diffusion_decoding_token_gb300._binding import CapParams, DapdParams, DepcapParams
     dp = DepcapParams(1.0, 8, 2, 0)  # even smoothing width
     assert libdlm.dlm_depcap_boundary(fake, fake, 1, 32, None, ctypes.byref(dp), fake, None, None) == INVALID

@@ -189,3 +189,27 @@ def test_vocab_split_with_empty_and_nan_slices(dlm):
     o = oracle.row_stats(x[[0, 2]])
     np.testing.assert_array_equal(g.argmax.cpu().numpy()[[0, 2]], o["argmax"])
     assert np.all(np.abs(g.lse.cpu().numpy()[[0, 2]] - o["lse"]) <= 1e-4 + 1e-4 * np.abs(o["lse"]))
+
+
+def test_tail_grid_of_half_rows(dlm):
+    """Rows beyond whole waves of the GPU run as half rows in a second grid:
+    the count query says so, and rows on both sides of the cut match the
+    oracle (the batched workload's 2048 rows are checked in full above)."""
+    L = dlm.lib()
+    slots_rows = torch.cuda.get_device_properties(0).multi_processor_count * 4
+    assert L.dlm_row_stats_launches(1, 1, slots_rows, 152064) == 1
+    assert L.dlm_row_stats_launches(1, 1, slots_rows + 37, 152064) == 2
+    rng = np.random.default_rng(9)
+    R, V = slots_rows + 37, 8192
+    x = synth.to_bf16_bits((rng.standard_normal((R, V)) * 2).astype(np.float32))
+    xp = synth.to_bf16_bits((rng.standard_normal((R, V)) * 2).astype(np.float32))
+    g = dlm.row_stats(to_torch(x, synth.BF16, "cuda"), to_torch(xp, synth.BF16, "cuda"))
+    torch.cuda.synchronize()
+    rows = np.array([0, slots_rows - 1, slots_rows, R - 1])
+    o = oracle.row_stats(x[rows], xp[rows], dtype=synth.BF16)
+    for k in ("argmax", "conf", "lse", "entropy", "kl", "lse_prev"):
+        gv = getattr(g, k).cpu().numpy()[rows]
+        if k == "argmax":
+            np.testing.assert_array_equal(gv, o[k])
+        else:
+            assert close(gv, o[k]).all(), k
