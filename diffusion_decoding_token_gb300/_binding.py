@@ -76,7 +76,8 @@ def lib():
                                          P, P, ctypes.POINTER(DapdParams), P, P, P, P, P, P, Z, P, P]
         L.dlm_depcap_boundary_ragged.argtypes = [P, P, I32, I32, P, P, ctypes.POINTER(DepcapParams), P, P, P]
         L.dlm_row_stats_partial.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, I64, P, P]
-        L.dlm_row_stats_launches.argtypes = [ctypes.c_int, I32, I64, I64]
+        L.dlm_row_stats_launches.argtypes = [ctypes.c_int, I32, I64, I64, ctypes.c_uint32]
+        L.dlm_row_stats_ex.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, P, P, P, P, P, P, P, ctypes.c_uint32, P]
         L.dlm_row_stats_launches.restype = I32
         L.dlm_row_stats_merge.argtypes = [P, I32, I64, I64, P, I32, P, P, P, P, P, P, P, P]
         L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
@@ -148,9 +149,13 @@ def alloc_row_stats(n: int, device, with_prev: bool = True) -> RowStats:
                     torch.empty(n, **f) if with_prev else None, torch.empty(n, **f) if with_prev else None)
 
 
+ROWS_SINGLE_GRID = 1  # DLM_ROWS_SINGLE_GRID
+
+
 def row_stats(cur: torch.Tensor, prev: torch.Tensor | None = None, *, row_index: torch.Tensor | None = None,
-              out: RowStats | None = None, status: torch.Tensor | None = None) -> RowStats:
-    """dlm_row_stats over the rows of ``cur`` ([rows, V] with unit column stride)."""
+              out: RowStats | None = None, status: torch.Tensor | None = None, single_grid: bool = False) -> RowStats:
+    """dlm_row_stats over the rows of ``cur`` ([rows, V] with unit column stride);
+    ``single_grid`` passes DLM_ROWS_SINGLE_GRID (dlm_row_stats_ex)."""
     _need_cuda(cur, prev, row_index)
     if cur.dim() != 2 or cur.stride(1) != 1:
         raise ValueError("cur must be [rows, V] with contiguous rows")
@@ -163,11 +168,11 @@ def row_stats(cur: torch.Tensor, prev: torch.Tensor | None = None, *, row_index:
     if row_index is not None:
         row_index = row_index.to(torch.int32).contiguous()
         n = row_index.numel()
-    _check(lib().dlm_row_stats(_p(cur), _p(prev), _dt(cur), n, V, cur.stride(0), _p(row_index),
-                               _p(out.argmax), _p(out.conf), _p(out.lse), _p(out.entropy),
-                               _p(out.kl) if prev is not None else None,
-                               _p(out.lse_prev) if prev is not None else None, _p(status),
-                               _stream(cur.device)))
+    _check(lib().dlm_row_stats_ex(_p(cur), _p(prev), _dt(cur), n, V, cur.stride(0), _p(row_index),
+                                  _p(out.argmax), _p(out.conf), _p(out.lse), _p(out.entropy),
+                                  _p(out.kl) if prev is not None else None,
+                                  _p(out.lse_prev) if prev is not None else None, _p(status),
+                                  ROWS_SINGLE_GRID if single_grid else 0, _stream(cur.device)))
     return out
 
 
@@ -479,7 +484,7 @@ class StepPlan:
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
                  row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0,
-                 parallel_rules=False):
+                 parallel_rules=False, row_tail="auto"):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -497,13 +502,25 @@ class StepPlan:
             n_rows = row_index.numel()
             self.stats = RowStats(*[None if t is None else t.zero_() for t in self.stats])
         self.keep = [cur, prev, attn, self.masked, row_index]
-        self._row_shape = (_dt(cur), int(prev is not None), n_rows, cur.shape[1])
+        # the row pass's tail grid of half rows fills its own draining wave;
+        # when a large DAPD attention pass starts with the step on the
+        # low-priority stream, those slots are better left to it (measured:
+        # 36.7 MB of attention against 1.25 GB of logits gains from the tail
+        # grid, 335 MB against 1.04 GB loses)
+        esz = cur.element_size()
+        if row_tail == "auto":
+            attn_bytes = 0 if attn is None else attn.shape[1] * attn.shape[2] * B * blk * blk * attn.element_size()
+            row_bytes = n_rows * cur.shape[1] * esz * (2 if prev is not None else 1)
+            early = concurrent_dapd and dapd_early and "dapd" in rules
+            row_tail = not (early and attn_bytes >= 0.1 * row_bytes)
+        self.row_flags = 0 if row_tail else ROWS_SINGLE_GRID
+        self._row_shape = (_dt(cur), int(prev is not None), n_rows, cur.shape[1], self.row_flags)
         st = self.stats
         self._calls = []
-        self._calls.append((L.dlm_row_stats, (_p(cur), _p(prev), _dt(cur), n_rows, cur.shape[1], cur.stride(0),
-                                               _p(row_index),
-                                               _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
-                                               _p(st.lse_prev), _p(self.status))))
+        self._calls.append((L.dlm_row_stats_ex, (_p(cur), _p(prev), _dt(cur), n_rows, cur.shape[1], cur.stride(0),
+                                                  _p(row_index),
+                                                  _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
+                                                  _p(st.lse_prev), _p(self.status), ctypes.c_uint32(self.row_flags))))
         u8 = dict(dtype=torch.uint8, device=dev)
         i32 = dict(dtype=torch.int32, device=dev)
         self.out = {}

@@ -84,10 +84,11 @@ static dlm_status row_stats_prepare(dlm::RowStatsArgs& a, const void* cur, const
     return DLM_OK;
 }
 
-dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
-                         int64_t vocab, int64_t row_stride, const int32_t* row_index,
-                         int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
-                         float* lse_prev, uint32_t* dev_status, dlm_stream_t stream) {
+dlm_status dlm_row_stats_ex(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows, int64_t vocab,
+                            int64_t row_stride, const int32_t* row_index, int32_t* argmax, float* conf, float* lse,
+                            float* entropy, float* kl, float* lse_prev, uint32_t* dev_status, uint32_t flags,
+                            dlm_stream_t stream) {
+    if (flags & ~DLM_ROWS_SINGLE_GRID) return DLM_ERR_INVALID_ARG;
     dlm::RowStatsArgs a{};
     const dlm_status st = row_stats_prepare(a, cur, prev, dtype, n_rows, vocab, row_stride, row_index);
     if (st != DLM_OK || n_rows == 0) return st;
@@ -99,11 +100,22 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
     a.kl = kl;
     a.lse_prev = lse_prev;
     a.dev_status = dev_status;
+    a.single_grid = (flags & DLM_ROWS_SINGLE_GRID) ? 1 : 0;
     return from_cuda(dlm::launch_row_stats(a, dtype, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab) {
-    if (!dtype_ok(dtype) || n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL) return -1;
+dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows,
+                         int64_t vocab, int64_t row_stride, const int32_t* row_index,
+                         int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
+                         float* lse_prev, uint32_t* dev_status, dlm_stream_t stream) {
+    return dlm_row_stats_ex(cur, prev, dtype, n_rows, vocab, row_stride, row_index, argmax, conf, lse, entropy, kl,
+                            lse_prev, dev_status, 0u, stream);
+}
+
+int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab,
+                               uint32_t flags) {
+    if (!dtype_ok(dtype) || n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL || (flags & ~DLM_ROWS_SINGLE_GRID))
+        return -1;
     if (n_rows == 0) return 0;
     dlm::RowStatsArgs a{};
     // alignment does not change the launch shape: use a dummy aligned pointer
@@ -112,6 +124,7 @@ int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows
     const int64_t stride = (vocab * esz + 15) / 16 * 16 / esz;
     if (row_stats_prepare(a, &dummy, has_prev ? &dummy : nullptr, dtype, n_rows, vocab, stride, nullptr) != DLM_OK)
         return -1;
+    a.single_grid = (flags & DLM_ROWS_SINGLE_GRID) ? 1 : 0;
     return dlm::row_stats_grids(a, dtype);
 }
 

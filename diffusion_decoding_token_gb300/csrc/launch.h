@@ -27,6 +27,7 @@ struct RowStatsArgs {
     int64_t row_base;      // first row of this grid (a tail grid after whole waves)
     int wait_prior;        // complete only after the previous grid on the stream
     int num_sms;
+    int single_grid;       // no tail grid of half rows
 };
 cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s);
 int row_stats_grids(const RowStatsArgs& a, int dtype);  // kernel launches launch_row_stats makes

@@ -455,7 +455,7 @@ constexpr int kTailSplit = 2;
 
 template <int DT, bool PREV>
 int64_t tail_rows(const RowStatsArgs& a) {
-    if (a.split != 1 || a.num_sms <= 0 || a.partial) return 0;
+    if (a.split != 1 || a.num_sms <= 0 || a.partial || a.single_grid) return 0;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<DT, PREV>, kThreads, 0) !=
             cudaSuccess ||

@@ -104,13 +104,29 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
                          float* lse_prev, uint32_t* dev_status, dlm_stream_t stream);
 
 /*
- * dlm_row_stats_launches -- how many kernel launches dlm_row_stats makes for
- * these sizes (1, or 2 when the rows left over after whole waves of the GPU
- * run as half rows in a second grid that overlaps the first one's last
- * wave); 0 for no rows, -1 for arguments dlm_row_stats would reject.  Reads
- * device attributes of the current device; launches nothing.
+ * dlm_row_stats_launches -- how many kernel launches dlm_row_stats_ex makes
+ * for these sizes and flags (1, or 2 when the rows left over after whole
+ * waves of the GPU run as half rows in a second grid that overlaps the first
+ * one's last wave); 0 for no rows, -1 for arguments the call would reject.
+ * Reads device attributes of the current device; launches nothing.
  */
-int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab);
+int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab,
+                               uint32_t flags);
+
+/*
+ * dlm_row_stats_ex -- dlm_row_stats with launch flags (same outputs):
+ *   DLM_ROWS_SINGLE_GRID  never run the rows past whole waves as a second grid
+ *                         of half rows.  The second grid fills the first one's
+ *                         draining wave; when another kernel is meant to take
+ *                         those slots (a lower-priority stream started with
+ *                         the pass), one grid leaves them to it.
+ */
+#define DLM_ROWS_SINGLE_GRID 1u
+
+dlm_status dlm_row_stats_ex(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows, int64_t vocab,
+                            int64_t row_stride, const int32_t* row_index, int32_t* argmax, float* conf, float* lse,
+                            float* entropy, float* kl, float* lse_prev, uint32_t* dev_status, uint32_t flags,
+                            dlm_stream_t stream);
 
 /*
  * dlm_row_stats_partial / dlm_row_stats_merge -- dlm_row_stats over a row

@@ -81,10 +81,12 @@ def test_selection_argument_errors(libdlm):
     # the launch-count query launches nothing and rejects what dlm_row_stats rejects
     from diffusion_decoding_token_gb300 import _binding as B
     B.lib()
-    assert libdlm.dlm_row_stats_launches(1, 1, 0, 1000) == 0
-    assert libdlm.dlm_row_stats_launches(7, 1, 10, 1000) == -1
-    assert libdlm.dlm_row_stats_launches(1, 1, 10, 0) == -1
-    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000) in (1, 2)
+    assert libdlm.dlm_row_stats_launches(1, 1, 0, 1000, 0) == 0
+    assert libdlm.dlm_row_stats_launches(7, 1, 10, 1000, 0) == -1
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 0, 0) == -1
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000, 0) in (1, 2)
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000, 2) == -1   # unknown flag
+    assert libdlm.dlm_row_stats_launches(1, 1, 10 ** 6, 152064, 1) == 1  # single grid
 
     from diffusion_decoding_token_gb300._binding import CapParams, DapdParams, DepcapParams
     dp = DepcapParams(1.0, 8, 2, 0)  # even smoothing width

@@ -197,8 +197,9 @@ def test_tail_grid_of_half_rows(dlm):
     oracle (the batched workload's 2048 rows are checked in full above)."""
     L = dlm.lib()
     slots_rows = torch.cuda.get_device_properties(0).multi_processor_count * 4
-    assert L.dlm_row_stats_launches(1, 1, slots_rows, 152064) == 1
-    assert L.dlm_row_stats_launches(1, 1, slots_rows + 37, 152064) == 2
+    assert L.dlm_row_stats_launches(1, 1, slots_rows, 152064, 0) == 1
+    assert L.dlm_row_stats_launches(1, 1, slots_rows + 37, 152064, 0) == 2
+    assert L.dlm_row_stats_launches(1, 1, slots_rows + 37, 152064, 1) == 1
     rng = np.random.default_rng(9)
     R, V = slots_rows + 37, 8192
     x = synth.to_bf16_bits((rng.standard_normal((R, V)) * 2).astype(np.float32))
@@ -213,3 +214,19 @@ def test_tail_grid_of_half_rows(dlm):
             np.testing.assert_array_equal(gv, o[k])
         else:
             assert close(gv, o[k]).all(), k
+
+
+def test_single_grid_flag_same_statistics(dlm):
+    """DLM_ROWS_SINGLE_GRID only changes how the rows are launched: the
+    statistics agree with the two-grid pass (summation order aside)."""
+    rows = torch.cuda.get_device_properties(0).multi_processor_count * 4 + 100
+    rng = np.random.default_rng(11)
+    x = synth.to_bf16_bits((rng.standard_normal((rows, 4096)) * 2).astype(np.float32))
+    xp = synth.to_bf16_bits((rng.standard_normal((rows, 4096)) * 2).astype(np.float32))
+    cur, prev = to_torch(x, synth.BF16, "cuda"), to_torch(xp, synth.BF16, "cuda")
+    a = dlm.row_stats(cur, prev)
+    b = dlm.row_stats(cur, prev, single_grid=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(a.argmax.cpu().numpy(), b.argmax.cpu().numpy())
+    for k in ("conf", "lse", "entropy", "kl", "lse_prev"):
+        assert close(getattr(a, k).cpu().numpy(), getattr(b, k).cpu().numpy(), atol=2e-5, rtol=2e-5).all(), k
