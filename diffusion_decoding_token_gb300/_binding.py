@@ -509,9 +509,16 @@ class StepPlan:
         # grid, 335 MB against 1.04 GB loses)
         esz = cur.element_size()
         if row_tail == "auto":
-            attn_bytes = 0 if attn is None else attn.shape[1] * attn.shape[2] * B * blk * blk * attn.element_size()
+            early = concurrent_dapd and dapd_early and "dapd" in rules and attn is not None
+            attn_bytes = 0
+            if early:
+                # attention rows the pass reads for the mask at construction: the
+                # masked rows of sequences on the graph path (late-phase
+                # sequences read none); one host read of the mask, here only
+                m = self.masked.sum(dim=1).cpu()
+                graph = m.to(torch.float32) >= float(bulk_frac) * blk
+                attn_bytes = int((m * graph).sum()) * attn.shape[1] * attn.shape[2] * blk * attn.element_size()
             row_bytes = n_rows * cur.shape[1] * esz * (2 if prev is not None else 1)
-            early = concurrent_dapd and dapd_early and "dapd" in rules
             row_tail = not (early and attn_bytes >= 0.1 * row_bytes)
         self.row_flags = 0 if row_tail else ROWS_SINGLE_GRID
         self._row_shape = (_dt(cur), int(prev is not None), n_rows, cur.shape[1], self.row_flags)
