@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     // 3. greedy over the pool order
     const int W = (n + 31) >> 5;
     if (t < 32) {
-        const uint32_t kept = greedy_scan(s_adj, kFusedWords, nullptr, s_tier, n, W);
+        const uint32_t kept = greedy_scan_chunked(s_adj, kFusedWords, s_tier, n);  // slots are in pool order
         if (t < W) s_kept[t] = kept;
     }
     __syncthreads();
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
     }
     const int W = (n + 31) >> 5;
     if (t < 32) {
-        const uint32_t kept = greedy_scan(s_adj, kMaxPoolWords, nullptr, s_tier, n, W);
+        const uint32_t kept = greedy_scan_chunked(s_adj, kMaxPoolWords, s_tier, n);  // slots are in pool order
         if (t < W) s_kept[t] = kept;
     }
     __syncthreads();

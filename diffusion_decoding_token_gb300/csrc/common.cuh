@@ -191,4 +191,47 @@ __device__ __forceinline__ uint32_t greedy_scan(const uint32_t* adj_in_order, in
     return kept;
 }
 
+// Greedy scan by one warp over nodes 0..n-1 in order, the adjacency given in
+// ORDER coordinates (bit k of word w of row r: node 32w+k is a neighbour of
+// node r): keep a node iff it is forced or has no kept earlier neighbour.
+// The nodes go 32 at a time: lane l takes node 32c+l, tests it against the
+// kept nodes of earlier chunks in parallel, and the chunk's own order is then
+// resolved by every lane alike with bit operations (the 32 rows' in-chunk
+// words come by shuffle, ahead of the dependency chain).  Returns word c of
+// the kept set (order coordinates) in lane c, as greedy_scan does for its
+// coordinates.
+__device__ __forceinline__ uint32_t greedy_scan_chunked(const uint32_t* adj_ord, int row_words,
+                                                        const unsigned char* force_keep, int n) {
+    const int lane = threadIdx.x & 31;
+    uint32_t kept_words = 0;  // lane c: kept set of chunk c
+    const int chunks = (n + 31) >> 5;
+    for (int c = 0; c < chunks; ++c) {
+        const int r = c * 32 + lane;
+        const bool valid = r < n;
+        const uint32_t* row = adj_ord + (size_t)min(r, n - 1) * row_words;  // a real row for every lane
+        bool blocked = false;
+        for (int w = 0; w < c; ++w) {
+            const uint32_t kw = __shfl_sync(DLM_FULL_MASK, kept_words, w);
+            blocked |= valid && (row[w] & kw) != 0u;
+        }
+        const uint32_t intra = valid ? (row[c] & ((1u << lane) - 1u)) : 0u;  // earlier nodes of this chunk
+        const bool forced = valid && force_keep != nullptr && force_keep[r];
+        // candidate: valid and (forced, or not blocked by an earlier chunk)
+        const uint32_t cand = __ballot_sync(DLM_FULL_MASK, valid && (forced || !blocked));
+        const uint32_t fmask = __ballot_sync(DLM_FULL_MASK, forced);
+        uint32_t in_w[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) in_w[k] = __shfl_sync(DLM_FULL_MASK, intra, k);
+        uint32_t kc = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const uint32_t bit = 1u << k;
+            const bool keep = (cand & bit) && ((fmask & bit) || (in_w[k] & kc) == 0u);
+            kc |= keep ? bit : 0u;
+        }
+        if (lane == c) kept_words = kc;
+    }
+    return kept_words;
+}
+
 }  // namespace dlm
