@@ -507,3 +507,37 @@ def test_cap_out_of_vocab_token_is_not_gathered(dlm, p_max):
     assert int(st.item()) & dlm.DEV_NONFINITE
     s = sel.cpu().numpy()[0]
     assert s[0] == 1 and s[2] == 0 and s[1] == 1 and s[3] == 1   # only the 0-2 conflict removes a position
+
+
+def test_whole_steps_as_one_graph_match_eager(dlm):
+    """Steps captured back to back in one CUDA graph, with external timing
+    events around each row pass (the benchmark's timed form), give the same
+    selections as eager steps."""
+    w, dw, o = workload("llada_step")
+    cfg = w.cfg
+    kw = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
+              gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, attn=dw.attn, block_start=dw.block_start,
+              concurrent_dapd=True, dapd_early=True, parallel_rules=True)
+    eager = dlm.StepPlan(dw.cur, dw.prev, dw.masked, **kw)
+    graphed = dlm.StepPlan(dw.cur, dw.prev, dw.masked, **kw)
+    _, hi = torch.cuda.Stream.priority_range()
+    main = torch.cuda.Stream(priority=hi)
+    evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+           for _ in range(3)]
+    with torch.cuda.stream(main):
+        eager.run(main)
+        graphed.run(main)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for e in evs:
+                graphed.run(main, events=e)
+        for v in graphed.out.values():
+            v[0].zero_()
+        g.replay()
+        eager.run(main)
+    torch.cuda.synchronize()
+    for k in eager.out:
+        np.testing.assert_array_equal(eager.out[k][0].cpu().numpy(), graphed.out[k][0].cpu().numpy())
+        np.testing.assert_array_equal(eager.out[k][1].cpu().numpy(), graphed.out[k][1].cpu().numpy())
+    assert all(a.elapsed_time(b) > 0 for a, b in evs)
