@@ -111,6 +111,22 @@ def recorded_traffic():
     return int(kv["traffic_bytes_per_launch"])
 
 
+def device_info(local):
+    """GPU name, SM count, CUDA runtime and driver versions of this rank's GPU."""
+    import torch
+    p = torch.cuda.get_device_properties(local)
+    info = {"name": p.name, "sm_count": p.multi_processor_count, "cuda_runtime": torch.version.cuda,
+            "torch": torch.__version__}
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader", "-i", str(local)],
+                             capture_output=True, text=True, timeout=20)
+        if out.returncode == 0:
+            info["driver"] = out.stdout.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return info
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -679,7 +695,9 @@ def main():
                           f"no flush: {k1_bytes / 1e9:.3f} GB of logit rows per step, larger than L2"),
                    "parallelism": f"dp{world}"},
         "logit_gbps": k1_gbs,
-        "kernels_ms": {"row_stats": k1_ms, "rules_graph": r["rules_ms"]},
+        "kernels_ms": {"row_stats": k1_ms, "row_stats_median": statistics.median(r["k1"]),
+                       "rules_graph": r["rules_ms"]},
+        "device": device_info(local),
         "step_structure": ("row pass on a high-priority stream; DAPD attention graph on a low-priority side stream "
                            "from the step's start (" + ("after the row pass" if args.late_dapd_fork else
                                                           "it shares the row pass's last wave") +
