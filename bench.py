@@ -453,39 +453,46 @@ def run_native(args, rank, world, local):
         attention = {"gbps": a_bytes / (a_ms / 1e3) / 1e9, "ms": a_ms, "algorithmic_bytes": a_bytes,
                      "kernels": "dapd_accum + dapd_graph, alone on the GPU"}
 
-    # --- end to end through host buffers (pinned), same public API
+    # --- end to end through host buffers (pinned), same public API.  Each step
+    # uploads its new logits, its attention block and its mask, decides, and
+    # reads the selections back.  As in a decode loop, the previous step's
+    # logits are the previous step's upload and stay resident as `prev`: two
+    # device buffers alternate (step k reads D[k % 2] as cur, D[(k + 1) % 2] as
+    # prev), fed from two pinned host buffers that alternate the same way.
     e2e = None
     if args.e2e_steps > 0:
-        cur_h = cur.cpu().pin_memory()
-        prev_h = prev.cpu().pin_memory()
+        host_rows = [prev.cpu().pin_memory(), cur.cpu().pin_memory()]
         attn_h = None if w.attn is None else (torch.from_numpy(w.attn) if cfg.attn_dtype == synth.F32 else
                                               torch.from_numpy(w.attn.view(np.int16)).view(tdt[cfg.attn_dtype]))
         attn_h = None if attn_h is None else attn_h.pin_memory()
         masked_h = torch.from_numpy(w.masked).pin_memory()
-        cur_d2 = torch.empty_like(cur)
-        prev_d2 = torch.empty_like(prev)
+        dev_rows = [prev.clone(), cur.clone()]
         attn_c = None if attn_h is None else torch.empty(attn_h.shape, dtype=attn_h.dtype, device=dev)
         masked_d2 = torch.empty_like(masked)
         blen_h = torch.empty(B, dtype=torch.int32).pin_memory()
 
-        plan2 = dlm.StepPlan(cur_d2, prev_d2, masked_d2, attn=attn_c, block_start=0, row_index=row_index, **common)
-        outs_h = {k: torch.empty((B, blk), dtype=torch.uint8).pin_memory() for k in plan2.out}
-        nsel_h = {k: torch.empty(B, dtype=torch.int32).pin_memory() for k in plan2.out}
+        plans2 = [dlm.StepPlan(dev_rows[j], dev_rows[1 - j], masked_d2, attn=attn_c, block_start=0,
+                               row_index=row_index, **common) for j in range(2)]
+        outs_h = {k: torch.empty((B, blk), dtype=torch.uint8).pin_memory() for k in plans2[0].out}
+        nsel_h = {k: torch.empty(B, dtype=torch.int32).pin_memory() for k in plans2[0].out}
+        e2e_k = [0]
 
         def e2e_step():
-            cur_d2.copy_(cur_h, non_blocking=True)
-            prev_d2.copy_(prev_h, non_blocking=True)
+            j = e2e_k[0] % 2
+            e2e_k[0] += 1
+            p = plans2[j]
+            dev_rows[j].copy_(host_rows[j], non_blocking=True)
             if attn_c is not None:
                 attn_c.copy_(attn_h, non_blocking=True)
             masked_d2.copy_(masked_h, non_blocking=True)
-            plan2.run(stream)
-            for k in plan2.out:
-                outs_h[k].copy_(plan2.out[k][0], non_blocking=True)
-                nsel_h[k].copy_(plan2.out[k][1], non_blocking=True)
-            if plan2.block_len is not None:
-                blen_h.copy_(plan2.block_len, non_blocking=True)
+            p.run(stream)
+            for k in p.out:
+                outs_h[k].copy_(p.out[k][0], non_blocking=True)
+                nsel_h[k].copy_(p.out[k][1], non_blocking=True)
+            if p.block_len is not None:
+                blen_h.copy_(p.block_len, non_blocking=True)
 
-        for _ in range(2):
+        for _ in range(2):  # both device buffers hold an upload before the timed steps
             e2e_step()
         torch.cuda.synchronize()
         a0 = torch.cuda.Event(enable_timing=True)
@@ -496,11 +503,14 @@ def run_native(args, rank, world, local):
         a1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a0.elapsed_time(a1) / args.e2e_steps
-        h2d = (cur_h.numel() * cur_h.element_size() + prev_h.numel() * prev_h.element_size() + masked_h.numel()
+        h2d = (host_rows[0].numel() * host_rows[0].element_size() + masked_h.numel()
                + (0 if attn_h is None else attn_h.numel() * attn_h.element_size()))
         d2h = (sum(t.numel() for t in outs_h.values()) + sum(t.numel() * 4 for t in nsel_h.values())
-               + (blen_h.numel() * 4 if plan2.block_len is not None else 0))
-        e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               + (blen_h.numel() * 4 if plans2[0].block_len is not None else 0))
+        e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "prev": "resident: the previous step's upload"}
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} during the end-to-end steps")
 
     return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, per_rule=per_rule, attention=attention, clocks=clocks,
                 e2e=e2e, host_ms=host_ms, flush=flush,
@@ -725,7 +735,7 @@ def main():
         e = r["e2e"]
         line["e2e"] = {"value": r["decisions"] * world / (e["ms_per_step"] / 1000.0), "unit": "decisions/s",
                        "h2d_bytes_per_step": e["h2d_bytes_per_step"], "d2h_bytes_per_step": e["d2h_bytes_per_step"],
-                       "ms_per_step": e["ms_per_step"]}
+                       "ms_per_step": e["ms_per_step"], "prev": e["prev"]}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(r["w"])
     line["config"]["workload_name"] = cfg.name
