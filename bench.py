@@ -51,6 +51,9 @@ def parse():
                     help="fork the DAPD chain after the row pass (default: the attention graph starts with the "
                          "step on the low-priority side stream and takes the SMs the row pass's last wave leaves "
                          "free; the selection waits for the statistics)")
+    ap.add_argument("--dapd-priority", default="low", choices=["low", "high"],
+                    help="priority of the DAPD side stream (high: the attention pass takes SMs from the step's "
+                         "start and the row pass shares them)")
     ap.add_argument("--flush-l2", default="auto", choices=["auto", "on", "off"],
                     help="write a 512 MB buffer between timed steps (auto: when a step reads less than twice L2)")
     ap.add_argument("--serial-rules", action="store_true",
@@ -271,15 +274,17 @@ def run_native(args, rank, world, local):
     # the step runs on a high-priority stream so the DAPD side stream (lowest
     # priority) only takes SMs the row pass leaves free
     torch.cuda.synchronize()
-    _, hi = torch.cuda.Stream.priority_range()
-    torch.cuda.set_stream(torch.cuda.Stream(device=dev, priority=hi))
+    lo, hi = torch.cuda.Stream.priority_range()
+    # the row pass's stream outranks the DAPD side stream (or, with
+    # --dapd-priority high, is outranked by it)
+    torch.cuda.set_stream(torch.cuda.Stream(device=dev, priority=lo if args.dapd_priority == "high" else hi))
     stream = torch.cuda.current_stream(dev)
     common = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
                   gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
                   bulk_frac=cfg.bulk_frac, status=status)
     extra = tuple(r for r in args.extra_rules.split(",") if r)
     common.update(rules=tuple(cfg.rules) + extra, cap_scope_from_boundary=(cfg.name == "depcap_window"),
-                  concurrent_dapd=not args.serial_dapd, dapd_early=not args.late_dapd_fork,
+                  concurrent_dapd=not args.serial_dapd, dapd_early=not args.late_dapd_fork, dapd_priority=args.dapd_priority,
                   parallel_rules=not args.serial_rules)
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 

@@ -484,7 +484,7 @@ class StepPlan:
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
                  row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0,
-                 parallel_rules=False, row_tail="auto"):
+                 parallel_rules=False, row_tail="auto", dapd_priority="low"):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -593,8 +593,10 @@ class StepPlan:
                 # only as the row pass's last wave drains; the selection then
                 # waits for the statistics.  Run the plan on a higher-priority
                 # stream for that to hold.
-                lo, _ = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, 0)
-                self.side = torch.cuda.Stream(device=dev, priority=lo)
+                lo, hi = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") else (0, 0)
+                if dapd_priority not in ("low", "high"):
+                    raise ValueError("dapd_priority is 'low' or 'high'")
+                self.side = torch.cuda.Stream(device=dev, priority=hi if dapd_priority == "high" else lo)
                 self._ev_start = torch.cuda.Event()
                 self._ev_rows = torch.cuda.Event()
                 self._ev_side = torch.cuda.Event()

@@ -395,9 +395,9 @@ dlm_status dlm_dapd_graph(const void* attn, dlm_dtype dtype, int32_t batch, int3
     a.dtilde_out = dtilde_out;
     a.deg_out = deg_out;
     a.dev_status = dev_status;
-    // the graph kernel runs when the selection will not build the graph itself
-    // or when its float outputs are asked for
-    const bool graph_kernel = !dlm::dapd_select_builds_graph(blk) || s_out || dtilde_out || deg_out;
+    // the selection rebuilds the graph from the sums; the graph kernel runs
+    // only for the float outputs
+    const bool graph_kernel = s_out || dtilde_out || deg_out;
     return from_cuda(dlm::launch_dapd_graph(a, sm_count(), reinterpret_cast<cudaStream_t>(stream), graph_kernel));
 }
 

@@ -162,35 +162,6 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_
         : "memory");
 }
 
-// Greedy scan by one warp over nodes given in order, each with its adjacency
-// row (words of 32 neighbours) already laid out in that order: keep a node
-// iff it has no kept neighbour.  Lane w holds word w of the kept set; the
-// loads of the next 8 rows are issued before their decisions.
-__device__ __forceinline__ uint32_t greedy_scan(const uint32_t* adj_in_order, int row_words, const int* node_of /* nullptr: node = position */,
-                                                const unsigned char* force_keep, int n, int nw) {
-    const int lane = threadIdx.x & 31;
-    uint32_t kept = 0;
-    for (int r0 = 0; r0 < n; r0 += 8) {
-        uint32_t w[8];
-        int v[8];
-        bool f[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int r = r0 + u;
-            w[u] = (r < n && lane < nw) ? adj_in_order[r * row_words + lane] : 0u;
-            v[u] = r < n ? (node_of ? node_of[r] : r) : 0;
-            f[u] = r < n && force_keep != nullptr && force_keep[r];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (r0 + u >= n) break;
-            const bool blocked = __any_sync(DLM_FULL_MASK, (w[u] & kept) != 0u);
-            if ((f[u] || !blocked) && lane == (v[u] >> 5)) kept |= 1u << (v[u] & 31);
-        }
-    }
-    return kept;
-}
-
 // Greedy scan by one warp over nodes 0..n-1 in order, the adjacency given in
 // ORDER coordinates (bit k of word w of row r: node 32w+k is a neighbour of
 // node r): keep a node iff it is forced or has no kept earlier neighbour.

@@ -1,27 +1,33 @@
 // dapd.cu -- DAPD: attention -> tau-graph -> Welsh-Powell greedy independent
 // set, with the late-phase confidence rule (DAPD, "整体框架", "关键设计 1-3").
 //
-// Three launches on the caller's stream:
-//   dapd_accum   the HBM-bound part: for every masked row i of the block and
+// Two launches on the caller's stream:
+//   attention    the HBM-bound part: for every masked row i of the block and
 //                every column j, the sum over the given layers and heads of
-//                attention[i][j].  Grid = sequences x row tiles x split, the
-//                split CTAs of one tile forming a thread-block cluster that
-//                divides the layer*head range and merges through distributed
-//                shared memory.  Loads are 16-byte vectors; the sums are exact:
-//                each value x is split as hi = (x + 256) - 256 (a multiple of
-//                2^-15) and lo = x - hi (a multiple of 2^-24 for f16 input,
-//                |lo| <= 2^-16), hi and lo are summed separately in fp32 --
-//                both sums stay exactly representable for f16 values in
-//                [0, 256) whose total stays below 512 -- and the pair is
-//                stored as a 64-bit fixed-point number in units of 2^-32.
-//   dapd_graph   one warp per masked row: I_ij = A_ij + A_ji (= 2 L H 2^32 s_ij),
-//                the edge test I_ij > floor(2 L H 2^32 tau) (exact), the
-//                adjacency words by ballot, the row sum D_i (= 2 L H 2^32 d~_i)
-//                and the edge degree.
-//   dapd_select  one CTA per sequence: the 50% switch, then either the
-//                late-phase rule or the exact ordering of key_i = d~_i conf_i
-//                (compared as 128-bit integer mantissas with a shared exponent)
-//                and the greedy scan over the shared-memory adjacency bitmask.
+//                attention[i][j] (dapd_accum_tma_kernel: bulk tensor copies
+//                into a shared-memory ring; dapd_accum_kernel: 16-byte register
+//                loads, for views a tensor map cannot describe).  Grid =
+//                sequences x row tiles x split, the split CTAs of one tile
+//                forming a thread-block cluster that divides the layer*head
+//                range and merges through distributed shared memory.  The sums
+//                are exact: each value x is split as hi = (x + 256) - 256 (a
+//                multiple of 2^-15) and lo = x - hi (a multiple of 2^-24 for
+//                f16 input, |lo| <= 2^-16), hi and lo are summed separately in
+//                fp32 -- both sums stay exactly representable for f16 values in
+//                [0, 256) whose total stays below 512 -- and the pair is stored
+//                as a 64-bit fixed-point number in units of 2^-32.
+//   decide       per sequence, the graph and the selection: one warp per
+//                masked row builds I_ij = A_ij + A_ji (= 2 L H 2^32 s_ij), the
+//                edge test I_ij > floor(2 L H 2^32 tau) (exact), the adjacency
+//                words by ballot and the row sum D_i (= 2 L H 2^32 d~_i) in
+//                shared memory (dapd_decide_kernel: one CTA, blocks of up to 64;
+//                dapd_decide_cluster_kernel: a cluster of 32-row CTAs writing
+//                into the leader's shared memory); then the 50% switch, and
+//                either the late-phase rule or the exact ordering of
+//                key_i = d~_i conf_i (128-bit sortable keys) and the greedy
+//                scan over the adjacency bitmask.
+// dapd_graph_kernel writes the graph's float outputs for a separate
+// dlm_dapd_graph call that asks for them.
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <algorithm>
@@ -453,30 +459,44 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
 // bitmask (words of 32 neighbours, kMaxWords per row) and the proxy degree D
 // (sum over masked j != i); optional float outputs.  adj_row / D_out may point
 // to global or shared memory.
-__device__ __forceinline__ void graph_row(const DapdArgs& a, int b, int i, long long thresh, float scale,
-                                          uint32_t* adj_row, long long* D_out) {
+// Ai is row i of A (global or shared memory); with col_T, A_ji comes from a
+// shared-memory copy of the block's columns [col0, col0 + 32):
+// col_T[j * kColStride + (i - col0)], else from A in global memory.
+constexpr int kColStride = 33;  // padded: a warp's column reads hit distinct bank pairs
+
+struct RowLoad {
+    long long Iv[kMaxWords];  // I_ij for the lane's column j of each word
+    bool in[kMaxWords];       // j is masked
+};
+
+// the row's loads (one round trip), issued before any decision
+__device__ __forceinline__ void graph_row_load(const DapdArgs& a, int b, int i, const long long* Ai,
+                                               const long long* col_T, int col0, const uint8_t* mk, RowLoad& L) {
     const int lane = threadIdx.x & 31;
-    const uint8_t* mk = a.masked + (int64_t)b * a.blk;
     const long long* A = a.A + (int64_t)b * a.blk * a.blk;
-    long long D = 0;
-    int deg = 0;
     const int nw = (a.blk + 31) >> 5;
-    // all of the row's loads first (one round trip), then the decisions
-    long long Iv[kMaxWords];
-    bool in[kMaxWords];
 #pragma unroll
     for (int c = 0; c < kMaxWords; ++c) {
         const int j = c * 32 + lane;
-        in[c] = c < nw && j < a.blk && mk[j];
-        Iv[c] = in[c] ? A[(int64_t)i * a.blk + j] + A[(int64_t)j * a.blk + i] : 0;
+        L.in[c] = c < nw && j < a.blk && mk[j];
+        const long long Aji = !L.in[c] ? 0 : (col_T ? col_T[j * kColStride + (i - col0)] : A[(int64_t)j * a.blk + i]);
+        L.Iv[c] = L.in[c] ? Ai[j] + Aji : 0;
     }
+}
+
+__device__ __forceinline__ void graph_row_finish(const DapdArgs& a, int b, int i, long long thresh, float scale,
+                                                 const RowLoad& L, uint32_t* adj_row, long long* D_out) {
+    const int lane = threadIdx.x & 31;
+    long long D = 0;
+    int deg = 0;
+    const int nw = (a.blk + 31) >> 5;
 #pragma unroll
     for (int c = 0; c < kMaxWords; ++c) {
         if (c >= nw) break;
         const int j = c * 32 + lane;
         bool edge = false;
-        if (in[c]) {
-            const long long I = Iv[c];
+        if (L.in[c]) {
+            const long long I = L.Iv[c];
             if (a.s_out) a.s_out[((int64_t)b * a.blk + i) * a.blk + j] = __ll2float_rn(I) * scale;
             if (j != i) {
                 D += I;
@@ -494,6 +514,13 @@ __device__ __forceinline__ void graph_row(const DapdArgs& a, int b, int i, long 
         if (a.dtilde_out) a.dtilde_out[(int64_t)b * a.blk + i] = __ll2float_rn(D) * scale;
         if (a.deg_out) a.deg_out[(int64_t)b * a.blk + i] = deg;
     }
+}
+
+__device__ __forceinline__ void graph_row(const DapdArgs& a, int b, int i, long long thresh, float scale,
+                                          uint32_t* adj_row, long long* D_out) {
+    RowLoad L;
+    graph_row_load(a, b, i, a.A + ((int64_t)b * a.blk + i) * a.blk, nullptr, 0, a.masked + (int64_t)b * a.blk, L);
+    graph_row_finish(a, b, i, thresh, scale, L, adj_row, D_out);
 }
 
 __global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
@@ -573,6 +600,51 @@ __device__ __forceinline__ bool key_before(unsigned long long ah, unsigned long 
     return ai < bi;
 }
 
+// Greedy scan over the nodes order[0..n) of the symmetric tau-graph, with
+// adjacency rows in node coordinates (bit k of word w of row v: node 32w + k
+// is a neighbour of v): keep a node iff no neighbour earlier in the order is
+// kept.  The nodes go 32 at a time.  intra[r] holds, for the node at order
+// position r, which earlier nodes of its chunk are neighbours (bit k: the node
+// at position (r & ~31) + k).  One warp runs the scan: lane l takes the node at
+// position 32c + l, drops it when an earlier chunk's kept node is a neighbour
+// (the union of the kept nodes' rows, word w in lane w), and the chunk is
+// resolved in rounds of ballots: a node whose earlier in-chunk neighbours are
+// all decided is kept if none of them was kept, dropped otherwise (the first
+// undecided node is always decided, so a chunk takes at most 32 rounds and
+// sparse graphs a few).  Leaves the kept set (node coordinates) in
+// s_kept[0..kMaxWords).
+__device__ __forceinline__ void greedy_scan_sym(const uint32_t* adj, const int* order, const uint32_t* intra_in,
+                                                int n, int nw, uint32_t* s_kept) {
+    const int lane = threadIdx.x & 31;
+    uint32_t blocked_w = 0u, kept_w = 0u;  // lane w: word w of the kept nodes' neighbours / of the kept set
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const bool valid = c0 + lane < n;
+        const int v = valid ? order[c0 + lane] : 0;
+        const uint32_t vb = 1u << (v & 31);
+        const uint32_t bw = __shfl_sync(DLM_FULL_MASK, blocked_w, v >> 5);
+        const uint32_t cand = __ballot_sync(DLM_FULL_MASK, valid && (bw & vb) == 0u);
+        const uint32_t intra = valid ? intra_in[c0 + lane] : 0u;
+        uint32_t und = cand, kept = 0u;
+        while (und) {
+            const bool u = (und >> lane) & 1u;
+            const uint32_t km = __ballot_sync(DLM_FULL_MASK, u && (intra & (und | kept)) == 0u);
+            const uint32_t dm = __ballot_sync(DLM_FULL_MASK, u && (intra & kept) != 0u);
+            kept |= km;
+            und &= ~(km | dm);
+        }
+        const bool mine = (kept >> lane) & 1u;
+        for (int w = 0; w < nw; ++w) {
+            const uint32_t nb = __reduce_or_sync(DLM_FULL_MASK, mine ? adj[v * kMaxWords + w] : 0u);
+            const uint32_t kb = __reduce_or_sync(DLM_FULL_MASK, (mine && (v >> 5) == w) ? vb : 0u);
+            if (lane == w) {
+                blocked_w |= nb;
+                kept_w |= kb;
+            }
+        }
+    }
+    if (lane < kMaxWords) s_kept[lane] = kept_w;
+}
+
 // The selection of sequence b (DAPD, key designs 2-3) from its graph: proxy
 // degrees D_b[i] and adjacency rows adj_b[i * kMaxWords ..] (global or shared
 // memory).  Every thread of the CTA calls it.
@@ -580,7 +652,7 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
                                             const uint32_t* adj_b) {
     __shared__ unsigned long long s_kh[DLM_MAX_BLK], s_kl[DLM_MAX_BLK];
     __shared__ int s_ix[DLM_MAX_BLK];
-    __shared__ uint32_t s_adj[DLM_MAX_BLK * kMaxWords];
+    __shared__ uint32_t s_intra[DLM_MAX_BLK];
     __shared__ uint32_t s_kept[kMaxWords];
     __shared__ float s_v[kThreads / 32];
     __shared__ int s_i[kThreads / 32];
@@ -617,55 +689,73 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
         if (t == 0) a.n_selected[b] = n;
         return;
     }
-    // keys of the masked nodes; unused slots sort last
+    // keys of the masked nodes, one per thread; unused slots sort last
     int n2 = 1;
     while (n2 < a.blk) n2 <<= 1;
-    if (t < n2) {
-        if (m) {
-            const SortKey k = make_sort_key(D_b[t], a.conf[o], a.order_mode);
-            s_kh[t] = k.hi;
-            s_kl[t] = k.lo;
-            s_ix[t] = t;
-        } else {
-            s_kh[t] = 0;
-            s_kl[t] = 0;
-            s_ix[t] = 0x7fffffff;
-        }
+    unsigned long long kh = 0, kl = 0;
+    int ix = 0x7fffffff;
+    if (m) {
+        const SortKey k = make_sort_key(D_b[t], a.conf[o], a.order_mode);
+        kh = k.hi;
+        kl = k.lo;
+        ix = t;
     }
     if (t < a.blk) sel[t] = 0;
-    // bitonic sort into "goes before" order
+    // bitonic sort into "goes before" order, slot t in thread t: exchanges with
+    // a partner in the same warp go by shuffles, the others (distance >= 32)
+    // through shared memory
+    const bool sorter = (t & ~31) < n2;  // whole warps that hold slots
     for (int k = 2; k <= n2; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            __syncthreads();
-            const int l = t ^ j;
-            if (t < n2 && l > t) {
-                const bool asc = (t & k) == 0;
-                const unsigned long long ah = s_kh[t], al = s_kl[t], bh = s_kh[l], bl = s_kl[l];
-                const int ai = s_ix[t], bi = s_ix[l];
-                const bool ab = key_before(ah, al, ai, bh, bl, bi);
-                if (asc ? !ab : ab) {
-                    s_kh[t] = bh;
-                    s_kl[t] = bl;
-                    s_ix[t] = bi;
-                    s_kh[l] = ah;
-                    s_kl[l] = al;
-                    s_ix[l] = ai;
+            unsigned long long ph = 0, pl = 0;
+            int pi = 0;
+            if (j >= 32) {
+                __syncthreads();  // the previous exchange's reads are done
+                if (t < n2) {
+                    s_kh[t] = kh;
+                    s_kl[t] = kl;
+                    s_ix[t] = ix;
+                }
+                __syncthreads();
+                if (t < n2) {
+                    ph = s_kh[t ^ j];
+                    pl = s_kl[t ^ j];
+                    pi = s_ix[t ^ j];
+                }
+            } else if (sorter) {
+                ph = __shfl_xor_sync(DLM_FULL_MASK, kh, j);
+                pl = __shfl_xor_sync(DLM_FULL_MASK, kl, j);
+                pi = __shfl_xor_sync(DLM_FULL_MASK, ix, j);
+            }
+            if (t < n2) {
+                // the lower slot of an ascending pair (and the upper one of a
+                // descending pair) keeps the element that goes first
+                const bool keep_first = ((t & j) == 0) == ((t & k) == 0);
+                const bool mine_first = key_before(kh, kl, ix, ph, pl, pi);
+                if (keep_first != mine_first) {
+                    kh = ph;
+                    kl = pl;
+                    ix = pi;
                 }
             }
         }
     }
     __syncthreads();
-    // adjacency rows in visiting order
-    const int nw = (a.blk + 31) >> 5;
-    for (int k = t; k < M * nw; k += blockDim.x) {
-        const int r = k / nw, w = k - r * nw;
-        s_adj[r * kMaxWords + w] = adj_b[(int64_t)s_ix[r] * kMaxWords + w];
+    if (t < n2) s_ix[t] = ix;
+    __syncthreads();
+    // greedy scan in key order over the graph (node coordinates); first, for
+    // every order position at once, its earlier neighbours within its chunk of
+    // 32 (read from their rows: bit v of row v_k, the graph being symmetric)
+    if (t < M) {
+        const int c0 = t & ~31, v = s_ix[t];
+        uint32_t intra = 0u;
+        for (int q = 0; q < (t & 31); ++q)
+            intra |= ((adj_b[s_ix[c0 + q] * kMaxWords + (v >> 5)] >> (v & 31)) & 1u) << q;
+        s_intra[t] = intra;
     }
     __syncthreads();
-    if (t < 32) {
-        const uint32_t kept = greedy_scan(s_adj, kMaxWords, s_ix, nullptr, M, nw);
-        if (t < kMaxWords) s_kept[t] = kept;
-    }
+    const int nw = (a.blk + 31) >> 5;
+    if (t < 32) greedy_scan_sym(adj_b, s_ix, s_intra, M, nw, s_kept);
     __syncthreads();
     int mine = 0;
     if (m && (((s_kept[t >> 5] >> (t & 31)) & 1u) || (a.preunmask_certain && a.conf[o] == 1.0f))) {
@@ -674,13 +764,6 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
     }
     const int total = __syncthreads_count(mine);
     if (t == 0) a.n_selected[b] = total;
-}
-
-__global__ void __launch_bounds__(kThreads) dapd_select_kernel(DapdArgs a) {
-    const int b = blockIdx.x;
-    int M;
-    const bool late = late_phase(a, b, &M);
-    select_core(a, b, late, M, a.Dsum + (int64_t)b * a.blk, a.adj + (int64_t)b * a.blk * kMaxWords);
 }
 
 // Blocks of up to kDecideMaxBlk positions: the graph (from the sums A left by
@@ -705,6 +788,90 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
         __syncthreads();
     }
     select_core(a, b, late, M, s_D, s_gadj);
+}
+
+// Larger blocks: a cluster of ceil(blk / 32) CTAs per sequence.  CTA r
+// copies the columns [32r, 32r + 32) of the sums A (every masked row: 256-byte
+// runs, asynchronous 8-byte copies) into shared memory, so the transposed
+// reads A_ji of its 32 rows are coalesced, builds those graph rows straight
+// into the leader CTA's shared memory (distributed shared memory), and the
+// leader then selects; the graph never goes through global memory.
+constexpr int kClusterRows = 32;
+
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+size_t cluster_dyn_smem(int blk) { return ((size_t)blk * kColStride + (size_t)kClusterRows * blk) * sizeof(long long); }
+
+__global__ void __launch_bounds__(kThreads) dapd_decide_cluster_kernel(DapdArgs a) {
+    __shared__ uint32_t s_gadj[DLM_MAX_BLK * kMaxWords];
+    __shared__ long long s_D[DLM_MAX_BLK];
+    extern __shared__ long long s_dyn[];  // columns [blk][kColStride], then rows [32][blk]
+    long long* const s_colT = s_dyn;
+    long long* const s_rowA = s_dyn + a.blk * kColStride;
+    __shared__ uint8_t s_mk[DLM_MAX_BLK];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x / (int)cluster.num_blocks();
+    const int col0 = rank * kClusterRows;
+    const int ncol = min(kClusterRows, a.blk - col0);
+    if (threadIdx.x < DLM_MAX_BLK)
+        s_mk[threadIdx.x] = threadIdx.x < (unsigned)a.blk ? a.masked[(int64_t)b * a.blk + threadIdx.x] : 0;
+    int M;
+    const bool late = late_phase(a, b, &M);  // the same for the whole cluster (and a barrier for s_mk)
+    if (!late) {
+        // asynchronous copies into shared memory: lane c of warp w takes column
+        // col0 + c of the masked rows w, w + 8, ...; the CTA's own masked rows
+        // go whole, in 16-byte pieces (8-byte ones when a row is not 16-byte
+        // aligned: odd blk)
+        const long long* A = a.A + (int64_t)b * a.blk * a.blk;
+        const int c = threadIdx.x & 31;
+        if (c < ncol)
+            for (int j = threadIdx.x >> 5; j < a.blk; j += kThreads / 32)
+                if (s_mk[j]) cp_async8(&s_colT[j * kColStride + c], A + (int64_t)j * a.blk + col0 + c);
+        if ((a.blk & 1) == 0) {
+            const int ppr = a.blk / 2;  // 16-byte pieces per row
+            for (int q = threadIdx.x; q < ncol * ppr; q += kThreads) {
+                const int r = q / ppr, k = q - r * ppr;
+                if (s_mk[col0 + r]) cp_async16(&s_rowA[r * a.blk + 2 * k], A + (int64_t)(col0 + r) * a.blk + 2 * k);
+            }
+        } else {
+            for (int q = threadIdx.x; q < ncol * a.blk; q += kThreads) {
+                const int r = q / a.blk, k = q - r * a.blk;
+                if (s_mk[col0 + r]) cp_async8(&s_rowA[r * a.blk + k], A + (int64_t)(col0 + r) * a.blk + k);
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    cluster.sync();  // the cluster runs and every column copy is in place
+    if (!late) {
+        const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
+        const float scale = a.thresh_from_ws ? __int_as_float((int)a.hdr[1]) : a.s_scale;
+        uint32_t* adj0 = cluster.map_shared_rank(s_gadj, 0);
+        long long* D0 = cluster.map_shared_rank(s_D, 0);
+        // the warp's rows i = col0 + warp + 8r: every row's loads first, then the decisions
+        constexpr int R = kClusterRows / (kThreads / 32);
+        const int warp = threadIdx.x >> 5;
+        RowLoad L[R];
+        bool live[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = col0 + warp + r * (kThreads / 32);
+            live[r] = i < col0 + ncol && s_mk[i];
+            if (live[r]) graph_row_load(a, b, i, s_rowA + (i - col0) * a.blk, s_colT, col0, s_mk, L[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int i = col0 + warp + r * (kThreads / 32);
+            if (live[r]) graph_row_finish(a, b, i, thresh, scale, L[r], adj0 + i * kMaxWords, D0 + i);
+        }
+        cluster.sync();  // every row is in the leader's shared memory
+    }
+    if (rank == 0) select_core(a, b, late, M, s_D, s_gadj);
 }
 
 template <int DT>
@@ -811,6 +978,24 @@ cudaError_t tma_smem_attribute() {
     return cudaSuccess;
 }
 
+// allow the column copy's dynamic shared memory (once per device)
+cudaError_t cluster_smem_attribute() {
+    static std::mutex mu;
+    static bool smem_set[kMaxDev] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    const bool cached = dev >= 0 && dev < kMaxDev;
+    if (!cached || !smem_set[dev]) {
+        e = cudaFuncSetAttribute(dapd_decide_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)cluster_dyn_smem(DLM_MAX_BLK));
+        if (e != cudaSuccess) return e;
+        if (cached) smem_set[dev] = true;
+    }
+    return cudaSuccess;
+}
+
 template <int DT>
 cudaError_t launch_accum_tma(const DapdArgs& a, const CUtensorMap& map, cudaStream_t s) {
     const size_t dyn = tma_dyn_smem(a);
@@ -854,8 +1039,6 @@ void dapd_carve(DapdArgs& a, void* ws) {
     a.hdr = reinterpret_cast<long long*>(p);
 }
 
-bool dapd_select_builds_graph(int blk) { return blk <= kDecideMaxBlk; }
-
 cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel) {
     const int epv = a.dtype == DLM_F32 ? 4 : 8;
     const int vpr = (a.blk + epv - 1) / epv;
@@ -880,7 +1063,7 @@ cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool gra
     default: e = tma ? launch_accum_tma<DLM_F32>(a, map, s) : launch_accum<DLM_F32>(a, s); break;
     }
     if (e != cudaSuccess) return e;
-    if (!graph_kernel) return cudaSuccess;  // the selection builds the graph (dapd_decide_kernel)
+    if (!graph_kernel) return cudaSuccess;  // the selection builds the graph
     cudaLaunchConfig_t cfg = {};
     cfg.stream = s;
     cfg.gridDim = dim3((unsigned)((a.blk + kThreads / 32 - 1) / (kThreads / 32)), (unsigned)a.batch);
@@ -894,13 +1077,25 @@ cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s) {
     cfg.gridDim = dim3((unsigned)a.batch);
     cfg.blockDim = dim3(kThreads);
     if (a.blk <= kDecideMaxBlk) return cudaLaunchKernelEx(&cfg, dapd_decide_kernel, a);
-    return cudaLaunchKernelEx(&cfg, dapd_select_kernel, a);
+    const int csize = (a.blk + kClusterRows - 1) / kClusterRows;  // 3..8
+    const cudaError_t e = cluster_smem_attribute();
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)(a.batch * csize));
+    cfg.dynamicSmemBytes = cluster_dyn_smem(a.blk);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, dapd_decide_cluster_kernel, a);
 }
 
 cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
-    // small blocks: attention pass + one graph-and-selection kernel (which also
-    // writes the float outputs); larger ones: attention pass, graph, selection
-    cudaError_t e = launch_dapd_graph(a, num_sms, s, !dapd_select_builds_graph(a.blk));
+    // attention pass, then one graph-and-selection kernel (which also writes
+    // the float outputs when they are asked for)
+    cudaError_t e = launch_dapd_graph(a, num_sms, s, false);
     if (e != cudaSuccess) return e;
     return launch_dapd_select(a, s);
 }

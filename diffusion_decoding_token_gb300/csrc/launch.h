@@ -163,10 +163,9 @@ struct DapdArgs {
 size_t dapd_workspace_bytes(int batch, int blk);
 void dapd_carve(DapdArgs& a, void* ws);
 cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);  // attention -> selection
-// attention -> sums, and the graph when graph_kernel (always needed when the
-// selection does not build it itself, see dapd_select_builds_graph)
+// attention -> sums; with graph_kernel also the graph's float outputs (the
+// selection rebuilds the graph from the sums itself)
 cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel);
-bool dapd_select_builds_graph(int blk);
 cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s);  // (graph +) conf -> selection
 
 }  // namespace dlm

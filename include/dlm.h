@@ -415,9 +415,8 @@ dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, 
  * while dlm_row_stats reads the logits; the selection then needs conf.
  * dlm_dapd_graph takes the arguments of dlm_dapd_graph_mis except conf and the
  * selection outputs, and leaves in `workspace` what the selection needs: the
- * exact attention sums and the edge threshold, plus the graph itself for
- * blocks of more than 64 positions (for up to 64 the selection rebuilds the
- * small graph from the sums in the same launch); s_out / dtilde_out /
+ * exact attention sums and the edge threshold (the selection rebuilds the
+ * graph from the sums in its own launch); s_out / dtilde_out /
  * deg_out are written when given.
  * dlm_dapd_select reads that graph and conf and writes the selection exactly
  * as dlm_dapd_graph_mis does (late-phase sequences are decided from conf
