@@ -713,9 +713,12 @@ def main():
         "kernels_ms": {"row_stats": k1_ms, "row_stats_median": statistics.median(r["k1"]),
                        "rules_graph": r["rules_ms"]},
         "device": device_info(local),
-        "step_structure": ("row pass on a high-priority stream; DAPD attention graph on a low-priority side stream "
-                           "from the step's start (" + ("after the row pass" if args.late_dapd_fork else
-                                                          "it shares the row pass's last wave") +
+        "step_structure": ("row pass on a " + ("low" if args.dapd_priority == "high" else "high") +
+                           "-priority stream; DAPD attention graph on a " + args.dapd_priority +
+                           "-priority side stream from the step's start (" +
+                           ("after the row pass" if args.late_dapd_fork else
+                            "it takes SMs from the start" if args.dapd_priority == "high" else
+                            "it shares the row pass's last wave") +
                            "), DAPD selection after the row pass; threshold / boundary / CAP as " +
                            ("one chain" if args.serial_rules else "parallel branches") + "; " +
                            ("eager launches" if args.no_graph else
