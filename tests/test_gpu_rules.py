@@ -338,7 +338,8 @@ def test_cap_edges(dlm, blk, p_maxes):
         assert bool(int(st.item()) & dlm.DEV_POOL_CLIPPED) == r["clipped"]
 
 
-@pytest.mark.parametrize("blk,M", [(30, 30), (30, 15), (30, 14), (256, 256), (9, 9), (64, 40)])
+@pytest.mark.parametrize("blk,M", [(30, 30), (30, 15), (30, 14), (256, 256), (9, 9), (64, 40), (65, 65),
+                                   (100, 60), (127, 127), (200, 150)])
 def test_dapd_edges(dlm, blk, M):
     """Ragged block (partial last vector), the 50% switch on both sides,
     the maximum block, and the page's 9-node MRF size."""
@@ -367,6 +368,41 @@ def test_dapd_edges(dlm, blk, M):
             if r["path"][b] == 0:
                 nodes = np.nonzero(masked[b])[0]
                 np.testing.assert_array_equal(deg.cpu().numpy()[b][nodes], r["deg"][b][nodes])
+
+
+@pytest.mark.parametrize("blk", [48, 100, 127])
+def test_dapd_split_calls_float_outputs(dlm, blk):
+    """dlm_dapd_graph with its float outputs, then dlm_dapd_select: the graph
+    outputs and the selection match the oracle (one-CTA and cluster paths,
+    even and odd blocks)."""
+    rng = np.random.default_rng(blk)
+    B, L, H, bs = 2, 2, 3, 8
+    N = (blk + 24 + 7) // 8 * 8
+    sub = rng.random((B, L, H, blk, blk)) ** 6 * 0.3
+    sub = (sub / (sub.sum(-1, keepdims=True) + 1.0)).astype(np.float32)
+    sub16 = synth.to_f16_bits(sub)
+    full = torch.zeros((B, L, H, N, N), dtype=torch.float16, device="cuda")
+    full[:, :, :, bs:bs + blk, bs:bs + blk] = to_torch(sub16, synth.F16, "cuda")
+    masked = np.zeros((B, blk), np.uint8)
+    for b in range(B):
+        masked[b, rng.choice(blk, blk - b * (blk // 4), replace=False)] = 1
+    conf = rng.random((B, blk)).astype(np.float32)
+    tau = 0.02
+    s = torch.full((B, blk, blk), float("nan"), device="cuda")
+    dt = torch.full((B, blk), float("nan"), device="cuda")
+    deg = torch.full((B, blk), -1, dtype=torch.int32, device="cuda")
+    ws = dlm.dapd_graph(full, cuda(masked), tau, 0.9, 0.5, 0, bs, s_out=s, dtilde_out=dt, deg_out=deg)
+    gs, gn = dlm.dapd_select(ws, cuda(masked), cuda(conf), tau, 0.9, 0.5, 0)
+    r = oracle.dapd(sub16, masked, conf.astype(np.float64), tau, 0.9, 0.5, 0, dtype=synth.F16)
+    np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+    np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+    for b in range(B):
+        assert r["path"][b] == 0
+        nodes = np.nonzero(masked[b])[0]
+        np.testing.assert_array_equal(deg.cpu().numpy()[b][nodes], r["deg"][b][nodes])
+        np.testing.assert_allclose(dt.cpu().numpy()[b][nodes], r["dtilde"][b][nodes], rtol=1e-4, atol=1e-4)
+        sb = s.cpu().numpy()[b][np.ix_(nodes, nodes)]
+        np.testing.assert_allclose(sb, r["s"][b][np.ix_(nodes, nodes)], rtol=1e-4, atol=1e-4)
 
 
 def test_dapd_key_ties_break_to_lower_position(dlm):
