@@ -74,8 +74,8 @@ constexpr int kFusedWords = kFusedMaxPool / 32;
 constexpr int kPairUnroll = 4;  // 64 * 63 / 2 pairs = 8 per thread at most
 
 __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
-    __shared__ float s_c[kThreads];
-    __shared__ int s_cand[kThreads];
+    __shared__ __align__(16) float s_c[kThreads];
+    __shared__ __align__(4) unsigned char s_cand[kThreads];
     __shared__ int s_pool[kFusedMaxPool];
     __shared__ int s_y[kFusedMaxPool];
     __shared__ float s_lse[kFusedMaxPool];
@@ -97,18 +97,13 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     const int y = in ? a.argmax[o] : 0;
     const float l = in ? a.lse[o] : 0.f;
     const bool cand = m && c >= a.tau_low;
-    s_c[t] = cand ? c : 0.f;
+    s_c[t] = c;
     s_cand[t] = cand;
     if (t < kFusedMaxPool * kFusedWords) s_adj[t] = 0u;
     const int n_cand = __syncthreads_count(cand);
     const int n = min(n_cand, a.p_max);
     if (cand) {
-        int rank = 0;
-        for (int j = 0; j < scope; ++j) {
-            if (!s_cand[j]) continue;
-            const float cj = s_c[j];
-            rank += (cj > c) || (cj == c && j < t);
-        }
+        const int rank = rank_desc(s_c, s_cand, (scope + 3) & ~3, c, t);
         if (rank < a.p_max) {
             s_pool[rank] = t;
             s_y[rank] = y;
@@ -204,8 +199,8 @@ constexpr int kCapCluster = 8;
 constexpr int kClusterPairUnroll = 8;
 
 __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
-    __shared__ float s_c[kThreads];
-    __shared__ int s_cand[kThreads];
+    __shared__ __align__(16) float s_c[kThreads];
+    __shared__ __align__(4) unsigned char s_cand[kThreads];
     __shared__ int s_pool[DLM_MAX_BLK];
     __shared__ int s_y[DLM_MAX_BLK];
     __shared__ float s_lse[DLM_MAX_BLK];
@@ -228,18 +223,13 @@ __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
     const int y = in ? a.argmax[o] : 0;
     const float l = in ? a.lse[o] : 0.f;
     const bool cand = m && c >= a.tau_low;
-    s_c[t] = cand ? c : 0.f;
+    s_c[t] = c;
     s_cand[t] = cand;
     for (int k = t; k < DLM_MAX_BLK * kMaxPoolWords; k += kThreads) s_adj[k] = 0u;
     const int n_cand = __syncthreads_count(cand);
     const int n = min(n_cand, a.p_max);
     if (cand) {
-        int rank = 0;
-        for (int j = 0; j < scope; ++j) {
-            if (!s_cand[j]) continue;
-            const float cj = s_c[j];
-            rank += (cj > c) || (cj == c && j < t);
-        }
+        const int rank = rank_desc(s_c, s_cand, (scope + 3) & ~3, c, t);
         if (rank < a.p_max) {
             s_pool[rank] = t;
             s_y[rank] = y;

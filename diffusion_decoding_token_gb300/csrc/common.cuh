@@ -113,6 +113,28 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// Rank of slot i (key ki) among the flagged slots of shared-memory arrays in
+// (key descending, slot ascending) order: the number of flagged slots j with
+// key_j > ki, or key_j == ki and j < i.  n is a multiple of 4, key is 16-byte
+// and flag 4-byte aligned; every thread reads the same vectors at a time
+// (broadcast) and the count has no branches.
+__device__ __forceinline__ int rank_desc(const float* key, const unsigned char* flag, int n, float ki, int i) {
+    const float4* k4 = reinterpret_cast<const float4*>(key);
+    const uchar4* f4 = reinterpret_cast<const uchar4*>(flag);
+    int r = 0;
+#pragma unroll 4
+    for (int q = 0; q < n / 4; ++q) {
+        const float4 v = k4[q];
+        const uchar4 f = f4[q];
+        const int j = 4 * q;
+        r += (f.x != 0) & ((v.x > ki) | ((v.x == ki) & (j < i)));
+        r += (f.y != 0) & ((v.y > ki) | ((v.y == ki) & (j + 1 < i)));
+        r += (f.z != 0) & ((v.z > ki) | ((v.z == ki) & (j + 2 < i)));
+        r += (f.w != 0) & ((v.w > ki) | ((v.w == ki) & (j + 3 < i)));
+    }
+    return r;
+}
+
 __device__ __forceinline__ void raise_status(uint32_t* st, uint32_t bits) {
     if (st) atomicOr(st, bits);
 }
@@ -167,10 +189,8 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const void* tmap, uint64_
 // node r): keep a node iff it is forced or has no kept earlier neighbour.
 // The nodes go 32 at a time: lane l takes node 32c+l, tests it against the
 // kept nodes of earlier chunks in parallel, and the chunk's own order is then
-// resolved by every lane alike with bit operations (the 32 rows' in-chunk
-// words come by shuffle, ahead of the dependency chain).  Returns word c of
-// the kept set (order coordinates) in lane c, as greedy_scan does for its
-// coordinates.
+// resolved in rounds of ballots.  Returns word c of the kept set (order
+// coordinates) in lane c.
 __device__ __forceinline__ uint32_t greedy_scan_chunked(const uint32_t* adj_ord, int row_words,
                                                         const unsigned char* force_keep, int n) {
     const int lane = threadIdx.x & 31;
@@ -189,16 +209,17 @@ __device__ __forceinline__ uint32_t greedy_scan_chunked(const uint32_t* adj_ord,
         const bool forced = valid && force_keep != nullptr && force_keep[r];
         // candidate: valid and (forced, or not blocked by an earlier chunk)
         const uint32_t cand = __ballot_sync(DLM_FULL_MASK, valid && (forced || !blocked));
-        const uint32_t fmask = __ballot_sync(DLM_FULL_MASK, forced);
-        uint32_t in_w[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) in_w[k] = __shfl_sync(DLM_FULL_MASK, intra, k);
-        uint32_t kc = 0;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const uint32_t bit = 1u << k;
-            const bool keep = (cand & bit) && ((fmask & bit) || (in_w[k] & kc) == 0u);
-            kc |= keep ? bit : 0u;
+        // the chunk in rounds: a candidate is kept once it is forced or every
+        // earlier in-chunk neighbour is decided and none of them is kept, and
+        // dropped once one of them is kept; the first undecided candidate is
+        // always decided, so this ends (in a few rounds on sparse graphs)
+        uint32_t und = cand, kc = 0u;
+        while (und) {
+            const bool u = (und >> lane) & 1u;
+            const uint32_t km = __ballot_sync(DLM_FULL_MASK, u && (forced || (intra & (und | kc)) == 0u));
+            const uint32_t dm = __ballot_sync(DLM_FULL_MASK, u && !forced && (intra & kc) != 0u);
+            kc |= km;
+            und &= ~(km | dm);
         }
         if (lane == c) kept_words = kc;
     }

@@ -16,22 +16,9 @@ namespace {
 
 constexpr int kRevThreads = 256;  // >= DLM_MAX_BLK
 
-// Rank of position i among the flagged positions in (key desc, position asc)
-// order.
-__device__ __forceinline__ int flagged_rank(const float* key, const unsigned char* flag, int blk, int i) {
-    const float ki = key[i];
-    int r = 0;
-    for (int j = 0; j < blk; ++j) {
-        if (!flag[j]) continue;
-        const float kj = key[j];
-        r += (kj > ki) || (kj == ki && j < i);
-    }
-    return r;
-}
-
 __global__ void __launch_bounds__(kRevThreads) revocable_kernel(RevocableArgs a) {
-    __shared__ float s_key[kRevThreads];
-    __shared__ unsigned char s_flag[kRevThreads];
+    __shared__ __align__(16) float s_key[kRevThreads];
+    __shared__ __align__(4) unsigned char s_flag[kRevThreads];
     __shared__ float s_v[kRevThreads / 32];
     __shared__ int s_i[kRevThreads / 32];
     const int b = blockIdx.x, i = threadIdx.x;
@@ -81,7 +68,7 @@ __global__ void __launch_bounds__(kRevThreads) revocable_kernel(RevocableArgs a)
     int n_drafted;
     if (n_cand > 0) {
         n_drafted = a.draft_budget > 0 ? min(n_cand, a.draft_budget) : n_cand;
-        drafted = cand && flagged_rank(s_key, s_flag, a.blk, i) < n_drafted;
+        drafted = cand && rank_desc(s_key, s_flag, (a.blk + 3) & ~3, s_key[i], i) < n_drafted;
     } else {  // nothing clears the threshold: the most confident masked position
         float v = m0 ? c : -INFINITY;
         int idx = m0 ? i : 0x7fffffff;
@@ -125,7 +112,7 @@ __global__ void __launch_bounds__(kRevThreads) revocable_kernel(RevocableArgs a)
     const int n_elig = __syncthreads_count(elig);
     const float kf = ceilf(__fmul_rn(__fsqrt_rn((float)n_elig), a.pi));
     const int k = kf < (float)n_elig ? (int)kf : n_elig;
-    const bool seed_next = elig && flagged_rank(s_key, s_flag, a.blk, i) < k;
+    const bool seed_next = elig && rank_desc(s_key, s_flag, (a.blk + 3) & ~3, s_key[i], i) < k;
     if (seed_next) last_seed = a.step;
 
     if (valid) {

@@ -167,26 +167,13 @@ __global__ void __launch_bounds__(kBndThreads) boundary_kernel(BoundaryArgs a) {
     }
 }
 
-// Rank of each masked position in (conf desc, position asc) order, counted
-// against all masked positions of the block (all-pairs in shared memory).
-__device__ __forceinline__ int conf_rank(const float* s_c, const unsigned char* s_m, int blk, int i) {
-    const float c = s_c[i];
-    int r = 0;
-    for (int j = 0; j < blk; ++j) {
-        if (!s_m[j]) continue;
-        const float cj = s_c[j];
-        r += (cj > c) || (cj == c && j < i);
-    }
-    return r;
-}
-
 // Fixed top-K (Fast-dLLM review, Prior limitations: LLaDA's default commits
 // K tokens per step whatever their confidence) and factor decoding (Fast-dLLM
 // review, Method, appendix variant: the largest n with (n+1)(1 - c^(n)) < f,
 // the top position alone when no n qualifies).  mode 0 = top-K, 1 = factor.
 __global__ void __launch_bounds__(kSelThreads) rank_select_kernel(RankSelectArgs a) {
-    __shared__ float s_c[kSelThreads];
-    __shared__ unsigned char s_m[kSelThreads];
+    __shared__ __align__(16) float s_c[kSelThreads];
+    __shared__ __align__(4) unsigned char s_m[kSelThreads];
     const int b = blockIdx.x, i = threadIdx.x;
     const bool valid = i < a.blk;
     const int64_t o = (int64_t)b * a.blk + i;
@@ -194,7 +181,8 @@ __global__ void __launch_bounds__(kSelThreads) rank_select_kernel(RankSelectArgs
     s_c[i] = m ? a.conf[o] : 0.f;
     s_m[i] = m;
     const int M = __syncthreads_count(m);
-    const int r = m ? conf_rank(s_c, s_m, a.blk, i) : 0x7fffffff;
+    // rank in (conf desc, position asc) order among the masked positions
+    const int r = m ? rank_desc(s_c, s_m, (a.blk + 3) & ~3, s_c[i], i) : 0x7fffffff;
     int n;
     if (a.mode == 0) {
         n = min(a.k, M);
