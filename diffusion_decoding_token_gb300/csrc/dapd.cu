@@ -46,10 +46,11 @@ constexpr int kThreads = 256;
 constexpr int kMaxWords = DLM_MAX_BLK / 32;
 constexpr int kSliceUnroll = 8;
 
-__device__ __forceinline__ bool late_phase(const DapdArgs& a, int b, int* count_out) {
+// The 50% switch of sequence b (every thread of the CTA calls it): fewer than
+// bulk_frac * blk masked positions left -> the late-phase confidence rule.
+__device__ __forceinline__ bool late_phase(const DapdArgs& a, int b) {
     const bool m = threadIdx.x < (unsigned)a.blk && a.masked[(int64_t)b * a.blk + threadIdx.x] != 0;
     const int M = __syncthreads_count(m);
-    if (count_out) *count_out = M;
     return (float)M < a.bulk_frac * (float)a.blk;
 }
 
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
     const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
     const int tile = tb % tiles;
     const int b = tb / tiles;
-    if (late_phase(a, b, nullptr)) return;  // the whole cluster takes the same branch
+    if (late_phase(a, b)) return;  // the whole cluster takes the same branch
 
     const int r0 = tile * a.row_tile, r1 = min(a.blk, r0 + a.row_tile);
     {
@@ -324,7 +325,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
     const int tiles = (a.blk + a.row_tile - 1) / a.row_tile;
     const int tile = tb % tiles;
     const int b = tb / tiles;
-    if (late_phase(a, b, nullptr)) return;  // the whole cluster takes the same branch
+    if (late_phase(a, b)) return;  // the whole cluster takes the same branch
 
     const int RB = a.row_tile, CB = a.box_cols, HB = a.box_heads;
     const int r0 = tile * RB;
@@ -460,9 +461,18 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
 // (sum over masked j != i); optional float outputs.  adj_row / D_out may point
 // to global or shared memory.
 // Ai is row i of A (global or shared memory); with col_T, A_ji comes from a
-// shared-memory copy of the block's columns [col0, col0 + 32):
-// col_T[j * kColStride + (i - col0)], else from A in global memory.
+// shared-memory copy of the block's columns from col0 on, col_ld words per row
+// j: col_T[j * col_ld + (i - col0)], else from A in global memory.
 constexpr int kColStride = 33;  // padded: a warp's column reads hit distinct bank pairs
+
+// asynchronous global -> shared copies (completed by cp.async.wait_all)
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
 
 struct RowLoad {
     long long Iv[kMaxWords];  // I_ij for the lane's column j of each word
@@ -471,7 +481,8 @@ struct RowLoad {
 
 // the row's loads (one round trip), issued before any decision
 __device__ __forceinline__ void graph_row_load(const DapdArgs& a, int b, int i, const long long* Ai,
-                                               const long long* col_T, int col0, const uint8_t* mk, RowLoad& L) {
+                                               const long long* col_T, int col_ld, int col0, const uint8_t* mk,
+                                               RowLoad& L) {
     const int lane = threadIdx.x & 31;
     const long long* A = a.A + (int64_t)b * a.blk * a.blk;
     const int nw = (a.blk + 31) >> 5;
@@ -479,7 +490,7 @@ __device__ __forceinline__ void graph_row_load(const DapdArgs& a, int b, int i, 
     for (int c = 0; c < kMaxWords; ++c) {
         const int j = c * 32 + lane;
         L.in[c] = c < nw && j < a.blk && mk[j];
-        const long long Aji = !L.in[c] ? 0 : (col_T ? col_T[j * kColStride + (i - col0)] : A[(int64_t)j * a.blk + i]);
+        const long long Aji = !L.in[c] ? 0 : (col_T ? col_T[j * col_ld + (i - col0)] : A[(int64_t)j * a.blk + i]);
         L.Iv[c] = L.in[c] ? Ai[j] + Aji : 0;
     }
 }
@@ -519,13 +530,13 @@ __device__ __forceinline__ void graph_row_finish(const DapdArgs& a, int b, int i
 __device__ __forceinline__ void graph_row(const DapdArgs& a, int b, int i, long long thresh, float scale,
                                           uint32_t* adj_row, long long* D_out) {
     RowLoad L;
-    graph_row_load(a, b, i, a.A + ((int64_t)b * a.blk + i) * a.blk, nullptr, 0, a.masked + (int64_t)b * a.blk, L);
+    graph_row_load(a, b, i, a.A + ((int64_t)b * a.blk + i) * a.blk, nullptr, 0, 0, a.masked + (int64_t)b * a.blk, L);
     graph_row_finish(a, b, i, thresh, scale, L, adj_row, D_out);
 }
 
 __global__ void __launch_bounds__(kThreads) dapd_graph_kernel(DapdArgs a) {
     const int b = blockIdx.y;
-    if (late_phase(a, b, nullptr)) return;
+    if (late_phase(a, b)) return;
     const int warp = threadIdx.x >> 5;
     const int i = blockIdx.x * (kThreads / 32) + warp;
     if (i >= a.blk) return;
@@ -648,8 +659,8 @@ __device__ __forceinline__ void greedy_scan_sym(const uint32_t* adj, const int* 
 // The selection of sequence b (DAPD, key designs 2-3) from its graph: proxy
 // degrees D_b[i] and adjacency rows adj_b[i * kMaxWords ..] (global or shared
 // memory).  Every thread of the CTA calls it.
-__device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late, int M, const long long* D_b,
-                                            const uint32_t* adj_b) {
+__device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late, int M, bool m, float c,
+                                            const long long* D_b, const uint32_t* adj_b) {
     __shared__ unsigned long long s_kh[DLM_MAX_BLK], s_kl[DLM_MAX_BLK];
     __shared__ int s_ix[DLM_MAX_BLK];
     __shared__ uint32_t s_intra[DLM_MAX_BLK];
@@ -657,11 +668,8 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
     __shared__ float s_v[kThreads / 32];
     __shared__ int s_i[kThreads / 32];
     const int t = threadIdx.x;
-    const int64_t o = (int64_t)b * a.blk + t;
-    const bool m = t < a.blk && a.masked[o] != 0;
     uint8_t* sel = a.selected + (int64_t)b * a.blk;
     if (late) {
-        const float c = m ? a.conf[o] : 0.f;
         bool s = m && c > a.bulk_conf;
         int n = __syncthreads_count(s);
         if (n == 0 && M > 0) {
@@ -695,7 +703,7 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
     unsigned long long kh = 0, kl = 0;
     int ix = 0x7fffffff;
     if (m) {
-        const SortKey k = make_sort_key(D_b[t], a.conf[o], a.order_mode);
+        const SortKey k = make_sort_key(D_b[t], c, a.order_mode);
         kh = k.hi;
         kl = k.lo;
         ix = t;
@@ -758,7 +766,7 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
     if (t < 32) greedy_scan_sym(adj_b, s_ix, s_intra, M, nw, s_kept);
     __syncthreads();
     int mine = 0;
-    if (m && (((s_kept[t >> 5] >> (t & 31)) & 1u) || (a.preunmask_certain && a.conf[o] == 1.0f))) {
+    if (m && (((s_kept[t >> 5] >> (t & 31)) & 1u) || (a.preunmask_certain && c == 1.0f))) {
         sel[t] = 1;
         mine = 1;
     }
@@ -772,22 +780,42 @@ __device__ __forceinline__ void select_core(const DapdArgs& a, int b, bool late,
 constexpr int kDecideMaxBlk = 64;
 
 __global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
+    constexpr int LD = kDecideMaxBlk + 1;  // odd row length: a warp's column reads hit distinct bank pairs
     __shared__ uint32_t s_gadj[kDecideMaxBlk * kMaxWords];
     __shared__ long long s_D[kDecideMaxBlk];
-    const int b = blockIdx.x;
-    int M;
-    const bool late = late_phase(a, b, &M);
+    __shared__ long long s_A[kDecideMaxBlk * LD];  // the masked rows of the sums A
+    __shared__ uint8_t s_mk[kDecideMaxBlk];
+    const int b = blockIdx.x, t = threadIdx.x;
+    // the per-position inputs and the header in one round trip
+    const bool in = t < a.blk;
+    const bool m = in && a.masked[(int64_t)b * a.blk + t] != 0;
+    const float c = in ? a.conf[(int64_t)b * a.blk + t] : 0.f;
+    // called after a separate attention pass (dlm_dapd_select), the edge
+    // threshold and score scale come from the workspace header it wrote
+    const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
+    const float scale = a.thresh_from_ws ? __int_as_float((int)a.hdr[1]) : a.s_scale;
+    if (in) s_mk[t] = m;
+    const int M = __syncthreads_count(m);
+    const bool late = (float)M < a.bulk_frac * (float)a.blk;
     if (!late) {
-        // called after a separate attention pass (dlm_dapd_select), the edge
-        // threshold and score scale come from the workspace header it wrote
-        const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
-        const float scale = a.thresh_from_ws ? __int_as_float((int)a.hdr[1]) : a.s_scale;
-        const uint8_t* mk = a.masked + (int64_t)b * a.blk;
-        for (int i = threadIdx.x >> 5; i < a.blk; i += kThreads / 32)
-            if (mk[i]) graph_row(a, b, i, thresh, scale, s_gadj + i * kMaxWords, s_D + i);
+        // the masked rows of A into shared memory (one round trip, coalesced),
+        // so the transposed reads A_ji are shared-memory reads too
+        const long long* A = a.A + (int64_t)b * a.blk * a.blk;
+        for (int q = threadIdx.x; q < a.blk * a.blk; q += kThreads) {
+            const int r = q / a.blk, k = q - r * a.blk;
+            if (s_mk[r]) cp_async8(&s_A[r * LD + k], A + q);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+        for (int i = threadIdx.x >> 5; i < a.blk; i += kThreads / 32) {
+            if (!s_mk[i]) continue;  // warp-uniform
+            RowLoad L;
+            graph_row_load(a, b, i, s_A + i * LD, s_A, LD, 0, s_mk, L);
+            graph_row_finish(a, b, i, thresh, scale, L, s_gadj + i * kMaxWords, s_D + i);
+        }
         __syncthreads();
     }
-    select_core(a, b, late, M, s_D, s_gadj);
+    select_core(a, b, late, M, m, c, s_D, s_gadj);
 }
 
 // Larger blocks: a cluster of ceil(blk / 32) CTAs per sequence.  CTA r
@@ -797,13 +825,6 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
 // into the leader CTA's shared memory (distributed shared memory), and the
 // leader then selects; the graph never goes through global memory.
 constexpr int kClusterRows = 32;
-
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
 
 size_t cluster_dyn_smem(int blk) { return ((size_t)blk * kColStride + (size_t)kClusterRows * blk) * sizeof(long long); }
 
@@ -819,20 +840,25 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_cluster_kernel(DapdArgs 
     const int b = blockIdx.x / (int)cluster.num_blocks();
     const int col0 = rank * kClusterRows;
     const int ncol = min(kClusterRows, a.blk - col0);
-    if (threadIdx.x < DLM_MAX_BLK)
-        s_mk[threadIdx.x] = threadIdx.x < (unsigned)a.blk ? a.masked[(int64_t)b * a.blk + threadIdx.x] : 0;
-    int M;
-    const bool late = late_phase(a, b, &M);  // the same for the whole cluster (and a barrier for s_mk)
+    const int t = threadIdx.x;
+    const bool in = t < a.blk;
+    const bool m = in && a.masked[(int64_t)b * a.blk + t] != 0;
+    const float c = in ? a.conf[(int64_t)b * a.blk + t] : 0.f;
+    const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
+    const float scale = a.thresh_from_ws ? __int_as_float((int)a.hdr[1]) : a.s_scale;
+    if (t < DLM_MAX_BLK) s_mk[t] = m;
+    const int M = __syncthreads_count(m);
+    const bool late = (float)M < a.bulk_frac * (float)a.blk;  // the same for the whole cluster
     if (!late) {
-        // asynchronous copies into shared memory: lane c of warp w takes column
-        // col0 + c of the masked rows w, w + 8, ...; the CTA's own masked rows
+        // asynchronous copies into shared memory: lane l of warp w takes column
+        // col0 + l of the masked rows w, w + 8, ...; the CTA's own masked rows
         // go whole, in 16-byte pieces (8-byte ones when a row is not 16-byte
         // aligned: odd blk)
         const long long* A = a.A + (int64_t)b * a.blk * a.blk;
-        const int c = threadIdx.x & 31;
-        if (c < ncol)
+        const int l = threadIdx.x & 31;
+        if (l < ncol)
             for (int j = threadIdx.x >> 5; j < a.blk; j += kThreads / 32)
-                if (s_mk[j]) cp_async8(&s_colT[j * kColStride + c], A + (int64_t)j * a.blk + col0 + c);
+                if (s_mk[j]) cp_async8(&s_colT[j * kColStride + l], A + (int64_t)j * a.blk + col0 + l);
         if ((a.blk & 1) == 0) {
             const int ppr = a.blk / 2;  // 16-byte pieces per row
             for (int q = threadIdx.x; q < ncol * ppr; q += kThreads) {
@@ -849,8 +875,6 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_cluster_kernel(DapdArgs 
     }
     cluster.sync();  // the cluster runs and every column copy is in place
     if (!late) {
-        const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
-        const float scale = a.thresh_from_ws ? __int_as_float((int)a.hdr[1]) : a.s_scale;
         uint32_t* adj0 = cluster.map_shared_rank(s_gadj, 0);
         long long* D0 = cluster.map_shared_rank(s_D, 0);
         // the warp's rows i = col0 + warp + 8r: every row's loads first, then the decisions
@@ -862,7 +886,7 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_cluster_kernel(DapdArgs 
         for (int r = 0; r < R; ++r) {
             const int i = col0 + warp + r * (kThreads / 32);
             live[r] = i < col0 + ncol && s_mk[i];
-            if (live[r]) graph_row_load(a, b, i, s_rowA + (i - col0) * a.blk, s_colT, col0, s_mk, L[r]);
+            if (live[r]) graph_row_load(a, b, i, s_rowA + (i - col0) * a.blk, s_colT, kColStride, col0, s_mk, L[r]);
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -871,7 +895,7 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_cluster_kernel(DapdArgs 
         }
         cluster.sync();  // every row is in the leader's shared memory
     }
-    if (rank == 0) select_core(a, b, late, M, s_D, s_gadj);
+    if (rank == 0) select_core(a, b, late, M, m, c, s_D, s_gadj);
 }
 
 template <int DT>
