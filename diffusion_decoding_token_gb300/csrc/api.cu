@@ -262,8 +262,8 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
                           int32_t* n_selected, float* D_out, void* workspace, size_t ws_bytes,
                           uint32_t* dev_status, dlm_stream_t stream) {
     if (!dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
-    if (!params || batch < 0 || blk < 1 || blk > DLM_MAX_BLK || vocab < 1 || row_stride < vocab ||
-        params->p_max < 1 || params->p_max > DLM_MAX_BLK ||
+    if (!params || batch < 0 || batch > DLM_MAX_BATCH || blk < 1 || blk > DLM_MAX_BLK || vocab < 1 ||
+        row_stride < vocab || params->p_max < 1 || params->p_max > DLM_MAX_BLK ||
         (params->high_tier_unconditional != 0 && params->high_tier_unconditional != 1))
         return DLM_ERR_INVALID_ARG;
     if (batch == 0) return DLM_OK;
@@ -311,7 +311,8 @@ dlm_status dapd_prepare(dlm::DapdArgs& a, const void* attn, dlm_dtype dtype, int
                         int32_t block_start, int32_t blk, const uint8_t* masked, const dlm_dapd_params* params,
                         void* workspace, size_t ws_bytes, bool need_attn) {
     if (need_attn && !dtype_ok(dtype)) return DLM_ERR_UNSUPPORTED;
-    if (!params || batch < 0 || blk < 1 || blk > DLM_MAX_BLK || (params->order_mode != 0 && params->order_mode != 1) ||
+    if (!params || batch < 0 || batch > DLM_MAX_BATCH || blk < 1 || blk > DLM_MAX_BLK ||
+        (params->order_mode != 0 && params->order_mode != 1) ||
         (params->preunmask_certain != 0 && params->preunmask_certain != 1) || !isfinite(params->tau_edge))
         return DLM_ERR_INVALID_ARG;
     if (need_attn && (n_layers < 1 || n_heads < 1 || (int64_t)n_layers * n_heads > (1 << 20) || block_start < 0 ||

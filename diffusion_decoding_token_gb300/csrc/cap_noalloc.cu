@@ -54,7 +54,7 @@ extern "C" dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype
                                              uint8_t* selected, int32_t* n_selected, float* D_out,
                                              uint32_t* dev_status, dlm_stream_t stream) {
     if (dtype != DLM_F32 && dtype != DLM_BF16 && dtype != DLM_F16) return DLM_ERR_UNSUPPORTED;
-    if (!params || batch < 0 || blk < 1 || blk > DLM_MAX_BLK || vocab < 1 || row_stride < vocab ||
+    if (!params || batch < 0 || batch > DLM_MAX_BATCH || blk < 1 || blk > DLM_MAX_BLK || vocab < 1 || row_stride < vocab ||
         params->p_max < 1 || params->p_max > DLM_MAX_BLK ||
         (params->high_tier_unconditional != 0 && params->high_tier_unconditional != 1))
         return DLM_ERR_INVALID_ARG;

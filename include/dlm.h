@@ -26,7 +26,10 @@
  *    the logits.
  *  - Float decisions (threshold tests, orderings) are taken in fp32 on the
  *    values the caller passes; DAPD's graph decisions are exact (see there).
- *  - Sizes: 1 <= blk <= 256 for the selection calls; a batch of 0 is a no-op.
+ *  - Sizes: 1 <= blk <= 256 for the selection calls; a batch of 0 is a no-op;
+ *    CAP and DAPD take at most DLM_MAX_BATCH sequences per call (their grids
+ *    hold up to 2048 CTAs per sequence), larger batches return
+ *    DLM_ERR_INVALID_ARG.
  */
 #ifndef DLM_H
 #define DLM_H
@@ -60,6 +63,7 @@ typedef enum dlm_dtype { DLM_F32 = 0, DLM_BF16 = 1, DLM_F16 = 2 } dlm_dtype;
 
 /* Maximum block size accepted by the selection calls. */
 #define DLM_MAX_BLK 256
+#define DLM_MAX_BATCH 1048575 /* 2^20 - 1: CAP / DAPD launch grids stay below 2^31 CTAs */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* dlm_status_string(dlm_status s);

@@ -130,6 +130,15 @@ def test_selection_argument_errors(libdlm):
     bad = (fake, fake, ctypes.byref(pp), fake, fake, None, None, None)
     assert libdlm.dlm_dapd_graph_mis(*base, 256, 32, *bad, fake, 1 << 30, None, None) == INVALID
 
+    # batches whose launch grids would not fit are refused before any check of the workspace
+    huge = 1 << 20   # DLM_MAX_BATCH + 1
+    cp = CapParams(0.8, 0.95, -16.0, 256, 0)
+    args = (fake, 1, 100, 100, fake, fake, fake, fake, None, huge, 256, ctypes.byref(cp), fake, fake, None)
+    assert libdlm.dlm_cap_select(*args, fake, 1 << 40, None, None) == INVALID
+    pp = DapdParams(0.01, 0.9, 0.5, 0)
+    big = (fake, 2, huge, 10, 32, 10 * 32 * 512 * 512, 32 * 512 * 512, 512 * 512, 512)
+    assert libdlm.dlm_dapd_graph_mis(*big, 256, 32, *ok_tail, fake, 1 << 40, None, None) == INVALID
+
 
 def test_binding_refuses_cpu_tensors():
     import torch
