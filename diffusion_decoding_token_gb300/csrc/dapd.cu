@@ -1074,9 +1074,11 @@ cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool gra
     const bool tma = encode_attention_map(a, &map);
     const int units = tma ? a.n_layers * a.head_groups : LH;  // work items split over a cluster
     // cluster size over the layer*head range: the register-load kernel wants
-    // about two CTAs per SM; the bulk-copy kernel keeps 64 KB in flight per CTA
-    // and is fastest with fewer, longer CTAs (~1.5 per SM; measured on the
-    // 64 x 32 and 8 x 256 blocks: 33.5 us at split 4, 102 us at split 1)
+    // about two CTAs per SM; the bulk-copy kernel keeps 96 KB in flight per CTA
+    // and is fastest in the step with ~1.5 CTAs per SM (on the 64 x 32 block a
+    // split of 2 reads cold attention 7 % faster alone but makes the step
+    // 2 us slower: in the step the pass fills the row pass's draining wave,
+    // where more CTAs take more of the freed slots)
     int split = tma ? (int)((3LL * num_sms + base) / (2 * base)) : (int)((2LL * num_sms + base - 1) / base);
     split = max(1, min(8, min(split, units)));
     a.split = split;
