@@ -393,7 +393,7 @@ typedef struct dlm_dapd_params {
     float tau_edge;
     float bulk_conf;  /* 0.9 on the page */
     float bulk_frac;  /* 0.5 on the page */
-    int32_t order_mode; /* 0: d~ * conf, 1: d~ (DAPD ablation "排序键") */
+    int32_t order_mode; /* 0: d~ * conf, 1: d~ (DAPD, 消融实验: the sort-key ablation) */
     int32_t preunmask_certain; /* 1: also select every masked position whose
                                   conf is exactly 1.0 in fp32 (DAPD, 关键设计 3,
                                   appendix remark: such a position can be
