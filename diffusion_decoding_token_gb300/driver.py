@@ -231,7 +231,7 @@ class SyntheticDecoder:
 
 class DepCapDecoder:
     """DepCap's block loop over a whole generation (DepCap, "Methodology"):
-    DepGA-Block picks each block's length from the KL shift that the last
+    DepGA-Block picks each block's length from the change in KL that the last
     decoded block caused in the window of future positions, against their
     entropy; CAP-Decoding then unmasks a conflict-free subset of the block
     per step until the block is done.

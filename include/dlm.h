@@ -222,7 +222,7 @@ dlm_status dlm_parallel_certificate(const float* conf, const uint8_t* selected, 
  *
  * DepCap, "Methodology" and "Technical Contribution": over a window of
  * L_window future positions with KL influence I_k and entropy H_k,
- * smooth and locally normalise both, form S_k = I~_k - lambda H~_k, stop
+ * smooth both and normalise them within the window, form S_k = I~_k - lambda H~_k, stop
  * before the first S_k < 0 and clip the length to [L_min, L_window]; a cold
  * start uses L_min.  Readings of the unstated operators:
  *   smooth_w  : centred moving average of odd width (1 = none); at the
@@ -285,7 +285,7 @@ dlm_status dlm_depcap_boundary_ragged(const float* kl, const float* entropy, int
  *   greedy: scan the pool in order, keep a position iff it conflicts with no
  *   kept one.  high_tier_unconditional = 1 keeps every tier member first,
  *   then scans the rest.  Empty pool: the highest-confidence masked position
- *   of the scope ("if no safe set exists").
+ *   of the scope (the page's fallback when nothing is safe to unmask).
  *
  * logits      : the current logit rows (as given to dlm_row_stats), row
  *               b*blk + i, stride row_stride elements; 16-byte alignment is

@@ -201,8 +201,8 @@ void oracle_select_threshold(const double* conf, const uint8_t* masked, int batc
 
 /* ------------------------------------------------------------------------
  * DepGA-Block boundary (DepCap, Methodology and Technical Contribution).
- * I_k, H_k for the k-th future position; "smooth and locally normalize"
- * is read as a centred moving average of odd width w (edges average the
+ * I_k, H_k for the k-th future position; the unspecified smoothing and
+ * local normalisation are read as a centred moving average of odd width w (edges average the
  * neighbours that exist) followed by a window-local normalisation:
  * norm_mode 0 divides by the window mean (floored at 1e-12), 1 rescales to
  * [0,1] by the window min and max, 2 leaves the values as they are.
@@ -277,7 +277,8 @@ void oracle_depcap_boundary(const double* kl, const double* entropy, int batch, 
 
 /* ------------------------------------------------------------------------
  * CAP-Decoding (DepCap, Methodology; defaults from Experiments and the
- * executive summary).  Within the selected block (positions [0, scope)):
+ * executive summary).  Inside the block the boundary rule chose (positions
+ * [0, scope)):
  *   pool  = masked positions with c_i >= tau_low (fp32 test), ordered by
  *           confidence, ties to the lower position; at most p_max kept.
  *           The tau_high tier is the head of this order.
