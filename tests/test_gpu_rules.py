@@ -165,47 +165,40 @@ def test_unit_rules(dlm, name):
 
 
 # -------------------------------------------------------------- pipeline
-@pytest.mark.parametrize("name", synth.ORDER + LITERAL)
-def test_pipeline(dlm, name):
-    w, dw, o = workload(name)
+def check_rules(name, w, o, sel, block_len):
+    """Compare GPU selections (``sel``: rule -> [B][blk] uint8 array;
+    ``block_len``: [B] int array or None) with the oracle's rules on the
+    oracle's statistics: exact where the decisions clear the margins, valid
+    results elsewhere.  Returns (exact, validity-checked) counts."""
     cfg = w.cfg
     B, blk = cfg.batch, cfg.blk
-    st = dlm.new_status()
-    g = gpu_stats(dw, status=st)
-    gconf, glse = g.conf.view(B, blk), g.lse.view(B, blk)
     oconf = o["conf"].reshape(B, blk)
     exact = valid = 0
     if "threshold" in cfg.rules:
-        gs, _ = dlm.select_threshold(gconf, dw.masked, cfg.tau)
         os_, _ = oracle.select_threshold(oconf, w.masked, cfg.tau)
-        gs = gs.cpu().numpy()
         for b in range(B):
             if threshold_margin_ok(oconf[b], w.masked[b], cfg.tau):
-                np.testing.assert_array_equal(gs[b], os_[b])
+                np.testing.assert_array_equal(sel["threshold"][b], os_[b])
                 exact += 1
             else:
                 valid += 1
-    scope_g = scope_o = None
+    scope_o = None
     if "boundary" in cfg.rules:
-        gl, _ = dlm.depcap_boundary(g.kl.view(B, blk), g.entropy.view(B, blk), cfg.lam, cfg.L_min)
         ol, osc = oracle.depcap_boundary(o["kl"].reshape(B, blk), o["entropy"].reshape(B, blk), cfg.lam, cfg.L_min)
-        gl_np = gl.cpu().numpy()
         for b in range(B):
             if boundary_margin_ok(osc[b]):
-                assert gl_np[b] == ol[b]
+                assert block_len[b] == ol[b]
                 exact += 1
             else:
                 valid += 1
         if name.startswith("depcap_window"):
-            scope_g, scope_o = gl, ol
+            scope_o = ol
     if "cap" in cfg.rules:
-        gs, _ = dlm.cap_select(dw.cur, g.argmax.view(B, blk), gconf, glse, dw.masked, cfg.tau_low, cfg.tau_high,
-                               cfg.gamma, cfg.p_max, scope_len=scope_g)
         code = None if cfg.logit_dtype == synth.F32 else cfg.logit_dtype
         am = np.where(o["argmax"] < 0, 0, o["argmax"]).reshape(B, blk)
         r = oracle.cap_select(w.cur, am, oconf, o["lse"].reshape(B, blk), w.masked, cfg.tau_low, cfg.tau_high,
                               cfg.gamma, cfg.p_max, scope_len=scope_o, dtype=code)
-        gs = gs.cpu().numpy()
+        gs = sel["cap"]
         for b in range(B):
             sc = blk if scope_o is None else int(scope_o[b])
             if cap_margin_ok(cfg, oconf[b], w.masked[b], r["D"][b], r["pool"][b], r["pool_n"][b], sc):
@@ -217,11 +210,9 @@ def test_pipeline(dlm, name):
                 assert not pool or greedy_valid(adj, set(np.nonzero(gs[b])[0].tolist()), oconf[b], pool, 1e-4)
                 valid += 1
     if "dapd" in cfg.rules:
-        gs, _ = dlm.dapd_graph_mis(dw.attn, dw.masked, gconf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0,
-                                   dw.block_start)
         code = None if cfg.attn_dtype == synth.F32 else cfg.attn_dtype
         r = oracle.dapd(w.attn, w.masked, oconf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0, dtype=code)
-        gs = gs.cpu().numpy()
+        gs = sel["dapd"]
         for b in range(B):
             if dapd_margin_ok(cfg, oconf[b], w.masked[b], r["s"][b], r["dtilde"][b]):
                 np.testing.assert_array_equal(gs[b], r["selected"][b])
@@ -233,11 +224,76 @@ def test_pipeline(dlm, name):
                     adj = (S > cfg.tau_edge) & ~np.eye(len(nodes), dtype=bool)
                     key = r["dtilde"][b][nodes] * oconf[b][nodes]
                     loc = {int(v): k for k, v in enumerate(nodes)}
-                    sel = {loc[int(v)] for v in np.nonzero(gs[b])[0]}
-                    assert greedy_valid(adj, sel, key, range(len(nodes)), 1e-4)
+                    chosen = {loc[int(v)] for v in np.nonzero(gs[b])[0]}
+                    assert greedy_valid(adj, chosen, key, range(len(nodes)), 1e-4)
                 valid += 1
+    return exact, valid
+
+
+@pytest.mark.parametrize("name", synth.ORDER + LITERAL)
+def test_pipeline(dlm, name):
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    B, blk = cfg.batch, cfg.blk
+    st = dlm.new_status()
+    g = gpu_stats(dw, status=st)
+    gconf, glse = g.conf.view(B, blk), g.lse.view(B, blk)
+    sel, block_len, scope_g = {}, None, None
+    if "threshold" in cfg.rules:
+        sel["threshold"] = dlm.select_threshold(gconf, dw.masked, cfg.tau)[0].cpu().numpy()
+    if "boundary" in cfg.rules:
+        gl, _ = dlm.depcap_boundary(g.kl.view(B, blk), g.entropy.view(B, blk), cfg.lam, cfg.L_min)
+        block_len = gl.cpu().numpy()
+        if name.startswith("depcap_window"):
+            scope_g = gl
+    if "cap" in cfg.rules:
+        sel["cap"] = dlm.cap_select(dw.cur, g.argmax.view(B, blk), gconf, glse, dw.masked, cfg.tau_low,
+                                    cfg.tau_high, cfg.gamma, cfg.p_max, scope_len=scope_g)[0].cpu().numpy()
+    if "dapd" in cfg.rules:
+        sel["dapd"] = dlm.dapd_graph_mis(dw.attn, dw.masked, gconf, cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0,
+                                         dw.block_start)[0].cpu().numpy()
+    exact, valid = check_rules(name, w, o, sel, block_len)
     assert int(st.item()) == 0
     print(f"{name}: {exact} exact, {valid} validity-checked decisions")
+    assert exact >= 3 * valid
+
+
+@pytest.mark.parametrize("name", ["batched", "stress_graph", "depcap_window"])
+def test_bench_launch_configuration_matches_oracle(dlm, name):
+    """The step as the benchmark times it -- one StepPlan with the DAPD
+    attention pass on a side stream from the step's start, the other rules as
+    parallel graph branches, the row pass's tail grid where it applies, steps
+    captured back to back in one CUDA graph with timing events -- at full
+    size, against the oracle."""
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    kw = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
+              gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
+              bulk_frac=cfg.bulk_frac, rules=tuple(cfg.rules), cap_scope_from_boundary=(cfg.name == "depcap_window"),
+              concurrent_dapd=True, dapd_early=True, parallel_rules=True)
+    if "dapd" in cfg.rules:
+        kw.update(attn=dw.attn, block_start=dw.block_start)
+    plan = dlm.StepPlan(dw.cur, dw.prev, dw.masked, row_index=dw.row_index, **kw)
+    _, hi = torch.cuda.Stream.priority_range()
+    main = torch.cuda.Stream(priority=hi)
+    evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+           for _ in range(2)]
+    with torch.cuda.stream(main):
+        plan.run(main)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for e in evs:
+                plan.run(main, events=e)
+        for v in plan.out.values():
+            v[0].fill_(7)
+        g.replay()
+    torch.cuda.synchronize()
+    sel = {k: v[0].cpu().numpy() for k, v in plan.out.items()}
+    block_len = None if plan.block_len is None else plan.block_len.cpu().numpy()
+    exact, valid = check_rules(name, w, o, sel, block_len)
+    assert int(plan.status.item()) == 0
+    assert all(a.elapsed_time(b) > 0 for a, b in evs)
     assert exact >= 3 * valid
 
 
