@@ -364,14 +364,15 @@ def test_boundary_ragged_windows(dlm, w_):
     assert gl[0] == 0
 
 
+@pytest.mark.parametrize("code", [synth.F32, synth.BF16, synth.F16])
 @pytest.mark.parametrize("blk,p_maxes", [(37, (8, 37, 65)), (100, (64, 65, 100))])
-def test_cap_edges(dlm, blk, p_maxes):
+def test_cap_edges(dlm, blk, p_maxes, code):
     """Pool clipping, an empty pool, scope limits, the unconditional tier and
-    a ragged block, on a tiny fp32 case; pools up to 64 take the fused
-    single-CTA kernel, larger ones the three-launch path, and the pool is
-    clipped on both sides of that line."""
+    a ragged block, on small cases in each logit storage type; pools up to 64
+    take the fused single-CTA kernel, larger ones the cluster kernel, and the
+    pool is clipped on both sides of that line."""
     rng = np.random.default_rng(21 + blk)
-    B, V = 4, 300
+    B, V = 4, 304
     z = (rng.standard_normal((B * blk, V)) * 1.0).astype(np.float32)
     tok = rng.integers(0, V, B * blk)
     for r in range(B * blk):
@@ -381,17 +382,20 @@ def test_cap_edges(dlm, blk, p_maxes):
         z[r, tok[r + 1]] = z[r, tok[r]] - 3
         z[r + 1, tok[r]] = z[r + 1, tok[r + 1]] - 3
     z[blk:2 * blk, :] = rng.standard_normal((blk, V)).astype(np.float32)  # sequence 1: no candidate
-    o = oracle.row_stats(z)
+    zs = {synth.F32: lambda a: a, synth.BF16: synth.to_bf16_bits, synth.F16: synth.to_f16_bits}[code](z)
+    dcode = None if code == synth.F32 else code
+    o = oracle.row_stats(zs, dtype=dcode)
     masked = (rng.random((B, blk)) < 0.9).astype(np.uint8)
     scope = np.array([blk, blk, 11, 0], np.int32)
     am = o["argmax"].reshape(B, blk)
     c32, l32 = f32(o["conf"]).reshape(B, blk), f32(o["lse"]).reshape(B, blk)
+    zt = to_torch(zs, code, "cuda")
     for p_max, htu in [(p_maxes[0], False), (p_maxes[1], False), (p_maxes[1], True), (p_maxes[2], True)]:
         st = dlm.new_status()
-        gs, gn = dlm.cap_select(cuda(z), cuda(am), cuda(c32), cuda(l32), cuda(masked), 0.8, 0.95, -16.0, p_max,
+        gs, gn = dlm.cap_select(zt, cuda(am), cuda(c32), cuda(l32), cuda(masked), 0.8, 0.95, -16.0, p_max,
                                 high_tier_unconditional=htu, scope_len=cuda(scope), status=st)
-        r = oracle.cap_select(z, am, c32.astype(np.float64), l32.astype(np.float64), masked, 0.8, 0.95, -16.0,
-                              p_max, high_tier_unconditional=htu, scope_len=scope)
+        r = oracle.cap_select(zs, am, c32.astype(np.float64), l32.astype(np.float64), masked, 0.8, 0.95, -16.0,
+                              p_max, high_tier_unconditional=htu, scope_len=scope, dtype=dcode)
         np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
         np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
         assert bool(int(st.item()) & dlm.DEV_POOL_CLIPPED) == r["clipped"]
