@@ -656,3 +656,69 @@ def test_whole_steps_as_one_graph_match_eager(dlm):
         np.testing.assert_array_equal(eager.out[k][0].cpu().numpy(), graphed.out[k][0].cpu().numpy())
         np.testing.assert_array_equal(eager.out[k][1].cpu().numpy(), graphed.out[k][1].cpu().numpy())
     assert all(a.elapsed_time(b) > 0 for a, b in evs)
+
+
+# ------------------------------------------------------------------ fuzz
+@pytest.mark.parametrize("trial", range(12))
+def test_cap_random_shapes(dlm, trial):
+    """Random block sizes (both kernels), pool caps, masks, scopes and tiers
+    on fp32 logits with planted conflicts: selections, counts and the clip
+    flag equal the oracle's."""
+    rng = np.random.default_rng(500 + trial)
+    blk = int(rng.integers(1, 257))
+    B = int(rng.integers(1, 5))
+    V = int(rng.integers(1, 64)) * 8
+    p_max = int(rng.integers(1, blk + 1)) if rng.random() < 0.5 else blk
+    z = rng.standard_normal((B * blk, V)).astype(np.float32)
+    tok = rng.integers(0, V, B * blk)
+    boosted = rng.random(B * blk) < 0.7
+    z[np.arange(B * blk)[boosted], tok[boosted]] += rng.uniform(6, 14, int(boosted.sum())).astype(np.float32)
+    for r in range(0, B * blk - 1, 4):   # cross-boosted pairs: D near -6, a conflict
+        z[r, tok[r + 1]] = z[r, tok[r]] - 3
+        z[r + 1, tok[r]] = z[r + 1, tok[r + 1]] - 3
+    o = oracle.row_stats(z)
+    masked = (rng.random((B, blk)) < rng.uniform(0.3, 1.0)).astype(np.uint8)
+    scope = rng.integers(0, blk + 1, B).astype(np.int32) if rng.random() < 0.5 else None
+    htu = bool(rng.random() < 0.3)
+    am = o["argmax"].reshape(B, blk)
+    c32, l32 = f32(o["conf"]).reshape(B, blk), f32(o["lse"]).reshape(B, blk)
+    st = dlm.new_status()
+    gs, gn = dlm.cap_select(cuda(z), cuda(am), cuda(c32), cuda(l32), cuda(masked), 0.8, 0.95, -16.0, p_max,
+                            high_tier_unconditional=htu, scope_len=None if scope is None else cuda(scope),
+                            status=st)
+    r = oracle.cap_select(z, am, c32.astype(np.float64), l32.astype(np.float64), masked, 0.8, 0.95, -16.0,
+                          p_max, high_tier_unconditional=htu, scope_len=scope)
+    np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+    np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+    assert bool(int(st.item()) & dlm.DEV_POOL_CLIPPED) == r["clipped"]
+
+
+@pytest.mark.parametrize("trial", range(12))
+def test_dapd_random_shapes(dlm, trial):
+    """Random block sizes (one-CTA and cluster decide), layer/head counts,
+    masks on both sides of the 50 % switch and both key orders, on f16
+    attention (exact graph arithmetic): selections, counts and degrees equal
+    the oracle's."""
+    rng = np.random.default_rng(700 + trial)
+    blk = int(rng.integers(1, 257))
+    B = int(rng.integers(1, 4))
+    L, H = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+    bs = 8 * int(rng.integers(0, 4))
+    N = (bs + blk + 8 + 7) // 8 * 8
+    sub = rng.random((B, L, H, blk, blk)) ** 6 * 0.3
+    sub = (sub / (sub.sum(-1, keepdims=True) + 1.0)).astype(np.float32)
+    sub16 = synth.to_f16_bits(sub)
+    full = torch.zeros((B, L, H, N, N), dtype=torch.float16, device="cuda")
+    full[:, :, :, bs:bs + blk, bs:bs + blk] = to_torch(sub16, synth.F16, "cuda")
+    masked = (rng.random((B, blk)) < rng.uniform(0.2, 1.0)).astype(np.uint8)
+    conf = rng.random((B, blk)).astype(np.float32)
+    om = int(rng.integers(0, 2))
+    deg = torch.full((B, blk), -1, dtype=torch.int32, device="cuda")
+    gs, gn = dlm.dapd_graph_mis(full, cuda(masked), cuda(conf), 0.02, 0.9, 0.5, om, bs, deg_out=deg)
+    r = oracle.dapd(sub16, masked, conf.astype(np.float64), 0.02, 0.9, 0.5, om, dtype=synth.F16)
+    np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+    np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+    for b in range(B):
+        if r["path"][b] == 0:
+            nodes = np.nonzero(masked[b])[0]
+            np.testing.assert_array_equal(deg.cpu().numpy()[b][nodes], r["deg"][b][nodes])
