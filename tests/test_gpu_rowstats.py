@@ -230,3 +230,36 @@ def test_single_grid_flag_same_statistics(dlm):
     np.testing.assert_array_equal(a.argmax.cpu().numpy(), b.argmax.cpu().numpy())
     for k in ("conf", "lse", "entropy", "kl", "lse_prev"):
         assert close(getattr(a, k).cpu().numpy(), getattr(b, k).cpu().numpy(), atol=2e-5, rtol=2e-5).all(), k
+
+
+@pytest.mark.parametrize("trial", range(16))
+def test_row_stats_random_shapes(dlm, trial):
+    """Random row counts (one grid, tail grid, split rows), vocab sizes with
+    ragged tails, padded strides, storage types, with and without the
+    previous rows and a row index: every output within tolerance of the
+    oracle, argmax exact."""
+    rng = np.random.default_rng(900 + trial)
+    rows = int(rng.choice([1, 3, 17, 150, 700, 1300]))
+    V = int(rng.integers(1, 6000)) if rng.random() < 0.7 else int(rng.integers(6000, 40000))
+    stride = (V + 7) // 8 * 8 + 8 * int(rng.integers(0, 3))
+    code = int(rng.choice([synth.F32, synth.BF16, synth.F16]))
+    with_prev = bool(rng.random() < 0.75)
+    x = (rng.standard_normal((rows, stride)) * rng.uniform(0.5, 3.0)).astype(np.float32)
+    hot = rng.integers(0, V, rows)
+    x[np.arange(rows), hot] += rng.uniform(0, 12, rows).astype(np.float32)
+    y = x + (rng.standard_normal((rows, stride)) * 0.3).astype(np.float32)
+    st = {synth.F32: lambda a: a, synth.BF16: synth.to_bf16_bits, synth.F16: synth.to_f16_bits}[code]
+    xs, ys = st(x), st(y)
+    dcode = None if code == synth.F32 else code
+    cur = to_torch(xs, code, "cuda")[:, :V]
+    prev = to_torch(ys, code, "cuda")[:, :V] if with_prev else None
+    if rng.random() < 0.4:   # a gathered subset of the rows, outputs at the row positions
+        sel = np.sort(rng.choice(rows, max(1, rows // 2), replace=False)).astype(np.int32)
+        out = dlm.alloc_row_stats(rows, "cuda", with_prev)
+        g = dlm.row_stats(cur, prev, row_index=torch.from_numpy(sel).cuda(), out=out)
+    else:
+        sel = np.arange(rows)
+        g = dlm.row_stats(cur, prev)
+    o = oracle.row_stats(np.ascontiguousarray(xs[:, :V]), np.ascontiguousarray(ys[:, :V]) if with_prev else None,
+                         dtype=dcode)
+    _compare(g, o, sel, with_prev)
