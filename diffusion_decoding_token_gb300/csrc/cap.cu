@@ -25,7 +25,6 @@ namespace dlm {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kConflictWarps = 8;
 constexpr int kMaxPoolWords = DLM_MAX_BLK / 32;  // p_max <= 256
 
 __device__ __forceinline__ float load_logit(const void* base, int dtype, int64_t i) {
