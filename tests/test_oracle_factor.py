@@ -3,8 +3,6 @@ fixed top-K baseline (Fast-dLLM review: Method appendix variant, Key idea,
 Prior limitations)."""
 import numpy as np
 
-import pytest
-
 
 def test_factor_worked_example(oracle):
     # sorted c: 0.99, 0.97, 0.9, 0.5 (positions 2, 0, 3, 1)
