@@ -565,11 +565,27 @@ def oracle_sample(w, n_seq):
     return time.perf_counter() - t, int(masked.sum())
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """The oracle, as it stands, on repeated passes over a bounded sample of
-    the same workload until about ``budget_s`` seconds of CPU work."""
-    import oracle
-    oracle.build()
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _oracle_rate(w, budget_s):
+    """Decisions per second of the oracle on repeated passes over a bounded
+    sample of the workload, about ``budget_s`` seconds of work; (rate, sample)."""
     dt1, _ = oracle_sample(w, 1)
     n_seq = int(max(1, min(w.cfg.batch, budget_s / max(dt1, 1e-3))))
     total, count, reps = 0.0, 0, 0
@@ -578,9 +594,24 @@ def cpu_baseline(w, budget_s=12.0):
         total += dt
         count += n
         reps += 1
-    return {"value": count / total, "unit": "decisions/s", "cores": oracle.get_threads(), "kind": "oracle",
-            "sample": f"{reps} pass(es) of the full path (stats + four rules) over {n_seq} of {w.cfg.batch} "
-                      f"sequences ({count} decisions) of the same workload, {total:.1f} s"}
+    return count / total, (f"{reps} pass(es) of the full path (stats + four rules) over {n_seq} of "
+                           f"{w.cfg.batch} sequences ({count} decisions) of the same workload, {total:.1f} s")
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The oracle, as it stands, on all host cores and on one thread, each
+    on repeated passes over a bounded sample of the same workload."""
+    import oracle
+    oracle.build()
+    cores = oracle.get_threads()
+    value, sample = _oracle_rate(w, budget_s)
+    oracle.set_threads(1)
+    try:
+        one, sample1 = _oracle_rate(w, budget_s / 4)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": value, "unit": "decisions/s", "cores": cores, "kind": "oracle", "sample": sample,
+            "cpu_model": cpu_model(), "one_thread": {"value": one, "unit": "decisions/s", "sample": sample1}}
 
 
 def run_reference(args, rank, world):
@@ -607,7 +638,7 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload_desc(cfg) + f"; each step a sample of {n_seq} sequences"},
             "cpu_baseline": {"value": value, "unit": "decisions/s", "cores": oracle.get_threads(), "kind": "oracle",
-                             "sample": f"{n_seq} of {cfg.batch} sequences per step"},
+                             "sample": f"{n_seq} of {cfg.batch} sequences per step", "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": "decisions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
