@@ -366,8 +366,8 @@ dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype, int64_t v
  *       position) keeping every node with no kept neighbour.
  *   r <  bulk_frac: select masked positions with conf > bulk_conf; if none,
  *       the highest-confidence masked one.
- * The "last ~30% of layers" choice is the caller's: pass exactly the layers
- * to average.  The per-pair sums are accumulated exactly in fixed point, so
+ * Which layers to average (the page uses roughly the last 30 %) is the
+ * caller's choice: pass exactly those layers.  The per-pair sums are accumulated exactly in fixed point, so
  * the edge test and the key order are exact decisions when every attention
  * value is an f16 in [0, 256) and the sum over layers*heads of each entry
  * stays below 512 (true for softmax rows with layers*heads <= 511); other
