@@ -13,8 +13,10 @@ All work runs in hand-written sm_103a kernels behind the C ABI of
 ``libdlm.so`` (``include/dlm.h``); this package only marshals CUDA tensors.
 """
 from ._binding import (  # noqa: F401
+    DEV_BAD_INDEX,
     DEV_NONFINITE,
     DEV_POOL_CLIPPED,
+    DEV_TIMEOUT,
     DLM_BF16,
     DLM_F16,
     DLM_F32,

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdlm.so")
 
 DLM_F32, DLM_BF16, DLM_F16 = 0, 1, 2
-DEV_NONFINITE, DEV_POOL_CLIPPED = 1, 2
+DEV_NONFINITE, DEV_POOL_CLIPPED, DEV_TIMEOUT, DEV_BAD_INDEX = 1, 2, 4, 8
 MAX_BLK = 256
 
 _DT = {torch.float32: DLM_F32, torch.bfloat16: DLM_BF16, torch.float16: DLM_F16}
@@ -68,7 +68,7 @@ def lib():
         L.dlm_depcap_boundary.argtypes = [P, P, I32, I32, P, ctypes.POINTER(DepcapParams), P, P, P]
         L.dlm_cap_workspace_size.restype = Z
         L.dlm_cap_workspace_size.argtypes = [I32, I32]
-        L.dlm_cap_select.argtypes = [P, ctypes.c_int, I64, I64, P, P, P, P, P, I32, I32,
+        L.dlm_cap_select.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, P, P, P, I32, I32,
                                      ctypes.POINTER(CapParams), P, P, P, P, Z, P, P]
         L.dlm_dapd_workspace_size.restype = Z
         L.dlm_dapd_workspace_size.argtypes = [I32, I32]
@@ -77,7 +77,8 @@ def lib():
         L.dlm_depcap_boundary_ragged.argtypes = [P, P, I32, I32, P, P, ctypes.POINTER(DepcapParams), P, P, P]
         L.dlm_row_stats_partial.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, I64, P, P]
         L.dlm_row_stats_launches.argtypes = [ctypes.c_int, I32, I64, I64, ctypes.c_uint32]
-        L.dlm_row_stats_ex.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, P, P, P, P, P, P, P, ctypes.c_uint32, P]
+        L.dlm_row_stats_ex.argtypes = [P, P, ctypes.c_int, I64, I64, I64, P, I64, P, P, P, P, P, P, P,
+                                       ctypes.c_uint32, P]
         L.dlm_row_stats_launches.restype = I32
         L.dlm_row_stats_merge.argtypes = [P, I32, I64, I64, P, I32, P, P, P, P, P, P, P, P]
         L.dlm_select_topk.argtypes = [P, P, I32, I32, I32, P, P, P]
@@ -150,29 +151,36 @@ def alloc_row_stats(n: int, device, with_prev: bool = True) -> RowStats:
 
 
 ROWS_SINGLE_GRID = 1  # DLM_ROWS_SINGLE_GRID
+ROWS_GATHER = 2       # DLM_ROWS_GATHER
 
 
 def row_stats(cur: torch.Tensor, prev: torch.Tensor | None = None, *, row_index: torch.Tensor | None = None,
-              out: RowStats | None = None, status: torch.Tensor | None = None, single_grid: bool = False) -> RowStats:
-    """dlm_row_stats over the rows of ``cur`` ([rows, V] with unit column stride);
-    ``single_grid`` passes DLM_ROWS_SINGLE_GRID (dlm_row_stats_ex)."""
+              out: RowStats | None = None, status: torch.Tensor | None = None, single_grid: bool = False,
+              gather: bool = False) -> RowStats:
+    """dlm_row_stats_ex over the rows of ``cur`` ([rows, V] with unit column
+    stride), every row index checked against the rows of ``cur``;
+    ``single_grid`` passes DLM_ROWS_SINGLE_GRID, ``gather`` DLM_ROWS_GATHER
+    (results of row_index[r] stored at r)."""
     _need_cuda(cur, prev, row_index)
     if cur.dim() != 2 or cur.stride(1) != 1:
         raise ValueError("cur must be [rows, V] with contiguous rows")
     if prev is not None and (prev.shape != cur.shape or prev.stride() != cur.stride() or prev.dtype != cur.dtype):
         raise ValueError("prev must match cur in shape, strides and dtype")
     rows, V = cur.shape
-    if out is None:
-        out = alloc_row_stats(rows, cur.device, prev is not None)
     n = rows
     if row_index is not None:
         row_index = row_index.to(torch.int32).contiguous()
         n = row_index.numel()
-    _check(lib().dlm_row_stats_ex(_p(cur), _p(prev), _dt(cur), n, V, cur.stride(0), _p(row_index),
+    elif gather:
+        raise ValueError("gather needs a row_index")
+    if out is None:
+        out = alloc_row_stats(n if gather else rows, cur.device, prev is not None)
+    flags = (ROWS_SINGLE_GRID if single_grid else 0) | (ROWS_GATHER if gather else 0)
+    _check(lib().dlm_row_stats_ex(_p(cur), _p(prev), _dt(cur), n, V, cur.stride(0), _p(row_index), rows,
                                   _p(out.argmax), _p(out.conf), _p(out.lse), _p(out.entropy),
                                   _p(out.kl) if prev is not None else None,
                                   _p(out.lse_prev) if prev is not None else None, _p(status),
-                                  ROWS_SINGLE_GRID if single_grid else 0, _stream(cur.device)))
+                                  flags, _stream(cur.device)))
     return out
 
 
@@ -369,12 +377,20 @@ def cap_select(logits: torch.Tensor, argmax: torch.Tensor, conf: torch.Tensor, l
                masked: torch.Tensor, tau_low: float = 0.8, tau_high: float = 0.95, gamma: float = -16.0,
                p_max: int | None = None, high_tier_unconditional: bool = False,
                scope_len: torch.Tensor | None = None, *, D_out=None, workspace=None, status=None,
-               selected=None, n_selected=None):
-    """dlm_cap_select; logits are the [B*blk, V] current rows.  Returns (selected, n_selected)."""
-    _need_cuda(logits, argmax, conf, lse, masked, scope_len, D_out)
+               selected=None, n_selected=None, row_index: torch.Tensor | None = None):
+    """dlm_cap_select; logits are the current rows, [rows, V]: position i of
+    sequence b reads row ``row_index[b*blk + i]`` (default b*blk + i).
+    Returns (selected, n_selected)."""
+    _need_cuda(logits, argmax, conf, lse, masked, scope_len, D_out, row_index)
     B, blk = masked.shape
-    if logits.dim() != 2 or logits.stride(1) != 1 or logits.shape[0] < B * blk:
-        raise ValueError("logits must be [B*blk, V] with contiguous rows")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [rows, V] with contiguous rows")
+    if row_index is None and logits.shape[0] < B * blk:
+        raise ValueError("logits must hold B*blk rows when no row_index is given")
+    if row_index is not None:
+        if row_index.numel() != B * blk:
+            raise ValueError("row_index must hold B*blk entries")
+        row_index = row_index.to(torch.int32).contiguous()
     p_max = blk if p_max is None else int(p_max)
     masked = _u8(masked)
     dev = logits.device
@@ -387,8 +403,9 @@ def cap_select(logits: torch.Tensor, argmax: torch.Tensor, conf: torch.Tensor, l
     if scope_len is not None:
         scope_len = scope_len.to(torch.int32).contiguous()
     prm = CapParams(float(tau_low), float(tau_high), float(gamma), p_max, int(bool(high_tier_unconditional)))
-    _check(lib().dlm_cap_select(_p(logits), _dt(logits), logits.shape[1], logits.stride(0),
-                                _p(argmax.contiguous()), _p(conf.contiguous()), _p(lse.contiguous()), _p(masked),
+    _check(lib().dlm_cap_select(_p(logits), _dt(logits), logits.shape[1], logits.stride(0), _p(row_index),
+                                logits.shape[0], _p(argmax.contiguous()), _p(conf.contiguous()),
+                                _p(lse.contiguous()), _p(masked),
                                 _p(scope_len), B, blk, ctypes.byref(prm), _p(selected), _p(n_selected), _p(D_out),
                                 _p(workspace), workspace.numel(), _p(status), _stream(dev)))
     return selected, n_selected
@@ -525,7 +542,7 @@ class StepPlan:
         st = self.stats
         self._calls = []
         self._calls.append((L.dlm_row_stats_ex, (_p(cur), _p(prev), _dt(cur), n_rows, cur.shape[1], cur.stride(0),
-                                                  _p(row_index),
+                                                  _p(row_index), cur.shape[0],
                                                   _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
                                                   _p(st.lse_prev), _p(self.status), ctypes.c_uint32(self.row_flags))))
         u8 = dict(dtype=torch.uint8, device=dev)
@@ -563,7 +580,8 @@ class StepPlan:
             self._cap = CapParams(float(tau_low), float(tau_high), float(gamma), p_max,
                                   int(bool(high_tier_unconditional)))
             scope = self.block_len if cap_scope_from_boundary else None
-            self._calls.append((L.dlm_cap_select, (_p(cur), _dt(cur), cur.shape[1], cur.stride(0), _p(st.argmax),
+            self._calls.append((L.dlm_cap_select, (_p(cur), _dt(cur), cur.shape[1], cur.stride(0), None,
+                                                    cur.shape[0], _p(st.argmax),
                                                     _p(st.conf), _p(st.lse), _p(self.masked), _p(scope), B, blk,
                                                     ctypes.byref(self._cap), _p(s), _p(n), None, _p(self.cap_ws),
                                                     self.cap_ws.numel(), _p(self.status))))

@@ -85,14 +85,17 @@ static dlm_status row_stats_prepare(dlm::RowStatsArgs& a, const void* cur, const
 }
 
 dlm_status dlm_row_stats_ex(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows, int64_t vocab,
-                            int64_t row_stride, const int32_t* row_index, int32_t* argmax, float* conf, float* lse,
-                            float* entropy, float* kl, float* lse_prev, uint32_t* dev_status, uint32_t flags,
-                            dlm_stream_t stream) {
-    if (flags & ~DLM_ROWS_SINGLE_GRID) return DLM_ERR_INVALID_ARG;
+                            int64_t row_stride, const int32_t* row_index, int64_t n_src_rows, int32_t* argmax,
+                            float* conf, float* lse, float* entropy, float* kl, float* lse_prev,
+                            uint32_t* dev_status, uint32_t flags, dlm_stream_t stream) {
+    if ((flags & ~(DLM_ROWS_SINGLE_GRID | DLM_ROWS_GATHER)) || n_src_rows < 0) return DLM_ERR_INVALID_ARG;
+    if (!row_index && n_src_rows > 0 && n_rows > n_src_rows) return DLM_ERR_INVALID_ARG;
     dlm::RowStatsArgs a{};
     const dlm_status st = row_stats_prepare(a, cur, prev, dtype, n_rows, vocab, row_stride, row_index);
     if (st != DLM_OK || n_rows == 0) return st;
     if (!argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    a.n_src = n_src_rows;
+    a.gather = (flags & DLM_ROWS_GATHER) ? 1 : 0;
     a.argmax = argmax;
     a.conf = conf;
     a.lse = lse;
@@ -108,13 +111,14 @@ dlm_status dlm_row_stats(const void* cur, const void* prev, dlm_dtype dtype, int
                          int64_t vocab, int64_t row_stride, const int32_t* row_index,
                          int32_t* argmax, float* conf, float* lse, float* entropy, float* kl,
                          float* lse_prev, uint32_t* dev_status, dlm_stream_t stream) {
-    return dlm_row_stats_ex(cur, prev, dtype, n_rows, vocab, row_stride, row_index, argmax, conf, lse, entropy, kl,
-                            lse_prev, dev_status, 0u, stream);
+    return dlm_row_stats_ex(cur, prev, dtype, n_rows, vocab, row_stride, row_index, 0, argmax, conf, lse, entropy,
+                            kl, lse_prev, dev_status, 0u, stream);
 }
 
 int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows, int64_t vocab,
                                uint32_t flags) {
-    if (!dtype_ok(dtype) || n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL || (flags & ~DLM_ROWS_SINGLE_GRID))
+    if (!dtype_ok(dtype) || n_rows < 0 || vocab < 1 || vocab > 0x7fffffffLL ||
+        (flags & ~(DLM_ROWS_SINGLE_GRID | DLM_ROWS_GATHER)))
         return -1;
     if (n_rows == 0) return 0;
     dlm::RowStatsArgs a{};
@@ -256,8 +260,8 @@ size_t dlm_cap_workspace_size(int32_t batch, int32_t p_max) {
 }
 
 dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
-                          const int32_t* argmax, const float* conf, const float* lse,
-                          const uint8_t* masked, const int32_t* scope_len, int32_t batch,
+                          const int32_t* row_index, int64_t n_rows, const int32_t* argmax, const float* conf,
+                          const float* lse, const uint8_t* masked, const int32_t* scope_len, int32_t batch,
                           int32_t blk, const dlm_cap_params* params, uint8_t* selected,
                           int32_t* n_selected, float* D_out, void* workspace, size_t ws_bytes,
                           uint32_t* dev_status, dlm_stream_t stream) {
@@ -267,6 +271,7 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
         (params->high_tier_unconditional != 0 && params->high_tier_unconditional != 1))
         return DLM_ERR_INVALID_ARG;
     if (batch == 0) return DLM_OK;
+    if (n_rows < 1 || (!row_index && n_rows < (int64_t)batch * blk)) return DLM_ERR_INVALID_ARG;
     if (!logits || !argmax || !conf || !lse || !masked || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
     if (!workspace || ws_bytes < dlm::cap_workspace_bytes(batch, params->p_max)) return DLM_ERR_WORKSPACE;
     if (!aligned16(workspace)) return DLM_ERR_ALIGNMENT;
@@ -280,6 +285,8 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
     a.lse = lse;
     a.masked = masked;
     a.scope_len = scope_len;
+    a.row_index = row_index;
+    a.n_rows = n_rows;
     a.batch = batch;
     a.blk = blk;
     a.tau_low = params->tau_low;

@@ -8,8 +8,9 @@
 // Both rank the candidates (masked, conf >= tau_low) by (conf desc, position
 // asc) with an all-pairs count, clip to p_max, score every unordered pool
 // pair once (D_ij = log p_i(yhat_j) + log p_j(yhat_i), two scattered logit
-// reads), keep the conflict bits in shared memory and run the greedy scan
-// over the pool order, or the top-confidence fallback on an empty pool.  The
+// reads from the rows the caller's row_index names), keep the conflict bits
+// in shared memory and run the greedy scan over the pool order, or the
+// top-confidence fallback on an empty pool.  The
 // caller's workspace is validated but not used by these kernels (their
 // scratch is shared memory); it stays in the interface as the scratch of any
 // later variant that needs global memory.
@@ -34,14 +35,26 @@ __device__ __forceinline__ float load_logit(const void* base, int dtype, int64_t
 }
 
 // log p_i(token): the logit of `token` in row `row` minus the row's LSE.  A
-// token outside the vocabulary (an argmax of a row that held only NaN) is
-// not read: the value is NaN (never a conflict) and the status word says so.
-__device__ __forceinline__ float logp_at(const CapArgs& a, int64_t row, int token, float lse) {
+// token outside the vocabulary (an argmax of a row that held only NaN) or a
+// row outside the caller's logits is not read: the value is NaN (never a
+// conflict) and the status word says so.
+__device__ __forceinline__ float logp_at(const CapArgs& a, int row, int token, float lse) {
+    if ((unsigned long long)(int64_t)row >= (unsigned long long)a.n_rows) {
+        raise_status(a.dev_status, DLM_DEV_BAD_INDEX);
+        return __int_as_float(0x7fc00000);
+    }
     if ((unsigned)token >= (unsigned long long)a.vocab) {
         raise_status(a.dev_status, DLM_DEV_NONFINITE);
         return __int_as_float(0x7fc00000);
     }
-    return load_logit(a.logits, a.dtype, row * a.row_stride + token) - lse;
+    return load_logit(a.logits, a.dtype, (int64_t)row * a.row_stride + token) - lse;
+}
+
+// Logit row of block position t of sequence b (the caller's row_index, else
+// b*blk + t; within int32 because batch*blk < 2^28).
+__device__ __forceinline__ int row_of(const CapArgs& a, int b, int t) {
+    const int64_t o = (int64_t)b * a.blk + t;
+    return a.row_index ? a.row_index[o] : (int)o;
 }
 
 // The q-th unordered pair (i < j) of n items in row-major order (row i holds
@@ -76,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     __shared__ __align__(16) float s_c[kThreads];
     __shared__ __align__(4) unsigned char s_cand[kThreads];
     __shared__ int s_pool[kFusedMaxPool];
+    __shared__ int s_row[kFusedMaxPool];
     __shared__ int s_y[kFusedMaxPool];
     __shared__ float s_lse[kFusedMaxPool];
     __shared__ uint32_t s_adj[kFusedMaxPool * kFusedWords];
@@ -89,13 +103,14 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
     uint8_t* sel = a.selected + (int64_t)b * a.blk;
 
     // 1. pool: masked in scope with conf >= tau_low, by (conf desc, position asc);
-    // the token and LSE are loaded with the confidence (one round trip)
+    // the token, LSE and logit row are loaded with the confidence (one round trip)
     const bool in = t < a.blk;
     const bool m = t < scope && a.masked[o] != 0;
     const float c = in ? a.conf[o] : 0.f;
     const int y = in ? a.argmax[o] : 0;
     const float l = in ? a.lse[o] : 0.f;
     const bool cand = m && c >= a.tau_low;
+    const int row = cand ? row_of(a, b, t) : 0;
     s_c[t] = c;
     s_cand[t] = cand;
     if (t < kFusedMaxPool * kFusedWords) s_adj[t] = 0u;
@@ -105,6 +120,7 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
         const int rank = rank_desc(s_c, s_cand, (scope + 3) & ~3, c, t);
         if (rank < a.p_max) {
             s_pool[rank] = t;
+            s_row[rank] = row;
             s_y[rank] = y;
             s_lse[rank] = l;
             s_tier[rank] = a.high_tier_unconditional && c >= a.tau_high;
@@ -150,10 +166,8 @@ __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
         }
 #pragma unroll
         for (int u = 0; u < kPairUnroll; ++u) {
-            const int64_t ri = (int64_t)b * a.blk + s_pool[pi[u]];
-            const int64_t rj = (int64_t)b * a.blk + s_pool[pj[u]];
-            z1[u] = logp_at(a, ri, s_y[pj[u]], s_lse[pi[u]]);
-            z2[u] = logp_at(a, rj, s_y[pi[u]], s_lse[pj[u]]);
+            z1[u] = logp_at(a, s_row[pi[u]], s_y[pj[u]], s_lse[pi[u]]);
+            z2[u] = logp_at(a, s_row[pj[u]], s_y[pi[u]], s_lse[pj[u]]);
         }
 #pragma unroll
         for (int u = 0; u < kPairUnroll; ++u) {
@@ -201,6 +215,7 @@ __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
     __shared__ __align__(16) float s_c[kThreads];
     __shared__ __align__(4) unsigned char s_cand[kThreads];
     __shared__ int s_pool[DLM_MAX_BLK];
+    __shared__ int s_row[DLM_MAX_BLK];
     __shared__ int s_y[DLM_MAX_BLK];
     __shared__ float s_lse[DLM_MAX_BLK];
     __shared__ uint32_t s_adj[DLM_MAX_BLK * kMaxPoolWords];
@@ -222,6 +237,7 @@ __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
     const int y = in ? a.argmax[o] : 0;
     const float l = in ? a.lse[o] : 0.f;
     const bool cand = m && c >= a.tau_low;
+    const int row = cand ? row_of(a, b, t) : 0;
     s_c[t] = c;
     s_cand[t] = cand;
     for (int k = t; k < DLM_MAX_BLK * kMaxPoolWords; k += kThreads) s_adj[k] = 0u;
@@ -231,6 +247,7 @@ __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
         const int rank = rank_desc(s_c, s_cand, (scope + 3) & ~3, c, t);
         if (rank < a.p_max) {
             s_pool[rank] = t;
+            s_row[rank] = row;
             s_y[rank] = y;
             s_lse[rank] = l;
             s_tier[rank] = a.high_tier_unconditional && c >= a.tau_high;
@@ -253,9 +270,8 @@ __global__ void __launch_bounds__(kThreads) cap_cluster_kernel(CapArgs a) {
         }
 #pragma unroll
         for (int u = 0; u < kClusterPairUnroll; ++u) {
-            const int64_t ri = (int64_t)b * a.blk + s_pool[pi[u]];
-            const int64_t rj = (int64_t)b * a.blk + s_pool[pj[u]];
-            dv[u] = logp_at(a, ri, s_y[pj[u]], s_lse[pi[u]]) + logp_at(a, rj, s_y[pi[u]], s_lse[pj[u]]);
+            dv[u] = logp_at(a, s_row[pi[u]], s_y[pj[u]], s_lse[pi[u]]) +
+                    logp_at(a, s_row[pj[u]], s_y[pi[u]], s_lse[pj[u]]);
         }
 #pragma unroll
         for (int u = 0; u < kClusterPairUnroll; ++u) {

@@ -48,8 +48,9 @@ cudaError_t scratch_address(void** out) {
 }  // namespace
 
 extern "C" dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype, int64_t vocab,
-                                             int64_t row_stride, const int32_t* argmax, const float* conf,
-                                             const float* lse, const uint8_t* masked, const int32_t* scope_len,
+                                             int64_t row_stride, const int32_t* row_index, int64_t n_rows,
+                                             const int32_t* argmax, const float* conf, const float* lse,
+                                             const uint8_t* masked, const int32_t* scope_len,
                                              int32_t batch, int32_t blk, const dlm_cap_params* params,
                                              uint8_t* selected, int32_t* n_selected, float* D_out,
                                              uint32_t* dev_status, dlm_stream_t stream) {
@@ -59,6 +60,7 @@ extern "C" dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype
         (params->high_tier_unconditional != 0 && params->high_tier_unconditional != 1))
         return DLM_ERR_INVALID_ARG;
     if (batch == 0) return DLM_OK;
+    if (n_rows < 1 || (!row_index && n_rows < (int64_t)batch * blk)) return DLM_ERR_INVALID_ARG;
     if (!logits || !argmax || !conf || !lse || !masked || !selected || !n_selected) return DLM_ERR_INVALID_ARG;
     // the library-owned scratch has a fixed size: larger problems are refused
     if (dlm::cap_workspace_bytes(batch, params->p_max) > kScratchBytes) return DLM_ERR_WORKSPACE;
@@ -74,6 +76,8 @@ extern "C" dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype
     a.lse = lse;
     a.masked = masked;
     a.scope_len = scope_len;
+    a.row_index = row_index;
+    a.n_rows = n_rows;
     a.batch = batch;
     a.blk = blk;
     a.tau_low = params->tau_low;

@@ -28,6 +28,8 @@ struct RowStatsArgs {
     int wait_prior;        // complete only after the previous grid on the stream
     int num_sms;
     int single_grid;       // no tail grid of half rows
+    int64_t n_src;         // rows cur/prev hold: q >= n_src is skipped (0 = unchecked)
+    int gather;            // outputs at r (the gathered order) instead of q
 };
 cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s);
 int row_stats_grids(const RowStatsArgs& a, int dtype);  // kernel launches launch_row_stats makes
@@ -113,6 +115,8 @@ struct CapArgs {
     const float* lse;
     const uint8_t* masked;
     const int32_t* scope_len;
+    const int32_t* row_index;  // [batch*blk] logit row of each block position (nullable)
+    int64_t n_rows;            // rows the logits hold: others are never read
     int batch, blk;
     float tau_low, tau_high, gamma;
     int p_max, high_tier_unconditional;
@@ -159,6 +163,10 @@ struct DapdArgs {
     int row_tile;      // rows per CTA
     // bulk-tensor (TMA) path: box = [box_cols x row_tile rows x box_heads]
     int box_cols, box_heads, head_groups, box_bytes;
+    // >= 0: the first bulk-copy wait of the attention pass gives up after this
+    // many clock cycles (non-blocking probes), a test of the timeout path;
+    // < 0: every wait has the normal ~1 s limit
+    long long first_wait_limit;
 };
 size_t dapd_workspace_bytes(int batch, int blk);
 void dapd_carve(DapdArgs& a, void* ws);

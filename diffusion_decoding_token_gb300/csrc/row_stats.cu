@@ -23,7 +23,7 @@
 // Every quantity is independent of the reference r:
 //   S = sum 2^{a_v}, a_v = (z_v - r) log2 e,  T = sum 2^{a_v} a_v,
 //   K = sum 2^{a_v} (z_v - z'_v):
-//   lse = r + ln S, conf = exp(max z - lse), H = ln S - ln2 T/S,
+//   lse = r + ln S, conf = exp(max z - r) / S, H = ln S - ln2 T/S,
 //   KL = K/S - (r - r') - (ln S - ln S').
 #include <cooperative_groups.h>
 
@@ -299,7 +299,9 @@ __device__ __forceinline__ void write_outputs(const RowStatsArgs& args, const Pa
     // a row of NaN only has no maximum: position 0 (the status flags the row)
     args.argmax[q] = p.idx != 0x7fffffff ? p.idx : 0;
     args.lse[q] = lse;
-    args.conf[q] = expf((p.mx - p.ref) - lnS);
+    // max p = e^{max - ref} / S: max - ref is exact (nearby values) and in
+    // [0, kRebase], so no cancellation against ln S
+    args.conf[q] = expf(p.mx - p.ref) / p.S;
     args.entropy[q] = lnS - kLn2 * (p.T / p.S);
     bool ok = isfinite(p.S) && p.S > 0.f && isfinite(p.T) && isfinite(p.mx) && p.mx > kDegenerate;
     if (PREV) {
@@ -312,7 +314,7 @@ __device__ __forceinline__ void write_outputs(const RowStatsArgs& args, const Pa
 }
 
 template <int DT, bool PREV>
-__global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) {
+__global__ void __launch_bounds__(kThreads, 4) row_stats_kernel(RowStatsArgs args) {  // 4 CTAs per SM
     constexpr int EPV = Fmt<DT>::EPV;
     constexpr int ESZ = Fmt<DT>::ESZ;
     __shared__ Part s_warp[kWarps];
@@ -325,6 +327,13 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) 
     const int64_t r = args.row_base + blockIdx.x / split;
     const int rank = blockIdx.x - (int)((blockIdx.x / split) * split);
     const int64_t q = args.row_index ? (int64_t)args.row_index[r] : r;
+    if (q < 0 || (args.n_src > 0 && q >= args.n_src)) {
+        // a row index outside the caller's rows: nothing is read or written
+        // (every CTA of a cluster sees the same q, so none waits at a barrier)
+        if (rank == 0 && threadIdx.x == 0) raise_status(args.dev_status, DLM_DEV_BAD_INDEX);
+        if (args.wait_prior && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        return;
+    }
     const char* cur_row = static_cast<const char*>(args.cur) + q * args.row_stride * ESZ;
     const char* prev_row = PREV ? static_cast<const char*>(args.prev) + q * args.row_stride * ESZ : nullptr;
     const uint4* cv = reinterpret_cast<const uint4*>(cur_row);
@@ -425,12 +434,16 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(RowStatsArgs args) 
     // whatever follows on the stream sees both grids' results
     if (args.wait_prior && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (rank != 0 || threadIdx.x != 0) return;
+    // where this row's results go, recomputed here so that nothing extra is
+    // live across the streaming loop: q (default) or r (gathered outputs)
+    const int64_t r_out = args.row_base + blockIdx.x / split;
+    const int64_t out = (args.gather || !args.row_index) ? r_out : (int64_t)args.row_index[r_out];
     if (args.partial) {  // a slice of the row: its state, positions made global
         if (p.idx != 0x7fffffff) p.idx += (int)args.vocab_offset;
-        static_cast<Part*>(args.partial)[q] = p;
+        static_cast<Part*>(args.partial)[out] = p;
         return;
     }
-    write_outputs<PREV>(args, p, q);
+    write_outputs<PREV>(args, p, out);
 }
 
 // Merge the partial states of n_shards slices of each row (slice order fixed)
@@ -441,6 +454,10 @@ __global__ void __launch_bounds__(256) row_merge_kernel(RowStatsArgs args, const
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= args.n_rows) return;
     const int64_t q = args.row_index ? (int64_t)args.row_index[r] : r;
+    if (q < 0 || (shard_stride > 0 && q >= shard_stride)) {
+        raise_status(args.dev_status, DLM_DEV_BAD_INDEX);
+        return;
+    }
     Part p = parts[q];
     for (int sh = 1; sh < n_shards; ++sh) part_merge(p, parts[(int64_t)sh * shard_stride + q]);
     write_outputs<PREV>(args, p, q);

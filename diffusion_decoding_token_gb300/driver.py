@@ -240,17 +240,24 @@ class DepCapDecoder:
     sequence b with cursor_b (its first undecoded position):
 
     1. model over all N positions (as in :class:`SyntheticDecoder`);
-    2. gather the window rows cursor_b + k, k < L_max (row b*L_max + k; rows
-       past the end repeat the last position and are never used);
-    3. ``dlm_row_stats`` on the gathered window rows against the same rows
-       of the snapshot -> ŷ, c, LSE, H, KL (row b*L_max + k);
+    2. the window rows are rows b*N + cursor_b + k, k < L_max, of the
+       generation's logits (positions past the end repeat the last one and
+       are never used), named by a row index -- nothing is copied;
+    3. ``dlm_row_stats_ex`` in gather mode over those rows against the same
+       rows of the snapshot -> ŷ, c, LSE, H, KL at window slot b*L_max + k;
     4. sequences without a block: ``dlm_depcap_boundary_ragged`` with
        L_window = min(L_max, N - cursor_b) (cold start for the first block)
        sets the block length, and this forward pass becomes the sequence's
        snapshot, the "before" of the next boundary's KL;
-    5. ``dlm_cap_select`` over the window rows with scope = the block length;
+    5. ``dlm_cap_select`` over the window (the same row index) with scope =
+       the block length;
     6. commit ŷ at the selected positions; a block with nothing masked left
        advances the cursor.
+
+    The stand-in model rewrites only the target and decoy logit of each row
+    (the background never changes), so taking a sequence's snapshot copies
+    those two entries of its rows; the snapshot equals a full copy of the
+    forward pass's logits.
 
     Reading: p_prev of the KL is the model's distribution at the forward pass
     where the last block began (before any of its tokens were committed),
@@ -294,8 +301,6 @@ class DepCapDecoder:
         self.n_blocks = torch.zeros(Bn, **i32)
         self.status = B.new_status(dev)
         self.stats = B.alloc_row_stats(Bn * L_max, dev, with_prev=True)
-        self.win = torch.empty((Bn * L_max, V), **f32)         # window rows of this forward pass
-        self.win_prev = torch.empty((Bn * L_max, V), **f32)    # the same rows of the snapshot
         self.new_len = torch.zeros(Bn, **i32)
         self.score = torch.zeros((Bn, L_max), **f32)
         self.sel = torch.zeros((Bn, L_max), dtype=torch.uint8, device=dev)
@@ -323,9 +328,8 @@ class DepCapDecoder:
         pos = (self.cursor[:, None] + self.k[None, :]).clamp(max=N - 1)               # [B, L_max]
         row_index = (self.seq[:, None] * N + pos).reshape(-1).to(torch.int32)
         window_len = (N - self.cursor).clamp(min=0, max=Lm)
-        torch.index_select(self.logits, 0, row_index, out=self.win)
-        torch.index_select(self.snapshot, 0, row_index, out=self.win_prev)
-        st = B.row_stats(self.win, self.win_prev, out=self.stats, status=self.status)
+        st = B.row_stats(self.logits, self.snapshot, row_index=row_index, gather=True, out=self.stats,
+                         status=self.status)
         need = active & (self.blen == 0)
         B.depcap_boundary(st.kl.view(Bn, Lm), st.entropy.view(Bn, Lm), p["lam"], p["L_min"], p["smooth_w"],
                           p["norm_mode"], cold_start=self.cold, window_len=window_len, block_len=self.new_len,
@@ -333,13 +337,15 @@ class DepCapDecoder:
         self.blen.copy_(torch.where(need, self.new_len, self.blen))
         self.n_blocks += need.to(torch.int32)
         self.cold.mul_((~need).to(torch.uint8))
-        needv = need.repeat_interleave(N)[:, None]
-        self.snapshot.copy_(torch.where(needv, self.logits, self.snapshot))
+        needv = need.repeat_interleave(N)
+        for tok in (self.target, self.decoy):
+            now = self.logits[self.rows, tok]
+            self.snapshot[self.rows, tok] = torch.where(needv, now, self.snapshot[self.rows, tok])
         in_block = self.k[None, :] < self.blen[:, None]
         mwin = (torch.gather(self.masked, 1, pos.to(torch.int64)) * in_block.to(torch.uint8)).contiguous()
-        B.cap_select(self.win, st.argmax.view(Bn, Lm), st.conf.view(Bn, Lm), st.lse.view(Bn, Lm), mwin,
+        B.cap_select(self.logits, st.argmax.view(Bn, Lm), st.conf.view(Bn, Lm), st.lse.view(Bn, Lm), mwin,
                      p["tau_low"], p["tau_high"], p["gamma"], Lm, scope_len=self.blen, workspace=self.cap_ws,
-                     status=self.status, selected=self.sel, n_selected=self.nsel)
+                     status=self.status, selected=self.sel, n_selected=self.nsel, row_index=row_index)
         if self.trace is not None:
             self.trace.append(dict(cursor=self.cursor.cpu().numpy(), need=need.cpu().numpy(),
                                    blen=self.blen.cpu().numpy(), sel=self.sel.cpu().numpy(),

@@ -60,6 +60,9 @@ typedef enum dlm_dtype { DLM_F32 = 0, DLM_BF16 = 1, DLM_F16 = 2 } dlm_dtype;
 #define DLM_DEV_POOL_CLIPPED 2u /* a CAP pool had more than p_max candidates    */
 #define DLM_DEV_TIMEOUT 4u      /* a kernel's bounded wait for its own copies gave
                                    up (~1 s); that call's outputs are unspecified */
+#define DLM_DEV_BAD_INDEX 8u    /* a row index outside [0, rows) was skipped: that
+                                   row was neither read nor written (row pass), or
+                                   its pairs scored NaN (CAP) */
 
 /* Maximum block size accepted by the selection calls. */
 #define DLM_MAX_BLK 256
@@ -95,7 +98,9 @@ int dlm_version(void);
  * row_index   : nullable int32[n_rows]; row r processed is q = row_index[r]
  *               (else q = r).  Results are stored at index q, so the output
  *               arrays must hold max(q)+1 entries; entries of rows not
- *               processed are left unchanged.
+ *               processed are left unchanged.  An entry q < 0 is skipped (no
+ *               read, no write) and sets DLM_DEV_BAD_INDEX; the upper bound
+ *               is checked only by dlm_row_stats_ex (n_src_rows).
  * argmax      : int32 output (a row holding only NaN gets 0); conf, lse,
  *               entropy: float outputs (required).
  * kl, lse_prev: float outputs, nullable (ignored when prev is NULL).
@@ -118,19 +123,30 @@ int32_t dlm_row_stats_launches(dlm_dtype dtype, int32_t has_prev, int64_t n_rows
                                uint32_t flags);
 
 /*
- * dlm_row_stats_ex -- dlm_row_stats with launch flags (same outputs):
+ * dlm_row_stats_ex -- dlm_row_stats with a source-row bound and launch flags
+ * (same definitions):
+ *   n_src_rows            rows that cur and prev hold (0 = not checked).  With
+ *                         row_index, an entry q >= n_src_rows is skipped like
+ *                         a negative one (DLM_DEV_BAD_INDEX); without it,
+ *                         n_rows > n_src_rows is DLM_ERR_INVALID_ARG.
  *   DLM_ROWS_SINGLE_GRID  never run the rows past whole waves as a second grid
  *                         of half rows.  The second grid fills the first one's
  *                         draining wave; when another kernel is meant to take
  *                         those slots (a lower-priority stream started with
  *                         the pass), one grid leaves them to it.
+ *   DLM_ROWS_GATHER       store row r's results at index r instead of
+ *                         q = row_index[r]: the outputs are [n_rows] arrays
+ *                         of the gathered rows (e.g. a window of rows
+ *                         cursor_b + k of a longer generation, in window
+ *                         order).  A skipped row leaves its outputs unchanged.
  */
 #define DLM_ROWS_SINGLE_GRID 1u
+#define DLM_ROWS_GATHER 2u
 
 dlm_status dlm_row_stats_ex(const void* cur, const void* prev, dlm_dtype dtype, int64_t n_rows, int64_t vocab,
-                            int64_t row_stride, const int32_t* row_index, int32_t* argmax, float* conf, float* lse,
-                            float* entropy, float* kl, float* lse_prev, uint32_t* dev_status, uint32_t flags,
-                            dlm_stream_t stream);
+                            int64_t row_stride, const int32_t* row_index, int64_t n_src_rows, int32_t* argmax,
+                            float* conf, float* lse, float* entropy, float* kl, float* lse_prev,
+                            uint32_t* dev_status, uint32_t flags, dlm_stream_t stream);
 
 /*
  * dlm_row_stats_partial / dlm_row_stats_merge -- dlm_row_stats over a row
@@ -148,7 +164,8 @@ dlm_status dlm_row_stats_ex(const void* cur, const void* prev, dlm_dtype dtype, 
  * needs.  Alignment, row_index and dtype rules are those of dlm_row_stats (the
  * slice's first element must be 16-byte aligned); a slice without a finite
  * maximum is allowed (it contributes nothing), and the merge raises
- * DLM_DEV_NONFINITE as dlm_row_stats does.  has_prev in the merge says whether
+ * DLM_DEV_NONFINITE as dlm_row_stats does.  In the merge, a row index outside
+ * [0, shard_stride) is skipped and sets DLM_DEV_BAD_INDEX.  has_prev in the merge says whether
  * the partial states were computed with prev (kl / lse_prev outputs).
  */
 typedef struct dlm_row_partial {
@@ -287,9 +304,17 @@ dlm_status dlm_depcap_boundary_ragged(const float* kl, const float* entropy, int
  *   then scans the rest.  Empty pool: the highest-confidence masked position
  *   of the scope (the page's fallback when nothing is safe to unmask).
  *
- * logits      : the current logit rows (as given to dlm_row_stats), row
- *               b*blk + i, stride row_stride elements; 16-byte alignment is
- *               not required (scattered 2-byte reads).
+ * logits      : the current logit rows (as given to dlm_row_stats), stride
+ *               row_stride elements; 16-byte alignment is not required
+ *               (scattered 2-byte reads).
+ * row_index   : nullable int32 [batch][blk]: position i of sequence b reads
+ *               logit row row_index[b*blk + i] (NULL: row b*blk + i), so the
+ *               block can be a window of a longer generation (rows
+ *               cursor_b + k) without copying its rows.  A pool member whose
+ *               row lies outside [0, n_rows) is not read: its pairs score NaN
+ *               (no conflict) and DLM_DEV_BAD_INDEX is set.
+ * n_rows      : number of rows the logits array holds, >= 1; without
+ *               row_index it must be at least batch*blk.
  * argmax, conf, lse : [batch][blk] from dlm_row_stats.  A token outside
  *                     [0, vocab) is never read from the logits: its pairs
  *                     score NaN (no conflict) and DLM_DEV_NONFINITE is set.
@@ -316,7 +341,8 @@ typedef struct dlm_cap_params {
 size_t dlm_cap_workspace_size(int32_t batch, int32_t p_max);
 
 dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
-                          const int32_t* argmax, const float* conf, const float* lse,
+                          const int32_t* row_index, int64_t n_rows, const int32_t* argmax, const float* conf,
+                          const float* lse,
                           const uint8_t* masked, const int32_t* scope_len, int32_t batch,
                           int32_t blk, const dlm_cap_params* params, uint8_t* selected,
                           int32_t* n_selected, float* D_out, void* workspace, size_t ws_bytes,
@@ -348,7 +374,8 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
 #define DLM_CAP_NOALLOC_MAX_BYTES (1u << 20)
 
 dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
-                                  const int32_t* argmax, const float* conf, const float* lse,
+                                  const int32_t* row_index, int64_t n_rows, const int32_t* argmax,
+                                  const float* conf, const float* lse,
                                   const uint8_t* masked, const int32_t* scope_len, int32_t batch,
                                   int32_t blk, const dlm_cap_params* params, uint8_t* selected,
                                   int32_t* n_selected, float* D_out, uint32_t* dev_status,

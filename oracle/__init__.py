@@ -51,7 +51,7 @@ def _load():
             lib.oracle_row_stats.argtypes = [_P, _P, _I32, _I64, _I64, _I64, _P, _P, _P, _P, _P, _P, _P]
             lib.oracle_select_threshold.argtypes = [_P, _P, _I32, _I32, _F, _P, _P]
             lib.oracle_depcap_boundary.argtypes = [_P, _P, _I32, _I32, _P, _P, _F, _I32, _I32, _I32, _P, _P]
-            lib.oracle_cap_select.argtypes = [_P, _I32, _I64, _P, _P, _P, _P, _P, _I32, _I32,
+            lib.oracle_cap_select.argtypes = [_P, _I32, _I64, _P, _P, _P, _P, _P, _P, _I32, _I32,
                                               _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P]
             lib.oracle_revocable_step.argtypes = [_P, _P, _P, _P, _I32, _I32, _I32, _F, _F, _I32, _F, _F, _F,
                                                   _F, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
@@ -157,8 +157,9 @@ def depcap_boundary(kl, entropy, lam, L_min, smooth_w=1, norm_mode=0, cold_start
 
 
 def cap_select(logits, argmax, conf, lse, masked, tau_low, tau_high, gamma, p_max,
-               high_tier_unconditional=False, scope_len=None, dtype=None):
-    """CAP-Decoding (DepCap, Methodology).  ``logits`` is [B*blk, V] (row b*blk+i).
+               high_tier_unconditional=False, scope_len=None, dtype=None, row_index=None):
+    """CAP-Decoding (DepCap, Methodology).  ``logits`` is [rows, V]; position
+    i of sequence b reads row ``row_index[b*blk + i]`` (default b*blk + i).
 
     Returns dict(selected, n_selected, D, pool, pool_n, clipped)."""
     lib = _load()
@@ -170,12 +171,18 @@ def cap_select(logits, argmax, conf, lse, masked, tau_low, tau_high, gamma, p_ma
     conf = np.ascontiguousarray(conf, dtype=np.float64).reshape(B * blk)
     lse = np.ascontiguousarray(lse, dtype=np.float64).reshape(B * blk)
     sl = None if scope_len is None else np.ascontiguousarray(scope_len, dtype=np.int32)
+    ri = None
+    if row_index is not None:
+        ri = np.ascontiguousarray(row_index, dtype=np.int32).reshape(B * blk)
+        assert ri.min() >= 0 and ri.max() < logits.shape[0]
+    else:
+        assert logits.shape[0] >= B * blk
     sel = np.zeros((B, blk), np.uint8)
     n = np.zeros(B, np.int32)
     D = np.zeros((B, blk, blk))
     pool = np.zeros((B, blk), np.int32)
     pool_n = np.zeros(B, np.int32)
-    clipped = lib.oracle_cap_select(_ptr(logits), code, logits.shape[1], _ptr(argmax), _ptr(conf),
+    clipped = lib.oracle_cap_select(_ptr(logits), code, logits.shape[1], _ptr(ri), _ptr(argmax), _ptr(conf),
                                     _ptr(lse), _ptr(masked), _ptr(sl), B, blk, float(tau_low),
                                     float(tau_high), float(gamma), int(p_max),
                                     int(bool(high_tier_unconditional)), _ptr(sel), _ptr(n), _ptr(D),

@@ -290,7 +290,9 @@ void oracle_depcap_boundary(const double* kl, const double* entropy, int batch, 
  *   no pool -> the highest-confidence masked position of the scope.
  * Outputs the selection, the pool (in order) and D over pool pairs
  * (D[i][j] at block positions; NaN elsewhere).  Returns 1 when the pool was
- * clipped at p_max.
+ * clipped at p_max.  Position i of sequence b reads logit row
+ * row_index[b*blk + i] when row_index is given (the block as a window of a
+ * longer generation), else row b*blk + i.
  * ------------------------------------------------------------------------ */
 static int conf_before(const double* c, int a, int b) {
     float ca = (float)c[a], cb = (float)c[b];
@@ -298,7 +300,7 @@ static int conf_before(const double* c, int a, int b) {
     return a < b;
 }
 
-int oracle_cap_select(const void* logits, int dtype, int64_t row_stride,
+int oracle_cap_select(const void* logits, int dtype, int64_t row_stride, const int32_t* row_index,
                       const int32_t* argmax, const double* conf, const double* lse,
                       const uint8_t* masked, const int32_t* scope_len, int batch, int blk,
                       float tau_low, float tau_high, float gamma, int p_max,
@@ -345,11 +347,11 @@ int oracle_cap_select(const void* logits, int dtype, int64_t row_stride,
         uint8_t* conf_mat = (uint8_t*)calloc((size_t)n * n, 1);
         for (int a = 0; a < n; ++a) {
             int i = pool[a];
-            int64_t ri = (base + i) * row_stride;
+            int64_t ri = (row_index ? (int64_t)row_index[base + i] : base + i) * row_stride;
             for (int e = 0; e < n; ++e) {
                 if (e == a) continue;
                 int j = pool[e];
-                int64_t rj = (base + j) * row_stride;
+                int64_t rj = (row_index ? (int64_t)row_index[base + j] : base + j) * row_stride;
                 double lpi = load_elem(logits, dtype, ri + argmax[base + j]) - lse[base + i];
                 double lpj = load_elem(logits, dtype, rj + argmax[base + i]) - lse[base + j];
                 double d = lpi + lpj;

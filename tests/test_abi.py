@@ -85,7 +85,15 @@ def test_selection_argument_errors(libdlm):
     assert libdlm.dlm_row_stats_launches(7, 1, 10, 1000, 0) == -1
     assert libdlm.dlm_row_stats_launches(1, 1, 10, 0, 0) == -1
     assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000, 0) in (1, 2)
-    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000, 2) == -1   # unknown flag
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000, 4) == -1   # unknown flag
+    assert libdlm.dlm_row_stats_launches(1, 1, 10, 1000, 2) in (1, 2)  # gathered outputs
+
+    # the source-row bound: negative, or smaller than the rows read without a row index
+    ex = libdlm.dlm_row_stats_ex
+    outs = [fake] * 4
+    assert ex(fake, None, 1, 4, 16, 16, None, -1, *outs, None, None, None, 0, None) == INVALID
+    assert ex(fake, None, 1, 4, 16, 16, None, 3, *outs, None, None, None, 0, None) == INVALID
+    assert ex(fake, None, 1, 4, 16, 16, None, 4, *outs, None, None, None, 8, None) == INVALID  # unknown flag
     assert libdlm.dlm_row_stats_launches(1, 1, 10 ** 6, 152064, 1) == 1  # single grid
 
     from diffusion_decoding_token_gb300._binding import CapParams, DapdParams, DepcapParams
@@ -112,12 +120,17 @@ def test_selection_argument_errors(libdlm):
     assert libdlm.dlm_revocable_step(fake, fake, None, None, 0, 32, 0, ctypes.byref(rp), *state) == 0
 
     cp = CapParams(0.8, 0.95, -16.0, 32, 0)
-    args = (fake, 1, 100, 100, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
+    args = (fake, 1, 100, 100, None, 64, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
     assert libdlm.dlm_cap_select(*args, None, 0, None, None) == WS
     assert libdlm.dlm_cap_select(*args, fake, 16, None, None) == WS
     assert libdlm.dlm_cap_select(*args, P(0x10004), 1 << 20, None, None) == ALIGN
+    # the logits must hold every row read: batch*blk without a row index, at least one with one
+    short = (fake, 1, 100, 100, None, 63, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
+    assert libdlm.dlm_cap_select(*short, fake, 1 << 20, None, None) == INVALID
+    none = (fake, 1, 100, 100, fake, 0, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
+    assert libdlm.dlm_cap_select(*none, fake, 1 << 20, None, None) == INVALID
     cp = CapParams(0.8, 0.95, -16.0, 300, 0)
-    args = (fake, 1, 100, 100, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
+    args = (fake, 1, 100, 100, None, 64, fake, fake, fake, fake, None, 2, 32, ctypes.byref(cp), fake, fake, None)
     assert libdlm.dlm_cap_select(*args, fake, 1 << 20, None, None) == INVALID
 
     pp = DapdParams(0.01, 0.9, 0.5, 0)
@@ -133,7 +146,8 @@ def test_selection_argument_errors(libdlm):
     # batches whose launch grids would not fit are refused before any check of the workspace
     huge = 1 << 20   # DLM_MAX_BATCH + 1
     cp = CapParams(0.8, 0.95, -16.0, 256, 0)
-    args = (fake, 1, 100, 100, fake, fake, fake, fake, None, huge, 256, ctypes.byref(cp), fake, fake, None)
+    args = (fake, 1, 100, 100, None, 1 << 40, fake, fake, fake, fake, None, huge, 256, ctypes.byref(cp), fake, fake,
+            None)
     assert libdlm.dlm_cap_select(*args, fake, 1 << 40, None, None) == INVALID
     pp = DapdParams(0.01, 0.9, 0.5, 0)
     big = (fake, 2, huge, 10, 32, 10 * 32 * 512 * 512, 32 * 512 * 512, 512 * 512, 512)

@@ -263,3 +263,56 @@ def test_row_stats_random_shapes(dlm, trial):
     o = oracle.row_stats(np.ascontiguousarray(xs[:, :V]), np.ascontiguousarray(ys[:, :V]) if with_prev else None,
                          dtype=dcode)
     _compare(g, o, sel, with_prev)
+
+
+@pytest.mark.parametrize("gather", [False, True])
+@pytest.mark.parametrize("rows,V", [(6, 126464), (700, 8192)])
+def test_row_index_bounds_and_gather(dlm, rows, V, gather):
+    """Row indices outside [0, n_src) -- negative, or past the rows the
+    arrays hold -- are skipped: nothing is read or written for them and
+    DLM_DEV_BAD_INDEX is set, on a cluster-split launch (6 rows) and on the
+    tail grid of half rows (700 rows, bad entries among the last ones).  The
+    other rows match the oracle, stored at q (default) or at r (gather)."""
+    rng = np.random.default_rng(rows + int(gather))
+    n_src = rows + 9
+    x = (rng.standard_normal((n_src, V)) * 2).astype(np.float32)
+    y = x + (rng.standard_normal((n_src, V)) * 0.3).astype(np.float32)
+    xs, ys = synth.to_bf16_bits(x), synth.to_bf16_bits(y)
+    ri = rng.permutation(n_src)[:rows].astype(np.int32)
+    bad = [1, rows - 1, rows - 3]
+    ri[bad] = [-3, n_src + 7, n_src]
+    good = np.setdiff1d(np.arange(rows), bad)
+    n_out = rows if gather else n_src
+    out = dlm.RowStats(*[torch.full((n_out,), -5, dtype=dt, device="cuda") for dt in
+                         (torch.int32, torch.float32, torch.float32, torch.float32, torch.float32, torch.float32)])
+    st = dlm.new_status()
+    g = dlm.row_stats(to_torch(xs, synth.BF16, "cuda"), to_torch(ys, synth.BF16, "cuda"),
+                      row_index=torch.from_numpy(ri).cuda(), out=out, status=st, gather=gather)
+    torch.cuda.synchronize()
+    assert int(st.item()) == dlm.DEV_BAD_INDEX
+    o = oracle.row_stats(xs, ys, dtype=synth.BF16, row_index=ri[good], n_out=n_src)
+    if gather:   # outputs in gathered order: slot r holds row ri[r]
+        o = {k: v[np.where(np.isin(np.arange(rows), good), ri, 0)] for k, v in o.items()}
+        _compare(g, o, good)
+        untouched = np.array(bad)
+    else:
+        _compare(g, o, ri[good])
+        untouched = np.setdiff1d(np.arange(n_src), ri[good])
+    assert (g.lse.cpu().numpy()[untouched] == -5).all() and (g.argmax.cpu().numpy()[untouched] == -5).all()
+
+
+def test_merge_skips_row_indices_outside_the_partials(dlm):
+    x = np.random.default_rng(8).standard_normal((5, 64)).astype(np.float32)
+    t = to_torch(x, synth.F32, "cuda")
+    parts = torch.stack([dlm.row_stats_partial(t[:, a:a + 32], vocab_offset=a) for a in (0, 32)]).contiguous()
+    ri = torch.tensor([4, -1, 5, 0], dtype=torch.int32, device="cuda")      # 5 rows of partials: 5 is past them
+    out = dlm.RowStats(*[torch.full((8,), -5, dtype=dt, device="cuda") for dt in
+                         (torch.int32, torch.float32, torch.float32, torch.float32, torch.float32, torch.float32)])
+    st = dlm.new_status()
+    g = dlm.row_stats_merge(parts, False, row_index=ri, out=out, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == dlm.DEV_BAD_INDEX
+    o = oracle.row_stats(x[[4, 0]])
+    np.testing.assert_array_equal(g.argmax.cpu().numpy()[[4, 0]], o["argmax"])
+    assert close(g.lse.cpu().numpy()[[4, 0]], o["lse"]).all()
+    assert (g.lse.cpu().numpy()[[1, 2, 3, 5, 6, 7]] == -5).all()

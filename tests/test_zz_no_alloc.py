@@ -28,7 +28,8 @@ def _api():
     P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
     f = L.dlm_cap_select_noalloc
     f.restype = ctypes.c_int
-    f.argtypes = [P, ctypes.c_int, I64, I64, P, P, P, P, P, I32, I32, ctypes.POINTER(CapParams), P, P, P, P, P]
+    f.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, P, P, P, I32, I32, ctypes.POINTER(CapParams), P, P, P,
+                  P, P]
     return dlm, L, CapParams
 
 
@@ -55,11 +56,13 @@ def _both(dlm, L, CapParams, cfg, dw, tau_low):
         status = dlm.new_status()
         if name == "workspace":
             ws = dlm.cap_workspace(B, cfg.p_max, "cuda")
-            rc = L.dlm_cap_select(_ptr(dw.cur), dlm.DLM_BF16, dw.cur.shape[1], dw.cur.stride(0), _ptr(am),
+            rc = L.dlm_cap_select(_ptr(dw.cur), dlm.DLM_BF16, dw.cur.shape[1], dw.cur.stride(0), None,
+                                  dw.cur.shape[0], _ptr(am),
                                   _ptr(conf), _ptr(lse), _ptr(dw.masked), None, B, blk, ctypes.byref(prm),
                                   _ptr(sel), _ptr(n), _ptr(D), _ptr(ws), ws.numel(), _ptr(status), stream)
         else:
-            rc = L.dlm_cap_select_noalloc(_ptr(dw.cur), dlm.DLM_BF16, dw.cur.shape[1], dw.cur.stride(0), _ptr(am),
+            rc = L.dlm_cap_select_noalloc(_ptr(dw.cur), dlm.DLM_BF16, dw.cur.shape[1], dw.cur.stride(0), None,
+                                          dw.cur.shape[0], _ptr(am),
                                           _ptr(conf), _ptr(lse), _ptr(dw.masked), None, B, blk, ctypes.byref(prm),
                                           _ptr(sel), _ptr(n), _ptr(D), _ptr(status), stream)
         assert rc == 0, L.dlm_status_string(rc)
@@ -93,6 +96,6 @@ def test_noalloc_refuses_problems_beyond_its_scratch():
     assert L.dlm_cap_workspace_size(B, p_max) > cap_bytes
     prm = CapParams(0.8, 0.95, -16.0, p_max, 0)
     fake = ctypes.c_void_p(0x10000)
-    rc = L.dlm_cap_select_noalloc(fake, dlm.DLM_BF16, 1024, 1024, fake, fake, fake, fake, None, B, 256,
+    rc = L.dlm_cap_select_noalloc(fake, dlm.DLM_BF16, 1024, 1024, None, B * 256, fake, fake, fake, fake, None, B, 256,
                                   ctypes.byref(prm), fake, fake, None, None, None)
     assert rc == 4  # DLM_ERR_WORKSPACE, before anything is launched
