@@ -31,6 +31,7 @@
 #include <cooperative_groups.h>
 #include <cuda.h>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -318,6 +319,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
     extern __shared__ __align__(128) unsigned char s_ring[];
     float* const s_red = reinterpret_cast<float*>(s_ring);
     __shared__ __align__(8) uint64_t s_full[kStages];
+    __shared__ int s_timed_out;  // read by the cluster's rank 0 before it stores the sums
 
     const int split = a.split;
     const int g = blockIdx.x % split;
@@ -365,7 +367,9 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
     for (int j = 0; j < n; ++j) {
         const int stage = j % kStages;
         const uint32_t parity = (uint32_t)((j / kStages) & 1);
-        const int late = !mbar_wait_bounded(&s_full[stage], parity, kWaitLimit);
+        const int late = (j == 0 && a.first_wait_limit >= 0)
+                             ? !mbar_wait_bounded_probe(&s_full[stage], parity, a.first_wait_limit)
+                             : !mbar_wait_bounded(&s_full[stage], parity, kWaitLimit);
         if (__syncthreads_or(late)) {
             timed_out = 1;
             j_stop = j;
@@ -384,14 +388,16 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
         if (t == 0 && j + kStages < n) issue(j + kStages, stage);
     }
     if (timed_out) {
-        // give the copies already issued a bounded chance to land before the
-        // shared memory they target is released, then report and stop
+        // wait (with the full limit) for the copies already issued to land
+        // before the shared memory they target is reused, then report; the
+        // sums of this tile are not stored
         if (t == 0) {
             for (int j = j_stop; j < min(n, j_stop + kStages); ++j)
                 mbar_wait_bounded(&s_full[j % kStages], (uint32_t)((j / kStages) & 1), kWaitLimit);
             raise_status(a.dev_status, DLM_DEV_TIMEOUT);
         }
     }
+    if (t == 0) s_timed_out = timed_out;
     __syncthreads();  // every read of the ring is done before it is reused
 
     // partial sums, component-major: s_red[k * kThreads + thread], so stores
@@ -425,6 +431,8 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
             for (int k = 0; k < 2 * EPV; ++k) s_red[k * kThreads + t] = acc[k];
         }
         cluster.sync();
+        if (g == 0)  // a rank that gave up waiting leaves the tile's sums incomplete: none is stored
+            for (int r = 1; r < split; ++r) timed_out |= *cluster.map_shared_rank(&s_timed_out, r);
         if (g == 0 && active && grp == 0) {
             for (int r = 1; r < split; ++r) {
                 const float* o = cluster.map_shared_rank(s_red, r);
@@ -1063,7 +1071,12 @@ void dapd_carve(DapdArgs& a, void* ws) {
     a.hdr = reinterpret_cast<long long*>(p);
 }
 
+// Test hook: a first-wait limit (clock cycles) for the next attention passes
+// of this process, < 0 for none.  Exported without a declaration in dlm.h.
+std::atomic<long long> g_test_first_wait_limit{-1};
+
 cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel) {
+    a.first_wait_limit = g_test_first_wait_limit.load(std::memory_order_relaxed);
     const int epv = a.dtype == DLM_F32 ? 4 : 8;
     const int vpr = (a.blk + epv - 1) / epv;
     a.row_tile = max(1, min(a.blk, kThreads / vpr));
@@ -1127,3 +1140,11 @@ cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {
 }
 
 }  // namespace dlm
+
+// Test-only entry (not declared in dlm.h): the first bulk-copy wait of every
+// later attention pass gives up after `cycles` clock cycles of non-blocking
+// probes and takes the timeout path (the copies in flight are still waited
+// for, with the normal limit); cycles < 0 restores the normal limit.
+extern "C" void dlm_test_set_first_wait_limit(long long cycles) {
+    dlm::g_test_first_wait_limit.store(cycles < 0 ? -1 : cycles, std::memory_order_relaxed);
+}
