@@ -319,9 +319,12 @@ class DecodeConfig:
     tau_edge: float = 0.05
 
 
-def decode_problem(cfg: DecodeConfig, seed: int) -> dict:
-    """Static inputs of one multi-step decoding problem (numpy arrays)."""
+def decode_problem(cfg: DecodeConfig, seed: int, attempts=None) -> dict:
+    """Static inputs of one multi-step decoding problem (numpy arrays);
+    ``attempts[b]`` picks the stream of sequence b (default 0), so one
+    sequence can be redrawn without touching the others."""
     B, blk, V = cfg.batch, cfg.blk, cfg.vocab
+    att = np.zeros(B, np.int64) if attempts is None else np.asarray(attempts, np.int64)
     base = np.empty((B * blk, V), np.float32)
     target = np.empty((B, blk), np.int64)
     decoy = np.empty((B, blk), np.int64)
@@ -333,15 +336,16 @@ def decode_problem(cfg: DecodeConfig, seed: int) -> dict:
                   boost_hi=0, boost_frac=0, prev_sigma=0, n_layers=cfg.n_layers, n_heads=cfg.n_heads,
                   seq_len=blk, band=cfg.band, p_link=cfg.p_link, tau_edge=cfg.tau_edge, attn_sigma=0.25)
     for b in range(B):
-        rng = _rng(seed, b, 0, 10)
+        rng = _rng(seed, b, int(att[b]), 10)
         base[b * blk:(b + 1) * blk] = rng.standard_normal((blk, V), dtype=np.float32) * np.float32(cfg.sigma)
         t = rng.integers(0, V, blk)
         d = (t + rng.integers(1, V, blk)) % V
         target[b], decoy[b] = t, d
         u[b] = rng.uniform(cfg.u_lo, cfg.u_hi, blk).astype(np.float32)
         v[b] = rng.uniform(0.0, cfg.v_hi, blk).astype(np.float32)
-        a, P = sequence_attention(acfg, seed + 7919, b, 0)
+        a, P = sequence_attention(acfg, seed + 7919, b, int(att[b]))
         attn[b] = a
         links[b] = P
     c0 = np.float32(math.log(V - 1) + cfg.sigma * cfg.sigma / 2.0)
-    return dict(cfg=cfg, base=base, target=target, decoy=decoy, u=u, v=v, links=links, attn=attn, c0=c0)
+    return dict(cfg=cfg, base=base, target=target, decoy=decoy, u=u, v=v, links=links, attn=attn, c0=c0,
+                attempts=att.copy())
