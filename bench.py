@@ -74,6 +74,10 @@ def parse():
                     help="logit boost reading of the input recipe (absolute = literal: no confidence reaches the "
                          "thresholds; the bytes are the same)")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the short runs of the other workloads after the headline one")
+    ap.add_argument("--per-workload-steps", type=int, default=200,
+                    help="timed steps of each other workload in the per_workload block")
     ap.add_argument("--compact-attn", action="store_true",
                     help="hold only the attention block [B, L, H, blk, blk] on the device (small profiling cases)")
     return ap.parse_args()
@@ -238,7 +242,10 @@ def bench_config(args):
     return cfg
 
 
-def run_native(args, rank, world, local):
+def run_native(args, rank, world, local, light=False):
+    """The timed steps of one workload.  ``light``: only the whole steps
+    (no per-rule runs, no attention-alone timing, no end-to-end steps, no
+    clock sampling) -- the short runs of the per_workload block."""
     import torch
 
     import diffusion_decoding_token_gb300 as dlm
@@ -351,7 +358,7 @@ def run_native(args, rank, world, local):
         step_graphs[0].replay()  # upload / warm-up (untimed)
         torch.cuda.synchronize()
 
-    sampler = ClockSampler(local) if rank == 0 else None
+    sampler = ClockSampler(local) if rank == 0 and not light else None
     if sampler:
         sampler.start()
         # load phase (untimed): keeps the GPU busy for ~1 s so the clock
@@ -386,6 +393,9 @@ def run_native(args, rank, world, local):
     k1 = [e[0].elapsed_time(e[1]) for e in evs]
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
+    if light:
+        return dict(total_ms=total_ms, k1=k1, flush=flush, cfg=cfg, w=w, decisions=int(w.masked.sum()),
+                    rows=int(w.masked.sum()), launches=plan.n_launches * args.steps)
 
     # the four rules alone, on the statistics of the last step
     r0 = torch.cuda.Event(enable_timing=True)
@@ -781,7 +791,49 @@ def main():
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(r["w"])
     line["config"]["workload_name"] = cfg.name
+    if world == 1 and not args.no_per_workload and not args.batch and not args.compact_attn:
+        del r
+        line["per_workload"] = per_workload(args, cfg.name, peak, local)
     print(json.dumps(line), flush=True)
+
+
+def per_workload(args, headline, peak, local):
+    """Short runs of the other workloads in the same launch configuration
+    (whole steps captured as CUDA graphs, L2 flushed before every step when
+    the step's rows fit in it): ms per step, decisions/s, the row pass's
+    GB/s against the peak, and the oracle's rate on the host cores."""
+    import torch
+
+    import synth
+    out = {}
+    for name in synth.ORDER:
+        if name == headline:
+            continue
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.steps, a.warmup, a.e2e_steps = name, args.per_workload_steps, 3, 0
+        a.seed = 1000 + synth.ORDER.index(name)
+        r = run_native(a, 0, 1, local, light=True)
+        cfg = r["cfg"]
+        esz = 4 if cfg.logit_dtype == synth.F32 else 2
+        k1_bytes = 2 * r["rows"] * cfg.vocab * esz
+        k1_ms = statistics.mean(r["k1"])
+        ms = r["total_ms"] / a.steps
+        rec = {"workload": workload_desc(cfg), "steps": a.steps, "ms_per_step": ms,
+               "decisions_per_s": r["decisions"] / (ms / 1000.0),
+               "row_pass": {"ms": k1_ms, "gbps": k1_bytes / (k1_ms / 1000.0) / 1e9,
+                            "frac": k1_bytes / (k1_ms / 1000.0) / 1e9 / peak, "algorithmic_bytes": k1_bytes},
+               "l2": "flushed before every step" if r["flush"] else "not flushed (rows larger than L2)",
+               "gpu_launches": r["launches"]}
+        if not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            v, sample = _oracle_rate(r["w"], 2.0)
+            rec["cpu_baseline"] = {"value": v, "unit": "decisions/s", "cores": oracle.get_threads(),
+                                   "kind": "oracle", "sample": sample}
+        out[name] = rec
+        del r
+        torch.cuda.empty_cache()
+    return out
 
 
 if __name__ == "__main__":
