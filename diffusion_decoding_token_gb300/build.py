@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libdlm.so")
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ["api.cu", "row_stats.cu", "select.cu", "cap.cu", "dapd.cu", "cap_noalloc.cu", "revocable.cu"]
+SOURCES = ["api.cu", "row_stats.cu", "select.cu", "cap.cu", "dapd.cu", "dapd_noalloc.cu", "revocable.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -349,39 +349,6 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
                           uint32_t* dev_status, dlm_stream_t stream);
 
 /*
- * dlm_cap_select_noalloc -- dlm_cap_select for callers that cannot allocate.
- *
- * The pages have no counterpart to this call: it is a deployment variant of
- * dlm_cap_select.  Some callers cannot call cudaMalloc (a serving runtime whose
- * allocator reserved all device memory up front, a plug-in inside a framework
- * that owns every allocation, a decode loop that cannot afford cudaMalloc's
- * implicit synchronisation), so they cannot pass the CAP workspace.  This call
- * takes the same arguments as dlm_cap_select minus the workspace, computes the
- * same results, and keeps its scratch in an array inside libdlm.
- *
- * Limit: the scratch holds DLM_CAP_NOALLOC_MAX_BYTES (1 MiB); a call whose
- * dlm_cap_workspace_size(batch, params->p_max) is larger returns
- * DLM_ERR_WORKSPACE (e.g. batch 64 with p_max 256 fits, batch 128 does not).
- * The array exists on every GPU that loads the library until the process
- * exits.  The first call on a device looks up the array's device address with
- * that device current (an internal runtime query); make that first call before
- * any stream capture.  Every call shares the one array and leaves its contents
- * behind: calls that can overlap on the GPU (other streams, other host threads)
- * race on it and must be ordered by the caller.  The kernels rewrite every
- * scratch entry they read, so nothing needs clearing between calls.  No
- * cudaMalloc, cudaFree or allocating routine is called.
- */
-#define DLM_CAP_NOALLOC_MAX_BYTES (1u << 20)
-
-dlm_status dlm_cap_select_noalloc(const void* logits, dlm_dtype dtype, int64_t vocab, int64_t row_stride,
-                                  const int32_t* row_index, int64_t n_rows, const int32_t* argmax,
-                                  const float* conf, const float* lse,
-                                  const uint8_t* masked, const int32_t* scope_len, int32_t batch,
-                                  int32_t blk, const dlm_cap_params* params, uint8_t* selected,
-                                  int32_t* n_selected, float* D_out, uint32_t* dev_status,
-                                  dlm_stream_t stream);
-
-/*
  * dlm_dapd_graph_mis -- DAPD: attention graph and Welsh-Powell selection.
  *
  * DAPD, "整体框架" and "关键设计 1-3".  V_t = masked positions of the block,
@@ -437,6 +404,46 @@ dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, 
                               int32_t* n_selected, float* s_out, float* dtilde_out,
                               int32_t* deg_out, void* workspace, size_t ws_bytes,
                               uint32_t* dev_status, dlm_stream_t stream);
+
+/*
+ * dlm_dapd_graph_mis_noalloc -- dlm_dapd_graph_mis without a workspace.
+ *
+ * The pages have no counterpart to this call: it serves callers that cannot
+ * allocate device memory, so cannot pass the DAPD workspace -- a serving
+ * engine whose allocator reserved nearly all of HBM at start-up and hands out
+ * nothing while decoding, a plug-in inside a framework that owns every
+ * device allocation, a decode loop that must not pay cudaMalloc's implicit
+ * device synchronisation.  It takes the arguments of dlm_dapd_graph_mis
+ * except the workspace, gives the same results (it is that call with the
+ * library's array as the workspace), and keeps the scratch -- the attention
+ * pass's fixed-point sums, which the selection kernel reads back -- in one
+ * array inside libdlm.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Limit: the array holds DLM_DAPD_NOALLOC_MAX_BYTES (8 MiB); a call whose
+ * dlm_dapd_workspace_size(batch, blk) is larger returns DLM_ERR_WORKSPACE
+ * before anything is launched (8 sequences of 256 positions need 4.3 MB and
+ * fit; 16 of them do not).  The array exists on every GPU that loads the
+ * library, until the process exits.
+ * Set-up: the first call in a CUDA context looks up the array's device
+ * address with that context's device current, and later calls reuse it (a
+ * device reset starts a new context, whose first call looks it up again).
+ * Make that first call on each device -- and the first after a reset --
+ * before any stream capture.
+ * Sharing: every call uses the same array and leaves its contents behind.
+ * Nothing needs clearing between calls (a call writes every entry it reads
+ * first), but calls that can overlap on the GPU -- other streams, other host
+ * threads, concurrent graph branches -- race on the array and must be
+ * ordered by the caller.
+ */
+#define DLM_DAPD_NOALLOC_MAX_BYTES (8u << 20)
+
+dlm_status dlm_dapd_graph_mis_noalloc(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
+                                      int32_t n_heads, int64_t stride_b, int64_t stride_l, int64_t stride_h,
+                                      int64_t stride_row, int32_t block_start, int32_t blk, const uint8_t* masked,
+                                      const float* conf, const dlm_dapd_params* params, uint8_t* selected,
+                                      int32_t* n_selected, float* s_out, float* dtilde_out, int32_t* deg_out,
+                                      uint32_t* dev_status, dlm_stream_t stream);
 
 /*
  * dlm_dapd_graph / dlm_dapd_select -- dlm_dapd_graph_mis in two halves.

@@ -1,13 +1,14 @@
-"""dlm_cap_select_noalloc, the CAP entry point for callers that cannot
-allocate device memory (their allocator owns all of HBM, or they run inside a
-framework that owns every allocation), against dlm_cap_select with a caller
-workspace.
+"""dlm_dapd_graph_mis_noalloc, the DAPD call for callers that cannot allocate
+device memory (an engine whose allocator holds all of HBM, a plug-in inside a
+framework that owns every allocation, a loop that must not pay cudaMalloc's
+synchronisation), against dlm_dapd_graph_mis with a caller workspace.
 
-Both are called through the C ABI.  The no-allocation call keeps its scratch in
-one array inside the library, shared by every call; two calls in a row on
-different inputs must each match the workspace entry point (selections and
-counts exactly, D_ij within 1e-4 abs + 1e-4 rel), so nothing left in the array
-by the first call may leak into the second.  This file is collected last.
+Both are called through the C ABI.  The no-allocation call keeps its scratch
+(the attention sums) in one array inside the library, shared by every call;
+two calls in a row on different problems -- laid out differently over that
+array -- must each match the workspace call: selections, counts and degrees
+exactly, s_ij and d~_i within 1e-4 abs + 1e-4 rel.  Nothing the first call
+leaves in the array may leak into the second.  This file is collected last.
 """
 import ctypes
 
@@ -23,79 +24,83 @@ pytestmark = pytest.mark.gpu
 
 def _api():
     import diffusion_decoding_token_gb300 as dlm
-    from diffusion_decoding_token_gb300._binding import CapParams
+    from diffusion_decoding_token_gb300._binding import DapdParams
     L = dlm.lib()
     P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-    f = L.dlm_cap_select_noalloc
+    f = L.dlm_dapd_graph_mis_noalloc
     f.restype = ctypes.c_int
-    f.argtypes = [P, ctypes.c_int, I64, I64, P, I64, P, P, P, P, P, I32, I32, ctypes.POINTER(CapParams), P, P, P,
-                  P, P]
-    return dlm, L, CapParams
+    f.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32, P, P, ctypes.POINTER(DapdParams),
+                  P, P, P, P, P, P, P]
+    return dlm, L, DapdParams
 
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _case(seed, batch, blk, p_max, vocab):
-    cfg = synth.scaled(synth.CONFIGS["llada_step"], batch=batch, blk=blk, vocab=vocab, p_max=p_max)
-    return cfg, DeviceWorkload(synth.make(cfg, seed=seed), compact_attn=True)
-
-
-def _both(dlm, L, CapParams, cfg, dw, tau_low):
+def _both(dlm, L, DapdParams, cfg, dw, conf):
     B, blk = cfg.batch, cfg.blk
-    st = dlm.row_stats(dw.cur, dw.prev)
-    am, conf, lse = st.argmax.view(B, blk), st.conf.view(B, blk), st.lse.view(B, blk)
-    prm = CapParams(tau_low, cfg.tau_high, cfg.gamma, cfg.p_max, 0)
+    prm = DapdParams(cfg.tau_edge, cfg.bulk_conf, cfg.bulk_frac, 0, 0)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    a = dw.attn
+    sb, sl, sh, sr, _ = a.stride()
+    head = (_ptr(a), dlm.DLM_F16, B, a.shape[1], a.shape[2], sb, sl, sh, sr, dw.block_start, blk, _ptr(dw.masked),
+            _ptr(conf), ctypes.byref(prm))
     out = {}
     for name in ("workspace", "noalloc"):
         sel = torch.full((B, blk), 7, dtype=torch.uint8, device="cuda")
         n = torch.full((B,), -1, dtype=torch.int32, device="cuda")
-        D = torch.full((B, blk, blk), float("nan"), device="cuda")
+        s = torch.full((B, blk, blk), float("nan"), device="cuda")
+        dt = torch.full((B, blk), float("nan"), device="cuda")
+        deg = torch.full((B, blk), -1, dtype=torch.int32, device="cuda")
         status = dlm.new_status()
+        tail = (_ptr(sel), _ptr(n), _ptr(s), _ptr(dt), _ptr(deg))
         if name == "workspace":
-            ws = dlm.cap_workspace(B, cfg.p_max, "cuda")
-            rc = L.dlm_cap_select(_ptr(dw.cur), dlm.DLM_BF16, dw.cur.shape[1], dw.cur.stride(0), None,
-                                  dw.cur.shape[0], _ptr(am),
-                                  _ptr(conf), _ptr(lse), _ptr(dw.masked), None, B, blk, ctypes.byref(prm),
-                                  _ptr(sel), _ptr(n), _ptr(D), _ptr(ws), ws.numel(), _ptr(status), stream)
+            ws = dlm.dapd_workspace(B, blk, "cuda")
+            rc = L.dlm_dapd_graph_mis(*head, *tail, _ptr(ws), ws.numel(), _ptr(status), stream)
         else:
-            rc = L.dlm_cap_select_noalloc(_ptr(dw.cur), dlm.DLM_BF16, dw.cur.shape[1], dw.cur.stride(0), None,
-                                          dw.cur.shape[0], _ptr(am),
-                                          _ptr(conf), _ptr(lse), _ptr(dw.masked), None, B, blk, ctypes.byref(prm),
-                                          _ptr(sel), _ptr(n), _ptr(D), _ptr(status), stream)
+            rc = L.dlm_dapd_graph_mis_noalloc(*head, *tail, _ptr(status), stream)
         assert rc == 0, L.dlm_status_string(rc)
         torch.cuda.synchronize()
-        out[name] = (sel.cpu().numpy(), n.cpu().numpy(), D.cpu().numpy(), int(status.item()))
+        out[name] = [t.cpu().numpy() for t in (sel, n, s, dt, deg)] + [int(status.item())]
     return out
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
-    dlm, L, CapParams = _api()
-    # first call: 64 sequences whose pools hold every position (p_max 256),
-    # about 590 KB of the 1 MiB scratch; second call: a different, smaller
-    # problem laid out differently over the same scratch
-    for seed, batch, blk, p_max, tau_low, vocab in [(31, 64, 256, 256, 0.0, 2048), (32, 16, 32, 32, 0.8, 8192)]:
-        cfg, dw = _case(seed, batch, blk, p_max, vocab)
-        out = _both(dlm, L, CapParams, cfg, dw, tau_low)
+    dlm, L, DapdParams = _api()
+    # first call: 8 sequences of 256 positions, 4.3 MB of the 8 MiB scratch,
+    # clustered decide; second call: 64 sequences of 32 positions laid out
+    # differently over the same scratch, one-CTA decide, some in the late phase
+    cases = [synth.scaled(synth.CONFIGS["stress_graph"], batch=8, vocab=256, seq_len=320, block_start=64),
+             synth.scaled(synth.CONFIGS["batched"], batch=64, vocab=256, n_layers=4, n_heads=8, seq_len=96,
+                          block_start=32, masked_count=-1)]
+    for k, cfg in enumerate(cases):
+        w = synth.make(cfg, seed=41 + k)
+        if k == 1:
+            w.masked[::4, : cfg.blk // 2 + 4] = 0       # a quarter of the sequences below the 50 % switch
+        dw = DeviceWorkload(w)
+        rng = np.random.default_rng(k)
+        conf = torch.from_numpy(rng.random((cfg.batch, cfg.blk)).astype(np.float32)).cuda()
+        out = _both(dlm, L, DapdParams, cfg, dw, conf)
         ws, na = out["workspace"], out["noalloc"]
         np.testing.assert_array_equal(na[0], ws[0])
         np.testing.assert_array_equal(na[1], ws[1])
-        assert na[3] == ws[3]
-        pool_pairs = ~np.isnan(ws[2])
-        np.testing.assert_array_equal(~np.isnan(na[2]), pool_pairs)
-        assert close(na[2][pool_pairs], ws[2][pool_pairs]).all()
-        assert (ws[1] >= 1).all()
+        np.testing.assert_array_equal(na[4], ws[4])
+        assert na[5] == ws[5] == 0
+        for j in (2, 3):
+            seen = ~np.isnan(ws[j])
+            np.testing.assert_array_equal(~np.isnan(na[j]), seen)
+            assert close(na[j][seen], ws[j][seen]).all()
+        assert (ws[1] >= 1).all() and seen.any()
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch():
-    dlm, L, CapParams = _api()
-    cap_bytes = 1 << 20
-    B, p_max = 128, 256
-    assert L.dlm_cap_workspace_size(B, p_max) > cap_bytes
-    prm = CapParams(0.8, 0.95, -16.0, p_max, 0)
+    dlm, L, DapdParams = _api()
+    cap_bytes = 8 << 20
+    B, blk = 16, 256
+    assert L.dlm_dapd_workspace_size(B, blk) > cap_bytes >= L.dlm_dapd_workspace_size(8, blk)
+    prm = DapdParams(0.01, 0.9, 0.5, 0, 0)
     fake = ctypes.c_void_p(0x10000)
-    rc = L.dlm_cap_select_noalloc(fake, dlm.DLM_BF16, 1024, 1024, None, B * 256, fake, fake, fake, fake, None, B, 256,
-                                  ctypes.byref(prm), fake, fake, None, None, None)
+    rc = L.dlm_dapd_graph_mis_noalloc(fake, dlm.DLM_F16, B, 10, 32, 1 << 24, 1 << 20, 1 << 10, 1024, 0, blk, fake,
+                                      fake, ctypes.byref(prm), fake, fake, None, None, None, None, None)
     assert rc == 4  # DLM_ERR_WORKSPACE, before anything is launched
