@@ -59,6 +59,8 @@ def _load():
             lib.oracle_dapd.argtypes = [_P, _I32, _I32, _I32, _I32, _I64, _I64, _I64, _I64, _I32, _I32,
                                         _P, _P, _F, _F, _F, _I32, _I32, _P, _P, _P, _P, _P, _P]
             lib.oracle_greedy_mis.argtypes = [_I32, _P, _P, _P]
+            lib.oracle_attention_influence.argtypes = [_P, _I32, _I32, _I32, _I32, _I64, _I64, _I64, _I64, _I32,
+                                                       _I32, _P, _P]
             lib.oracle_select_topk.argtypes = [_P, _P, _I32, _I32, _I32, _P, _P]
             lib.oracle_select_factor.argtypes = [_P, _P, _I32, _I32, _F, _P, _P]
             lib.oracle_parallel_certificate.argtypes = [_P, _P, _I32, _I32, _P]
@@ -217,6 +219,26 @@ def dapd(attn, masked, conf, tau_edge, bulk_conf=0.9, bulk_frac=0.5, order_mode=
                     _ptr(conf), float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode),
                     int(bool(preunmask_certain)), _ptr(sel), _ptr(n), _ptr(s), _ptr(dt), _ptr(deg), _ptr(path))
     return dict(selected=sel, n_selected=n, s=s, dtilde=dt, deg=deg, path=path)
+
+
+def attention_influence(attn, masked, block_start=0, dtype=None):
+    """Downstream influence of every block position: the attention it
+    receives from the masked queries, averaged over layers and heads (COVER
+    page, Method; the reading is stated in the C source).  ``attn`` is
+    [B, L, H, N, N] (or the compact block with block_start 0).  Returns
+    [B, blk] fp64."""
+    lib = _load()
+    attn = np.ascontiguousarray(attn)
+    code = _dtype_code(attn, dtype)
+    B, L, H, N, N2 = attn.shape
+    assert N == N2
+    masked = np.ascontiguousarray(masked, dtype=np.uint8)
+    blk = masked.shape[1]
+    assert block_start + blk <= N
+    out = np.zeros((B, blk))
+    lib.oracle_attention_influence(_ptr(attn), code, B, L, H, L * H * N * N, H * N * N, N * N, N, int(block_start),
+                                   blk, _ptr(masked), _ptr(out))
+    return out
 
 
 def greedy_mis(adj, order):

@@ -517,6 +517,40 @@ void oracle_dapd(const void* attn, int dtype, int batch, int n_layers, int n_hea
     }
 }
 
+/* ------------------------------------------------------------------------
+ * Downstream influence for the revocable rule's seed score (COVER page,
+ * "Method": a seed's score combines its uncertainty, its downstream
+ * influence and its cache drift; the page does not define influence).
+ * Reading: the influence of block position i is the attention it receives
+ * from the positions still to be decoded -- the masked queries q of the
+ * block -- averaged over the given layers and heads:
+ *   infl_i = (1 / (L H)) sum_{q masked} sum_{l, h} A[l][h][q][i]
+ * for every position i of the block (masked or not).  Element (b,l,h,row,col)
+ * of attn at b*sb + l*sl + h*sh + row*sr + col; the block is rows and
+ * columns [block_start, block_start + blk).
+ * ------------------------------------------------------------------------ */
+void oracle_attention_influence(const void* attn, int dtype, int batch, int n_layers, int n_heads, int64_t sb,
+                                int64_t sl, int64_t sh, int64_t sr, int block_start, int blk,
+                                const uint8_t* masked, double* infl) {
+    int b;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (b = 0; b < batch; ++b) {
+        const uint8_t* mk = masked + (int64_t)b * blk;
+        double LH = (double)n_layers * (double)n_heads;
+        for (int i = 0; i < blk; ++i) {
+            double acc = 0.0;
+            for (int q = 0; q < blk; ++q) {
+                if (!mk[q]) continue;
+                for (int l = 0; l < n_layers; ++l)
+                    for (int h = 0; h < n_heads; ++h)
+                        acc += load_elem(attn, dtype, b * sb + l * sl + h * sh + (int64_t)(block_start + q) * sr +
+                                                          block_start + i);
+            }
+            infl[(int64_t)b * blk + i] = acc / LH;
+        }
+    }
+}
+
 /* Greedy maximal independent set over an explicit order (used by the tests
  * to evaluate alternative orders of near-tied keys): adj is n x n bytes,
  * order lists node ids; kept[x] = 1 for the nodes taken. */

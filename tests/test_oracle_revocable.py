@@ -137,3 +137,62 @@ def test_invariants_random_runs():
             assert (st["remasks"][b] <= 2).all()
             assert ((st["seed"][b] == 1) <= (st["masked"][b] == 0)).all()              # seeds are decoded
     assert st["masked"].sum() == 0
+
+
+# ------------------------------------------------------------ influence
+def test_influence_closed_form_permutation_attention():
+    """One layer and head whose query q attends only to column pi(q): the
+    influence of i is 1 when the query pointing at i is masked, else 0."""
+    import oracle
+    rng = np.random.default_rng(3)
+    B, blk = 3, 17
+    A = np.zeros((B, 1, 1, blk, blk), np.float32)
+    perms = [rng.permutation(blk) for _ in range(B)]
+    for b in range(B):
+        A[b, 0, 0, np.arange(blk), perms[b]] = 1.0
+    masked = (rng.random((B, blk)) < 0.5).astype(np.uint8)
+    infl = oracle.attention_influence(A, masked)
+    for b in range(B):
+        want = np.zeros(blk)
+        want[perms[b][masked[b] > 0]] = 1.0
+        np.testing.assert_array_equal(infl[b], want)
+
+
+def test_influence_of_row_stochastic_attention_sums_to_the_masked_count():
+    """Rows softmaxed over the block (N = blk): every masked query spreads a
+    unit of attention over the block, so the influences sum to the number of
+    masked positions; with layers/heads averaged the same holds, and a
+    block inside a larger map reads only the block."""
+    import oracle
+    rng = np.random.default_rng(4)
+    B, L, H, blk = 4, 3, 5, 24
+    x = np.exp(rng.standard_normal((B, L, H, blk, blk)))
+    A = x / x.sum(-1, keepdims=True)
+    masked = (rng.random((B, blk)) < 0.6).astype(np.uint8)
+    infl = oracle.attention_influence(A.astype(np.float32), masked)
+    np.testing.assert_allclose(infl.sum(-1), masked.sum(-1), rtol=1e-6)
+    big = np.zeros((B, L, H, blk + 9, blk + 9), np.float32)
+    big[:, :, :, 5:5 + blk, 5:5 + blk] = A
+    np.testing.assert_array_equal(oracle.attention_influence(big, masked, block_start=5), infl)
+
+
+def test_influence_identity_with_dapd_degree():
+    """For a masked i, DAPD's d~_i = sum_{j in V_t, j != i} (a_ij + a_ji) / 2,
+    so 2 d~_i = (row sum of a over masked columns) + infl_i - 2 a_ii: the
+    influence pinned against the DAPD oracle's proxy degree."""
+    import oracle
+    import synth
+    rng = np.random.default_rng(5)
+    B, L, H, blk = 3, 2, 4, 32
+    A = (rng.random((B, L, H, blk, blk)) ** 4 * 0.1).astype(np.float32)
+    A16 = synth.to_f16_bits(A)
+    masked = np.ones((B, blk), np.uint8)
+    masked[:, ::5] = 0
+    r = oracle.dapd(A16, masked, np.full((B, blk), 0.5), 0.05, dtype=synth.F16)
+    infl = oracle.attention_influence(A16, masked, dtype=synth.F16)
+    a = A16.view(np.float16).astype(np.float64).mean(axis=(1, 2))
+    for b in range(B):
+        assert r["path"][b] == 0
+        for i in np.nonzero(masked[b])[0]:
+            row = a[b, i, masked[b] > 0].sum()
+            np.testing.assert_allclose(2 * r["dtilde"][b][i], row + infl[b][i] - 2 * a[b, i, i], rtol=1e-12)
