@@ -25,6 +25,7 @@ from ._binding import (  # noqa: F401
     RowStats,
     StepPlan,
     alloc_row_stats,
+    attention_influence,
     cap_select,
     cap_workspace,
     dapd_graph,

@@ -89,10 +89,12 @@ def lib():
         L.dlm_dapd_graph.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                      P, ctypes.POINTER(DapdParams), P, P, P, P, Z, P, P]
         L.dlm_dapd_select.argtypes = [P, P, I32, I32, ctypes.POINTER(DapdParams), P, P, P, Z, P]
+        L.dlm_attention_influence.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32, P, P, P,
+                                              Z, P, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
                   "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select", "dlm_select_topk",
                   "dlm_select_factor", "dlm_parallel_certificate", "dlm_depcap_boundary_ragged",
-                  "dlm_revocable_step"):
+                  "dlm_revocable_step", "dlm_attention_influence"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -464,6 +466,28 @@ def dapd_graph(attn: torch.Tensor, masked: torch.Tensor, tau_edge: float = 0.01,
                                 ctypes.byref(prm), _p(s_out), _p(dtilde_out), _p(deg_out), _p(workspace),
                                 workspace.numel(), _p(status), _stream(attn.device)))
     return workspace
+
+
+def attention_influence(attn: torch.Tensor, masked: torch.Tensor, block_start: int = 0, *, out=None, workspace=None,
+                        status=None) -> torch.Tensor:
+    """dlm_attention_influence on ``attn`` = [B, L, H, N, N] (unit column
+    stride): the attention each block position receives from the masked
+    queries, averaged over layers and heads, as a float [B, blk] tensor."""
+    _need_cuda(attn, masked, out)
+    if attn.dim() != 5 or attn.stride(4) != 1:
+        raise ValueError("attn must be [B, L, H, N, N] with unit column stride")
+    B, L, H = attn.shape[:3]
+    blk = masked.shape[1]
+    masked = _u8(masked)
+    if workspace is None:
+        workspace = dapd_workspace(B, blk, attn.device)
+    if out is None:
+        out = torch.empty((B, blk), dtype=torch.float32, device=attn.device)
+    sb, sl, sh, sr, _ = attn.stride()
+    _check(lib().dlm_attention_influence(_p(attn), _dt(attn), B, L, H, sb, sl, sh, sr, int(block_start), blk,
+                                         _p(masked), _p(out), _p(workspace), workspace.numel(), _p(status),
+                                         _stream(attn.device)))
+    return out
 
 
 def dapd_select(workspace: torch.Tensor, masked: torch.Tensor, conf: torch.Tensor, tau_edge: float = 0.01,

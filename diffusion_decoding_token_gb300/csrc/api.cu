@@ -367,6 +367,21 @@ dlm_status dapd_prepare(dlm::DapdArgs& a, const void* attn, dlm_dtype dtype, int
 
 extern "C" {
 
+dlm_status dlm_attention_influence(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
+                                   int32_t n_heads, int64_t stride_b, int64_t stride_l, int64_t stride_h,
+                                   int64_t stride_row, int32_t block_start, int32_t blk, const uint8_t* masked,
+                                   float* influence, void* workspace, size_t ws_bytes, uint32_t* dev_status,
+                                   dlm_stream_t stream) {
+    const dlm_dapd_params prm = {0.f, 0.f, 0.f, 0, 0};
+    dlm::DapdArgs a{};
+    const dlm_status st = dapd_prepare(a, attn, dtype, batch, n_layers, n_heads, stride_b, stride_l, stride_h,
+                                       stride_row, block_start, blk, masked, &prm, workspace, ws_bytes, true);
+    if (st != DLM_OK || batch == 0) return st;
+    if (!influence) return DLM_ERR_INVALID_ARG;
+    a.dev_status = dev_status;
+    return from_cuda(dlm::launch_attention_influence(a, sm_count(), influence, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dlm_status dlm_dapd_graph_mis(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
                               int32_t n_heads, int64_t stride_b, int64_t stride_l,
                               int64_t stride_h, int64_t stride_row, int32_t block_start,

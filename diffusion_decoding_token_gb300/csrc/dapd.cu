@@ -1051,6 +1051,25 @@ cudaError_t launch_accum_tma(const DapdArgs& a, const CUtensorMap& map, cudaStre
     return cudaLaunchKernelEx(&cfg, dapd_accum_tma_kernel<DT>, map, a);
 }
 
+// Downstream influence of every block position from the exact sums:
+// infl_j = sum over masked rows i of A_ij / (L H 2^32), the attention j
+// receives from the masked queries averaged over layers and heads.  One CTA
+// per sequence, one thread per column; the 64-bit sum is exact (at most
+// 256 rows of at most 511 * 2^32 each) and converted once.
+__global__ void __launch_bounds__(kThreads) influence_kernel(DapdArgs a, float* infl) {
+    const int b = blockIdx.x, j = threadIdx.x;
+    __shared__ unsigned char s_mk[DLM_MAX_BLK];
+    if (j < a.blk) s_mk[j] = a.masked[(int64_t)b * a.blk + j];
+    __syncthreads();
+    if (j >= a.blk) return;
+    const long long* A = a.A + (int64_t)b * a.blk * a.blk + j;
+    long long sum = 0;
+    for (int i = 0; i < a.blk; ++i)
+        if (s_mk[i]) sum += A[(int64_t)i * a.blk];
+    const double unit = (double)a.n_layers * (double)a.n_heads * 4294967296.0;
+    infl[(int64_t)b * a.blk + j] = (float)((double)sum / unit);
+}
+
 }  // namespace
 
 size_t dapd_workspace_bytes(int batch, int blk) {
@@ -1129,6 +1148,17 @@ cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, dapd_decide_cluster_kernel, a);
+}
+
+cudaError_t launch_attention_influence(DapdArgs& a, int num_sms, float* infl, cudaStream_t s) {
+    a.bulk_frac = 0.f;  // every sequence's masked rows are summed, whatever its masked fraction
+    cudaError_t e = launch_dapd_graph(a, num_sms, s, false);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.gridDim = dim3((unsigned)a.batch);
+    cfg.blockDim = dim3(kThreads);
+    return cudaLaunchKernelEx(&cfg, influence_kernel, a, infl);
 }
 
 cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s) {

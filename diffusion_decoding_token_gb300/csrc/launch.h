@@ -175,5 +175,7 @@ cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);  // attention
 // selection rebuilds the graph from the sums itself)
 cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel);
 cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s);  // (graph +) conf -> selection
+// attention -> sums (every sequence) -> infl[b][j] = column sums over masked rows / (L H)
+cudaError_t launch_attention_influence(DapdArgs& a, int num_sms, float* infl, cudaStream_t s);
 
 }  // namespace dlm

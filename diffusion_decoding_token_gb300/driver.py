@@ -20,10 +20,11 @@ stand-in for the model, so the rules can be compared by the number of steps
   masked position.
 * rule "revocable" (COVER page, revocable parallel decoding): the step is
   model -> dlm_row_stats (KL to the previous step = the seeds' drift) ->
-  dlm_revocable_step, which verifies last step's seeds (the stand-in's
-  prediction at a decoded position depends on its neighbours only, so it is
-  a leave-one-out re-prediction), drafts masked positions and picks the next
-  seeds (influence = attention received from masked queries).
+  dlm_attention_influence (the attention each position receives from the
+  masked queries) -> dlm_revocable_step, which verifies last step's seeds
+  (the stand-in's prediction at a decoded position depends on its neighbours
+  only, so it is a leave-one-out re-prediction), drafts masked positions and
+  picks the next seeds.
 
 The static inputs come from ``synth.decode_problem``.  The whole decode
 (max_steps steps) can be captured as one CUDA graph and replayed
@@ -90,12 +91,13 @@ class SyntheticDecoder:
         if rule == "revocable":
             # seeds' cache drift = KL to the previous step's distribution; downstream
             # influence = attention received from masked queries, mean over layers x heads
+            # (dlm_attention_influence)
             self.rev = dict(REVOCABLE_DEFAULT, **(revocable or {}))
             self.state = B.revocable_state(Bn, blk, dev)
             self.tok, self.masked = self.state["tok"], self.state["masked"]
             self.prev_logits = self.logits.clone()
             self.stats = B.alloc_row_stats(Bn * blk, dev, with_prev=True)
-            self.attn_mean = self.attn.to(torch.float32).mean(dim=(1, 2))          # [B, q, i]
+            self.infl = torch.zeros((Bn, blk), dtype=torch.float32, device=dev)
             self.outcome = torch.zeros((Bn, blk), dtype=torch.uint8, device=dev)
             self.n_revised = torch.zeros(Bn, dtype=torch.int32, device=dev)
 
@@ -142,7 +144,8 @@ class SyntheticDecoder:
         Bn, blk = self.B, self.blk
         st = B.row_stats(self.logits, self.prev_logits, out=self.stats, status=self.status)
         self.prev_logits.copy_(self.logits)
-        infl = torch.bmm(self.masked.to(torch.float32)[:, None, :], self.attn_mean)[:, 0, :]
+        infl = B.attention_influence(self.attn, self.masked, 0, out=self.infl, workspace=self.dapd_ws,
+                                     status=self.status)
         r = self.rev
         B.revocable_step(st.argmax.view(Bn, blk), st.conf.view(Bn, blk), self.state, self.step_index,
                          tau_replace=r["tau_replace"], tau_draft=r["tau_draft"], draft_budget=r["draft_budget"],

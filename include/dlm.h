@@ -472,6 +472,31 @@ dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t bat
                            void* workspace, size_t ws_bytes, dlm_stream_t stream);
 
 /*
+ * dlm_attention_influence -- downstream influence of every block position,
+ * an input of dlm_revocable_step's seed score.
+ *
+ * COVER page, "Method": a seed's score combines its uncertainty, its
+ * downstream influence and its cache drift; the page does not define
+ * influence.  Reading: the attention position i receives from the positions
+ * still to be decoded (the masked queries q of the block), averaged over the
+ * given layers and heads:
+ *   influence[b][i] = (1 / (L H)) sum_{q masked} sum_{l,h} attention[q][i]
+ * for every position i of the block.  The sums are the DAPD attention pass's
+ * exact fixed-point sums (dlm_dapd_graph_mis describes the exactness), taken
+ * for every sequence whatever its masked fraction, then summed over the
+ * masked rows exactly and rounded once to fp32.
+ *
+ * Arguments as dlm_dapd_graph_mis for attn, dtype, sizes, strides,
+ * block_start, blk, masked and workspace (dlm_dapd_workspace_size bytes; the
+ * call overwrites it); influence: float [batch][blk] output.
+ */
+dlm_status dlm_attention_influence(const void* attn, dlm_dtype dtype, int32_t batch, int32_t n_layers,
+                                   int32_t n_heads, int64_t stride_b, int64_t stride_l, int64_t stride_h,
+                                   int64_t stride_row, int32_t block_start, int32_t blk, const uint8_t* masked,
+                                   float* influence, void* workspace, size_t ws_bytes, uint32_t* dev_status,
+                                   dlm_stream_t stream);
+
+/*
  * dlm_revocable_step -- one state update of revocable parallel decoding
  * (COVER page: "Revocable Parallel Diffusion Decoding" for the step and its
  * state update, "Method" for the three revision outcomes, stability-aware

@@ -191,7 +191,6 @@ def revocable_decode(problem, max_steps, prm=REVOCABLE_DEFAULT):
     final state."""
     cfg = problem["cfg"]
     B, blk = cfg.batch, cfg.blk
-    attn = problem["attn"].view(np.float16).astype(np.float64).mean(axis=(1, 2))        # [B, q, i]
     state = oracle.revocable_init(B, blk)
     prev = problem["base"].copy()
     trace = []
@@ -201,7 +200,7 @@ def revocable_decode(problem, max_steps, prm=REVOCABLE_DEFAULT):
         cur = full_logits(problem, state["masked"])
         o = oracle.row_stats(cur, prev)
         prev = cur
-        infl = np.einsum("bq,bqi->bi", state["masked"].astype(np.float64), attn)
+        infl = oracle.attention_influence(problem["attn"], state["masked"], dtype=oracle.F16)
         rec = dict(masked=state["masked"].copy(), seed=state["seed"].copy(), last_seed=state["last_seed"].copy(),
                    remasks=state["remasks"].copy(), tok=state["tok"].copy(), last_tok=state["last_tok"].copy(),
                    conf=o["conf"].reshape(B, blk), argmax=o["argmax"].reshape(B, blk), kl=o["kl"].reshape(B, blk),

@@ -58,3 +58,38 @@ def test_revocable_until_finished():
     st = _run(8, 16, 60, seed=5, tau_replace=0.99, tau_draft=0.5, draft_budget=4, pi=1.0, cooldown=1,
               remask_budget=1)
     assert st["masked"].sum() == 0
+
+
+@pytest.mark.parametrize("blk,code,layout", [(32, "f16", "full"), (1, "f16", "full"), (100, "bf16", "full"),
+                                             (256, "f16", "compact"), (77, "f32", "full")])
+def test_attention_influence_matches_oracle(blk, code, layout):
+    """dlm_attention_influence (the attention each block position receives
+    from the masked queries, mean over layers and heads) against the oracle:
+    full maps with the block inside and compact blocks, f16 / bf16 / f32
+    attention, masks on both sides of DAPD's 50 % switch (the influence sums
+    every sequence's masked rows whatever the fraction)."""
+    import torch
+
+    import diffusion_decoding_token_gb300 as dlm
+    import synth
+    from parity import close, to_torch
+    rng = np.random.default_rng(blk)
+    B, L, H = 5, 3, 4
+    dt = {"f16": synth.F16, "bf16": synth.BF16, "f32": synth.F32}[code]
+    sub = (rng.random((B, L, H, blk, blk)) ** 3 * 0.2).astype(np.float32)
+    st = {synth.F32: lambda a: a, synth.BF16: synth.to_bf16_bits, synth.F16: synth.to_f16_bits}[dt](sub)
+    bs = 0
+    if layout == "full":
+        bs = 16
+        N = (bs + blk + 8 + 7) // 8 * 8
+        full = np.zeros((B, L, H, N, N), st.dtype)
+        full[:, :, :, bs:bs + blk, bs:bs + blk] = st
+        st = full
+    masked = (rng.random((B, blk)) < np.array([0.9, 0.6, 0.3, 0.0, 1.0])[:, None]).astype(np.uint8)
+    status = dlm.new_status()
+    g = dlm.attention_influence(to_torch(st, dt, "cuda"), torch.from_numpy(masked).cuda(), bs, status=status)
+    o = oracle.attention_influence(st, masked, block_start=bs, dtype=None if dt == synth.F32 else dt)
+    assert int(status.item()) == 0
+    g = g.cpu().numpy()
+    assert close(g, o, atol=1e-6, rtol=1e-6).all(), np.max(np.abs(g - o))
+    assert (g[3] == 0).all()                                  # nothing masked: no influence
