@@ -74,6 +74,9 @@ def parse():
                     help="logit boost reading of the input recipe (absolute = literal: no confidence reaches the "
                          "thresholds; the bytes are the same)")
     ap.add_argument("--batch", type=int, default=0, help="override the sequences per GPU (small profiling cases)")
+    ap.add_argument("--fuse-rules", default="auto", choices=["auto", "on", "off"],
+                    help="run threshold, boundary and CAP inside the row pass (dlm_row_stats_rules); auto: only the "
+                         "DepCap chain (boundary -> CAP, no DAPD)")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the short runs of the other workloads after the headline one")
     ap.add_argument("--per-workload-steps", type=int, default=200,
@@ -292,7 +295,8 @@ def run_native(args, rank, world, local, light=False):
     extra = tuple(r for r in args.extra_rules.split(",") if r)
     common.update(rules=tuple(cfg.rules) + extra, cap_scope_from_boundary=(cfg.name == "depcap_window"),
                   concurrent_dapd=not args.serial_dapd, dapd_early=not args.late_dapd_fork, dapd_priority=args.dapd_priority,
-                  parallel_rules=not args.serial_rules)
+                  parallel_rules=not args.serial_rules,
+                  fuse_rules={"auto": "auto", "on": True, "off": False}[args.fuse_rules])
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 
     for _ in range(args.warmup):
@@ -395,7 +399,7 @@ def run_native(args, rank, world, local, light=False):
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
     if light:
         return dict(total_ms=total_ms, k1=k1, flush=flush, cfg=cfg, w=w, decisions=int(w.masked.sum()),
-                    rows=int(w.masked.sum()), launches=plan.n_launches * args.steps)
+                    rows=int(w.masked.sum()), launches=plan.n_launches * args.steps, fused=list(plan.fused))
 
     # the four rules alone, on the statistics of the last step
     r0 = torch.cuda.Event(enable_timing=True)
@@ -531,7 +535,7 @@ def run_native(args, rank, world, local, light=False):
             raise RuntimeError(f"device status {int(status.item())} during the end-to-end steps")
 
     return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, per_rule=per_rule, attention=attention, clocks=clocks,
-                e2e=e2e, host_ms=host_ms, flush=flush,
+                e2e=e2e, host_ms=host_ms, flush=flush, fused=list(plan.fused),
                 cfg=cfg, launches=plan.n_launches * args.steps, w=w, decisions=int(w.masked.sum()),
                 rows=int(w.masked.sum()))
 
@@ -776,6 +780,7 @@ def main():
                      "traffic": recorded_traffic() if (cfg.batch == 64 and not args.compact_attn) else None, "kernel": "row_stats", "peak_kind": peak_kind,
                      "algorithmic_bytes": k1_bytes},
         "gpu_launches": r["launches"],
+        "fused_rules": r["fused"],
         "per_rule": r["per_rule"],
     }
     if r["attention"]:
@@ -823,7 +828,7 @@ def per_workload(args, headline, peak, local):
                "row_pass": {"ms": k1_ms, "gbps": k1_bytes / (k1_ms / 1000.0) / 1e9,
                             "frac": k1_bytes / (k1_ms / 1000.0) / 1e9 / peak, "algorithmic_bytes": k1_bytes},
                "l2": "flushed before every step" if r["flush"] else "not flushed (rows larger than L2)",
-               "gpu_launches": r["launches"]}
+               "gpu_launches": r["launches"], "fused_rules": r["fused"]}
         if not args.no_cpu_baseline:
             import oracle
             oracle.build()

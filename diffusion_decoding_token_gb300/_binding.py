@@ -41,6 +41,14 @@ class DapdParams(ctypes.Structure):
                 ("preunmask_certain", ctypes.c_int32)]
 
 
+class StepRules(ctypes.Structure):
+    _fields_ = [("rules", ctypes.c_uint32), ("tau", ctypes.c_float), ("depcap", DepcapParams),
+                ("cold_start", ctypes.c_void_p), ("cap", CapParams), ("cap_scope_from_boundary", ctypes.c_int32)]
+
+
+RULE_THRESHOLD, RULE_BOUNDARY, RULE_CAP = 1, 2, 4
+
+
 class RevocableParams(ctypes.Structure):
     _fields_ = [("tau_replace", ctypes.c_float), ("tau_draft", ctypes.c_float), ("draft_budget", ctypes.c_int32),
                 ("w_unc", ctypes.c_float), ("w_infl", ctypes.c_float), ("w_drift", ctypes.c_float),
@@ -89,12 +97,16 @@ def lib():
         L.dlm_dapd_graph.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32,
                                      P, ctypes.POINTER(DapdParams), P, P, P, P, Z, P, P]
         L.dlm_dapd_select.argtypes = [P, P, I32, I32, ctypes.POINTER(DapdParams), P, P, P, Z, P]
+        L.dlm_row_stats_rules_workspace_size.restype = Z
+        L.dlm_row_stats_rules_workspace_size.argtypes = [I32]
+        L.dlm_row_stats_rules.argtypes = [P, P, ctypes.c_int, I32, I32, I64, I64, P, ctypes.POINTER(StepRules), P, P, P,
+                                          P, P, P, P, P, P, P, P, P, P, Z, P, P]
         L.dlm_attention_influence.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32, P, P, P,
                                               Z, P, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
                   "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select", "dlm_select_topk",
                   "dlm_select_factor", "dlm_parallel_certificate", "dlm_depcap_boundary_ragged",
-                  "dlm_revocable_step", "dlm_attention_influence"):
+                  "dlm_revocable_step", "dlm_attention_influence", "dlm_row_stats_rules"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -468,6 +480,58 @@ def dapd_graph(attn: torch.Tensor, masked: torch.Tensor, tau_edge: float = 0.01,
     return workspace
 
 
+def row_stats_rules_workspace(batch: int, device) -> torch.Tensor:
+    """A zeroed workspace for row_stats_rules (every call leaves it zero)."""
+    return torch.zeros(max(16, lib().dlm_row_stats_rules_workspace_size(batch)), dtype=torch.uint8, device=device)
+
+
+def row_stats_rules(cur: torch.Tensor, prev: torch.Tensor | None, masked: torch.Tensor, *,
+                    rules=("threshold", "boundary", "cap"), tau: float = 0.9, lam: float = 1.0, L_min: int = 8,
+                    smooth_w: int = 1, norm_mode: int = 0, cold_start=None, tau_low: float = 0.8,
+                    tau_high: float = 0.95, gamma: float = -16.0, p_max: int | None = None,
+                    high_tier_unconditional: bool = False, cap_scope_from_boundary: bool = False,
+                    out: RowStats | None = None, workspace=None, status=None) -> dict:
+    """dlm_row_stats_rules: the row pass over ``cur`` ([B*blk, V]) with the
+    threshold, boundary and CAP rules of each sequence run by the CTA that
+    finishes its last row.  Returns dict(stats, threshold, block_len, score,
+    cap) with (selected, n_selected) pairs for the rules."""
+    _need_cuda(cur, prev, masked, cold_start, workspace)
+    B, blk = masked.shape
+    if cur.dim() != 2 or cur.stride(1) != 1 or cur.shape[0] != B * blk:
+        raise ValueError("cur must be [B*blk, V] with contiguous rows")
+    if prev is not None and (prev.shape != cur.shape or prev.stride() != cur.stride() or prev.dtype != cur.dtype):
+        raise ValueError("prev must match cur in shape, strides and dtype")
+    dev = cur.device
+    masked = _u8(masked)
+    bits = sum(b for n, b in (("threshold", RULE_THRESHOLD), ("boundary", RULE_BOUNDARY), ("cap", RULE_CAP))
+               if n in rules)
+    p_max = blk if p_max is None else int(p_max)
+    if out is None:
+        out = alloc_row_stats(B * blk, dev, prev is not None)
+    if workspace is None:
+        workspace = row_stats_rules_workspace(B, dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    res = {"stats": out}
+    thr = (torch.zeros((B, blk), **u8), torch.zeros(B, **i32)) if "threshold" in rules else (None, None)
+    cap = (torch.zeros((B, blk), **u8), torch.zeros(B, **i32)) if "cap" in rules else (None, None)
+    bl = torch.zeros(B, **i32) if "boundary" in rules else None
+    sc = torch.full((B, blk), float("nan"), dtype=torch.float32, device=dev) if "boundary" in rules else None
+    cold = None if cold_start is None else _u8(cold_start)
+    prm = StepRules(bits, float(tau), DepcapParams(float(lam), int(L_min), int(smooth_w), int(norm_mode)),
+                    None if cold is None else cold.data_ptr(),
+                    CapParams(float(tau_low), float(tau_high), float(gamma), p_max, int(bool(high_tier_unconditional))),
+                    int(bool(cap_scope_from_boundary)))
+    _check(lib().dlm_row_stats_rules(_p(cur), _p(prev), _dt(cur), B, blk, cur.shape[1], cur.stride(0), _p(masked),
+                                     ctypes.byref(prm), _p(out.argmax), _p(out.conf), _p(out.lse), _p(out.entropy),
+                                     _p(out.kl) if prev is not None else None,
+                                     _p(out.lse_prev) if prev is not None else None, _p(thr[0]), _p(thr[1]), _p(bl),
+                                     _p(sc), _p(cap[0]), _p(cap[1]), _p(workspace), workspace.numel(), _p(status),
+                                     _stream(dev)))
+    res.update(threshold=thr, block_len=bl, score=sc, cap=cap, workspace=workspace)
+    return res
+
+
 def attention_influence(attn: torch.Tensor, masked: torch.Tensor, block_start: int = 0, *, out=None, workspace=None,
                         status=None) -> torch.Tensor:
     """dlm_attention_influence on ``attn`` = [B, L, H, N, N] (unit column
@@ -525,7 +589,7 @@ class StepPlan:
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
                  row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0,
-                 parallel_rules=False, row_tail="auto", dapd_priority="low"):
+                 parallel_rules=False, row_tail="auto", dapd_priority="low", fuse_rules="auto"):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -654,13 +718,54 @@ class StepPlan:
             else:
                 self._calls.append(call)
 
+        # fuse_rules: the threshold, boundary and CAP rules run inside the row
+        # pass (dlm_row_stats_rules: the CTA that finishes a sequence's last
+        # row runs its rules, one after another).  "auto" fuses only the
+        # DepCap chain -- CAP scoped by the boundary, no DAPD -- whose two
+        # rules are serial anyway (DepCap window: 35.4 -> 33.0 us per step);
+        # where the rules run concurrently, or DAPD is the step's tail, the
+        # separate launches are faster (batched 219 vs 242 us, LLaDA-like 43
+        # vs 47 us, tiny 27 vs 37 us)
+        if fuse_rules == "auto":
+            fuse_rules = bool(cap_scope_from_boundary and "dapd" not in rules and "boundary" in rules
+                              and "cap" in rules)
+        self.fused = ()
+        if fuse_rules and row_index is None:
+            main = [n for n in ("threshold", "topk", "factor", "boundary", "cap") if n in rules]
+            if "dapd" in rules and self.side is None:
+                main.append("dapd")
+            by_name = dict(zip(main, self._calls[1:]))
+            fused = [n for n in ("threshold", "boundary", "cap") if n in by_name]
+            if "cap" in fused and (self._cap.p_max > 64 or (cap_scope_from_boundary and "boundary" not in fused)):
+                fused.remove("cap")
+            if fused:
+                bits = ((RULE_THRESHOLD if "threshold" in fused else 0) | (RULE_BOUNDARY if "boundary" in fused else 0)
+                        | (RULE_CAP if "cap" in fused else 0))
+                dep = getattr(self, "_dep", DepcapParams(1.0, 1, 1, 0))
+                capp = self._cap if "cap" in fused else CapParams(0.8, 0.95, -16.0, 1, 0)
+                self._rules = StepRules(bits, float(tau), dep, None, capp,
+                                        int(bool(cap_scope_from_boundary and "cap" in fused)))
+                self.rules_ws = torch.zeros(max(16, L.dlm_row_stats_rules_workspace_size(B)), dtype=torch.uint8,
+                                            device=dev)
+                thr = self.out.get("threshold", (None, None))
+                capo = self.out.get("cap", (None, None))
+                bl = self.block_len if "boundary" in fused else None
+                sc = self.score if "boundary" in fused else None
+                self._calls[0] = (L.dlm_row_stats_rules, (
+                    _p(cur), _p(prev), _dt(cur), B, blk, cur.shape[1], cur.stride(0), _p(self.masked),
+                    ctypes.byref(self._rules), _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
+                    _p(st.lse_prev), _p(thr[0]), _p(thr[1]), _p(bl), _p(sc), _p(capo[0]), _p(capo[1]),
+                    _p(self.rules_ws), self.rules_ws.numel(), _p(self.status)))
+                self._calls = [self._calls[0]] + [by_name[n] for n in main if n not in fused]
+                self.fused = tuple(fused)
+
         # parallel_rules: the independent rules after the row pass run as
         # parallel branches (streams forked and joined inside the step, so a
         # captured graph gets parallel branches too); CAP scoped by the
         # boundary's length stays behind the boundary on one branch
         self._lanes = None
         if parallel_rules and len(self._calls) > 2:
-            names = [n for n in ("threshold", "topk", "factor", "boundary", "cap") if n in rules]
+            names = [n for n in ("threshold", "topk", "factor", "boundary", "cap") if n in rules and n not in self.fused]
             if "dapd" in rules and self.side is None:
                 names.append("dapd")
             assert len(names) == len(self._calls) - 1
@@ -691,7 +796,7 @@ class StepPlan:
         per = {"threshold": 1, "boundary": 1, "cap": 1, "dapd": 2 if self.blk <= 64 else 3, "topk": 1,
                "factor": 1}
         rows = max(0, lib().dlm_row_stats_launches(*self._row_shape))
-        return rows + sum(per[r] for r in self.rules)
+        return rows + sum(per[r] for r in self.rules if r not in self.fused)
 
     def run_rows(self, stream=None, events=None):
         """Issue the row pass (e.g. ahead of a captured graph of the rules,

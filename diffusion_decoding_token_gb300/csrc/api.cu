@@ -167,6 +167,88 @@ dlm_status dlm_row_stats_merge(const dlm_row_partial* partials, int32_t n_shards
                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t dlm_row_stats_rules_workspace_size(int32_t batch) {
+    if (batch < 0 || batch > DLM_MAX_BATCH) return 0;
+    return ((size_t)batch * sizeof(unsigned) + 255) & ~(size_t)255;
+}
+
+dlm_status dlm_row_stats_rules(const void* cur, const void* prev, dlm_dtype dtype, int32_t batch, int32_t blk,
+                               int64_t vocab, int64_t row_stride, const uint8_t* masked,
+                               const dlm_step_rules* rules, int32_t* argmax, float* conf, float* lse,
+                               float* entropy, float* kl, float* lse_prev, uint8_t* thr_selected,
+                               int32_t* thr_n_selected, int32_t* block_len, float* score, uint8_t* cap_selected,
+                               int32_t* cap_n_selected, void* workspace, size_t ws_bytes, uint32_t* dev_status,
+                               dlm_stream_t stream) {
+    if (!rules || batch < 0 || batch > DLM_MAX_BATCH || blk < 1 || blk > DLM_MAX_BLK) return DLM_ERR_INVALID_ARG;
+    const uint32_t on = rules->rules;
+    const uint32_t all = DLM_RULE_THRESHOLD | DLM_RULE_BOUNDARY | DLM_RULE_CAP;
+    if (on == 0 || (on & ~all)) return DLM_ERR_INVALID_ARG;
+    const bool thr = on & DLM_RULE_THRESHOLD, bnd = on & DLM_RULE_BOUNDARY, cap = on & DLM_RULE_CAP;
+    if (rules->cap_scope_from_boundary != 0 && rules->cap_scope_from_boundary != 1) return DLM_ERR_INVALID_ARG;
+    if (rules->cap_scope_from_boundary && !(bnd && cap)) return DLM_ERR_INVALID_ARG;
+    if (bnd) {
+        const dlm_depcap_params& d = rules->depcap;
+        if (d.L_min < 1 || d.smooth_w < 1 || d.smooth_w > 63 || (d.smooth_w % 2) == 0 || d.norm_mode < 0 ||
+            d.norm_mode > 2 || !isfinite(d.lambda))
+            return DLM_ERR_INVALID_ARG;
+    }
+    if (cap) {
+        const dlm_cap_params& c = rules->cap;
+        if (c.p_max < 1 || c.p_max > 64 || (c.high_tier_unconditional != 0 && c.high_tier_unconditional != 1))
+            return DLM_ERR_INVALID_ARG;
+    }
+    const int64_t n_rows = (int64_t)batch * blk;
+    dlm::RowStatsArgs a{};
+    const dlm_status st = row_stats_prepare(a, cur, prev, dtype, n_rows, vocab, row_stride, nullptr);
+    if (st != DLM_OK || batch == 0) return st;
+    if (!masked || !argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    if (thr && (!thr_selected || !thr_n_selected)) return DLM_ERR_INVALID_ARG;
+    if (bnd && (!prev || !kl || !block_len)) return DLM_ERR_INVALID_ARG;
+    if (cap && (!cap_selected || !cap_n_selected)) return DLM_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < dlm_row_stats_rules_workspace_size(batch)) return DLM_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DLM_ERR_ALIGNMENT;
+    a.argmax = argmax;
+    a.conf = conf;
+    a.lse = lse;
+    a.entropy = entropy;
+    a.kl = kl;
+    a.lse_prev = lse_prev;
+    a.dev_status = dev_status;
+    dlm::RowRules r{};
+    r.counter = static_cast<unsigned*>(workspace);
+    r.blk = blk;
+    r.thr = thr;
+    r.bnd = bnd;
+    r.cap = cap;
+    r.t = dlm::ThresholdArgs{conf, masked, batch, blk, rules->tau, thr_selected, thr_n_selected};
+    r.d = dlm::BoundaryArgs{kl, entropy, batch, blk, nullptr, rules->cold_start, rules->depcap.lambda,
+                            rules->depcap.L_min, rules->depcap.smooth_w, rules->depcap.norm_mode, block_len, score};
+    dlm::CapArgs& c = r.c;
+    c.logits = cur;
+    c.dtype = dtype;
+    c.vocab = vocab;
+    c.row_stride = row_stride;
+    c.argmax = argmax;
+    c.conf = conf;
+    c.lse = lse;
+    c.masked = masked;
+    c.scope_len = rules->cap_scope_from_boundary ? block_len : nullptr;
+    c.row_index = nullptr;
+    c.n_rows = n_rows;
+    c.batch = batch;
+    c.blk = blk;
+    c.tau_low = rules->cap.tau_low;
+    c.tau_high = rules->cap.tau_high;
+    c.gamma = rules->cap.gamma;
+    c.p_max = rules->cap.p_max;
+    c.high_tier_unconditional = rules->cap.high_tier_unconditional;
+    c.selected = cap_selected;
+    c.n_selected = cap_n_selected;
+    c.D_out = nullptr;
+    c.dev_status = dev_status;
+    return from_cuda(dlm::launch_row_stats_rules(a, r, dtype, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 dlm_status dlm_select_threshold(const float* conf, const uint8_t* masked, int32_t batch,
                                 int32_t blk, float tau, uint8_t* selected, int32_t* n_selected,
                                 dlm_stream_t stream) {

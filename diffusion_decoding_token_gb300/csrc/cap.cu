@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "rules.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -25,181 +26,15 @@ namespace dlm {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = kRuleThreads;
 constexpr int kMaxPoolWords = DLM_MAX_BLK / 32;  // p_max <= 256
+constexpr int kFusedMaxPool = kCapBlockMaxPool;
 
-__device__ __forceinline__ float load_logit(const void* base, int dtype, int64_t i) {
-    if (dtype == DLM_BF16) return __uint_as_float((uint32_t) static_cast<const uint16_t*>(base)[i] << 16);
-    if (dtype == DLM_F16) return __half2float(static_cast<const __half*>(base)[i]);
-    return static_cast<const float*>(base)[i];
-}
-
-// log p_i(token): the logit of `token` in row `row` minus the row's LSE.  A
-// token outside the vocabulary (an argmax of a row that held only NaN) or a
-// row outside the caller's logits is not read: the value is NaN (never a
-// conflict) and the status word says so.
-__device__ __forceinline__ float logp_at(const CapArgs& a, int row, int token, float lse) {
-    if ((unsigned long long)(int64_t)row >= (unsigned long long)a.n_rows) {
-        raise_status(a.dev_status, DLM_DEV_BAD_INDEX);
-        return __int_as_float(0x7fc00000);
-    }
-    if ((unsigned)token >= (unsigned long long)a.vocab) {
-        raise_status(a.dev_status, DLM_DEV_NONFINITE);
-        return __int_as_float(0x7fc00000);
-    }
-    return load_logit(a.logits, a.dtype, (int64_t)row * a.row_stride + token) - lse;
-}
-
-// Logit row of block position t of sequence b (the caller's row_index, else
-// b*blk + t; within int32 because batch*blk < 2^28).
-__device__ __forceinline__ int row_of(const CapArgs& a, int b, int t) {
-    const int64_t o = (int64_t)b * a.blk + t;
-    return a.row_index ? a.row_index[o] : (int)o;
-}
-
-// The q-th unordered pair (i < j) of n items in row-major order (row i holds
-// (i, i+1) .. (i, n-1)), in closed form: counted from the end, k = T-1-q falls
-// in the block of the last r+1 rows with r(r+1)/2 <= k < (r+1)(r+2)/2.
-__device__ __forceinline__ void pair_of(int q, int n, int& i, int& j) {
-    const int T = n * (n - 1) / 2;
-    const int k = T - 1 - q;
-    int r = (int)((sqrtf(8.0f * (float)k + 1.0f) - 1.0f) * 0.5f);
-    while ((r + 1) * (r + 2) / 2 <= k) ++r;  // correct a rounding of the root
-    while (r * (r + 1) / 2 > k) --r;
-    i = n - 2 - r;
-    j = n - 1 - (k - r * (r + 1) / 2);
-}
-
-__device__ __forceinline__ int scope_of(const CapArgs& a, int b) {
-    int sc = a.blk;
-    if (a.scope_len) sc = min(sc, max(0, a.scope_len[b]));
-    return sc;
-}
-
-// Small pools (p_max <= kFusedMaxPool): the three phases in one CTA per
-// sequence, the pool, its tokens / LSEs and the conflict bitmask in shared
-// memory.  D is symmetric (the two log-probabilities are added in either
-// order, and fp32 addition commutes), so each unordered pair is scored once
-// and both bits are set.
-constexpr int kFusedMaxPool = 64;
-constexpr int kFusedWords = kFusedMaxPool / 32;
-constexpr int kPairUnroll = 4;  // 64 * 63 / 2 pairs = 8 per thread at most
-
+// Small pools (p_max <= kFusedMaxPool): pool, conflict scores and greedy in
+// one CTA per sequence (rules.cuh: cap_block).
 __global__ void __launch_bounds__(kThreads) cap_fused_kernel(CapArgs a) {
-    __shared__ __align__(16) float s_c[kThreads];
-    __shared__ __align__(4) unsigned char s_cand[kThreads];
-    __shared__ int s_pool[kFusedMaxPool];
-    __shared__ int s_row[kFusedMaxPool];
-    __shared__ int s_y[kFusedMaxPool];
-    __shared__ float s_lse[kFusedMaxPool];
-    __shared__ uint32_t s_adj[kFusedMaxPool * kFusedWords];
-    __shared__ uint32_t s_kept[kFusedWords];
-    __shared__ unsigned char s_tier[kFusedMaxPool];
-    __shared__ float s_v[kThreads / 32];
-    __shared__ int s_i[kThreads / 32];
-    const int b = blockIdx.x, t = threadIdx.x;
-    const int scope = scope_of(a, b);
-    const int64_t o = (int64_t)b * a.blk + t;
-    uint8_t* sel = a.selected + (int64_t)b * a.blk;
-
-    // 1. pool: masked in scope with conf >= tau_low, by (conf desc, position asc);
-    // the token, LSE and logit row are loaded with the confidence (one round trip)
-    const bool in = t < a.blk;
-    const bool m = t < scope && a.masked[o] != 0;
-    const float c = in ? a.conf[o] : 0.f;
-    const int y = in ? a.argmax[o] : 0;
-    const float l = in ? a.lse[o] : 0.f;
-    const bool cand = m && c >= a.tau_low;
-    const int row = cand ? row_of(a, b, t) : 0;
-    s_c[t] = c;
-    s_cand[t] = cand;
-    if (t < kFusedMaxPool * kFusedWords) s_adj[t] = 0u;
-    const int n_cand = __syncthreads_count(cand);
-    const int n = min(n_cand, a.p_max);
-    if (cand) {
-        const int rank = rank_desc(s_c, s_cand, (scope + 3) & ~3, c, t);
-        if (rank < a.p_max) {
-            s_pool[rank] = t;
-            s_row[rank] = row;
-            s_y[rank] = y;
-            s_lse[rank] = l;
-            s_tier[rank] = a.high_tier_unconditional && c >= a.tau_high;
-        }
-    }
-    if (t < a.blk) sel[t] = 0;
-    if (t == 0 && n_cand > a.p_max) raise_status(a.dev_status, DLM_DEV_POOL_CLIPPED);
-    __syncthreads();
-
-    if (n == 0) {  // no candidate: the highest-confidence masked position of the scope
-        float v = m ? c : -INFINITY;
-        int idx = m ? t : 0x7fffffff;
-        const int any_m = __syncthreads_or(m);
-        warp_argmax(v, idx);
-        if ((t & 31) == 0) {
-            s_v[t >> 5] = v;
-            s_i[t >> 5] = idx;
-        }
-        __syncthreads();
-        if (t < 32) {
-            v = t < kThreads / 32 ? s_v[t] : -INFINITY;
-            idx = t < kThreads / 32 ? s_i[t] : 0x7fffffff;
-            warp_argmax(v, idx);
-            if (t == 0) {
-                if (any_m) sel[idx] = 1;
-                a.n_selected[b] = any_m ? 1 : 0;
-            }
-        }
-        return;
-    }
-
-    // 2. conflicts: unordered pairs (i < j) of pool slots, kPairUnroll per
-    // thread at a time with all their scattered logit loads issued together
-    const int pairs = n * (n - 1) / 2;
-    for (int q0 = t; q0 < pairs; q0 += kThreads * kPairUnroll) {
-        // an index past the last pair maps to the pair (0, 1), which exists
-        // (pairs >= 1), and its result is dropped
-        int pi[kPairUnroll], pj[kPairUnroll];
-        float z1[kPairUnroll], z2[kPairUnroll];
-#pragma unroll
-        for (int u = 0; u < kPairUnroll; ++u) {
-            pair_of(min(q0 + u * kThreads, pairs - 1), n, pi[u], pj[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < kPairUnroll; ++u) {
-            z1[u] = logp_at(a, s_row[pi[u]], s_y[pj[u]], s_lse[pi[u]]);
-            z2[u] = logp_at(a, s_row[pj[u]], s_y[pi[u]], s_lse[pj[u]]);
-        }
-#pragma unroll
-        for (int u = 0; u < kPairUnroll; ++u) {
-            if (q0 + u * kThreads >= pairs) break;
-            const int i = pi[u], j = pj[u];
-            const float d = z1[u] + z2[u];
-            if (d > a.gamma) {
-                atomicOr(&s_adj[i * kFusedWords + (j >> 5)], 1u << (j & 31));
-                atomicOr(&s_adj[j * kFusedWords + (i >> 5)], 1u << (i & 31));
-            }
-            if (a.D_out) {
-                a.D_out[((int64_t)b * a.blk + s_pool[i]) * a.blk + s_pool[j]] = d;
-                a.D_out[((int64_t)b * a.blk + s_pool[j]) * a.blk + s_pool[i]] = d;
-            }
-        }
-    }
-    __syncthreads();
-
-    // 3. greedy over the pool order
-    const int W = (n + 31) >> 5;
-    if (t < 32) {
-        const uint32_t kept = greedy_scan_chunked(s_adj, kFusedWords, s_tier, n);  // slots are in pool order
-        if (t < W) s_kept[t] = kept;
-    }
-    __syncthreads();
-    int mine = 0;
-    if (t < n && ((s_kept[t >> 5] >> (t & 31)) & 1u)) {
-        sel[s_pool[t]] = 1;
-        mine = 1;
-    }
-    const int total = __syncthreads_count(mine);
-    if (t == 0) a.n_selected[b] = total;
+    __shared__ CapSmem sm;
+    cap_block(a, blockIdx.x, sm);
 }
 
 // Large pools (p_max > kFusedMaxPool): one thread-block cluster of kCapCluster

@@ -175,6 +175,20 @@ cudaError_t launch_dapd(DapdArgs& a, int num_sms, cudaStream_t s);  // attention
 // selection rebuilds the graph from the sums itself)
 cudaError_t launch_dapd_graph(DapdArgs& a, int num_sms, cudaStream_t s, bool graph_kernel);
 cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s);  // (graph +) conf -> selection
+
+// The fused row pass: after the rows of sequence b are all written, the CTA
+// that wrote the last of them runs b's threshold, boundary and CAP rules
+// (rules.cuh) with the arguments below; counter[b] counts finished rows and
+// is reset to 0 by that CTA.  Rows are b*blk + i (no row index).
+struct RowRules {
+    unsigned* counter;  // [batch], zero before a call, left zero after it
+    int blk;
+    int thr, bnd, cap;  // which rules run (CAP reads the boundary's length when c.scope_len is set)
+    ThresholdArgs t;
+    BoundaryArgs d;
+    CapArgs c;
+};
+cudaError_t launch_row_stats_rules(const RowStatsArgs& a, const RowRules& r, int dtype, cudaStream_t s);
 // attention -> sums (every sequence) -> infl[b][j] = column sums over masked rows / (L H)
 cudaError_t launch_attention_influence(DapdArgs& a, int num_sms, float* infl, cudaStream_t s);
 

@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "rules.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -313,8 +314,24 @@ __device__ __forceinline__ void write_outputs(const RowStatsArgs& args, const Pa
     if (!ok) raise_status(args.dev_status, DLM_DEV_NONFINITE);
 }
 
-template <int DT, bool PREV>
-__global__ void __launch_bounds__(kThreads, 4) row_stats_kernel(RowStatsArgs args) {  // 4 CTAs per SM
+// The rules the CTA that finishes a sequence's last row runs (fused row
+// pass); one shared-memory area serves them in turn.
+union RuleSmem {
+    ThresholdSmem t;
+    BoundarySmem<DLM_MAX_BLK> d;
+    CapSmem c;
+};
+
+__device__ __forceinline__ void run_rules(const RowRules& rr, int b, RuleSmem& sm) {
+    if (rr.thr) threshold_block(rr.t, b, sm.t);
+    __syncthreads();
+    if (rr.bnd) boundary_block<DLM_MAX_BLK>(rr.d, b, sm.d);
+    __syncthreads();  // the block length is visible to CAP's scope
+    if (rr.cap) cap_block(rr.c, b, sm.c);
+}
+
+template <int DT, bool PREV, bool RULES>
+__device__ __forceinline__ void row_stats_body(const RowStatsArgs& args, const RowRules* rules) {
     constexpr int EPV = Fmt<DT>::EPV;
     constexpr int ESZ = Fmt<DT>::ESZ;
     __shared__ Part s_warp[kWarps];
@@ -433,17 +450,53 @@ __global__ void __launch_bounds__(kThreads, 4) row_stats_kernel(RowStatsArgs arg
     // a tail launch overlapping the previous grid completes only after it, so
     // whatever follows on the stream sees both grids' results
     if (args.wait_prior && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (rank != 0 || threadIdx.x != 0) return;
-    // where this row's results go, recomputed here so that nothing extra is
-    // live across the streaming loop: q (default) or r (gathered outputs)
-    const int64_t r_out = args.row_base + blockIdx.x / split;
-    const int64_t out = (args.gather || !args.row_index) ? r_out : (int64_t)args.row_index[r_out];
-    if (args.partial) {  // a slice of the row: its state, positions made global
-        if (p.idx != 0x7fffffff) p.idx += (int)args.vocab_offset;
-        static_cast<Part*>(args.partial)[out] = p;
-        return;
+    if constexpr (!RULES) {
+        if (rank != 0 || threadIdx.x != 0) return;
+        // where this row's results go, recomputed here so that nothing extra is
+        // live across the streaming loop: q (default) or r (gathered outputs)
+        const int64_t r_out = args.row_base + blockIdx.x / split;
+        const int64_t out = (args.gather || !args.row_index) ? r_out : (int64_t)args.row_index[r_out];
+        if (args.partial) {  // a slice of the row: its state, positions made global
+            if (p.idx != 0x7fffffff) p.idx += (int)args.vocab_offset;
+            static_cast<Part*>(args.partial)[out] = p;
+            return;
+        }
+        write_outputs<PREV>(args, p, out);
+    } else {
+        // fused rules: rows are b*blk + i.  The row's outputs are published
+        // (fence, then the count); the CTA whose row completes sequence b's
+        // count reads the other rows' outputs at L2 and runs b's rules.  No
+        // CTA waits for another.
+        __shared__ int s_seq;
+        __shared__ RuleSmem s_rules;
+        if (rank != 0) return;
+        if (threadIdx.x == 0) {
+            const int64_t out = args.row_base + blockIdx.x / split;
+            write_outputs<PREV>(args, p, out);
+            __threadfence();
+            const int b = (int)(out / rules->blk);
+            const unsigned done = atomicAdd(rules->counter + b, 1u) + 1u;
+            s_seq = done == (unsigned)rules->blk ? b : -1;
+        }
+        __syncthreads();
+        const int b = s_seq;
+        if (b < 0) return;
+        __threadfence();
+        if (threadIdx.x == 0) rules->counter[b] = 0u;  // zero again for the next call
+        run_rules(*rules, b, s_rules);
     }
-    write_outputs<PREV>(args, p, out);
+}
+
+template <int DT, bool PREV>
+__global__ void __launch_bounds__(kThreads, 4) row_stats_kernel(RowStatsArgs args) {  // 4 CTAs per SM
+    row_stats_body<DT, PREV, false>(args, nullptr);
+}
+
+// The row pass with the fused rules epilogue (few-row launches; no occupancy
+// floor, the epilogue's shared memory and registers come on top of the pass's).
+template <int DT, bool PREV>
+__global__ void __launch_bounds__(kThreads) row_stats_rules_kernel(RowStatsArgs args, RowRules rules) {
+    row_stats_body<DT, PREV, true>(args, &rules);
 }
 
 // Merge the partial states of n_shards slices of each row (slice order fixed)
@@ -470,22 +523,24 @@ __global__ void __launch_bounds__(256) row_merge_kernel(RowStatsArgs args, const
 // longer tail, were slower: the cluster merge costs more than they save).
 constexpr int kTailSplit = 2;
 
-template <int DT, bool PREV>
+template <int DT, bool PREV, bool RULES = false>
 int64_t tail_rows(const RowStatsArgs& a) {
     if (a.split != 1 || a.num_sms <= 0 || a.partial || a.single_grid) return 0;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<DT, PREV>, kThreads, 0) !=
-            cudaSuccess ||
-        per_sm <= 0)
-        return 0;
+    cudaError_t e;
+    if constexpr (RULES)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_rules_kernel<DT, PREV>, kThreads, 0);
+    else
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<DT, PREV>, kThreads, 0);
+    if (e != cudaSuccess || per_sm <= 0) return 0;
     const int64_t slots = (int64_t)a.num_sms * per_sm;
     const int64_t nvec = a.vocab / Fmt<DT>::EPV;
     if (a.n_rows <= slots || nvec / kTailSplit < 2LL * kThreads) return 0;
     return a.n_rows % slots;
 }
 
-template <int DT, bool PREV>
-cudaError_t launch_grid(const RowStatsArgs& a, bool programmatic, cudaStream_t s) {
+template <int DT, bool PREV, bool RULES = false>
+cudaError_t launch_grid(const RowStatsArgs& a, bool programmatic, cudaStream_t s, const RowRules* rules = nullptr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.n_rows * a.split));
     cfg.blockDim = dim3(kThreads);
@@ -507,23 +562,26 @@ cudaError_t launch_grid(const RowStatsArgs& a, bool programmatic, cudaStream_t s
     }
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, row_stats_kernel<DT, PREV>, a);
+    if constexpr (RULES)
+        return cudaLaunchKernelEx(&cfg, row_stats_rules_kernel<DT, PREV>, a, *rules);
+    else
+        return cudaLaunchKernelEx(&cfg, row_stats_kernel<DT, PREV>, a);
 }
 
-template <int DT, bool PREV>
-cudaError_t launch_typed(const RowStatsArgs& a, cudaStream_t s) {
-    const int64_t tail = tail_rows<DT, PREV>(a);
-    if (tail == 0) return launch_grid<DT, PREV>(a, false, s);
+template <int DT, bool PREV, bool RULES = false>
+cudaError_t launch_typed(const RowStatsArgs& a, cudaStream_t s, const RowRules* rules = nullptr) {
+    const int64_t tail = tail_rows<DT, PREV, RULES>(a);
+    if (tail == 0) return launch_grid<DT, PREV, RULES>(a, false, s, rules);
     RowStatsArgs head = a;
     head.n_rows = a.n_rows - tail;
-    cudaError_t e = launch_grid<DT, PREV>(head, false, s);
+    cudaError_t e = launch_grid<DT, PREV, RULES>(head, false, s, rules);
     if (e != cudaSuccess) return e;
     RowStatsArgs rest = a;
     rest.row_base = a.n_rows - tail;
     rest.n_rows = tail;
     rest.split = kTailSplit;
     rest.wait_prior = 1;
-    return launch_grid<DT, PREV>(rest, true, s);
+    return launch_grid<DT, PREV, RULES>(rest, true, s, rules);
 }
 
 template <int DT, bool PREV>
@@ -565,5 +623,17 @@ cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s) {
 }
 
 int row_stats_threads() { return kThreads; }
+
+cudaError_t launch_row_stats_rules(const RowStatsArgs& a, const RowRules& r, int dtype, cudaStream_t s) {
+    const bool prev = a.prev != nullptr;
+    switch (dtype) {
+    case DLM_BF16:
+        return prev ? launch_typed<DLM_BF16, true, true>(a, s, &r) : launch_typed<DLM_BF16, false, true>(a, s, &r);
+    case DLM_F16:
+        return prev ? launch_typed<DLM_F16, true, true>(a, s, &r) : launch_typed<DLM_F16, false, true>(a, s, &r);
+    default:
+        return prev ? launch_typed<DLM_F32, true, true>(a, s, &r) : launch_typed<DLM_F32, false, true>(a, s, &r);
+    }
+}
 
 }  // namespace dlm

@@ -349,6 +349,64 @@ dlm_status dlm_cap_select(const void* logits, dlm_dtype dtype, int64_t vocab, in
                           uint32_t* dev_status, dlm_stream_t stream);
 
 /*
+ * dlm_row_stats_rules -- dlm_row_stats with the threshold, boundary and CAP
+ * rules folded into the same launch.
+ *
+ * Computes exactly what these calls compute one after another on rows
+ * b*blk + i (b < batch, i < blk): dlm_row_stats (no row index), then, for
+ * the rules asked for in rules->rules, dlm_select_threshold(conf, masked,
+ * tau), dlm_depcap_boundary(kl, entropy, L_window = blk, cold_start,
+ * depcap) and dlm_cap_select(cur, no row index, argmax, conf, lse, masked,
+ * scope = this call's block_len when cap_scope_from_boundary, else the
+ * whole block; cap).  The rules of sequence b run in the CTA that writes the
+ * last of b's rows (the one whose row completes b's count in the
+ * workspace), so they overlap the rest of the row pass instead of following
+ * it as separate launches; no CTA waits for another.  This is a library
+ * arrangement with no counterpart on the pages (DepCap, "Methodology" and
+ * the Fast-dLLM review, "Method", define the rules; dlm_row_stats,
+ * dlm_select_threshold, dlm_depcap_boundary and dlm_cap_select cite them).
+ *
+ * cur, prev, dtype, vocab, row_stride : as dlm_row_stats (batch*blk rows;
+ *                      prev is required for the boundary rule).
+ * masked              : uint8 [batch][blk].
+ * rules               : DLM_RULE_* bits and the rules' parameters (CAP:
+ *                      p_max <= 64).
+ * argmax .. lse_prev  : the row statistics, as dlm_row_stats ([batch*blk]).
+ * thr_selected, thr_n_selected : threshold outputs (required with
+ *                      DLM_RULE_THRESHOLD), as dlm_select_threshold.
+ * block_len, score    : boundary outputs (block_len required with
+ *                      DLM_RULE_BOUNDARY; score nullable [batch][blk]).
+ * cap_selected, cap_n_selected : CAP outputs (required with DLM_RULE_CAP).
+ * workspace           : dlm_row_stats_rules_workspace_size(batch) bytes,
+ *                      16-byte aligned, ZERO before the first call (e.g.
+ *                      one cudaMemsetAsync); every call leaves it zero.
+ *                      Calls sharing a workspace must not overlap.
+ * Sizes: 1 <= blk <= 256; batch*blk rows.
+ */
+#define DLM_RULE_THRESHOLD 1u
+#define DLM_RULE_BOUNDARY 2u
+#define DLM_RULE_CAP 4u
+
+typedef struct dlm_step_rules {
+    uint32_t rules;                  /* OR of DLM_RULE_* (at least one) */
+    float tau;                       /* threshold rule */
+    dlm_depcap_params depcap;        /* boundary rule */
+    const uint8_t* cold_start;       /* boundary rule: nullable device [batch] */
+    dlm_cap_params cap;              /* CAP rule: p_max 1..64 */
+    int32_t cap_scope_from_boundary; /* 0 or 1 (needs DLM_RULE_BOUNDARY) */
+} dlm_step_rules;
+
+size_t dlm_row_stats_rules_workspace_size(int32_t batch);
+
+dlm_status dlm_row_stats_rules(const void* cur, const void* prev, dlm_dtype dtype, int32_t batch, int32_t blk,
+                               int64_t vocab, int64_t row_stride, const uint8_t* masked,
+                               const dlm_step_rules* rules, int32_t* argmax, float* conf, float* lse,
+                               float* entropy, float* kl, float* lse_prev, uint8_t* thr_selected,
+                               int32_t* thr_n_selected, int32_t* block_len, float* score, uint8_t* cap_selected,
+                               int32_t* cap_n_selected, void* workspace, size_t ws_bytes, uint32_t* dev_status,
+                               dlm_stream_t stream);
+
+/*
  * dlm_dapd_graph_mis -- DAPD: attention graph and Welsh-Powell selection.
  *
  * DAPD, "整体框架" and "关键设计 1-3".  V_t = masked positions of the block,

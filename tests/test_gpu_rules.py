@@ -12,6 +12,8 @@ decision margins of ``parity.py`` (sequences that miss one are redrawn):
 An unscreened draw of each workload is checked too: there the GPU's result
 must be one that some resolution of the near-tied decisions gives.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -851,3 +853,123 @@ def test_dapd_random_shapes(dlm, trial):
         if r["path"][b] == 0:
             nodes = np.nonzero(masked[b])[0]
             np.testing.assert_array_equal(deg.cpu().numpy()[b][nodes], r["deg"][b][nodes])
+
+
+# ------------------------------------------------------- fused row pass + rules
+FUSED = ["tiny", "llada_step", "depcap_window", "batched"]
+
+
+@pytest.mark.parametrize("name", FUSED)
+def test_fused_rules_match_oracle(dlm, name):
+    """dlm_row_stats_rules (threshold, boundary and CAP run by the CTA that
+    finishes each sequence's last row) on the screened workloads: every
+    decision equals the oracle's, the statistics match it within 1e-4, and a
+    second call on the same workspace (its counters left at zero) gives the
+    same results."""
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    B, blk = cfg.batch, cfg.blk
+    rules = tuple(r for r in cfg.rules if r in ("threshold", "boundary", "cap"))
+    ws = dlm.row_stats_rules_workspace(B, "cuda")
+    outs = []
+    for _ in range(2):
+        st = dlm.new_status()
+        r = dlm.row_stats_rules(dw.cur, dw.prev, dw.masked, rules=rules, tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min,
+                                tau_low=cfg.tau_low, tau_high=cfg.tau_high, gamma=cfg.gamma, p_max=cfg.p_max,
+                                cap_scope_from_boundary=(name == "depcap_window"), workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        sel = {k: r[k][0].cpu().numpy() for k in ("threshold", "cap") if k in rules}
+        block_len = r["block_len"].cpu().numpy() if "boundary" in rules else None
+        w3 = dataclasses.replace(w, cfg=synth.scaled(cfg, rules=rules))      # the three fused rules only
+        assert check_rules_exact(name, w3, o, sel, block_len) == B * len(rules)
+        g = r["stats"]
+        for k in ("conf", "lse", "entropy", "kl"):
+            assert close(getattr(g, k).cpu().numpy(), o[k]).all(), k
+        np.testing.assert_array_equal(g.argmax.cpu().numpy(), o["argmax"])
+        outs.append((sel, block_len))
+        assert int(ws.sum().item()) == 0                      # the counters are back at zero
+    for k in outs[0][0]:
+        np.testing.assert_array_equal(outs[0][0][k], outs[1][0][k])
+
+
+@pytest.mark.parametrize("trial", range(10))
+def test_fused_rules_random_shapes(dlm, trial):
+    """Random blocks (1-256 positions, pools up to 64), vocabularies, masks,
+    cold starts and rule subsets: the fused call's rule outputs equal the
+    separate rule calls run on the fused call's own statistics, and its
+    statistics equal a plain row pass within 1e-5."""
+    rng = np.random.default_rng(900 + trial)
+    blk = int(rng.integers(1, 257))
+    B = int(rng.integers(1, 6))
+    V = int(rng.integers(1, 200)) * 8
+    z = rng.standard_normal((B * blk, V)).astype(np.float32)
+    tok = rng.integers(0, V, B * blk)
+    boost = rng.random(B * blk) < 0.7
+    z[np.arange(B * blk)[boost], tok[boost]] += rng.uniform(4, 12, int(boost.sum())).astype(np.float32)
+    for r_ in range(0, B * blk - 1, 4):
+        z[r_, tok[r_ + 1]] = z[r_, tok[r_]] - 3
+    zp = z + (rng.standard_normal(z.shape) * 0.4).astype(np.float32)
+    cur, prev = cuda(z), cuda(zp)
+    masked = cuda((rng.random((B, blk)) < rng.uniform(0.3, 1.0)).astype(np.uint8))
+    cold = cuda((rng.random(B) < 0.3).astype(np.uint8))
+    subsets = [("threshold", "boundary", "cap"), ("threshold",), ("boundary", "cap"), ("cap",), ("boundary",)]
+    rules = subsets[trial % len(subsets)]
+    scoped = "boundary" in rules and "cap" in rules and trial % 2 == 0
+    p_max = int(rng.integers(1, min(64, blk) + 1))
+    L_min = int(rng.integers(1, 9))
+    kw = dict(tau=0.9, lam=1.2, L_min=L_min, tau_low=0.8, tau_high=0.95, gamma=-16.0, p_max=p_max)
+    r = dlm.row_stats_rules(cur, prev, masked, rules=rules, cold_start=cold, cap_scope_from_boundary=scoped, **kw)
+    g = r["stats"]
+    plain = dlm.row_stats(cur, prev)
+    for k in ("conf", "lse", "entropy", "kl"):
+        np.testing.assert_allclose(getattr(g, k).cpu().numpy(), getattr(plain, k).cpu().numpy(), rtol=1e-5,
+                                   atol=1e-5)
+    conf, lse, am = g.conf.view(B, blk), g.lse.view(B, blk), g.argmax.view(B, blk)
+    if "threshold" in rules:
+        s, n = dlm.select_threshold(conf, masked, 0.9)
+        np.testing.assert_array_equal(r["threshold"][0].cpu().numpy(), s.cpu().numpy())
+        np.testing.assert_array_equal(r["threshold"][1].cpu().numpy(), n.cpu().numpy())
+    if "boundary" in rules:
+        bl, sc = dlm.depcap_boundary(g.kl.view(B, blk), g.entropy.view(B, blk), 1.2, L_min, cold_start=cold)
+        np.testing.assert_array_equal(r["block_len"].cpu().numpy(), bl.cpu().numpy())
+        np.testing.assert_array_equal(r["score"].cpu().numpy(), sc.cpu().numpy())
+    if "cap" in rules:
+        s, n = dlm.cap_select(cur, am, conf, lse, masked, 0.8, 0.95, -16.0, p_max,
+                              scope_len=r["block_len"] if scoped else None)
+        np.testing.assert_array_equal(r["cap"][0].cpu().numpy(), s.cpu().numpy())
+        np.testing.assert_array_equal(r["cap"][1].cpu().numpy(), n.cpu().numpy())
+
+
+@pytest.mark.parametrize("name", ["batched", "depcap_window", "llada_step"])
+def test_bench_launch_configuration_fused_rules(dlm, name):
+    """The benchmark's step with the rules fused into the row pass (StepPlan
+    fuse_rules), captured as two back-to-back steps in a CUDA graph, against
+    the oracle."""
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    kw = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
+              gamma=cfg.gamma, p_max=cfg.p_max, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
+              bulk_frac=cfg.bulk_frac, rules=tuple(cfg.rules), cap_scope_from_boundary=(cfg.name == "depcap_window"),
+              concurrent_dapd=True, dapd_early=True, parallel_rules=True, fuse_rules=True)
+    if "dapd" in cfg.rules:
+        kw.update(attn=dw.attn, block_start=dw.block_start)
+    plan = dlm.StepPlan(dw.cur, dw.prev, dw.masked, **kw)
+    assert set(plan.fused) == {r for r in cfg.rules if r != "dapd"}
+    _, hi = torch.cuda.Stream.priority_range()
+    main = torch.cuda.Stream(priority=hi)
+    with torch.cuda.stream(main):
+        plan.run(main)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            for _ in range(2):
+                plan.run(main)
+        for v in plan.out.values():
+            v[0].fill_(7)
+        g.replay()
+    torch.cuda.synchronize()
+    sel = {k: v[0].cpu().numpy() for k, v in plan.out.items()}
+    block_len = None if plan.block_len is None else plan.block_len.cpu().numpy()
+    assert check_rules_exact(name, w, o, sel, block_len) == cfg.batch * len(cfg.rules)
+    assert int(plan.status.item()) == 0
