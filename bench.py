@@ -478,50 +478,70 @@ def run_native(args, rank, world, local, light=False):
     # --- end to end through host buffers (pinned), same public API.  Each step
     # uploads its new logits, its attention block and its mask, decides, and
     # reads the selections back.  As in a decode loop, the previous step's
-    # logits are the previous step's upload and stay resident as `prev`: two
-    # device buffers alternate (step k reads D[k % 2] as cur, D[(k + 1) % 2] as
-    # prev), fed from two pinned host buffers that alternate the same way.
+    # logits are the previous step's upload and stay resident as `prev`.  The
+    # uploads are pipelined: three device sets rotate (step k reads logits
+    # D[k % 3] as cur and D[(k - 1) % 3] as prev, with attention and mask set
+    # k % 3), and step k+1's upload runs on a copy stream while step k
+    # decides, after step k-1 -- the last reader of the set it overwrites --
+    # has finished.  Every step's copies are inside the timed region.
     e2e = None
     if args.e2e_steps > 0:
-        host_rows = [prev.cpu().pin_memory(), cur.cpu().pin_memory()]
+        NB = 3
+        host_rows = [t.cpu().pin_memory() for t in (cur, prev, cur)]
         attn_h = None if w.attn is None else (torch.from_numpy(w.attn) if cfg.attn_dtype == synth.F32 else
                                               torch.from_numpy(w.attn.view(np.int16)).view(tdt[cfg.attn_dtype]))
         attn_h = None if attn_h is None else attn_h.pin_memory()
         masked_h = torch.from_numpy(w.masked).pin_memory()
-        dev_rows = [prev.clone(), cur.clone()]
-        attn_c = None if attn_h is None else torch.empty(attn_h.shape, dtype=attn_h.dtype, device=dev)
-        masked_d2 = torch.empty_like(masked)
+        dev_rows = [cur.clone() for _ in range(NB)]
+        attn_c = [None if attn_h is None else torch.empty(attn_h.shape, dtype=attn_h.dtype, device=dev)
+                  for _ in range(NB)]
+        masked_d = [torch.empty_like(masked) for _ in range(NB)]
         blen_h = torch.empty(B, dtype=torch.int32).pin_memory()
-
-        plans2 = [dlm.StepPlan(dev_rows[j], dev_rows[1 - j], masked_d2, attn=attn_c, block_start=0,
-                               row_index=row_index, **common) for j in range(2)]
+        plans2 = [dlm.StepPlan(dev_rows[j], dev_rows[(j - 1) % NB], masked_d[j], attn=attn_c[j], block_start=0,
+                               row_index=row_index, **common) for j in range(NB)]
         outs_h = {k: torch.empty((B, blk), dtype=torch.uint8).pin_memory() for k in plans2[0].out}
         nsel_h = {k: torch.empty(B, dtype=torch.int32).pin_memory() for k in plans2[0].out}
-        e2e_k = [0]
+        copy_stream = torch.cuda.Stream(device=dev)
+        up_done = [torch.cuda.Event() for _ in range(NB)]
+        step_done = [torch.cuda.Event() for _ in range(NB)]
 
-        def e2e_step():
-            j = e2e_k[0] % 2
-            e2e_k[0] += 1
+        def upload(k):
+            j = k % NB
+            with torch.cuda.stream(copy_stream):
+                if k >= 2:   # step k-2 (prev = logits set k % 3) is the set's last reader
+                    copy_stream.wait_event(step_done[(k - 2) % NB])
+                dev_rows[j].copy_(host_rows[j], non_blocking=True)
+                if attn_c[j] is not None:
+                    attn_c[j].copy_(attn_h, non_blocking=True)
+                masked_d[j].copy_(masked_h, non_blocking=True)
+                up_done[j].record(copy_stream)
+
+        def decide(k):
+            j = k % NB
             p = plans2[j]
-            dev_rows[j].copy_(host_rows[j], non_blocking=True)
-            if attn_c is not None:
-                attn_c.copy_(attn_h, non_blocking=True)
-            masked_d2.copy_(masked_h, non_blocking=True)
+            stream.wait_event(up_done[j])
             p.run(stream)
-            for k in p.out:
-                outs_h[k].copy_(p.out[k][0], non_blocking=True)
-                nsel_h[k].copy_(p.out[k][1], non_blocking=True)
+            for key in p.out:
+                outs_h[key].copy_(p.out[key][0], non_blocking=True)
+                nsel_h[key].copy_(p.out[key][1], non_blocking=True)
             if p.block_len is not None:
                 blen_h.copy_(p.block_len, non_blocking=True)
+            step_done[j].record(stream)
 
-        for _ in range(2):  # both device buffers hold an upload before the timed steps
-            e2e_step()
+        def run_e2e(n):
+            upload(0)
+            for k in range(n):
+                if k + 1 < n:
+                    upload(k + 1)
+                decide(k)
+
+        run_e2e(NB + 1)                     # warm-up: every set used once
         torch.cuda.synchronize()
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        copy_stream.wait_event(a0)
+        run_e2e(args.e2e_steps)
         a1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = a0.elapsed_time(a1) / args.e2e_steps
@@ -530,7 +550,8 @@ def run_native(args, rank, world, local, light=False):
         d2h = (sum(t.numel() for t in outs_h.values()) + sum(t.numel() * 4 for t in nsel_h.values())
                + (blen_h.numel() * 4 if plans2[0].block_len is not None else 0))
         e2e = {"ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "prev": "resident: the previous step's upload"}
+               "prev": "resident: the previous step's upload",
+               "pipeline": "step k+1's upload (copy stream) overlaps step k's decisions; three device sets rotate"}
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())} during the end-to-end steps")
 
