@@ -320,13 +320,16 @@ def test_pipeline_unscreened(dlm, name):
     assert unique + ambiguous == cfg.batch * len(cfg.rules)
 
 
+@pytest.mark.parametrize("mode", ["rules", "whole"])
 @pytest.mark.parametrize("name", ["batched", "stress_graph", "depcap_window"])
-def test_bench_launch_configuration_matches_oracle(dlm, name):
+def test_bench_launch_configuration_matches_oracle(dlm, name, mode):
     """The step as the benchmark times it -- one StepPlan with the DAPD
     attention pass on a side stream from the step's start, the other rules as
-    parallel graph branches, the row pass's tail grid where it applies, steps
-    captured back to back in one CUDA graph with timing events -- at full
-    size, against the oracle."""
+    parallel graph branches, the row pass's tail grid where it applies; two
+    steps back to back, either as the benchmark's default runs them (row pass
+    and DAPD chain launched, the rules replayed as a captured graph, timing
+    events around the row pass) or captured whole in one CUDA graph with
+    external timing events -- at full size, against the oracle."""
     w, dw, o = workload(name)
     cfg = w.cfg
     kw = dict(tau=cfg.tau, lam=cfg.lam, L_min=cfg.L_min, tau_low=cfg.tau_low, tau_high=cfg.tau_high,
@@ -338,18 +341,31 @@ def test_bench_launch_configuration_matches_oracle(dlm, name):
     plan = dlm.StepPlan(dw.cur, dw.prev, dw.masked, row_index=dw.row_index, **kw)
     _, hi = torch.cuda.Stream.priority_range()
     main = torch.cuda.Stream(priority=hi)
-    evs = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-           for _ in range(2)]
+    external = mode == "whole"
+    evs = [(torch.cuda.Event(enable_timing=True, external=external),
+            torch.cuda.Event(enable_timing=True, external=external)) for _ in range(2)]
     with torch.cuda.stream(main):
         plan.run(main)
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=main):
-            for e in evs:
-                plan.run(main, events=e)
+        g = None
+        if external or plan.has_rules_after_rows:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=main):
+                if external:
+                    for e in evs:
+                        plan.run(main, events=e)
+                else:
+                    plan.run(rules_only=True)
         for v in plan.out.values():
             v[0].fill_(7)
-        g.replay()
+        if external:
+            g.replay()
+        else:
+            for e in evs:
+                plan.run_rows(main, events=e)
+                if g is not None:
+                    g.replay()
+                plan.join(main)
     torch.cuda.synchronize()
     sel = {k: v[0].cpu().numpy() for k, v in plan.out.items()}
     block_len = None if plan.block_len is None else plan.block_len.cpu().numpy()
