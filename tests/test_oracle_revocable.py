@@ -84,6 +84,7 @@ def test_seed_count_and_score_against_numpy():
     infl = rng.random((B, blk)) * 3
     drift = rng.random((B, blk)) * 0.5
     am = np.zeros((B, blk), np.int32)
+    checked = 0
     for pi in (0.3, 1.0, 2.5):
         st = oracle.revocable_init(B, blk)
         st["masked"][:] = (rng.random((B, blk)) < 0.5).astype(np.uint8)
@@ -106,6 +107,14 @@ def test_seed_count_and_score_against_numpy():
             idx = np.nonzero(elig)[0]
             order = idx[np.lexsort((idx, -score[b, idx]))]
             assert sorted(np.nonzero(st["seed"][b])[0].tolist()) == sorted(order[:k].tolist())
+            # the same seeds as the exact (fp64) score wherever the k-th and
+            # (k+1)-th exact scores are further apart than fp32 rounding
+            exact = 1.5 * (1.0 - conf[b]) + 0.7 * infl[b] - 2.0 * drift[b]
+            o64 = idx[np.lexsort((idx, -exact[idx]))]
+            if 0 < k < n and exact[o64[k - 1]] - exact[o64[k]] > 1e-5:
+                checked += 1
+                assert sorted(np.nonzero(st["seed"][b])[0].tolist()) == sorted(o64[:k].tolist())
+    assert checked >= 20
 
 
 def test_invariants_random_runs():
