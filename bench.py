@@ -249,9 +249,9 @@ def bench_config(args):
 
 
 def run_native(args, rank, world, local, light=False):
-    """The timed steps of one workload.  ``light``: only the whole steps
-    (no per-rule runs, no attention-alone timing, no end-to-end steps, no
-    clock sampling) -- the short runs of the per_workload block."""
+    """The timed steps of one workload.  ``light``: only the timed steps of
+    the full path (no per-rule runs, no attention-alone timing, no end-to-end
+    steps, no clock sampling) -- the short runs of the per_workload block."""
     import torch
 
     import diffusion_decoding_token_gb300 as dlm

@@ -794,7 +794,18 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
     __shared__ long long s_A[kDecideMaxBlk * LD];  // the masked rows of the sums A
     __shared__ uint8_t s_mk[kDecideMaxBlk];
     const int b = blockIdx.x, t = threadIdx.x;
-    // the per-position inputs and the header in one round trip
+    // the sums A into shared memory (coalesced asynchronous copies, so the
+    // transposed reads A_ji are shared-memory reads too), issued with the
+    // per-position inputs and the header: one round trip for all of them.
+    // Every row is copied; rows of unmasked positions (never stored by the
+    // attention pass) are never read.
+    {
+        const long long* A = a.A + (int64_t)b * a.blk * a.blk;
+        for (int q = threadIdx.x; q < a.blk * a.blk; q += kThreads) {
+            const int r = q / a.blk, k = q - r * a.blk;
+            cp_async8(&s_A[r * LD + k], A + q);
+        }
+    }
     const bool in = t < a.blk;
     const bool m = in && a.masked[(int64_t)b * a.blk + t] != 0;
     const float c = in ? a.conf[(int64_t)b * a.blk + t] : 0.f;
@@ -805,15 +816,8 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
     if (in) s_mk[t] = m;
     const int M = __syncthreads_count(m);
     const bool late = (float)M < a.bulk_frac * (float)a.blk;
+    asm volatile("cp.async.wait_all;" ::: "memory");  // (late too: no copy outlives the CTA)
     if (!late) {
-        // the masked rows of A into shared memory (one round trip, coalesced),
-        // so the transposed reads A_ji are shared-memory reads too
-        const long long* A = a.A + (int64_t)b * a.blk * a.blk;
-        for (int q = threadIdx.x; q < a.blk * a.blk; q += kThreads) {
-            const int r = q / a.blk, k = q - r * a.blk;
-            if (s_mk[r]) cp_async8(&s_A[r * LD + k], A + q);
-        }
-        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
         for (int i = threadIdx.x >> 5; i < a.blk; i += kThreads / 32) {
             if (!s_mk[i]) continue;  // warp-uniform
