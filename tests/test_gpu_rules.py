@@ -375,6 +375,42 @@ def test_bench_launch_configuration_matches_oracle(dlm, name, mode):
     assert exact == cfg.batch * len(cfg.rules)
 
 
+def test_dapd_selection_waits_for_the_row_pass(dlm):
+    """The DAPD selection follows the attention pass on the side stream, behind
+    an event on the row pass.  With a one-head attention pass (done long
+    before the 2048-row pass) and the statistics zeroed before the step, it
+    must still read the row pass's confidences: its selection equals the one
+    run again after a full synchronisation, and differs from what zeroed
+    confidences give."""
+    w, dw, o = workload("batched")
+    cfg = w.cfg
+    plan = dlm.StepPlan(dw.cur, dw.prev, dw.masked, tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf,
+                        bulk_frac=cfg.bulk_frac, rules=("dapd",), attn=dw.attn[:, :1, :1],
+                        block_start=dw.block_start, concurrent_dapd=True, dapd_early=True)
+    _, hi = torch.cuda.Stream.priority_range()
+    main = torch.cuda.Stream(priority=hi)
+    sel, n = plan.out["dapd"]
+    kw = dict(tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf, bulk_frac=cfg.bulk_frac)
+    with torch.cuda.stream(main):
+        plan.run(main)
+        torch.cuda.synchronize()
+        for t in plan.stats:
+            if t is not None:
+                t.zero_()
+        sel.fill_(7)
+        torch.cuda.synchronize()
+        plan.run_rows(main)
+        plan.join(main)
+        torch.cuda.synchronize()
+        got = sel.clone()
+        ref, _ = dlm.dapd_select(plan.dapd_ws, dw.masked, plan.stats.conf, **kw)
+        zero, _ = dlm.dapd_select(plan.dapd_ws, dw.masked, torch.zeros_like(plan.stats.conf), **kw)
+    torch.cuda.synchronize()
+    assert int(plan.status.item()) == 0
+    assert torch.equal(got, ref)
+    assert not torch.equal(zero, ref)
+
+
 # ------------------------------------------------------------- edge cases
 def test_threshold_edges(dlm):
     conf = np.array([[0.3, 0.5, 0.5, 0.1], [0.95, 0.2, 0.99, 0.3], [0.91, 0.2, 0.1, 0.95]], np.float32)
