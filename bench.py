@@ -80,6 +80,9 @@ def parse():
     ap.add_argument("--fuse-rules", default="auto", choices=["auto", "on", "off"],
                     help="run threshold, boundary and CAP inside the row pass (dlm_row_stats_rules); auto: only the "
                          "DepCap chain (boundary -> CAP, no DAPD)")
+    ap.add_argument("--fold-attention", default="auto", choices=["auto", "off"],
+                    help="compute the DAPD attention sums in the row pass's own CTAs (dlm_row_stats_attention) "
+                         "where the library can; off: a separate attention pass on the side stream")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the short runs of the other workloads after the headline one")
     ap.add_argument("--per-workload-steps", type=int, default=200,
@@ -299,7 +302,8 @@ def run_native(args, rank, world, local, light=False):
     common.update(rules=tuple(cfg.rules) + extra, cap_scope_from_boundary=(cfg.name == "depcap_window"),
                   concurrent_dapd=not args.serial_dapd, dapd_early=not args.late_dapd_fork, dapd_priority=args.dapd_priority,
                   parallel_rules=not args.serial_rules,
-                  fuse_rules={"auto": "auto", "on": True, "off": False}[args.fuse_rules])
+                  fuse_rules={"auto": "auto", "on": True, "off": False}[args.fuse_rules],
+                  fold_attention="auto" if args.fold_attention == "auto" else False)
     plan = dlm.StepPlan(cur, prev, masked, attn=attn, block_start=bs, row_index=row_index, **common)
 
     for _ in range(args.warmup):
@@ -402,7 +406,8 @@ def run_native(args, rank, world, local, light=False):
         raise RuntimeError(f"device status {int(status.item())} during the benchmark")
     if light:
         return dict(total_ms=total_ms, k1=k1, flush=flush, cfg=cfg, w=w, decisions=int(w.masked.sum()),
-                    rows=int(w.masked.sum()), launches=plan.n_launches * args.steps, fused=list(plan.fused))
+                    rows=int(w.masked.sum()), launches=plan.n_launches * args.steps, fused=list(plan.fused),
+                    folded=plan.folded)
 
     # the four rules alone, on the statistics of the last step
     r0 = torch.cuda.Event(enable_timing=True)
@@ -559,7 +564,7 @@ def run_native(args, rank, world, local, light=False):
             raise RuntimeError(f"device status {int(status.item())} during the end-to-end steps")
 
     return dict(total_ms=total_ms, k1=k1, rules_ms=rules_ms, per_rule=per_rule, attention=attention, clocks=clocks,
-                e2e=e2e, host_ms=host_ms, flush=flush, fused=list(plan.fused),
+                e2e=e2e, host_ms=host_ms, flush=flush, fused=list(plan.fused), folded=plan.folded,
                 cfg=cfg, launches=plan.n_launches * args.steps, w=w, decisions=int(w.masked.sum()),
                 rows=int(w.masked.sum()))
 
@@ -806,6 +811,7 @@ def main():
                      "algorithmic_bytes": k1_bytes},
         "gpu_launches": r["launches"],
         "fused_rules": r["fused"],
+        "folded_attention": r["folded"],
         "per_rule": r["per_rule"],
     }
     if r["attention"]:
@@ -853,7 +859,7 @@ def per_workload(args, headline, peak, local):
                "row_pass": {"ms": k1_ms, "gbps": k1_bytes / (k1_ms / 1000.0) / 1e9,
                             "frac": k1_bytes / (k1_ms / 1000.0) / 1e9 / peak, "algorithmic_bytes": k1_bytes},
                "l2": "flushed before every step" if r["flush"] else "not flushed (rows larger than L2)",
-               "gpu_launches": r["launches"], "fused_rules": r["fused"]}
+               "gpu_launches": r["launches"], "fused_rules": r["fused"], "folded_attention": r["folded"]}
         if not args.no_cpu_baseline:
             import oracle
             oracle.build()

@@ -44,6 +44,8 @@ from ._binding import (  # noqa: F401
     revocable_step,
     row_stats_partial,
     row_stats_merge,
+    row_stats_attention,
+    row_stats_attention_folds,
     row_stats_rules,
     row_stats_rules_workspace,
     allgather_row_partials,

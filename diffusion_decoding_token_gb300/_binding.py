@@ -103,10 +103,16 @@ def lib():
                                           P, P, P, P, P, P, P, P, P, P, Z, P, P]
         L.dlm_attention_influence.argtypes = [P, ctypes.c_int, I32, I32, I32, I64, I64, I64, I64, I32, I32, P, P, P,
                                               Z, P, P]
+        L.dlm_row_stats_attention_folds.restype = I32
+        L.dlm_row_stats_attention_folds.argtypes = [ctypes.c_int, I32, I32, I64, ctypes.c_int, I32, I32]
+        L.dlm_row_stats_attention.argtypes = [P, P, ctypes.c_int, I32, I32, I64, I64, P, P, P, P, P, P, P,
+                                              ctypes.c_int, I32, I32, I64, I64, I64, I64, I32, P,
+                                              ctypes.POINTER(DapdParams), P, Z, P, P]
         for f in ("dlm_row_stats", "dlm_select_threshold", "dlm_depcap_boundary", "dlm_cap_select",
                   "dlm_dapd_graph_mis", "dlm_dapd_graph", "dlm_dapd_select", "dlm_select_topk",
                   "dlm_select_factor", "dlm_parallel_certificate", "dlm_depcap_boundary_ragged",
-                  "dlm_revocable_step", "dlm_attention_influence", "dlm_row_stats_rules"):
+                  "dlm_revocable_step", "dlm_attention_influence", "dlm_row_stats_rules",
+                  "dlm_row_stats_attention"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -480,6 +486,43 @@ def dapd_graph(attn: torch.Tensor, masked: torch.Tensor, tau_edge: float = 0.01,
     return workspace
 
 
+def row_stats_attention_folds(cur: torch.Tensor, attn: torch.Tensor, batch: int, blk: int) -> bool:
+    """Whether dlm_row_stats_attention folds the attention into the row pass
+    for these shapes (rows too few to fill the GPU, attention that fits
+    shared memory); otherwise it runs the two passes one after the other."""
+    return bool(lib().dlm_row_stats_attention_folds(_dt(cur), int(batch), int(blk), cur.shape[1], _dt(attn),
+                                                    attn.shape[1], attn.shape[2]))
+
+
+def row_stats_attention(cur: torch.Tensor, prev: torch.Tensor | None, attn: torch.Tensor, masked: torch.Tensor,
+                        tau_edge: float = 0.01, bulk_conf: float = 0.9, bulk_frac: float = 0.5, order_mode: int = 0,
+                        block_start: int = 0, *, out: RowStats | None = None, workspace=None, status=None):
+    """dlm_row_stats_attention: the row pass over ``cur`` ([B*blk, V], row
+    b*blk + i = position i of sequence b) with the DAPD attention sums of
+    every masked row folded in; returns (stats, workspace) -- dapd_select on
+    that workspace then gives the DAPD selection."""
+    _need_cuda(cur, prev, attn, masked, workspace)
+    B, blk = masked.shape
+    if cur.dim() != 2 or cur.stride(1) != 1 or cur.shape[0] != B * blk:
+        raise ValueError("cur must be [B*blk, V] with contiguous rows")
+    if prev is not None and (prev.shape != cur.shape or prev.stride() != cur.stride() or prev.dtype != cur.dtype):
+        raise ValueError("prev must match cur in shape, strides and dtype")
+    if attn.dim() != 5 or attn.stride(4) != 1 or attn.shape[0] != B:
+        raise ValueError("attn must be [B, L, H, N, N] with unit column stride")
+    masked = _u8(masked)
+    st = out or alloc_row_stats(B * blk, cur.device, prev is not None)
+    if workspace is None:
+        workspace = dapd_workspace(B, blk, cur.device)
+    sb, sl, sh, sr, _ = attn.stride()
+    prm = DapdParams(float(tau_edge), float(bulk_conf), float(bulk_frac), int(order_mode))
+    _check(lib().dlm_row_stats_attention(_p(cur), _p(prev), _dt(cur), B, blk, cur.shape[1], cur.stride(0),
+                                         _p(st.argmax), _p(st.conf), _p(st.lse), _p(st.entropy), _p(st.kl),
+                                         _p(st.lse_prev), _p(attn), _dt(attn), attn.shape[1], attn.shape[2], sb, sl,
+                                         sh, sr, int(block_start), _p(masked), ctypes.byref(prm), _p(workspace),
+                                         workspace.numel(), _p(status), _stream(cur.device)))
+    return st, workspace
+
+
 def row_stats_rules_workspace(batch: int, device) -> torch.Tensor:
     """A zeroed workspace for row_stats_rules (every call leaves it zero)."""
     return torch.zeros(max(16, lib().dlm_row_stats_rules_workspace_size(batch)), dtype=torch.uint8, device=device)
@@ -589,7 +632,8 @@ class StepPlan:
                  cap_scope_from_boundary=False, attn=None, block_start=0, tau_edge=0.01, bulk_conf=0.9,
                  bulk_frac=0.5, order_mode=0, rules=("threshold", "boundary", "cap", "dapd"), status=None,
                  row_index=None, concurrent_dapd=False, dapd_early=False, topk_k=2, factor_f=1.0,
-                 parallel_rules=False, row_tail="auto", dapd_priority="low", fuse_rules="auto"):
+                 parallel_rules=False, row_tail="auto", dapd_priority="low", fuse_rules="auto",
+                 fold_attention="auto"):
         _need_cuda(cur, prev, masked, attn, row_index)
         L = lib()
         dev = cur.device
@@ -759,6 +803,28 @@ class StepPlan:
                 self._calls = [self._calls[0]] + [by_name[n] for n in main if n not in fused]
                 self.fused = tuple(fused)
 
+        # fold_attention: with the DAPD chain forked at the step's start, the
+        # row pass's own CTAs compute the attention sums
+        # (dlm_row_stats_attention: each copies its row's attention runs while
+        # it streams the logits) instead of a pass on the side stream; the
+        # selection then follows the row pass there.  "auto" folds where the
+        # library does (dlm_row_stats_attention_folds: rows too few to fill the
+        # GPU; measured on one LLaDA-like sequence: 39.9 -> 36.5 us per step).
+        self.folded = False
+        if fold_attention and "dapd" in rules and attn is not None and row_index is None \
+                and self.side is not None and self.dapd_early and not self.fused \
+                and (fold_attention != "auto" or row_stats_attention_folds(cur, attn, B, blk)):
+            sb, sl, sh, sr, _ = attn.stride()
+            self._calls[0] = (L.dlm_row_stats_attention, (
+                _p(cur), _p(prev), _dt(cur), B, blk, cur.shape[1], cur.stride(0), _p(st.argmax), _p(st.conf),
+                _p(st.lse), _p(st.entropy), _p(st.kl), _p(st.lse_prev), _p(attn), _dt(attn), attn.shape[1],
+                attn.shape[2], sb, sl, sh, sr, int(block_start), _p(self.masked), ctypes.byref(self._dapd),
+                _p(self.dapd_ws), self.dapd_ws.numel(), _p(self.status)))
+            self._graph_calls = []
+            self.folded = True
+            self.row_flags = 0  # the folded pass keeps its tail grid of half rows
+            self._row_shape = self._row_shape[:4] + (0,)
+
         # parallel_rules: the independent rules after the row pass run as
         # parallel branches (streams forked and joined inside the step, so a
         # captured graph gets parallel branches too); CAP scoped by the
@@ -795,6 +861,8 @@ class StepPlan:
         selection; blocks of up to 64) or 3."""
         per = {"threshold": 1, "boundary": 1, "cap": 1, "dapd": 2 if self.blk <= 64 else 3, "topk": 1,
                "factor": 1}
+        if self.folded:
+            per["dapd"] = 1  # the attention sums run in the row pass
         rows = max(0, lib().dlm_row_stats_launches(*self._row_shape))
         return rows + sum(per[r] for r in self.rules if r not in self.fused)
 

@@ -54,6 +54,17 @@ const char* dlm_status_string(dlm_status s) {
 
 int dlm_version(void) { return 100; }
 
+// CTAs per row: split a row over a cluster of CTAs only when the rows alone
+// cannot fill the GPU and each CTA still gets at least two vectors per thread.
+static int row_split(dlm_dtype dtype, int64_t n_rows, int64_t vocab) {
+    const int64_t nvec = vocab / dlm::row_stats_elems_per_vector(dtype);
+    const int threads = dlm::row_stats_threads();
+    const int64_t target = 2LL * sm_count();
+    int split = 1;
+    while (split < 8 && n_rows * split < target && nvec / (split * 2) >= 2LL * threads) split *= 2;
+    return split;
+}
+
 // Validation and launch shape shared by the whole-row and the slice calls.
 static dlm_status row_stats_prepare(dlm::RowStatsArgs& a, const void* cur, const void* prev, dlm_dtype dtype,
                                     int64_t n_rows, int64_t vocab, int64_t row_stride, const int32_t* row_index) {
@@ -63,14 +74,8 @@ static dlm_status row_stats_prepare(dlm::RowStatsArgs& a, const void* cur, const
     if (!cur) return DLM_ERR_INVALID_ARG;
     const int esz = dtype_size(dtype);
     if (!aligned16(cur) || (prev && !aligned16(prev)) || (row_stride * esz) % 16 != 0) return DLM_ERR_ALIGNMENT;
-    const int epv = dlm::row_stats_elems_per_vector(dtype);
-    const int64_t nvec = vocab / epv;
-    const int threads = dlm::row_stats_threads();
-    // split a row over a cluster of CTAs only when the rows alone cannot fill
-    // the GPU and each CTA still gets at least two vectors per thread
+    const int split = row_split(dtype, n_rows, vocab);
     const int64_t target = 2LL * sm_count();
-    int split = 1;
-    while (split < 8 && n_rows * split < target && nvec / (split * 2) >= 2LL * threads) split *= 2;
     if (n_rows * split > 0x7fffffffLL) return DLM_ERR_INVALID_ARG;
     a = dlm::RowStatsArgs{};
     a.cur = cur;
@@ -519,6 +524,89 @@ dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t bat
     a.n_selected = n_selected;
     a.thresh_from_ws = 1;
     return from_cuda(dlm::launch_dapd_select(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Folding pays where the rows are too few to fill the GPU (the row pass
+// splits each row over a cluster) and the copied attention fits shared
+// memory; with whole waves of rows the scattered attention reads cost the
+// same DRAM time inside the row pass as in a pass of their own, and the
+// separate pass beside the row pass is faster.
+static bool attention_folds(int64_t n_rows, int split, dlm_dtype attn_dtype, int32_t n_layers, int32_t n_heads,
+                            int32_t blk) {
+    if (split < 2 || n_rows < 1) return false;
+    dlm::RowAttn at{};
+    at.attn = &at;  // any non-null pointer: only the shape decides
+    at.esz = dtype_size(attn_dtype);
+    at.n_layers = n_layers;
+    at.n_heads = n_heads;
+    at.blk = blk;
+    return dlm::row_attn_smem(at) > 0;
+}
+
+int32_t dlm_row_stats_attention_folds(dlm_dtype dtype, int32_t batch, int32_t blk, int64_t vocab,
+                                      dlm_dtype attn_dtype, int32_t n_layers, int32_t n_heads) {
+    if (!dtype_ok(dtype) || !dtype_ok(attn_dtype) || n_layers < 1 || n_heads < 1 ||
+        (int64_t)n_layers * n_heads > (1 << 20) || batch < 1 || blk < 1 || blk > DLM_MAX_BLK || vocab < 1 ||
+        vocab > 0x7fffffffLL)
+        return 0;
+    const int64_t n_rows = (int64_t)batch * blk;
+    return attention_folds(n_rows, row_split(dtype, n_rows, vocab), attn_dtype, n_layers, n_heads, blk) ? 1 : 0;
+}
+
+dlm_status dlm_row_stats_attention(const void* cur, const void* prev, dlm_dtype dtype, int32_t batch, int32_t blk,
+                                   int64_t vocab, int64_t row_stride, int32_t* argmax, float* conf, float* lse,
+                                   float* entropy, float* kl, float* lse_prev, const void* attn,
+                                   dlm_dtype attn_dtype, int32_t n_layers, int32_t n_heads, int64_t stride_b,
+                                   int64_t stride_l, int64_t stride_h, int64_t stride_row, int32_t block_start,
+                                   const uint8_t* masked, const dlm_dapd_params* params, void* workspace,
+                                   size_t ws_bytes, uint32_t* dev_status, dlm_stream_t stream) {
+    if (batch < 0 || blk < 1 || blk > DLM_MAX_BLK) return DLM_ERR_INVALID_ARG;
+    const int64_t n_rows = (int64_t)batch * blk;
+    dlm::RowStatsArgs a{};
+    dlm_status st = row_stats_prepare(a, cur, prev, dtype, n_rows, vocab, row_stride, nullptr);
+    if (st != DLM_OK) return st;
+    dlm::DapdArgs d{};
+    st = dapd_prepare(d, attn, attn_dtype, batch, n_layers, n_heads, stride_b, stride_l, stride_h, stride_row,
+                      block_start, blk, masked, params, workspace, ws_bytes, true);
+    if (st != DLM_OK || n_rows == 0) return st;
+    if (!argmax || !conf || !lse || !entropy) return DLM_ERR_INVALID_ARG;
+    a.n_src = n_rows;
+    a.argmax = argmax;
+    a.conf = conf;
+    a.lse = lse;
+    a.entropy = entropy;
+    a.kl = kl;
+    a.lse_prev = lse_prev;
+    a.dev_status = dev_status;
+    d.dev_status = dev_status;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    dlm::RowAttn& at = a.at;
+    at.attn = attn;
+    at.dtype = attn_dtype;
+    at.esz = dtype_size(attn_dtype);
+    at.n_layers = n_layers;
+    at.n_heads = n_heads;
+    at.sb = stride_b;
+    at.sl = stride_l;
+    at.sh = stride_h;
+    at.sr = stride_row;
+    at.block_start = block_start;
+    at.blk = blk;
+    at.vpr = (int)((int64_t)blk * at.esz / 16);
+    at.masked = masked;
+    at.mask4 = (blk % 4 == 0 && (reinterpret_cast<uintptr_t>(masked) & 3u) == 0) ? 1 : 0;
+    at.bulk_frac = d.bulk_frac;
+    at.edge_thresh = d.edge_thresh;
+    at.s_scale = d.s_scale;
+    at.A = d.A;
+    at.hdr = d.hdr;
+    if (attention_folds(n_rows, a.split, attn_dtype, n_layers, n_heads, blk))
+        return from_cuda(dlm::launch_row_stats_attn(a, dtype, s));
+    // not foldable: the row pass, then the attention pass, on the stream
+    a.at = dlm::RowAttn{};
+    const cudaError_t e = dlm::launch_row_stats(a, dtype, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(dlm::launch_dapd_graph(d, sm_count(), s, false));
 }
 
 }  // extern "C"

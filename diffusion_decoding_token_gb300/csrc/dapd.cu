@@ -34,6 +34,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "attn_sum.cuh"
 #include "common.cuh"
 #include "launch.h"
 
@@ -55,64 +56,12 @@ __device__ __forceinline__ bool late_phase(const DapdArgs& a, int b) {
     return (float)M < a.bulk_frac * (float)a.blk;
 }
 
-template <int DT>
-struct AFmt;
-template <>
-struct AFmt<DLM_F16> {
-    static constexpr int EPV = 8;
-    static constexpr int ESZ = 2;
-    static __device__ __forceinline__ void to_f2(uint4 w, f2 (&x)[4]) {
-        x[0] = f16x2_to_f2(w.x);
-        x[1] = f16x2_to_f2(w.y);
-        x[2] = f16x2_to_f2(w.z);
-        x[3] = f16x2_to_f2(w.w);
-    }
-    static __device__ __forceinline__ float scalar(const void* p) { return __half2float(*static_cast<const __half*>(p)); }
-};
-template <>
-struct AFmt<DLM_BF16> {
-    static constexpr int EPV = 8;
-    static constexpr int ESZ = 2;
-    static __device__ __forceinline__ void to_f2(uint4 w, f2 (&x)[4]) {
-        x[0] = bf16x2_to_f2(w.x);
-        x[1] = bf16x2_to_f2(w.y);
-        x[2] = bf16x2_to_f2(w.z);
-        x[3] = bf16x2_to_f2(w.w);
-    }
-    static __device__ __forceinline__ float scalar(const void* p) {
-        return __uint_as_float((uint32_t) * static_cast<const uint16_t*>(p) << 16);
-    }
-};
-template <>
-struct AFmt<DLM_F32> {
-    static constexpr int EPV = 4;
-    static constexpr int ESZ = 4;
-    static __device__ __forceinline__ void to_f2(uint4 w, f2 (&x)[2]) {
-        x[0] = pack2(__uint_as_float(w.x), __uint_as_float(w.y));
-        x[1] = pack2(__uint_as_float(w.z), __uint_as_float(w.w));
-    }
-    static __device__ __forceinline__ float scalar(const void* p) { return *static_cast<const float*>(p); }
-};
-
 __device__ __forceinline__ uint4 ld_nc(const void* p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
         : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
         : "l"(p));
     return r;
-}
-
-// exact split accumulate: x = hi + lo, hi multiple of 2^-15 when 0 <= x < 256
-template <int NP>
-__device__ __forceinline__ void split_acc(const f2 (&x)[NP], f2 (&H)[NP], f2 (&L)[NP]) {
-    const f2 c = pack2(256.f, 256.f);
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-        f2 hi = sub2(add2(x[p], c), c);
-        f2 lo = sub2(x[p], hi);
-        H[p] = add2(H[p], hi);
-        L[p] = add2(L[p], lo);
-    }
 }
 
 template <int DT>
@@ -288,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_kernel(DapdArgs a) {
             const int col = col0 + 2 * p + k;
             if (col < a.blk) {
                 const float hi = acc[4 * p + k], lo = acc[4 * p + 2 + k];
-                A[col] = __float2ll_rn(hi * 32768.f) * 131072LL + __float2ll_rn(lo * 4294967296.f);
+                A[col] = attn_fixed(hi, lo);
             }
         }
     }
@@ -457,7 +406,7 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
             const int col = col0 + 2 * p + k;
             if (col < a.blk) {
                 const float hi = acc[4 * p + k], lo = acc[4 * p + 2 + k];
-                A[col] = __float2ll_rn(hi * 32768.f) * 131072LL + __float2ll_rn(lo * 4294967296.f);
+                A[col] = attn_fixed(hi, lo);
             }
         }
     }
@@ -473,13 +422,6 @@ __global__ void __launch_bounds__(kThreads) dapd_accum_tma_kernel(const __grid_c
 // j: col_T[j * col_ld + (i - col0)], else from A in global memory.
 constexpr int kColStride = 33;  // padded: a warp's column reads hit distinct bank pairs
 
-// asynchronous global -> shared copies (completed by cp.async.wait_all)
-__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
 
 
 struct RowLoad {

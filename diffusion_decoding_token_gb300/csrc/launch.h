@@ -9,6 +9,26 @@
 
 namespace dlm {
 
+// The DAPD attention sums folded into the row pass (dlm_row_stats_attention):
+// the CTA of row b*blk + i (rank 0 of its cluster) copies row i of sequence
+// b's attention block, for every layer and head, into shared memory while it
+// streams the logits, then sums it into row i of the DAPD workspace's A.
+struct RowAttn {
+    const void* attn;          // null: no attention sums (plain row pass)
+    int dtype, esz;
+    int n_layers, n_heads;
+    int64_t sb, sl, sh, sr;    // element strides
+    int block_start, blk;
+    int vpr;                   // 16-byte vectors per block row (blk * esz / 16)
+    const uint8_t* masked;
+    int mask4;                 // the mask rows are copied 4 bytes at a time (aligned, blk % 4 == 0)
+    float bulk_frac;
+    long long edge_thresh;
+    float s_scale;
+    long long* A;              // [batch][blk][blk] fixed-point sums (units 2^-32)
+    long long* hdr;            // edge threshold, score scale bits
+};
+
 struct RowStatsArgs {
     const void* cur;
     const void* prev;
@@ -30,8 +50,13 @@ struct RowStatsArgs {
     int single_grid;       // no tail grid of half rows
     int64_t n_src;         // rows cur/prev hold: q >= n_src is skipped (0 = unchecked)
     int gather;            // outputs at r (the gathered order) instead of q
+    RowAttn at;            // attention sums folded in (at.attn non-null; rows are b*blk + i)
 };
 cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s);
+// the row pass with the attention sums folded in (a.at set); shared memory
+// per CTA for it, or 0 when the attention cannot be folded in
+size_t row_attn_smem(const RowAttn& at);
+cudaError_t launch_row_stats_attn(const RowStatsArgs& a, int dtype, cudaStream_t s);
 int row_stats_grids(const RowStatsArgs& a, int dtype);  // kernel launches launch_row_stats makes
 // merge of dlm_row_partial states: a gives n_rows, row_index and the outputs
 cudaError_t launch_row_merge(const RowStatsArgs& a, const void* partials, int n_shards, int64_t shard_stride,

@@ -29,6 +29,7 @@
 
 #include <cstddef>
 
+#include "attn_sum.cuh"
 #include "common.cuh"
 #include "launch.h"
 #include "rules.cuh"
@@ -330,7 +331,146 @@ __device__ __forceinline__ void run_rules(const RowRules& rr, int b, RuleSmem& s
     if (rr.cap) cap_block(rr.c, b, sm.c);
 }
 
-template <int DT, bool PREV, bool RULES>
+// shared memory of the folded attention: the copied runs, the sequence's
+// mask flags, then the partials of the sums
+__host__ __device__ __forceinline__ size_t attn_buf_bytes(const RowAttn& at) {
+    return ((size_t)at.n_layers * at.n_heads * at.vpr * 16 + 15) & ~(size_t)15;
+}
+__host__ __device__ __forceinline__ size_t attn_red_offset(const RowAttn& at) {
+    return attn_buf_bytes(at) + (((size_t)at.blk + 15) & ~(size_t)15);
+}
+
+// The DAPD attention sums folded into the row pass.  Row r = b*blk + i: the
+// CTA copies row i of sequence b's attention block for every (layer, head)
+// -- L*H runs of blk contiguous values -- into shared memory with
+// asynchronous 16-byte copies issued before it streams the logits, so the
+// scattered reads wait under the stream instead of after it.
+__device__ __forceinline__ void attn_prefetch(const RowAttn& at, int64_t r, unsigned char* buf) {
+    const int b = (int)(r / at.blk), i = (int)(r - (int64_t)b * at.blk);
+    const char* base = static_cast<const char*>(at.attn) +
+                       ((int64_t)b * at.sb + (int64_t)(at.block_start + i) * at.sr + at.block_start) * at.esz;
+    const int LH = at.n_layers * at.n_heads, nq = LH * at.vpr;
+    for (int q = threadIdx.x; q < nq; q += kThreads) {
+        const int s = q / at.vpr, cv = q - s * at.vpr;
+        const int l = s / at.n_heads, h = s - l * at.n_heads;
+        cp_async16(buf + (size_t)q * 16, base + ((int64_t)l * at.sl + (int64_t)h * at.sh) * at.esz + cv * 16);
+    }
+    if (at.mask4 && (int)threadIdx.x < at.blk / 4)  // the sequence's mask flags, 4 at a time
+        cp_async4(buf + attn_buf_bytes(at) + threadIdx.x * 4, at.masked + (int64_t)b * at.blk + threadIdx.x * 4);
+}
+
+// Thread t sums column vector t % vpr of the runs t / vpr, t / vpr + per, ...
+// (exact hi / lo split); the partials meet in `red` (component-major) and
+// thread j < blk adds column j's and stores A[b][i][j] in fixed point.
+template <int AT>
+__device__ __forceinline__ void attn_row_sums_typed(const RowAttn& at, int b, int i, const unsigned char* buf,
+                                                    float* red) {
+    constexpr int EPV = AFmt<AT>::EPV;
+    constexpr int NP = EPV / 2;
+    const int t = threadIdx.x, vpr = at.vpr, per = kThreads / vpr;
+    const int LH = at.n_layers * at.n_heads;
+    const int g = t / vpr, cv = t - g * vpr;
+    f2 H[NP], L[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) H[p] = L[p] = pack2(0.f, 0.f);
+    if (g < per) {
+        for (int s = g; s < LH; s += per) {
+            const uint4 w = *reinterpret_cast<const uint4*>(buf + ((size_t)s * vpr + cv) * 16);
+            f2 x[NP];
+            AFmt<AT>::to_f2(w, x);
+            split_acc<NP>(x, H, L);
+        }
+    }
+    if ((32 % vpr) == 0) {
+        // lanes l, l + vpr, l + 2 vpr, ... of a warp hold the same column
+        // vector: shuffles add them, then lane cv < vpr of each warp leaves the
+        // warp's partial and thread j adds the warps' (kWarps terms)
+        for (int off = vpr; off < 32; off <<= 1) {
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                float h0, h1, l0, l1;
+                unpack2(H[p], h0, h1);
+                unpack2(L[p], l0, l1);
+                h0 += __shfl_xor_sync(DLM_FULL_MASK, h0, off);
+                h1 += __shfl_xor_sync(DLM_FULL_MASK, h1, off);
+                l0 += __shfl_xor_sync(DLM_FULL_MASK, l0, off);
+                l1 += __shfl_xor_sync(DLM_FULL_MASK, l1, off);
+                H[p] = pack2(h0, h1);
+                L[p] = pack2(l0, l1);
+            }
+        }
+        const int lane = t & 31, warp = t >> 5;
+        if (lane < vpr) {
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                float h0, h1, l0, l1;
+                unpack2(H[p], h0, h1);
+                unpack2(L[p], l0, l1);
+                float* o = red + (size_t)(warp * vpr + lane) * (2 * EPV);
+                o[4 * p + 0] = h0;
+                o[4 * p + 1] = h1;
+                o[4 * p + 2] = l0;
+                o[4 * p + 3] = l1;
+            }
+        }
+        __syncthreads();
+        if (t < at.blk) {
+            const int cj = t / EPV, e = t - cj * EPV, p = e >> 1, c = e & 1;
+            float hi = 0.f, lo = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float* o = red + (size_t)(w * vpr + cj) * (2 * EPV);
+                hi += o[4 * p + c];
+                lo += o[4 * p + 2 + c];
+            }
+            at.A[((int64_t)b * at.blk + i) * at.blk + t] = attn_fixed(hi, lo);
+        }
+        return;
+    }
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        float h0, h1, l0, l1;
+        unpack2(H[p], h0, h1);
+        unpack2(L[p], l0, l1);
+        red[(4 * p + 0) * kThreads + t] = h0;
+        red[(4 * p + 1) * kThreads + t] = h1;
+        red[(4 * p + 2) * kThreads + t] = l0;
+        red[(4 * p + 3) * kThreads + t] = l1;
+    }
+    __syncthreads();
+    if (t < at.blk) {
+        const int cj = t / EPV, e = t - cj * EPV, p = e >> 1, c = e & 1;
+        float hi = 0.f, lo = 0.f;
+        for (int gg = 0; gg < per; ++gg) {
+            hi += red[(4 * p + c) * kThreads + gg * vpr + cj];
+            lo += red[(4 * p + 2 + c) * kThreads + gg * vpr + cj];
+        }
+        at.A[((int64_t)b * at.blk + i) * at.blk + t] = attn_fixed(hi, lo);
+    }
+}
+
+// Every thread of the row's CTA (rank 0 of its cluster) calls it after the row
+// is streamed.  Rows of late-phase sequences (fewer than bulk_frac * blk
+// masked positions: no graph) and unmasked rows store nothing.
+__device__ __forceinline__ void attn_row_sums(const RowAttn& at, int64_t r, const unsigned char* buf, float* red) {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    const int b = (int)(r / at.blk), i = (int)(r - (int64_t)b * at.blk);
+    const int t = threadIdx.x;
+    const uint8_t* mk = at.mask4 ? buf + attn_buf_bytes(at) : at.masked + (int64_t)b * at.blk;
+    __syncthreads();  // every thread's copies have landed
+    const bool m = t < at.blk && mk[t] != 0;
+    const int M = __syncthreads_count(m);
+    if ((float)M < at.bulk_frac * (float)at.blk) return;
+    if (!mk[i]) return;
+    switch (at.dtype) {
+    case DLM_F16: attn_row_sums_typed<DLM_F16>(at, b, i, buf, red); break;
+    case DLM_BF16: attn_row_sums_typed<DLM_BF16>(at, b, i, buf, red); break;
+    default: attn_row_sums_typed<DLM_F32>(at, b, i, buf, red); break;
+    }
+}
+
+
+template <int DT, bool PREV, bool RULES, bool ATTN = false>
 __device__ __forceinline__ void row_stats_body(const RowStatsArgs& args, const RowRules* rules) {
     constexpr int EPV = Fmt<DT>::EPV;
     constexpr int ESZ = Fmt<DT>::ESZ;
@@ -350,6 +490,14 @@ __device__ __forceinline__ void row_stats_body(const RowStatsArgs& args, const R
         if (rank == 0 && threadIdx.x == 0) raise_status(args.dev_status, DLM_DEV_BAD_INDEX);
         if (args.wait_prior && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
         return;
+    }
+    extern __shared__ __align__(16) unsigned char s_attn[];  // folded attention (ATTN only)
+    if constexpr (ATTN) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) {  // for the DAPD selection
+            args.at.hdr[0] = args.at.edge_thresh;
+            args.at.hdr[1] = (long long)(uint32_t)__float_as_int(args.at.s_scale);
+        }
+        if (rank == 0) attn_prefetch(args.at, r, s_attn);
     }
     const char* cur_row = static_cast<const char*>(args.cur) + q * args.row_stride * ESZ;
     const char* prev_row = PREV ? static_cast<const char*>(args.prev) + q * args.row_stride * ESZ : nullptr;
@@ -447,6 +595,11 @@ __device__ __forceinline__ void row_stats_body(const RowStatsArgs& args, const R
         }
         cluster.sync();
     }
+    if constexpr (ATTN) {
+        if (rank == 0)
+            attn_row_sums(args.at, args.row_base + blockIdx.x / split, s_attn,
+                          reinterpret_cast<float*>(s_attn + attn_red_offset(args.at)));
+    }
     // a tail launch overlapping the previous grid completes only after it, so
     // whatever follows on the stream sees both grids' results
     if (args.wait_prior && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -492,6 +645,15 @@ __global__ void __launch_bounds__(kThreads, 4) row_stats_kernel(RowStatsArgs arg
     row_stats_body<DT, PREV, false>(args, nullptr);
 }
 
+// The row pass with the DAPD attention sums folded in (dynamic shared memory:
+// the copied attention runs, the mask flags and the partials of their sums).
+// Launched only for rows split over clusters (a grid well inside one wave),
+// so it takes the registers of 2 CTAs per SM rather than 4.
+template <int DT, bool PREV>
+__global__ void __launch_bounds__(kThreads, 2) row_stats_attn_kernel(RowStatsArgs args) {
+    row_stats_body<DT, PREV, false, true>(args, nullptr);
+}
+
 // The row pass with the fused rules epilogue (few-row launches; no occupancy
 // floor, the epilogue's shared memory and registers come on top of the pass's).
 template <int DT, bool PREV>
@@ -523,13 +685,16 @@ __global__ void __launch_bounds__(256) row_merge_kernel(RowStatsArgs args, const
 // longer tail, were slower: the cluster merge costs more than they save).
 constexpr int kTailSplit = 2;
 
-template <int DT, bool PREV, bool RULES = false>
+template <int DT, bool PREV, bool RULES = false, bool ATTN = false>
 int64_t tail_rows(const RowStatsArgs& a) {
     if (a.split != 1 || a.num_sms <= 0 || a.partial || a.single_grid) return 0;
     int per_sm = 0;
     cudaError_t e;
     if constexpr (RULES)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_rules_kernel<DT, PREV>, kThreads, 0);
+    else if constexpr (ATTN)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_attn_kernel<DT, PREV>, kThreads,
+                                                          row_attn_smem(a.at));
     else
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<DT, PREV>, kThreads, 0);
     if (e != cudaSuccess || per_sm <= 0) return 0;
@@ -539,12 +704,12 @@ int64_t tail_rows(const RowStatsArgs& a) {
     return a.n_rows % slots;
 }
 
-template <int DT, bool PREV, bool RULES = false>
+template <int DT, bool PREV, bool RULES = false, bool ATTN = false>
 cudaError_t launch_grid(const RowStatsArgs& a, bool programmatic, cudaStream_t s, const RowRules* rules = nullptr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(a.n_rows * a.split));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = ATTN ? row_attn_smem(a.at) : 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     int n = 0;
@@ -564,24 +729,26 @@ cudaError_t launch_grid(const RowStatsArgs& a, bool programmatic, cudaStream_t s
     cfg.numAttrs = n;
     if constexpr (RULES)
         return cudaLaunchKernelEx(&cfg, row_stats_rules_kernel<DT, PREV>, a, *rules);
+    else if constexpr (ATTN)
+        return cudaLaunchKernelEx(&cfg, row_stats_attn_kernel<DT, PREV>, a);
     else
         return cudaLaunchKernelEx(&cfg, row_stats_kernel<DT, PREV>, a);
 }
 
-template <int DT, bool PREV, bool RULES = false>
+template <int DT, bool PREV, bool RULES = false, bool ATTN = false>
 cudaError_t launch_typed(const RowStatsArgs& a, cudaStream_t s, const RowRules* rules = nullptr) {
-    const int64_t tail = tail_rows<DT, PREV, RULES>(a);
-    if (tail == 0) return launch_grid<DT, PREV, RULES>(a, false, s, rules);
+    const int64_t tail = tail_rows<DT, PREV, RULES, ATTN>(a);
+    if (tail == 0) return launch_grid<DT, PREV, RULES, ATTN>(a, false, s, rules);
     RowStatsArgs head = a;
     head.n_rows = a.n_rows - tail;
-    cudaError_t e = launch_grid<DT, PREV, RULES>(head, false, s, rules);
+    cudaError_t e = launch_grid<DT, PREV, RULES, ATTN>(head, false, s, rules);
     if (e != cudaSuccess) return e;
     RowStatsArgs rest = a;
     rest.row_base = a.n_rows - tail;
     rest.n_rows = tail;
     rest.split = kTailSplit;
     rest.wait_prior = 1;
-    return launch_grid<DT, PREV, RULES>(rest, true, s, rules);
+    return launch_grid<DT, PREV, RULES, ATTN>(rest, true, s, rules);
 }
 
 template <int DT, bool PREV>
@@ -623,6 +790,30 @@ cudaError_t launch_row_stats(const RowStatsArgs& a, int dtype, cudaStream_t s) {
 }
 
 int row_stats_threads() { return kThreads; }
+
+// The shared memory the folded attention needs, or 0 when a block row is not
+// whole 16-byte vectors or it would not fit the default 48 KB.
+size_t row_attn_smem(const RowAttn& at) {
+    if (!at.attn || at.esz <= 0 || ((int64_t)at.blk * at.esz) % 16 != 0) return 0;
+    const int epv = 16 / at.esz;
+    RowAttn t = at;
+    t.vpr = at.blk / epv;
+    const size_t bytes = attn_red_offset(t) + (size_t)kThreads * 2 * epv * sizeof(float);
+    return bytes <= 48 * 1024 ? bytes : 0;
+}
+
+cudaError_t launch_row_stats_attn(const RowStatsArgs& a, int dtype, cudaStream_t s) {
+    if (row_attn_smem(a.at) == 0) return cudaErrorInvalidValue;
+    const bool prev = a.prev != nullptr;
+    switch (dtype) {
+    case DLM_BF16:
+        return prev ? launch_typed<DLM_BF16, true, false, true>(a, s) : launch_typed<DLM_BF16, false, false, true>(a, s);
+    case DLM_F16:
+        return prev ? launch_typed<DLM_F16, true, false, true>(a, s) : launch_typed<DLM_F16, false, false, true>(a, s);
+    default:
+        return prev ? launch_typed<DLM_F32, true, false, true>(a, s) : launch_typed<DLM_F32, false, false, true>(a, s);
+    }
+}
 
 cudaError_t launch_row_stats_rules(const RowStatsArgs& a, const RowRules& r, int dtype, cudaStream_t s) {
     const bool prev = a.prev != nullptr;

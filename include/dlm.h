@@ -530,6 +530,46 @@ dlm_status dlm_dapd_select(const uint8_t* masked, const float* conf, int32_t bat
                            void* workspace, size_t ws_bytes, dlm_stream_t stream);
 
 /*
+ * dlm_row_stats_attention -- dlm_row_stats and dlm_dapd_graph in one pass.
+ *
+ * The pages give no such operation: it is the row statistics of the
+ * Fast-dLLM review ("Method") and DepCap ("Methodology") over rows
+ * b*blk + i, plus the DAPD attention sums of every masked row (DAPD,
+ * "关键设计 1"), computed by the same CTAs.  Where the rows are too few to
+ * fill the GPU (each row is split over a cluster of CTAs), the CTA holding
+ * the start of row b*blk + i copies row i of sequence b's attention block,
+ * for every layer and head, into shared memory while the cluster streams the
+ * logits, then sums it exactly into the DAPD workspace: the scattered
+ * attention reads wait under the logit stream instead of in a latency-bound
+ * pass beside it.  With whole waves of rows the scattered reads cost the
+ * same DRAM time either way and a separate attention pass beside the row
+ * pass is faster, so the call then runs the row pass and the attention pass
+ * one after the other on the stream (as it does when the attention is not
+ * foldable: a block row that is not whole 16-byte vectors, or more copied
+ * attention than fits 48 KB of shared memory).  Either way,
+ * dlm_dapd_select(masked, conf, ...) on the workspace afterwards gives
+ * exactly the selection dlm_dapd_graph followed by dlm_dapd_select gives.
+ *
+ * Arguments: those of dlm_row_stats_ex for n_rows = batch * blk rows with no
+ * row index (row b*blk + i is position i of sequence b), then those of
+ * dlm_dapd_graph (attention view, block, mask, params, workspace, status)
+ * without the float outputs.  Layouts, alignment rules and errors are
+ * theirs.  dlm_row_stats_attention_folds returns 1 when the call folds the
+ * attention into the row pass for these shapes, 0 otherwise (including
+ * invalid arguments); it launches nothing.
+ */
+int32_t dlm_row_stats_attention_folds(dlm_dtype dtype, int32_t batch, int32_t blk, int64_t vocab,
+                                      dlm_dtype attn_dtype, int32_t n_layers, int32_t n_heads);
+
+dlm_status dlm_row_stats_attention(const void* cur, const void* prev, dlm_dtype dtype, int32_t batch, int32_t blk,
+                                   int64_t vocab, int64_t row_stride, int32_t* argmax, float* conf, float* lse,
+                                   float* entropy, float* kl, float* lse_prev, const void* attn,
+                                   dlm_dtype attn_dtype, int32_t n_layers, int32_t n_heads, int64_t stride_b,
+                                   int64_t stride_l, int64_t stride_h, int64_t stride_row, int32_t block_start,
+                                   const uint8_t* masked, const dlm_dapd_params* params, void* workspace,
+                                   size_t ws_bytes, uint32_t* dev_status, dlm_stream_t stream);
+
+/*
  * dlm_attention_influence -- downstream influence of every block position,
  * an input of dlm_revocable_step's seed score.
  *

@@ -1025,3 +1025,104 @@ def test_bench_launch_configuration_fused_rules(dlm, name):
     block_len = None if plan.block_len is None else plan.block_len.cpu().numpy()
     assert check_rules_exact(name, w, o, sel, block_len) == cfg.batch * len(cfg.rules)
     assert int(plan.status.item()) == 0
+
+
+# ------------------------------------------------ attention folded into the row pass
+def _sums(ws, B, blk):
+    """The exact attention sums A ([B][blk][blk] int64) at the head of a DAPD workspace."""
+    return ws[:B * blk * blk * 8].view(torch.int64).view(B, blk, blk)
+
+
+def _graph_rows(masked, bulk_frac):
+    """[B][blk] bool: masked rows of sequences on the graph path (the rows whose sums the selection reads)."""
+    m = masked.bool()
+    graph = m.sum(dim=1).float() >= bulk_frac * m.shape[1]
+    return m & graph[:, None]
+
+
+@pytest.mark.parametrize("name,folds", [("tiny", False), ("llada_step", True), ("batched", False)])
+def test_row_stats_attention_matches_oracle(dlm, name, folds):
+    """dlm_row_stats_attention (the DAPD attention sums computed by the row
+    pass's CTAs where the rows are few, else the two passes in turn) on the
+    screened workloads: the statistics equal the plain row pass bit for bit,
+    the exact sums of every row the selection reads equal the separate
+    attention pass's, and the DAPD selection equals the oracle's."""
+    w, dw, o = workload(name)
+    cfg = w.cfg
+    B, blk = cfg.batch, cfg.blk
+    assert dlm.row_stats_attention_folds(dw.cur, dw.attn, B, blk) == folds
+    kw = dict(tau_edge=cfg.tau_edge, bulk_conf=cfg.bulk_conf, bulk_frac=cfg.bulk_frac)
+    status = dlm.new_status()
+    st, ws = dlm.row_stats_attention(dw.cur, dw.prev, dw.attn, dw.masked, block_start=dw.block_start, status=status,
+                                     **kw)
+    ref = dlm.row_stats(dw.cur, dw.prev)
+    ws_ref = dlm.dapd_graph(dw.attn, dw.masked, block_start=dw.block_start, **kw)
+    sel, n = dlm.dapd_select(ws, dw.masked, st.conf.view(B, blk), **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in ("argmax", "conf", "lse", "entropy", "kl", "lse_prev"):
+        assert torch.equal(getattr(st, k), getattr(ref, k)), k
+    rows = _graph_rows(dw.masked, cfg.bulk_frac)
+    assert torch.equal(_sums(ws, B, blk)[rows], _sums(ws_ref, B, blk)[rows])
+    w1 = dataclasses.replace(w, cfg=synth.scaled(cfg, rules=("dapd",)))
+    assert check_rules_exact(name, w1, o, {"dapd": sel.cpu().numpy()}, None) == B
+
+
+@pytest.mark.parametrize("attn_dt,blk,B,L,H,vocab,prev,folds", [
+    (torch.float16, 32, 3, 4, 6, 16384, True, True),     # few rows: split over clusters of 4
+    (torch.bfloat16, 8, 4, 3, 5, 32768, True, True),     # clusters of 8, one vector per block row
+    (torch.float32, 8, 9, 3, 2, 8195, False, True),      # ragged vocabulary, no previous step
+    (torch.float16, 64, 2, 2, 2, 8192, True, True),      # blocks of 64
+    (torch.bfloat16, 16, 40, 2, 3, 8192, True, False),   # 640 rows: the two passes in turn
+    (torch.bfloat16, 8, 1, 1, 1, 512, True, False),      # one short row per position
+])
+def test_row_stats_attention_shapes(dlm, attn_dt, blk, B, L, H, vocab, prev, folds):
+    """Random shapes, masks with late-phase sequences and unmasked rows: the
+    folded call against the separate row and attention passes (statistics and
+    the sums of the rows the selection reads bit for bit, selections equal)."""
+    g = torch.Generator(device="cuda").manual_seed(blk * 1000 + B)
+    bs = 8
+    N = (bs + blk + 5 + 7) // 8 * 8                  # rows of 16-byte multiples
+    ld = (vocab + 7) // 8 * 8                        # logit rows padded to 16 bytes
+    cur = torch.randn(B * blk, ld, device="cuda", generator=g).mul_(3).to(torch.bfloat16)[:, :vocab]
+    prv = torch.randn(B * blk, ld, device="cuda", generator=g).mul_(3).to(torch.bfloat16)[:, :vocab] if prev else None
+    attn = torch.rand(B, L, H, N, N, device="cuda", generator=g).to(attn_dt)
+    masked = (torch.rand(B, blk, device="cuda", generator=g) < 0.7).to(torch.uint8)
+    masked[0, :] = 1                                  # one sequence fully masked
+    if B > 2:
+        masked[1, :] = 0
+        masked[1, : max(1, blk // 4)] = 1             # one late-phase sequence
+    kw = dict(tau_edge=0.3, bulk_conf=0.9, bulk_frac=0.5)
+    assert dlm.row_stats_attention_folds(cur, attn, B, blk) == folds
+    status = dlm.new_status()
+    st, ws = dlm.row_stats_attention(cur, prv, attn, masked, block_start=bs, status=status, **kw)
+    ref = dlm.row_stats(cur, prv)
+    ws_ref = dlm.dapd_graph(attn, masked, block_start=bs, **kw)
+    sel, n = dlm.dapd_select(ws, masked, st.conf.view(B, blk), **kw)
+    sel_ref, n_ref = dlm.dapd_select(ws_ref, masked, ref.conf.view(B, blk), **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for k in ("argmax", "conf", "lse", "entropy", "kl", "lse_prev"):
+        a, b = getattr(st, k), getattr(ref, k)
+        assert (a is None and b is None) or torch.equal(a, b), k
+    rows = _graph_rows(masked, 0.5)
+    assert torch.equal(_sums(ws, B, blk)[rows], _sums(ws_ref, B, blk)[rows])
+    assert torch.equal(sel, sel_ref) and torch.equal(n, n_ref)
+
+
+def test_row_stats_attention_unfolded_falls_back(dlm):
+    """Blocks whose rows are not whole 16-byte vectors are not folded: the call
+    runs the row pass and the attention pass one after the other, with the
+    same results as the two calls."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    B, blk, L, H, vocab, bs = 4, 30, 2, 3, 2048, 8
+    cur = torch.randn(B * blk, vocab, device="cuda", generator=g).to(torch.bfloat16)
+    attn = torch.rand(B, L, H, bs + blk + 2, bs + blk + 2, device="cuda", generator=g).to(torch.float16)
+    masked = torch.ones(B, blk, dtype=torch.uint8, device="cuda")
+    assert not dlm.row_stats_attention_folds(cur, attn, B, blk)
+    st, ws = dlm.row_stats_attention(cur, cur, attn, masked, block_start=bs, tau_edge=0.3)
+    ref = dlm.row_stats(cur, cur)
+    ws_ref = dlm.dapd_graph(attn, masked, block_start=bs, tau_edge=0.3)
+    torch.cuda.synchronize()
+    assert torch.equal(st.conf, ref.conf) and torch.equal(st.argmax, ref.argmax)
+    assert torch.equal(_sums(ws, B, blk), _sums(ws_ref, B, blk))
