@@ -108,6 +108,21 @@ def workload_desc(cfg):
             f"{dt[cfg.logit_dtype]} current+previous logits{att}; rules: {', '.join(cfg.rules)}")
 
 
+def row_pass_bytes(cfg, w, rows, folded):
+    """Algorithmic bytes of one row pass: the current and previous logit rows
+    it reads, plus, when the DAPD attention sums are folded into it, the
+    attention runs of the masked rows of sequences on the graph path."""
+    import synth
+    esz = 4 if cfg.logit_dtype == synth.F32 else 2
+    b = 2 * rows * cfg.vocab * esz
+    if folded:
+        asz = 4 if cfg.attn_dtype == synth.F32 else 2
+        m = w.masked.sum(axis=1)
+        graph = m >= cfg.bulk_frac * cfg.blk
+        b += cfg.n_layers * cfg.n_heads * int((m * graph).sum()) * cfg.blk * asz
+    return b
+
+
 def recorded_traffic():
     """DRAM bytes per row-pass launch from the committed ncu summary, valid
     only while the kernel source still matches the one that was profiled."""
@@ -772,8 +787,7 @@ def main():
     value = job_throughput(r["decisions"], world, args.steps, total_ms)
     ms_step = total_ms / args.steps
     k1_ms = statistics.mean(r["k1"])
-    esz = 4 if cfg.logit_dtype == 0 else 2
-    k1_bytes = 2 * r["rows"] * cfg.vocab * esz  # current + previous rows actually read
+    k1_bytes = row_pass_bytes(cfg, r["w"], r["rows"], r["folded"])
     k1_gbs = k1_bytes / (k1_ms / 1000.0) / 1e9
     peak, peak_kind = load_peaks()
     line = {
@@ -782,9 +796,9 @@ def main():
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "batch_per_gpu": cfg.batch, "positions_per_seq": cfg.blk,
                    "vocab": cfg.vocab,
-                   "l2": (f"flushed: a 512 MB write before every timed step ({k1_bytes / 1e6:.1f} MB of logit "
-                          f"rows per step), each step timed alone" if r["flush"] else
-                          f"no flush: {k1_bytes / 1e9:.3f} GB of logit rows per step, larger than L2"),
+                   "l2": (f"flushed: a 512 MB write before every timed step ({k1_bytes / 1e6:.1f} MB read by the row pass "
+                          f"per step), each step timed alone" if r["flush"] else
+                          f"no flush: {k1_bytes / 1e9:.3f} GB read by the row pass per step, larger than L2"),
                    "parallelism": f"dp{world}"},
         "logit_gbps": k1_gbs,
         "kernels_ms": {"row_stats": k1_ms, "row_stats_median": statistics.median(r["k1"]),
@@ -850,8 +864,7 @@ def per_workload(args, headline, peak, local):
         a.seed = 1000 + synth.ORDER.index(name)
         r = run_native(a, 0, 1, local, light=True)
         cfg = r["cfg"]
-        esz = 4 if cfg.logit_dtype == synth.F32 else 2
-        k1_bytes = 2 * r["rows"] * cfg.vocab * esz
+        k1_bytes = row_pass_bytes(cfg, r["w"], r["rows"], r["folded"])
         k1_ms = statistics.mean(r["k1"])
         ms = r["total_ms"] / a.steps
         rec = {"workload": workload_desc(cfg), "steps": a.steps, "ms_per_step": ms,
