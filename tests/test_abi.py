@@ -154,6 +154,39 @@ def test_selection_argument_errors(libdlm):
     assert libdlm.dlm_dapd_graph_mis(*big, 256, 32, *ok_tail, fake, 1 << 40, None, None) == INVALID
 
 
+def test_row_stats_attention_argument_errors(libdlm):
+    """dlm_row_stats_attention: the row pass's and the DAPD graph's argument
+    checks, before any launch; the fold query launches nothing."""
+    from diffusion_decoding_token_gb300._binding import DapdParams
+    fake = P(0x10000)
+    pp = ctypes.byref(DapdParams(0.01, 0.9, 0.5, 0))
+    rows = (fake, fake, 1)                        # cur, prev, bf16
+    outs = (fake,) * 4 + (None, None)             # argmax, conf, lse, entropy, kl, lse_prev
+    attn = (fake, 2, 10, 32, 10 * 32 * 512 * 512, 32 * 512 * 512, 512 * 512, 512, 256)
+    f = libdlm.dlm_row_stats_attention
+
+    def call(batch=2, blk=32, vocab=4096, stride=4096, cur=fake, attn_args=attn, masked=fake, prm=pp, ws=fake,
+             ws_bytes=1 << 30, out=outs):
+        return f(cur, fake, 1, batch, blk, vocab, stride, *out, *attn_args, masked, prm, ws, ws_bytes, None, None)
+
+    assert call(ws_bytes=16) == WS                             # workspace too small
+    assert call(blk=0) == INVALID
+    assert call(blk=300) == INVALID
+    assert call(batch=-1) == INVALID
+    assert call(masked=None) == INVALID
+    assert call(cur=None) == INVALID
+    assert call(out=(None,) + outs[1:]) == INVALID              # argmax is required
+    assert call(cur=P(0x10002)) == ALIGN
+    assert call(attn_args=(P(0x10002),) + attn[1:]) == ALIGN    # misaligned attention
+    assert call(batch=0, blk=32, vocab=4096, stride=4096) == 0        # empty: no launch
+    q = libdlm.dlm_row_stats_attention_folds
+    assert q(1, 1, 32, 126464, 2, 10, 32) == 1    # one sequence: rows split over clusters, folded
+    assert q(1, 64, 32, 152064, 2, 10, 28) == 0   # whole waves of rows: two passes
+    assert q(1, 1, 30, 126464, 2, 10, 32) == 0    # block rows not whole 16-byte vectors
+    assert q(1, 1, 256, 126464, 2, 10, 32) == 0   # attention runs beyond 48 KB
+    assert q(7, 1, 32, 126464, 2, 10, 32) == 0    # unknown dtype
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     import diffusion_decoding_token_gb300 as d
