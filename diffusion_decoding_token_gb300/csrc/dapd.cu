@@ -772,6 +772,93 @@ __global__ void __launch_bounds__(kThreads) dapd_decide_kernel(DapdArgs a) {
     select_core(a, b, late, M, m, c, s_D, s_gadj);
 }
 
+// Blocks of up to 32 positions without the float outputs: one warp per
+// sequence, lane i holding node i.  Its graph row is a 32-bit adjacency mask
+// and its degree D_i in registers (the block's sums are copied into shared
+// memory in the same round trip as the per-position inputs), the keys are
+// ordered by a 15-stage bitonic network of shuffles, and the greedy walks the
+// order with two shuffles per node; no block barrier anywhere.  Same results
+// as dapd_decide_kernel.
+__global__ void __launch_bounds__(32) dapd_decide_warp_kernel(DapdArgs a) {
+    constexpr int LD = 33;  // odd row length: the row reads A_ij of a warp spread over the banks
+    __shared__ long long s_A[32 * LD];
+    const int b = blockIdx.x, t = threadIdx.x, blk = a.blk;
+    {
+        const long long* A = a.A + (int64_t)b * blk * blk;
+        for (int q = t; q < blk * blk; q += 32) {
+            const int r = q / blk, k = q - r * blk;
+            cp_async8(&s_A[r * LD + k], A + q);
+        }
+    }
+    const bool in = t < blk;
+    const bool m = in && a.masked[(int64_t)b * blk + t] != 0;
+    const float c = in ? a.conf[(int64_t)b * blk + t] : 0.f;
+    const long long thresh = a.thresh_from_ws ? a.hdr[0] : a.edge_thresh;
+    const uint32_t mm = __ballot_sync(DLM_FULL_MASK, m);
+    const int M = __popc(mm);
+    const bool late = (float)M < a.bulk_frac * (float)blk;
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    bool s;
+    if (late) {
+        s = m && c > a.bulk_conf;
+        if (__ballot_sync(DLM_FULL_MASK, s) == 0u && M > 0) {
+            float v = m ? c : -INFINITY;
+            int idx = m ? t : 0x7fffffff;
+            warp_argmax(v, idx);
+            s = (t == idx);
+        }
+    } else {
+        // graph row of node t: I_tj = A_tj + A_jt over masked j != t
+        uint32_t adj = 0u;
+        long long D = 0;
+        if (m) {
+            for (int j = 0; j < blk; ++j) {
+                if (j == t || !((mm >> j) & 1u)) continue;
+                const long long I = s_A[t * LD + j] + s_A[j * LD + t];
+                D += I;
+                if (I > thresh) adj |= 1u << j;
+            }
+        }
+        // keys in "goes before" order, slot q in lane q; unused slots last
+        unsigned long long kh = 0, kl = 0;
+        int ix = 0x7fffffff;
+        if (m) {
+            const SortKey k = make_sort_key(D, c, a.order_mode);
+            kh = k.hi;
+            kl = k.lo;
+            ix = t;
+        }
+#pragma unroll
+        for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const unsigned long long ph = __shfl_xor_sync(DLM_FULL_MASK, kh, j);
+                const unsigned long long pl = __shfl_xor_sync(DLM_FULL_MASK, kl, j);
+                const int pi = __shfl_xor_sync(DLM_FULL_MASK, ix, j);
+                const bool keep_first = ((t & j) == 0) == ((t & k) == 0);
+                if (keep_first != key_before(kh, kl, ix, ph, pl, pi)) {
+                    kh = ph;
+                    kl = pl;
+                    ix = pi;
+                }
+            }
+        }
+        // greedy in key order: keep a node iff no kept node is a neighbour
+        uint32_t kept = 0u;
+        for (int q = 0; q < M; ++q) {
+            const int v = __shfl_sync(DLM_FULL_MASK, ix, q);
+            const uint32_t nb = __shfl_sync(DLM_FULL_MASK, adj, v);
+            if ((nb & kept) == 0u) kept |= 1u << v;
+        }
+        s = m && ((kept >> t) & 1u);
+    }
+    if (a.preunmask_certain && m && !s && c == 1.0f) s = true;
+    const int n = __popc(__ballot_sync(DLM_FULL_MASK, s));
+    if (in) a.selected[(int64_t)b * blk + t] = s ? 1 : 0;
+    if (t == 0) a.n_selected[b] = n;
+}
+
 // Larger blocks: a cluster of ceil(blk / 32) CTAs per sequence.  CTA r
 // copies the columns [32r, 32r + 32) of the sums A (every masked row: 256-byte
 // runs, asynchronous 8-byte copies) into shared memory, so the transposed
@@ -1080,6 +1167,10 @@ cudaError_t launch_dapd_select(const DapdArgs& a, cudaStream_t s) {
     cfg.stream = s;
     cfg.gridDim = dim3((unsigned)a.batch);
     cfg.blockDim = dim3(kThreads);
+    if (a.blk <= 32 && !a.s_out && !a.dtilde_out && !a.deg_out) {
+        cfg.blockDim = dim3(32);
+        return cudaLaunchKernelEx(&cfg, dapd_decide_warp_kernel, a);
+    }
     if (a.blk <= kDecideMaxBlk) return cudaLaunchKernelEx(&cfg, dapd_decide_kernel, a);
     const int csize = (a.blk + kClusterRows - 1) / kClusterRows;  // 3..8
     const cudaError_t e = cluster_smem_attribute();
