@@ -1126,3 +1126,38 @@ def test_row_stats_attention_unfolded_falls_back(dlm):
     torch.cuda.synchronize()
     assert torch.equal(st.conf, ref.conf) and torch.equal(st.argmax, ref.argmax)
     assert torch.equal(_sums(ws, B, blk), _sums(ws_ref, B, blk))
+
+
+@pytest.mark.parametrize("trial", range(10))
+def test_dapd_warp_selection_random(dlm, trial):
+    """Blocks of up to 32 without float outputs take the one-warp selection
+    kernel; with them, the one-CTA kernel.  Random blocks, masks (graph path
+    and late phase), confidences with exact 1.0s and ties, both key orders and
+    the pre-unmask flag: the two kernels and the oracle select the same
+    positions."""
+    rng = np.random.default_rng(2300 + trial)
+    blk = int(rng.integers(1, 33))
+    B = int(rng.integers(1, 10))
+    L, H = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+    sub = (rng.random((B, L, H, blk, blk)) ** 4 * 0.4).astype(np.float32)
+    sub16 = synth.to_f16_bits(sub)
+    masked = (rng.random((B, blk)) < rng.uniform(0.2, 1.0)).astype(np.uint8)
+    masked[0, :] = 1
+    conf = rng.choice(np.array([0.25, 0.5, 0.75, 0.95, 1.0], np.float32), (B, blk))
+    conf = np.where(rng.random((B, blk)) < 0.5, rng.random((B, blk)).astype(np.float32), conf).astype(np.float32)
+    om = trial % 2
+    flag = (trial // 2) % 2 == 1
+    N = (blk + 7) // 8 * 8                      # rows of 16-byte multiples, the block at the origin
+    attn = torch.zeros((B, L, H, N, N), dtype=torch.float16, device="cuda")
+    attn[:, :, :, :blk, :blk] = to_torch(sub16, synth.F16, "cuda")
+    tau = float(rng.choice([0.01, 0.05, 0.2]))
+    gs, gn = dlm.dapd_graph_mis(attn, cuda(masked), cuda(conf), tau, 0.9, 0.5, om, 0, preunmask_certain=flag)
+    deg = torch.empty(B, blk, dtype=torch.int32, device="cuda")
+    gs2, gn2 = dlm.dapd_graph_mis(attn, cuda(masked), cuda(conf), tau, 0.9, 0.5, om, 0, deg_out=deg,
+                                  preunmask_certain=flag)
+    r = oracle.dapd(sub16, masked, conf.astype(np.float64), tau, 0.9, 0.5, om, dtype=synth.F16,
+                    preunmask_certain=flag)
+    np.testing.assert_array_equal(gs.cpu().numpy(), r["selected"])
+    np.testing.assert_array_equal(gn.cpu().numpy(), r["n_selected"])
+    np.testing.assert_array_equal(gs2.cpu().numpy(), r["selected"])
+    np.testing.assert_array_equal(gn2.cpu().numpy(), r["n_selected"])
