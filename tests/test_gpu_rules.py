@@ -321,7 +321,7 @@ def test_pipeline_unscreened(dlm, name):
 
 
 @pytest.mark.parametrize("mode", ["rules", "whole"])
-@pytest.mark.parametrize("name", ["batched", "stress_graph", "depcap_window"])
+@pytest.mark.parametrize("name", ["batched", "stress_graph", "depcap_window", "llada_step", "tiny"])
 def test_bench_launch_configuration_matches_oracle(dlm, name, mode):
     """The step as the benchmark times it -- one StepPlan with the DAPD
     attention pass on a side stream from the step's start, the other rules as
@@ -339,6 +339,8 @@ def test_bench_launch_configuration_matches_oracle(dlm, name, mode):
     if "dapd" in cfg.rules:
         kw.update(attn=dw.attn, block_start=dw.block_start)
     plan = dlm.StepPlan(dw.cur, dw.prev, dw.masked, row_index=dw.row_index, **kw)
+    # the one-sequence step folds its DAPD attention sums into the row pass
+    assert plan.folded == (name == "llada_step")
     _, hi = torch.cuda.Stream.priority_range()
     main = torch.cuda.Stream(priority=hi)
     external = mode == "whole"
