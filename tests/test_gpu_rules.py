@@ -1072,6 +1072,7 @@ def test_row_stats_attention_matches_oracle(dlm, name, folds):
 
 @pytest.mark.parametrize("attn_dt,blk,B,L,H,vocab,prev,folds", [
     (torch.float16, 32, 3, 4, 6, 16384, True, True),     # few rows: split over clusters of 4
+    (torch.float16, 32, 2, 3, 4, 16384, True, "odd"),    # a mask not 4-byte aligned: read from global
     (torch.bfloat16, 8, 4, 3, 5, 32768, True, True),     # clusters of 8, one vector per block row
     (torch.float32, 8, 9, 3, 2, 8195, False, True),      # ragged vocabulary, no previous step
     (torch.float16, 64, 2, 2, 2, 8192, True, True),      # blocks of 64
@@ -1090,6 +1091,12 @@ def test_row_stats_attention_shapes(dlm, attn_dt, blk, B, L, H, vocab, prev, fol
     prv = torch.randn(B * blk, ld, device="cuda", generator=g).mul_(3).to(torch.bfloat16)[:, :vocab] if prev else None
     attn = torch.rand(B, L, H, N, N, device="cuda", generator=g).to(attn_dt)
     masked = (torch.rand(B, blk, device="cuda", generator=g) < 0.7).to(torch.uint8)
+    if folds == "odd":
+        folds = True
+        buf = torch.zeros(B * blk + 1, dtype=torch.uint8, device="cuda")
+        buf[1:] = masked.view(-1)
+        masked = buf[1:].view(B, blk)
+        assert masked.data_ptr() % 4 != 0
     masked[0, :] = 1                                  # one sequence fully masked
     if B > 2:
         masked[1, :] = 0
