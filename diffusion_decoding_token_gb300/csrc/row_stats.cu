@@ -19,7 +19,11 @@
 //    lowest index everywhere;
 //  * partial states merge through warp shuffles, shared memory and, for split
 //    rows, distributed shared memory inside the cluster; the merge order is
-//    fixed, so results are deterministic.
+//    fixed, so results are deterministic;
+//  * row_stats_attn_kernel (few-row launches) also computes the DAPD
+//    attention sums of its row: the runs are copied into shared memory with
+//    asynchronous copies before the logits stream and summed afterwards
+//    (attn_sum.cuh), so their latency hides under the row.
 // Every quantity is independent of the reference r:
 //   S = sum 2^{a_v}, a_v = (z_v - r) log2 e,  T = sum 2^{a_v} a_v,
 //   K = sum 2^{a_v} (z_v - z'_v):
